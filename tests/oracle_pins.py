@@ -1,0 +1,412 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees with:
+
+* numpy's Philox generator (a library implementation of the SC'11 Philox);
+* numpy ``argmax`` (greedy = first maximum);
+* scipy's softmax (top_p = 1 with top_k = V is plain softmax sampling);
+* brute force on tiny rows: the top-k set from pairwise ranks, the nucleus as
+  the minimum-cardinality subset reaching top_p, and the exact draw map over
+  all 2^24 values of the 24-bit uniform;
+* a chi-square test of 10^6 draws against the truncated distribution;
+* the EOS-starvation invariant of the Qwen3-TTS handbook page (section
+  "一个真实问题：说完了却停不下来"): an EOS at p ~ 1e-14 outside the top-k
+  set is never drawn;
+* the cap rule of the Drama 3 article (section "能跑通的命令，和文档写明的边界"):
+  default 64, else a power of two in [32, 4096], read from tests/golden.
+
+``PINS`` lists them cheapest first; the mutation test runs them against
+deliberately broken copies of the oracle.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+from scipy import special, stats
+
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+TWO24 = 1 << 24
+
+
+def page_facts():
+    with open(os.path.join(GOLDEN, "page_facts.json"), encoding="utf-8") as f:
+        return json.load(f)
+
+
+def shared_row_batch(values, *, dtype="f32", n_rows=1, temp=1.0, top_k=0, top_p=1.0,
+                     cap=32, steps=None, seed=0, request=0, codebook=0, eos_id=-1):
+    """n_rows rows that all read the same logits (offset 0), one stream each."""
+    if dtype == "bf16":
+        logits = np.asarray(values, dtype=np.uint16)
+    else:
+        logits = np.asarray(values, dtype=np.float32)
+    v = logits.size
+    steps = np.arange(n_rows, dtype=np.int64) if steps is None else np.asarray(steps, np.int64)
+
+    def full(x, dt):
+        a = np.asarray(x, dtype=dt)
+        return np.broadcast_to(a, (n_rows,)).copy() if a.ndim == 0 else a.astype(dt)
+
+    return {
+        "dtype": dtype, "logits": logits, "n_rows": n_rows, "n_streams": n_rows,
+        "row_vocab": np.full(n_rows, v, np.int32), "row_offsets": np.zeros(n_rows, np.int64),
+        "max_row_vocab": max(v, 1),
+        "temp": full(temp, np.float32), "top_k": full(top_k, np.int32),
+        "top_p": full(top_p, np.float32), "seed": full(seed, np.uint64),
+        "request": full(request, np.uint64), "codebook": full(codebook, np.int32),
+        "row_stream": np.arange(n_rows, dtype=np.int32), "step": steps,
+        "eos_id": full(eos_id, np.int32), "feedback_slot": np.full(n_rows, -1, np.int32),
+        "cap": cap,
+    }
+
+
+# --------------------------------------------------------------------------
+# brute-force reference pieces (no sorting routine of the oracle's kind)
+# --------------------------------------------------------------------------
+def brute_rank(values):
+    """rank_i = number of tokens that beat i: larger value, or equal and lower index."""
+    v = [float(x) for x in values]
+    return [sum(1 for j in range(len(v)) if v[j] > v[i] or (v[j] == v[i] and j < i))
+            for i in range(len(v))]
+
+
+def brute_kept(values, top_k, cap):
+    v = len(values)
+    k = top_k if top_k > 0 else v
+    k = min(k, cap, v)
+    rank = brute_rank(values)
+    return sorted((i for i in range(v) if rank[i] < k), key=lambda i: rank[i])
+
+
+def brute_probs(values, kept, temp):
+    m = max(float(values[i]) for i in kept)
+    w = [math.exp((float(values[i]) - m) / temp) for i in kept]
+    s = math.fsum(w)
+    return [x / s for x in w]
+
+
+def brute_nucleus_size(q, top_p):
+    """Minimum cardinality of any subset of the kept set whose mass reaches top_p."""
+    if top_p >= 1.0:
+        return len(q)
+    if top_p <= 0.0:
+        return 1
+    for size in range(1, len(q) + 1):
+        for subset in itertools.combinations(range(len(q)), size):
+            if math.fsum(q[i] for i in subset) >= top_p:
+                return size
+    return len(q)
+
+
+def near_cutoff(q, top_p, eps=1e-9):
+    acc = 0.0
+    for x in q:
+        acc += x
+        if abs(acc - top_p) <= eps:
+            return True
+    return False
+
+
+# --------------------------------------------------------------------------
+# pins, cheapest first
+# --------------------------------------------------------------------------
+def pin_philox_matches_numpy(orc):
+    rng = np.random.default_rng(11)
+    cases = [([0, 0, 0, 0], [0, 0]), ([2**64 - 1] * 4, [2**64 - 1] * 2),
+             ([1, 2, 3, 4], [5, 6])]
+    for _ in range(300):
+        cases.append(([int(x) for x in rng.integers(0, 2**64, 4, dtype=np.uint64)],
+                      [int(x) for x in rng.integers(0, 2**64, 2, dtype=np.uint64)]))
+    for ctr, key in cases:
+        c = sum(int(x) << (64 * i) for i, x in enumerate(ctr))
+        k = int(key[0]) | (int(key[1]) << 64)
+        # numpy's Philox increments its 256-bit counter before each block
+        ref = np.random.Philox(key=k, counter=(c - 1) % (1 << 256)).random_raw(4)
+        assert orc.philox4x64_10(ctr, key) == tuple(int(x) for x in ref), (ctr, key)
+
+
+def pin_uniform24_mapping(orc):
+    """u24 = top 24 bits of word 0 of Philox(ctr=(step, codebook, 0, 0), key=(seed, request))."""
+    rng = np.random.default_rng(12)
+    for _ in range(300):
+        seed = int(rng.integers(0, 2**64, dtype=np.uint64))
+        request = int(rng.integers(0, 2**64, dtype=np.uint64))
+        step = int(rng.integers(0, 2**40))
+        cb = int(rng.integers(0, 16))
+        c = step | (cb << 64)
+        ref = np.random.Philox(key=seed | (request << 64), counter=(c - 1) % (1 << 256))
+        assert orc.uniform24(seed, request, step, cb) == int(ref.random_raw(1)[0]) >> 40
+
+
+def pin_cap_rule(orc):
+    cap = page_facts()["top_k_cap"]
+    allowed = {1 << e for e in range(13) if cap["allowed_min"] <= (1 << e) <= cap["allowed_max"]}
+    assert orc.cap(0) == cap["default"]
+    for req in range(-2, 5000):
+        if req == 0:
+            continue
+        want = req if req in allowed else -1
+        assert orc.cap(req) == want, req
+
+
+def pin_greedy_is_argmax(orc):
+    rng = np.random.default_rng(13)
+    for v in (1, 2, 7, 64, 1000):
+        for trial in range(6):
+            # coarse values so that ties at the maximum are common
+            x = np.round(rng.normal(0, 1, v) * 2) / 2
+            bits = workloads.to_bf16_bits(x)
+            for dtype, vals in (("f32", x.astype(np.float32)), ("bf16", bits)):
+                for temp, top_k, top_p in ((1.0, 1, 0.9), (0.0, 30, 0.9), (-1.0, 0, 1.0),
+                                           (0.7, 50, 0.0)):
+                    b = shared_row_batch(vals, dtype=dtype, n_rows=3, temp=temp, top_k=top_k,
+                                         top_p=top_p, cap=64)
+                    o = orc.sample(b, max_keep=64)
+                    assert np.all(o["err"] == 0)
+                    assert np.all(o["ids"] == int(np.argmax(x))), (v, trial, temp, top_k, top_p)
+                    if temp <= 0 or top_k == 1:
+                        probs = o["kept_probs"][0, : o["n_kept"][0]]
+                        assert probs[0] == 1.0 and np.all(probs[1:] == 0.0)
+
+
+def pin_topk_set_bruteforce(orc):
+    rng = np.random.default_rng(14)
+    for v in (1, 3, 9, 16):
+        x = np.round(rng.normal(0, 1, v) * 2) / 2
+        for top_k in range(-1, v + 2):
+            b = shared_row_batch(x, n_rows=1, temp=1.0, top_k=top_k, top_p=1.0, cap=32)
+            o = orc.sample(b, max_keep=32)
+            kept = brute_kept(x, top_k, 32)
+            assert o["n_kept"][0] == len(kept)
+            assert list(o["kept_ids"][0, : len(kept)]) == kept, (v, top_k)
+
+
+def pin_softmax_special_case(orc):
+    """top_p = 1, top_k = V <= cap: kept probabilities are the plain softmax."""
+    rng = np.random.default_rng(15)
+    for v, cap, dtype in ((32, 32, "f32"), (32, 32, "bf16"), (4096, 4096, "bf16"),
+                          (20, 64, "f32")):
+        x32 = rng.normal(0, 2, v).astype(np.float32)
+        vals = workloads.to_bf16_bits(x32) if dtype == "bf16" else x32
+        x = workloads.bf16_bits_to_f32(vals) if dtype == "bf16" else x32
+        for temp in (1.0, 0.6, 1.7):
+            b = shared_row_batch(vals, dtype=dtype, n_rows=64, temp=temp, top_k=v,
+                                 top_p=1.0, cap=cap)
+            o = orc.sample(b, max_keep=v)
+            order = np.lexsort((np.arange(v), -x.astype(np.float64)))
+            t = float(np.float32(temp))  # the row's temperature is an fp32 value
+            p = special.softmax(x.astype(np.float64) / t)[order]
+            assert np.array_equal(o["kept_ids"][0], order)
+            assert np.allclose(o["kept_probs"][0], p, rtol=1e-12, atol=0)
+            cdf = np.cumsum(p)
+            u = o["u24"].astype(np.float64) / TWO24
+            pick = np.searchsorted(cdf, u, side="right")
+            ok = np.min(np.abs(cdf[None, :] - u[:, None]), axis=1) > 1e-12
+            assert np.array_equal(o["ids"][ok], order[np.minimum(pick, v - 1)][ok])
+
+
+def pin_nucleus_bruteforce(orc):
+    rng = np.random.default_rng(16)
+    rows = [np.array([0.0, 0.0]), np.array([0.0, 0.0, 0.0, 0.0]),
+            np.array([1.0, 0.0, 0.5, 0.0, -1.0])]
+    rows += [np.round(rng.normal(0, 1.5, v) * 4) / 4 for v in (6, 9, 12)]
+    grid = [0.05, 0.25, 0.5, 0.75, 0.9, 0.97, 1.0]
+    for x in rows:
+        v = x.size
+        for top_k in range(1, v + 1):
+            for top_p in grid:
+                for temp in (1.0, 0.5):
+                    b = shared_row_batch(x, n_rows=1, temp=temp, top_k=top_k, top_p=top_p,
+                                         cap=32)
+                    o = orc.sample(b, max_keep=32)
+                    kept = brute_kept(x, top_k, 32)
+                    q = brute_probs(x, kept, temp)
+                    # dyadic cases are exact; others skip a boundary within 1e-9
+                    exact = all(float(t).is_integer() for t in (np.array(q) * 4))
+                    if not exact and near_cutoff(q, top_p):
+                        continue
+                    want = 1 if top_k == 1 else brute_nucleus_size(q, top_p)
+                    assert o["n_nucleus"][0] == want, (x, top_k, top_p, temp)
+                    if top_k > 1:
+                        assert np.allclose(o["kept_probs"][0, : len(q)], q, rtol=1e-12)
+                        assert abs(o["kept_probs"][0, : len(q)].sum() - 1.0) < 1e-12
+
+
+def pin_draw_map_exact(orc):
+    """All 2^24 draws: each nucleus token's count equals its interval on the grid."""
+    cases = [
+        (np.array([0.0, 0.0]), 1.0, 2, 1.0),            # exactly 1/2, 1/2
+        (np.array([0.0, 0.0, 0.0, 0.0]), 1.0, 4, 0.6),  # 1/4 each, nucleus of 3
+        (np.array([2.0, -1.0, 0.5, 0.5, 1.25, -3.0, 0.0]), 1.0, 5, 0.9),
+        (np.array([0.3, 1.1, -0.4, 2.2, 0.9, 0.0, -2.0, 1.7, 0.2]), 0.8, 0, 0.95),
+    ]
+    for x, temp, top_k, top_p in cases:
+        counts = orc.draw_map(x, temp, top_k, top_p, 32).astype(np.int64)
+        assert counts.sum() == TWO24
+        kept = brute_kept(x, top_k, 32)
+        q = brute_probs(x, kept, float(np.float32(temp)))
+        n_p = brute_nucleus_size(q, float(np.float32(top_p)))
+        s_p = math.fsum(q[:n_p])
+        nucleus = kept[:n_p]
+        # the sorted-order CDF on the grid: count_j = ceil(2^24 C_j) - ceil(2^24 C_{j-1})
+        acc = 0.0
+        for j, tok in enumerate(nucleus):
+            lo = acc
+            acc += q[j] / s_p
+            want = math.ceil(TWO24 * acc - 1e-9) - math.ceil(TWO24 * lo - 1e-9)
+            if j == n_p - 1:
+                want = TWO24 - sum(int(counts[t]) for t in nucleus[:-1])
+            dyadic = (TWO24 * acc).is_integer() and (TWO24 * lo).is_integer()
+            assert abs(int(counts[tok]) - want) <= (0 if dyadic else 1), \
+                (x, tok, counts[tok], want)
+        for tok in range(x.size):
+            if tok not in nucleus:
+                assert counts[tok] == 0
+
+
+def pin_eos_never_drawn(orc):
+    """Near-silence: EOS at p ~ 1e-14, ranked outside the top-k set, is never drawn.
+
+    Checked for every one of the 2^24 values of the uniform (a superset of any
+    10^6 draws), then through the Philox path on 20,000 steps.
+    """
+    facts = page_facts()["eos_starvation"]
+    rng = np.random.default_rng(17)
+    v, eos = 4096, 4095
+    x = 2.0 * rng.standard_normal(v).astype(np.float32)
+    x[int(rng.integers(0, v - 1))] = 20.0
+    x[eos] = np.float32(20.0 + np.log(facts["eos_probability"]))
+    bits = workloads.to_bf16_bits(x)
+    xf = workloads.bf16_bits_to_f32(bits).astype(np.float64)
+    counts = orc.draw_map(xf, 1.0, 30, 0.9, 64)
+    assert counts.sum() == TWO24 and counts[eos] == 0
+    n = 20000
+    b = shared_row_batch(bits, dtype="bf16", n_rows=n, temp=1.0, top_k=30, top_p=0.9,
+                         cap=64, eos_id=eos)
+    o = orc.sample(b, n_threads=4)
+    assert np.all(o["err"] == 0)
+    assert not np.any(o["ids"] == eos) and not np.any(o["eos"])
+    # the largest u takes the last nucleus token, still not EOS
+    last = shared_row_batch(bits, dtype="bf16", n_rows=1, temp=1.0, top_k=30, top_p=0.9,
+                            cap=64, eos_id=eos)
+    o1 = orc.sample(last, u24=[TWO24 - 1], max_keep=64)
+    assert o1["ids"][0] == o1["kept_ids"][0, o1["n_nucleus"][0] - 1] != eos
+    # positive control: an EOS inside the nucleus is drawn and flagged
+    y = x.copy()
+    y[eos] = 20.0
+    b2 = shared_row_batch(workloads.to_bf16_bits(y), dtype="bf16", n_rows=4000, temp=1.0,
+                          top_k=30, top_p=0.9, cap=64, eos_id=eos)
+    o2 = orc.sample(b2, n_threads=4)
+    frac = float(np.mean(o2["ids"] == eos))
+    assert 0.4 < frac < 0.6 and np.array_equal(o2["eos"].astype(bool), o2["ids"] == eos)
+
+
+def pin_chi_square(orc):
+    rng = np.random.default_rng(18)
+    x = workloads.to_bf16_bits(rng.normal(0, 2, 64).astype(np.float32))
+    xf = workloads.bf16_bits_to_f32(x).astype(np.float64)
+    n = 1_000_000
+    b = shared_row_batch(x, dtype="bf16", n_rows=n, temp=1.0, top_k=30, top_p=0.9, cap=64,
+                         seed=7, request=3)
+    o = orc.sample(b, n_threads=4)
+    kept = brute_kept(xf, 30, 64)
+    q = brute_probs(xf, kept, 1.0)
+    n_p = brute_nucleus_size(q, 0.9)
+    p = np.array(q[:n_p]) / math.fsum(q[:n_p])
+    counts = np.array([np.sum(o["ids"] == t) for t in kept[:n_p]])
+    assert counts.sum() == n
+    exp_counts = p * n
+    big = exp_counts >= 5
+    obs = np.append(counts[big], counts[~big].sum())
+    exp = np.append(exp_counts[big], exp_counts[~big].sum())
+    if exp[-1] == 0:
+        obs, exp = obs[:-1], exp[:-1]
+    assert stats.chisquare(obs, exp).pvalue > 0.001
+
+
+def pin_error_rows(orc):
+    nan = np.float32("nan")
+    rows = {
+        "nan": ([0.0, nan, 1.0], 4), "pinf": ([0.0, np.inf, 1.0], 4),
+        "all_ninf": ([-np.inf, -np.inf], 4), "ok": ([0.5, -np.inf, 2.0], 0),
+    }
+    for name, (vals, bit) in rows.items():
+        b = shared_row_batch(np.array(vals, np.float32), n_rows=2, temp=1.0, top_k=30,
+                             top_p=0.9, cap=64)
+        o = orc.sample(b)
+        assert np.all(o["err"] == bit), name
+        assert np.all(o["ids"] == (-1 if bit else 2)), name
+    x = np.array([0.0, 1.0, 2.0], np.float32)
+    for temp, top_p, bit in ((float("nan"), 0.9, 2), (float("inf"), 0.9, 2),
+                             (1.0, float("nan"), 2), (1.0, 0.9, 0)):
+        o = orc.sample(shared_row_batch(x, temp=temp, top_p=top_p, top_k=30, cap=64))
+        assert o["err"][0] == bit and (o["ids"][0] == -1) == bool(bit)
+    # shape errors: V <= 0, V > max_row_vocab, offset beyond the buffer, bad stream
+    b = shared_row_batch(x, n_rows=4, top_k=30, cap=64)
+    b["row_vocab"] = np.array([0, 3, 3, 3], np.int32)
+    b["row_offsets"] = np.array([0, 0, 1, 0], np.int64)
+    b["row_stream"] = np.array([0, 1, 2, 7], np.int32)
+    b["max_row_vocab"] = 3
+    o = orc.sample(b)
+    assert list(o["err"]) == [1, 0, 1, 1] and list(o["ids"][[0, 2, 3]]) == [-1, -1, -1]
+    # -inf tokens are never drawn even when they enter the top-k set
+    y = np.full(40, -np.inf, np.float32)
+    y[[3, 17]] = [0.0, 0.0]
+    o = orc.sample(shared_row_batch(y, n_rows=5000, top_k=30, top_p=1.0, cap=64))
+    assert set(np.unique(o["ids"])) == {3, 17}
+
+
+def pin_k_clamp(orc):
+    rng = np.random.default_rng(19)
+    x = rng.normal(0, 1, 100).astype(np.float32)
+    for top_k, cap, want in ((500, 64, 64), (0, 64, 64), (-3, 32, 32), (0, 4096, 100),
+                             (64, 64, 64), (10, 64, 10)):
+        o = orc.sample(shared_row_batch(x, n_rows=50, top_k=top_k, top_p=1.0, cap=cap),
+                       max_keep=128)
+        assert np.all(o["n_kept"] == want), (top_k, cap)
+        ref = orc.sample(shared_row_batch(x, n_rows=50, top_k=want, top_p=1.0, cap=cap))
+        assert np.array_equal(o["ids"], ref["ids"])
+
+
+def pin_writeback_and_frame(orc):
+    b = workloads.make("drama3", step=3)
+    fb = np.full(b["feedback_len"], -7, np.int32)
+    b["feedback_slot"] = b["feedback_slot"].copy()
+    b["feedback_slot"][5] = -1
+    o = orc.sample(b, feedback_buf=fb)
+    assert np.all(o["err"] == 0)
+    mask = np.ones(b["n_rows"], bool)
+    mask[5] = False
+    assert np.array_equal(fb[b["feedback_slot"][mask]], o["ids"][mask]) and fb[5] == -7
+    frame = fb.reshape(b["n_streams"], b["n_codebooks"])
+    assert frame.shape == (128, page_facts()["drama3_frame"]["codebooks_per_frame"])
+    b["feedback_slot"][6] = b["feedback_len"]
+    o = orc.sample(b, feedback_buf=fb)
+    assert o["err"][6] == 8 and o["ids"][6] == -1
+    o4 = orc.sample(workloads.make("drama3", step=3), n_threads=4)
+    o1 = orc.sample(workloads.make("drama3", step=3), n_threads=1)
+    assert np.array_equal(o4["ids"], o1["ids"])
+
+
+PINS = [
+    pin_philox_matches_numpy,
+    pin_uniform24_mapping,
+    pin_cap_rule,
+    pin_greedy_is_argmax,
+    pin_topk_set_bruteforce,
+    pin_softmax_special_case,
+    pin_k_clamp,
+    pin_error_rows,
+    pin_writeback_and_frame,
+    pin_nucleus_bruteforce,
+    pin_draw_map_exact,
+    pin_eos_never_drawn,
+    pin_chi_square,
+]
