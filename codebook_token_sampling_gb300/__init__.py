@@ -1,0 +1,312 @@
+"""Python binding of the GB300 per-step multi-codebook token sampler.
+
+Thin ctypes marshalling over the C ABI in ``include/ts_sampler.h``; every step
+of sampling runs in the CUDA kernels of ``libts_sampler.so``.  PyTorch is used
+only for device memory and streams.  The functions keep the C names:
+
+    ts_create, ts_destroy, ts_max_top_k, ts_sample, ts_sample_debug,
+    ts_advance_steps, ts_read_status, ts_set_option, ts_plan,
+    ts_status_string, ts_last_error
+
+``Sampler`` wraps a handle; ``DeviceBatch`` holds one step's per-row arrays on
+the GPU with a prebuilt ``ts_batch`` so that repeated calls marshal nothing.
+Importing this module loads the compiled library and raises if it is missing;
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+TS_OK = 0
+TS_ERR_INVALID_ARG = 1
+TS_ERR_UNSUPPORTED = 2
+TS_ERR_CUDA = 3
+TS_ERR_NO_MEMORY = 4
+TS_DTYPE_F32 = 0
+TS_DTYPE_BF16 = 1
+TS_ROW_BAD_SHAPE = 1
+TS_ROW_BAD_PARAM = 2
+TS_ROW_NONFINITE = 4
+TS_ROW_BAD_SLOT = 8
+TS_OPT_PATH = 1
+TS_OPT_CLUSTER = 2
+TS_MAX_VOCAB_BF16 = 163840
+TS_MAX_VOCAB_F32 = 81920
+
+EXPORTED = ("ts_create", "ts_destroy", "ts_max_top_k", "ts_sample", "ts_sample_debug",
+            "ts_advance_steps", "ts_read_status", "ts_set_option", "ts_plan",
+            "ts_status_string", "ts_last_error")
+
+
+class TsBatch(ctypes.Structure):
+    """Mirror of ``ts_batch``."""
+    _fields_ = [
+        ("logits", ctypes.c_void_p),
+        ("dtype", ctypes.c_int32),
+        ("logits_len", ctypes.c_int64),
+        ("n_rows", ctypes.c_int32),
+        ("max_row_vocab", ctypes.c_int32),
+        ("row_vocab", ctypes.c_void_p),
+        ("row_offsets", ctypes.c_void_p),
+        ("temp", ctypes.c_void_p),
+        ("top_k", ctypes.c_void_p),
+        ("top_p", ctypes.c_void_p),
+        ("seed", ctypes.c_void_p),
+        ("request", ctypes.c_void_p),
+        ("codebook", ctypes.c_void_p),
+        ("row_stream", ctypes.c_void_p),
+        ("step", ctypes.c_void_p),
+        ("n_streams", ctypes.c_int32),
+        ("eos_id", ctypes.c_void_p),
+        ("out_ids", ctypes.c_void_p),
+        ("out_eos", ctypes.c_void_p),
+        ("feedback_buf", ctypes.c_void_p),
+        ("feedback_slot", ctypes.c_void_p),
+        ("feedback_len", ctypes.c_int64),
+    ]
+
+
+class SamplerError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        detail = _lib.ts_last_error().decode() if status == TS_ERR_CUDA else ""
+        msg = f"{what}: {_lib.ts_status_string(status).decode()}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
+        self.status = status
+
+
+def _load(path: str):
+    if not os.path.exists(path):
+        raise ImportError(f"sampler library not built: {path} (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "ts_create": ([ctypes.c_int, ctypes.c_int, ctypes.POINTER(vp)], ctypes.c_int),
+        "ts_destroy": ([vp], ctypes.c_int),
+        "ts_max_top_k": ([vp], i32),
+        "ts_sample": ([vp, ctypes.POINTER(TsBatch), vp], ctypes.c_int),
+        "ts_sample_debug": ([vp, ctypes.POINTER(TsBatch), i32, vp, vp, vp, vp, vp], ctypes.c_int),
+        "ts_advance_steps": ([vp, i32, vp], ctypes.c_int),
+        "ts_read_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
+        "ts_set_option": ([vp, i32, i32], ctypes.c_int),
+        "ts_plan": ([vp, ctypes.POINTER(TsBatch)] + [ctypes.POINTER(i32)] * 5, ctypes.c_int),
+        "ts_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "ts_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    del i64
+    return lib
+
+
+LIB_PATH = _build.LIB_PATH
+_lib = _load(LIB_PATH)
+
+
+def library():
+    """The loaded ctypes library (for symbol checks)."""
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != TS_OK:
+        raise SamplerError(status, what)
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+# --------------------------------------------------------------------------
+# C-named functions
+# --------------------------------------------------------------------------
+def ts_create(device: int = 0, max_top_k: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(_lib.ts_create(device, max_top_k, ctypes.byref(h)), "ts_create")
+    return h.value
+
+
+def ts_destroy(handle: int) -> None:
+    _check(_lib.ts_destroy(handle), "ts_destroy")
+
+
+def ts_max_top_k(handle: int) -> int:
+    return int(_lib.ts_max_top_k(handle))
+
+
+def ts_sample(handle: int, batch: "DeviceBatch", stream=None) -> None:
+    _check(_lib.ts_sample(handle, ctypes.byref(batch.c), _stream_ptr(stream)), "ts_sample")
+
+
+def ts_sample_debug(handle: int, batch: "DeviceBatch", max_keep: int, kept_ids, kept_probs,
+                    n_kept, n_nucleus, stream=None) -> None:
+    _check(_lib.ts_sample_debug(handle, ctypes.byref(batch.c), max_keep, kept_ids.data_ptr(),
+                                kept_probs.data_ptr(), n_kept.data_ptr(), n_nucleus.data_ptr(),
+                                _stream_ptr(stream)), "ts_sample_debug")
+
+
+def ts_advance_steps(step, stream=None) -> None:
+    _check(_lib.ts_advance_steps(step.data_ptr(), step.numel(), _stream_ptr(stream)),
+           "ts_advance_steps")
+
+
+def ts_read_status(handle: int, stream=None) -> int:
+    bits = ctypes.c_uint32()
+    _check(_lib.ts_read_status(handle, ctypes.byref(bits), _stream_ptr(stream)), "ts_read_status")
+    return int(bits.value)
+
+
+def ts_set_option(handle: int, option: int, value: int) -> None:
+    _check(_lib.ts_set_option(handle, option, value), "ts_set_option")
+
+
+def ts_plan(handle: int, batch: "DeviceBatch") -> dict:
+    out = [ctypes.c_int32() for _ in range(5)]
+    _check(_lib.ts_plan(handle, ctypes.byref(batch.c), *[ctypes.byref(o) for o in out]),
+           "ts_plan")
+    keys = ("path", "ctas_per_row", "threads", "smem_bytes", "grid")
+    return {k: int(o.value) for k, o in zip(keys, out)}
+
+
+def ts_status_string(status: int) -> str:
+    return _lib.ts_status_string(status).decode()
+
+
+def ts_last_error() -> str:
+    return _lib.ts_last_error().decode()
+
+
+# --------------------------------------------------------------------------
+# Convenience wrappers
+# --------------------------------------------------------------------------
+class Sampler:
+    """Owns a ``ts_sampler`` handle on one device."""
+
+    def __init__(self, device: int = 0, max_top_k: int = 0):
+        self.handle = ts_create(device, max_top_k)
+        self.device = device
+
+    @property
+    def cap(self) -> int:
+        return ts_max_top_k(self.handle)
+
+    def sample(self, batch: "DeviceBatch", stream=None) -> None:
+        ts_sample(self.handle, batch, stream)
+
+    def sample_debug(self, batch: "DeviceBatch", max_keep: int, stream=None) -> dict:
+        import torch
+        n = batch.n_rows
+        dev = batch.out_ids.device
+        kept_ids = torch.full((n, max_keep), -1, dtype=torch.int32, device=dev)
+        kept_probs = torch.zeros((n, max_keep), dtype=torch.float32, device=dev)
+        n_kept = torch.zeros(n, dtype=torch.int32, device=dev)
+        n_nucleus = torch.zeros(n, dtype=torch.int32, device=dev)
+        ts_sample_debug(self.handle, batch, max_keep, kept_ids, kept_probs, n_kept, n_nucleus,
+                        stream)
+        return {"kept_ids": kept_ids, "kept_probs": kept_probs, "n_kept": n_kept,
+                "n_nucleus": n_nucleus}
+
+    def read_status(self, stream=None) -> int:
+        return ts_read_status(self.handle, stream)
+
+    def set_option(self, option: int, value: int) -> None:
+        ts_set_option(self.handle, option, value)
+
+    def plan(self, batch: "DeviceBatch") -> dict:
+        return ts_plan(self.handle, batch)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None):
+            ts_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+_ARRAYS = (("row_vocab", np.int32), ("row_offsets", np.int64), ("temp", np.float32),
+           ("top_k", np.int32), ("top_p", np.float32), ("seed", np.uint64),
+           ("request", np.uint64), ("codebook", np.int32), ("row_stream", np.int32),
+           ("eos_id", np.int32), ("feedback_slot", np.int32))
+
+
+def _to_device(a, dtype, device):
+    import torch
+    arr = np.ascontiguousarray(np.asarray(a, dtype=dtype))
+    if arr.dtype == np.uint64:
+        arr = arr.view(np.int64)
+    elif arr.dtype == np.uint16:
+        arr = arr.view(np.int16)
+    return torch.from_numpy(arr.copy()).to(device)
+
+
+class DeviceBatch:
+    """One step's inputs and outputs in device memory plus the ``ts_batch``.
+
+    ``host`` is a workload dict (see ``workloads.make``): numpy arrays that
+    are copied to ``device`` once.  ``logits`` may be replaced by any device
+    tensor of the same layout (``set_logits``), e.g. to rotate step buffers.
+    """
+
+    def __init__(self, host: dict, device="cuda", feedback: bool = True):
+        import torch
+        self.device = torch.device(device)
+        self.dtype = TS_DTYPE_BF16 if host["dtype"] == "bf16" else TS_DTYPE_F32
+        self.n_rows = int(host["n_rows"])
+        self.arrays = {}
+        logits = np.asarray(host["logits"],
+                            dtype=np.uint16 if self.dtype == TS_DTYPE_BF16 else np.float32)
+        self.logits = _to_device(logits, logits.dtype, self.device)
+        for name, dt in _ARRAYS:
+            self.arrays[name] = _to_device(host[name], dt, self.device)
+        self.step = _to_device(host["step"], np.int64, self.device)
+        self.out_ids = torch.full((self.n_rows,), -2, dtype=torch.int32, device=self.device)
+        self.out_eos = torch.zeros(self.n_rows, dtype=torch.uint8, device=self.device)
+        self.feedback = None
+        if feedback:
+            self.feedback = torch.full((int(host["feedback_len"]),), -1, dtype=torch.int32,
+                                       device=self.device)
+        c = TsBatch()
+        c.dtype = self.dtype
+        c.n_rows = self.n_rows
+        c.max_row_vocab = int(host.get("max_row_vocab",
+                                       int(np.max(host["row_vocab"], initial=1))))
+        for name, _ in _ARRAYS:
+            setattr(c, name, self.arrays[name].data_ptr())
+        c.step = self.step.data_ptr()
+        c.n_streams = int(host["n_streams"])
+        c.out_ids = self.out_ids.data_ptr()
+        c.out_eos = self.out_eos.data_ptr()
+        if self.feedback is not None:
+            c.feedback_buf = self.feedback.data_ptr()
+            c.feedback_len = self.feedback.numel()
+        else:
+            c.feedback_buf = None
+            c.feedback_slot = None
+            c.feedback_len = 0
+        self.c = c
+        self.set_logits(self.logits)
+
+    def set_logits(self, t) -> None:
+        """Point the batch at another device tensor of logits (same layout)."""
+        self.logits = t
+        self.c.logits = t.data_ptr()
+        self.c.logits_len = t.numel()
+
+    def ids(self) -> np.ndarray:
+        return self.out_ids.cpu().numpy()
+
+    def eos(self) -> np.ndarray:
+        return self.out_eos.cpu().numpy()

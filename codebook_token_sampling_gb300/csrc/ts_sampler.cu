@@ -1,0 +1,379 @@
+// ts_sampler.cu -- host side of the C ABI declared in include/ts_sampler.h:
+// argument validation, kernel-geometry choice and launches on the caller's
+// stream.  Nothing here reads device memory, allocates or synchronises on the
+// sampling path, so a decode step can be captured into a CUDA graph (Drama 3
+// article, section "两阶段共享一张卡": decode steps replay as one graph, with
+// no host synchronisation between steps).
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <type_traits>
+
+#include "../../include/ts_sampler.h"
+#include "ts_cluster.cuh"
+#include "ts_device.cuh"
+#include "ts_warp.cuh"
+
+struct ts_sampler {
+  int device;
+  int cap;
+  int num_sms;
+  int force_path;     // 0 auto, 1 warp per row, 2 CTA/cluster per row
+  int force_cluster;  // 0 auto, else CTAs per row
+  uint32_t *status;   // device word
+};
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+ts_status cuda_fail(cudaError_t e, const char *what) {
+  std::snprintf(g_last_error, sizeof g_last_error, "%s: %s", what, cudaGetErrorString(e));
+  return TS_ERR_CUDA;
+}
+
+int cap_of(int requested) {
+  if (requested == 0) return 64;
+  if (requested < 32 || requested > 4096 || (requested & (requested - 1))) return -1;
+  return requested;
+}
+
+constexpr int kWarpMaxBF16 = 4096;
+constexpr int kWarpMaxF32 = 2048;
+
+struct Plan {
+  int path;   // 1 warp, 2 cluster
+  int nch;    // warp path: 16-byte chunks per lane
+  int g;      // cluster path: CTAs per row
+  int slice;  // cluster path: elements per CTA
+  int threads;
+  int smem;
+  int grid;
+};
+
+ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
+  const bool bf16 = b->dtype == TS_DTYPE_BF16;
+  const int vmax = b->max_row_vocab;
+  if (vmax > (bf16 ? TS_MAX_VOCAB_BF16 : TS_MAX_VOCAB_F32)) return TS_ERR_UNSUPPORTED;
+  const int warp_max = bf16 ? kWarpMaxBF16 : kWarpMaxF32;
+  const bool warp_ok = s->cap <= 64 && vmax <= warp_max;
+  int path = s->force_path ? s->force_path : (warp_ok ? 1 : 2);
+  if (path == 1 && !warp_ok) return TS_ERR_INVALID_ARG;
+  std::memset(pl, 0, sizeof *pl);
+  pl->path = path;
+  if (path == 1) {
+    const int epc = bf16 ? 8 : 4;
+    const int per_lane = (vmax + 32 * epc - 1) / (32 * epc);
+    pl->nch = per_lane <= 4 ? 4 : (per_lane <= 8 ? 8 : 16);
+    pl->threads = ts::kWarpRowsPerBlock * 32;
+    pl->smem = ts::kWarpRowsPerBlock * pl->nch * 32 * 16;  // staged keys, one buffer per warp
+    pl->grid = (b->n_rows + ts::kWarpRowsPerBlock - 1) / ts::kWarpRowsPerBlock;
+    return TS_OK;
+  }
+  const int slice_max = bf16 ? ts::kSliceMaxBF16 : ts::kSliceMaxF32;
+  const int epc = bf16 ? 8 : 4;
+  int g = 1;
+  if (s->force_cluster) {
+    g = s->force_cluster;
+  } else {
+    while ((vmax + g - 1) / g > slice_max) g *= 2;
+    // few rows: spread each row over more SMs while slices stay sizeable
+    while (g < 8 && static_cast<long long>(b->n_rows) * g * 2 <= s->num_sms &&
+           (vmax + 2 * g - 1) / (2 * g) >= 4096)
+      g *= 2;
+  }
+  if (g != 1 && g != 2 && g != 4 && g != 8) return TS_ERR_INVALID_ARG;
+  int slice = (vmax + g - 1) / g;
+  slice = (slice + epc - 1) / epc * epc;
+  if (slice > slice_max) return TS_ERR_UNSUPPORTED;
+  const ts::ClusterLayout lay = ts::cluster_layout(slice, s->cap, bf16 ? 2 : 4, epc);
+  pl->g = g;
+  pl->slice = slice;
+  pl->threads = ts::kClusterThreads;
+  pl->smem = static_cast<int>(lay.total);
+  pl->grid = b->n_rows * g;
+  return TS_OK;
+}
+
+ts_status check_batch(const ts_batch *b) {
+  if (!b) return TS_ERR_INVALID_ARG;
+  if (b->n_rows < 0 || b->n_streams < 0 || b->logits_len < 0 || b->feedback_len < 0)
+    return TS_ERR_INVALID_ARG;
+  if (b->dtype != TS_DTYPE_F32 && b->dtype != TS_DTYPE_BF16) return TS_ERR_INVALID_ARG;
+  if (b->n_rows == 0) return TS_OK;
+  if (b->max_row_vocab <= 0) return TS_ERR_INVALID_ARG;
+  const size_t es = b->dtype == TS_DTYPE_BF16 ? 2 : 4;
+  if (!b->logits || reinterpret_cast<uintptr_t>(b->logits) % es) return TS_ERR_INVALID_ARG;
+  if (!b->row_vocab || !b->row_offsets || !b->temp || !b->top_k || !b->top_p || !b->seed ||
+      !b->request || !b->codebook || !b->row_stream || !b->step || !b->out_ids || !b->out_eos)
+    return TS_ERR_INVALID_ARG;
+  if (b->n_streams == 0) return TS_ERR_INVALID_ARG;
+  if (b->feedback_buf && !b->feedback_slot) return TS_ERR_INVALID_ARG;
+  return TS_OK;
+}
+
+ts::Params make_params(const ts_sampler *s, const ts_batch *b) {
+  ts::Params p;
+  std::memset(&p, 0, sizeof p);
+  p.logits = b->logits;
+  p.logits_len = b->logits_len;
+  p.n_rows = b->n_rows;
+  p.max_row_vocab = b->max_row_vocab;
+  p.row_vocab = b->row_vocab;
+  p.row_offsets = b->row_offsets;
+  p.temp = b->temp;
+  p.top_k = b->top_k;
+  p.top_p = b->top_p;
+  p.seed = b->seed;
+  p.request = b->request;
+  p.codebook = b->codebook;
+  p.row_stream = b->row_stream;
+  p.step = b->step;
+  p.n_streams = b->n_streams;
+  p.eos_id = b->eos_id;
+  p.out_ids = b->out_ids;
+  p.out_eos = b->out_eos;
+  p.feedback_buf = b->feedback_buf;
+  p.feedback_slot = b->feedback_slot;
+  p.feedback_len = b->feedback_len;
+  p.cap = s->cap;
+  p.status = s->status;
+  return p;
+}
+
+template <class K>
+void *warp_kernel_for(int nch) {
+  if (nch == 4) return reinterpret_cast<void *>(ts::warp_sampler_kernel<K, 4>);
+  if (nch == 8) return reinterpret_cast<void *>(ts::warp_sampler_kernel<K, 8>);
+  return reinterpret_cast<void *>(ts::warp_sampler_kernel<K, 16>);
+}
+
+template <class K>
+void *cluster_kernel_for(int g) {
+  if (g == 1) return reinterpret_cast<void *>(ts::cluster_sampler_kernel<K, 1>);
+  if (g == 2) return reinterpret_cast<void *>(ts::cluster_sampler_kernel<K, 2>);
+  if (g == 4) return reinterpret_cast<void *>(ts::cluster_sampler_kernel<K, 4>);
+  return reinterpret_cast<void *>(ts::cluster_sampler_kernel<K, 8>);
+}
+
+// Lets every kernel use the device's opt-in shared memory (less what the
+// kernel declares statically).  Done once in ts_create, before any capture.
+ts_status set_attributes(int device) {
+  int optin = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  void *fns[14];
+  int n = 0;
+  const int gs[4] = {1, 2, 4, 8};
+  for (int i = 0; i < 4; ++i) {
+    fns[n++] = cluster_kernel_for<ts::KeyBF16>(gs[i]);
+    fns[n++] = cluster_kernel_for<ts::KeyF32>(gs[i]);
+  }
+  const int nchs[3] = {4, 8, 16};
+  for (int i = 0; i < 3; ++i) {
+    fns[n++] = warp_kernel_for<ts::KeyBF16>(nchs[i]);
+    fns[n++] = warp_kernel_for<ts::KeyF32>(nchs[i]);
+  }
+  for (int i = 0; i < n; ++i) {
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fns[i]);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+    const int dyn = optin - static_cast<int>(fa.sharedSizeBytes);
+    e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+  }
+  return TS_OK;
+}
+
+ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base, cudaStream_t st) {
+  Plan pl;
+  ts_status rc = make_plan(s, b, &pl);
+  if (rc != TS_OK) return rc;
+  ts::Params p = base;
+  p.slice = pl.slice;
+  const bool bf16 = b->dtype == TS_DTYPE_BF16;
+  void *fn = nullptr;
+  if (pl.path == 1) {
+    fn = bf16 ? warp_kernel_for<ts::KeyBF16>(pl.nch) : warp_kernel_for<ts::KeyF32>(pl.nch);
+  } else {
+    fn = bf16 ? cluster_kernel_for<ts::KeyBF16>(pl.g) : cluster_kernel_for<ts::KeyF32>(pl.g);
+  }
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(pl.threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  if (pl.path == 2 && pl.g > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.g);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void *args[] = {&p};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
+  return TS_OK;
+}
+
+__global__ void advance_steps_kernel(int64_t *step, int32_t n) {
+  const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+  if (i < n) step[i] += 1;
+}
+
+}  // namespace
+
+extern "C" {
+
+ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
+  if (!out) return TS_ERR_INVALID_ARG;
+  *out = nullptr;
+  const int cap = cap_of(max_top_k);
+  if (cap < 0) return TS_ERR_INVALID_ARG;
+  int n_dev = 0;
+  cudaError_t e = cudaGetDeviceCount(&n_dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDeviceCount");
+  if (device < 0 || device >= n_dev) return TS_ERR_INVALID_ARG;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  e = cudaSetDevice(device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  ts_sampler *s = new (std::nothrow) ts_sampler;
+  if (!s) {
+    cudaSetDevice(prev);
+    return TS_ERR_NO_MEMORY;
+  }
+  s->device = device;
+  s->cap = cap;
+  s->force_path = 0;
+  s->force_cluster = 0;
+  s->status = nullptr;
+  ts_status rc = TS_OK;
+  e = cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) rc = cuda_fail(e, "cudaDeviceGetAttribute");
+  if (rc == TS_OK) {
+    e = cudaMalloc(reinterpret_cast<void **>(&s->status), sizeof(uint32_t));
+    if (e != cudaSuccess) rc = e == cudaErrorMemoryAllocation ? TS_ERR_NO_MEMORY
+                                                              : cuda_fail(e, "cudaMalloc");
+  }
+  if (rc == TS_OK) {
+    e = cudaMemset(s->status, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemset");
+  }
+  if (rc == TS_OK) rc = set_attributes(device);
+  cudaSetDevice(prev);
+  if (rc != TS_OK) {
+    if (s->status) cudaFree(s->status);
+    delete s;
+    return rc;
+  }
+  *out = s;
+  return TS_OK;
+}
+
+ts_status ts_destroy(ts_sampler *s) {
+  if (!s) return TS_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(s->device);
+  cudaError_t e = cudaFree(s->status);
+  cudaSetDevice(prev);
+  delete s;
+  return e == cudaSuccess ? TS_OK : cuda_fail(e, "cudaFree");
+}
+
+int32_t ts_max_top_k(const ts_sampler *s) { return s ? s->cap : -1; }
+
+ts_status ts_sample(ts_sampler *s, const ts_batch *b, void *stream) {
+  if (!s) return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK || b->n_rows == 0) return rc;
+  return launch(s, b, make_params(s, b), static_cast<cudaStream_t>(stream));
+}
+
+ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep, int32_t *kept_ids,
+                          float *kept_probs, int32_t *n_kept, int32_t *n_nucleus, void *stream) {
+  if (!s || max_keep <= 0 || !kept_ids || !kept_probs || !n_kept || !n_nucleus)
+    return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK || b->n_rows == 0) return rc;
+  ts::Params p = make_params(s, b);
+  p.max_keep = max_keep;
+  p.kept_ids = kept_ids;
+  p.kept_probs = kept_probs;
+  p.n_kept = n_kept;
+  p.n_nucleus = n_nucleus;
+  return launch(s, b, p, static_cast<cudaStream_t>(stream));
+}
+
+ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream) {
+  if (n_streams < 0 || (n_streams > 0 && !step)) return TS_ERR_INVALID_ARG;
+  if (n_streams == 0) return TS_OK;
+  const int threads = 256;
+  advance_steps_kernel<<<(n_streams + threads - 1) / threads, threads, 0,
+                         static_cast<cudaStream_t>(stream)>>>(step, n_streams);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? TS_OK : cuda_fail(e, "advance_steps launch");
+}
+
+ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream) {
+  if (!s || !bits) return TS_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, s->status, sizeof host, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(s->status, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "ts_read_status");
+  *bits = host;
+  return TS_OK;
+}
+
+ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value) {
+  if (!s) return TS_ERR_INVALID_ARG;
+  if (option == TS_OPT_PATH) {
+    if (value < 0 || value > 2) return TS_ERR_INVALID_ARG;
+    s->force_path = value;
+    return TS_OK;
+  }
+  if (option == TS_OPT_CLUSTER) {
+    if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
+      return TS_ERR_INVALID_ARG;
+    s->force_cluster = value;
+    return TS_OK;
+  }
+  return TS_ERR_INVALID_ARG;
+}
+
+ts_status ts_plan(const ts_sampler *s, const ts_batch *b, int32_t *path, int32_t *ctas_per_row,
+                  int32_t *threads, int32_t *smem_bytes, int32_t *grid) {
+  if (!s) return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK) return rc;
+  Plan pl;
+  rc = make_plan(s, b, &pl);
+  if (rc != TS_OK) return rc;
+  if (path) *path = pl.path;
+  if (ctas_per_row) *ctas_per_row = pl.path == 1 ? 0 : pl.g;
+  if (threads) *threads = pl.threads;
+  if (smem_bytes) *smem_bytes = pl.smem;
+  if (grid) *grid = pl.grid;
+  return TS_OK;
+}
+
+const char *ts_status_string(ts_status st) {
+  switch (st) {
+    case TS_OK: return "ok";
+    case TS_ERR_INVALID_ARG: return "invalid argument";
+    case TS_ERR_UNSUPPORTED: return "unsupported size";
+    case TS_ERR_CUDA: return "CUDA error";
+    case TS_ERR_NO_MEMORY: return "out of memory";
+  }
+  return "unknown status";
+}
+
+const char *ts_last_error(void) { return g_last_error; }
+
+}  // extern "C"

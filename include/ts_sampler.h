@@ -1,0 +1,176 @@
+/*
+ * ts_sampler.h -- C ABI of the GB300 (sm_103a) per-step multi-codebook token
+ * sampler.
+ *
+ * One call samples every row of one decode step: each (stream, codebook)
+ * pair of the batch is a row of logits, and each row gets one token drawn by
+ * temperature -> top-k -> top-p sampling, an EOS flag, and an optional
+ * write-back of the token into the frame buffer that the next step reads.
+ *
+ * Sources (page title, section):
+ *  - "vLLM-Omni 宣布支持 Fish Audio Drama 3 ..." (AREX article), section
+ *    "两阶段共享一张卡": one forward per frame for the whole batch, the
+ *    backbone sampling the main codebook and the codebook tower the rest,
+ *    top-k / top-p sampling fused on the device with no host synchronisation
+ *    between steps, decode steps replayed as one CUDA graph.
+ *  - same article, section "测试口径": temperature 1.0, top_p 0.9, top_k 30.
+ *  - same article, section "能跑通的命令，和文档写明的边界": top_k is capped at
+ *    64 by default and the cap may be set to any power of two in [32, 4096].
+ *  - "案例一：Qwen3-TTS——三个 stage 与首包延迟" (AI-infra handbook), section
+ *    "第二站：TTS 引擎": the whole frame of codes is written back into a
+ *    buffer as the next step's input; section "拓扑": codec EOS id 2150.
+ *  - same page, section "一个真实问题：说完了却停不下来": an EOS at p ~ 1e-14
+ *    ranked outside the top-k set is never sampled.
+ *
+ * Semantics where the pages are silent (the plainest reading):
+ *  - selection is on the raw logits; ties go to the lower token index;
+ *  - k_eff = min(top_k > 0 ? top_k : V, cap, V); top_k above the cap is
+ *    clamped, not rejected;
+ *  - temperature only shapes probabilities: w_j = exp((l_j - l_max) / T) over
+ *    the top-k set; T <= 0 or k_eff == 1 is greedy (first sorted token);
+ *  - nucleus = smallest prefix of the top-k set, in (logit desc, index asc)
+ *    order, whose renormalised mass reaches top_p (at least one token);
+ *    top_p >= 1 keeps all k_eff, top_p <= 0 keeps one;
+ *  - draw: u = (x0 >> 40) * 2^-24 with x0 the first word of
+ *    Philox4x64-10(counter = (step, codebook, 0, 0), key = (seed, request))
+ *    (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3", SC'11);
+ *    the token is the first nucleus position whose cumulative mass exceeds
+ *    u times the nucleus mass.  Masses are summed in 2^-40 fixed point, so a
+ *    result never depends on thread, block or cluster geometry.
+ *
+ * Every pointer in ts_batch is a DEVICE pointer owned by the caller and must
+ * stay valid until the work queued on `stream` has run.  The library never
+ * allocates, frees or synchronises inside ts_sample / ts_sample_debug /
+ * ts_advance_steps, so those calls may be captured into a CUDA graph.  They
+ * run on the device that is current when they are called, which must be the
+ * device the sampler was created on.
+ */
+#ifndef TS_SAMPLER_H
+#define TS_SAMPLER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TS_OK = 0,
+  TS_ERR_INVALID_ARG = 1,  /* bad pointer, size, dtype, cap or option */
+  TS_ERR_UNSUPPORTED = 2,  /* max_row_vocab beyond what the kernels hold */
+  TS_ERR_CUDA = 3,         /* a CUDA runtime call failed (see ts_last_error) */
+  TS_ERR_NO_MEMORY = 4     /* host or device allocation failed in ts_create */
+} ts_status;
+
+typedef enum { TS_DTYPE_F32 = 0, TS_DTYPE_BF16 = 1 } ts_dtype;
+
+/* Per-row error bits.  A row with an error gets out_ids = -1, out_eos = 0
+ * and no write-back; the bit is ORed into the sampler's device status word
+ * (read with ts_read_status).  The kernels never trap or assert. */
+#define TS_ROW_BAD_SHAPE 1u /* V <= 0, V > max_row_vocab, row outside logits_len,
+                               or row_stream outside [0, n_streams) */
+#define TS_ROW_BAD_PARAM 2u /* temperature NaN or +-inf, or top_p NaN */
+#define TS_ROW_NONFINITE 4u /* a NaN or +inf logit, or no finite logit */
+#define TS_ROW_BAD_SLOT 8u  /* feedback_slot >= feedback_len */
+
+/* Largest row width each dtype supports (TS_ERR_UNSUPPORTED above it). */
+#define TS_MAX_VOCAB_BF16 163840
+#define TS_MAX_VOCAB_F32 81920
+
+typedef struct ts_sampler ts_sampler; /* opaque; owns its config and a device status word */
+
+typedef struct {
+  /* Packed ragged logits: row r holds row_vocab[r] elements starting at
+   * element offset row_offsets[r].  dtype selects fp32 or bf16 (raw bits).
+   * `logits` must be aligned to its element size; logits_len is the number
+   * of elements the buffer holds (rows reaching past it are errors). */
+  const void *logits;
+  int32_t dtype;
+  int64_t logits_len;
+  int32_t n_rows;        /* rows in this call (0 is allowed: nothing runs) */
+  int32_t max_row_vocab; /* host-side upper bound on row_vocab[]; picks the
+                            kernel geometry (no device read); wider rows
+                            are errors */
+  const int32_t *row_vocab;   /* [n_rows] */
+  const int64_t *row_offsets; /* [n_rows] element offsets */
+  const float *temp;          /* [n_rows] temperature */
+  const int32_t *top_k;       /* [n_rows] (<= 0: no top-k; clamped to the cap) */
+  const float *top_p;         /* [n_rows] */
+  const uint64_t *seed;       /* [n_rows] Philox key word 0 */
+  const uint64_t *request;    /* [n_rows] Philox key word 1 */
+  const int32_t *codebook;    /* [n_rows] Philox counter word 1 */
+  const int32_t *row_stream;  /* [n_rows] index into step[] */
+  const int64_t *step;        /* [n_streams] Philox counter word 0; read only here,
+                                 advanced by ts_advance_steps */
+  int32_t n_streams;
+  const int32_t *eos_id;      /* [n_rows] EOS token of the row, -1 = none; may be NULL */
+  int32_t *out_ids;           /* [n_rows] sampled token id, -1 on a row error */
+  uint8_t *out_eos;           /* [n_rows] 1 if the sampled id is the row's EOS */
+  int32_t *feedback_buf;      /* frame buffer of the next step, or NULL (no write-back) */
+  const int32_t *feedback_slot; /* [n_rows] slot of the row in feedback_buf,
+                                   -1 = none; required when feedback_buf is set */
+  int64_t feedback_len;       /* elements in feedback_buf */
+} ts_batch;
+
+/* Creates a sampler on CUDA device `device`.  max_top_k: 0 selects the
+ * default cap 64; otherwise a power of two in [32, 4096] (else
+ * TS_ERR_INVALID_ARG).  Allocates a 4-byte device status word (the only
+ * allocation the library makes).  Safe to call before any stream capture. */
+ts_status ts_create(int device, int max_top_k, ts_sampler **out);
+
+/* Frees the sampler and its status word.  NULL is accepted. */
+ts_status ts_destroy(ts_sampler *s);
+
+/* Effective top-k cap of the sampler (or -1 for NULL). */
+int32_t ts_max_top_k(const ts_sampler *s);
+
+/* Samples every row of `b` on `stream` (a cudaStream_t; NULL = legacy default
+ * stream).  Asynchronous: it validates the host-side arguments, picks the
+ * kernel geometry from max_row_vocab, the cap and dtype, and launches; it
+ * reads no device memory and never synchronises.  Host-side errors return a
+ * status and launch nothing; per-row errors are reported through the status
+ * word. */
+ts_status ts_sample(ts_sampler *s, const ts_batch *b, void *stream);
+
+/* Same draw as ts_sample, and additionally writes, per row r: the top-k set
+ * (kept_ids[r * max_keep + j], unspecified order), each kept token's
+ * probability renormalised over the top-k set (kept_probs, fp32; greedy rows
+ * report 1 for the drawn token and 0 for the rest), n_kept[r] = k_eff and
+ * n_nucleus[r] = nucleus size.  Rows with errors get n_kept = n_nucleus = 0.
+ * Entries beyond max_keep are not written.  For parity tests and debugging. */
+ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep,
+                          int32_t *kept_ids, float *kept_probs, int32_t *n_kept,
+                          int32_t *n_nucleus, void *stream);
+
+/* step[i] += 1 for i < n_streams, on the device (graph-capturable).  Call it
+ * after the step's ts_sample so that sibling rows of one stream share a step. */
+ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream);
+
+/* Reads the OR of all row error bits since the last read, then clears it.
+ * Synchronises `stream`: for tests and debugging, not for the decode loop. */
+ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
+
+/* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = warp per row
+ * (requires cap <= 64 and max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or
+ * cluster per row.  TS_OPT_CLUSTER: 0 = automatic, else the CTAs per row of
+ * the CTA/cluster path (1, 2, 4 or 8).  Results never depend on either. */
+#define TS_OPT_PATH 1
+#define TS_OPT_CLUSTER 2
+ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value);
+
+/* Describes the kernel that ts_sample would launch for `b` (path 1 or 2,
+ * CTAs per row, threads per CTA, dynamic shared memory bytes, grid size).
+ * Any output pointer may be NULL. */
+ts_status ts_plan(const ts_sampler *s, const ts_batch *b, int32_t *path,
+                  int32_t *ctas_per_row, int32_t *threads, int32_t *smem_bytes,
+                  int32_t *grid);
+
+/* Static strings; ts_last_error describes the last TS_ERR_CUDA of this thread. */
+const char *ts_status_string(ts_status st);
+const char *ts_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TS_SAMPLER_H */

@@ -1,0 +1,47 @@
+"""The C-ABI library loads and exports every entry point its header declares
+(no GPU needed: nothing here launches work)."""
+import ctypes
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ts_sampler.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ts_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("ts_create", "ts_destroy", "ts_sample", "ts_sample_debug", "ts_advance_steps",
+                 "ts_read_status", "ts_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    import codebook_token_sampling_gb300 as ts
+    lib = ctypes.CDLL(ts.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(ts.EXPORTED) == set(declared_functions())
+
+
+def test_binding_exposes_c_names_and_constants():
+    import codebook_token_sampling_gb300 as ts
+    for name in declared_functions():
+        assert callable(getattr(ts, name)), name
+    text = open(HEADER, encoding="utf-8").read()
+    for macro, value in re.findall(r"#define (TS_[A-Z0-9_]+) (\d+)u?", text):
+        assert getattr(ts, macro) == int(value), macro
+    assert ts.ts_status_string(ts.TS_OK) == "ok"
+    assert ts.ts_status_string(ts.TS_ERR_UNSUPPORTED) == "unsupported size"
+
+
+def test_status_codes_match_the_oracle_bits():
+    import codebook_token_sampling_gb300 as ts
+    import oracle
+    assert (ts.TS_ROW_BAD_SHAPE, ts.TS_ROW_BAD_PARAM, ts.TS_ROW_NONFINITE, ts.TS_ROW_BAD_SLOT) == \
+        (oracle.ERR_BAD_SHAPE, oracle.ERR_BAD_PARAM, oracle.ERR_NONFINITE, oracle.ERR_BAD_SLOT)
