@@ -197,6 +197,8 @@ def run_ours(args, world, rank, local):
             base.append(src)
         bufs.append(torch.from_numpy(src.view(np_dt)).to(dev))
     sampler = ts.Sampler(local, host["cap"])
+    if args.path:
+        sampler.set_option(ts.TS_OPT_PATH, args.path)
     batch = ts.DeviceBatch(host, dev)
     plan = sampler.plan(batch)
     stream = torch.cuda.Stream(device=dev)
@@ -305,6 +307,23 @@ def run_ours(args, world, rank, local):
     }
 
 
+def profile_launches(args):
+    """A few plain launches of one step, for a profiler to capture."""
+    import torch
+    import codebook_token_sampling_gb300 as ts
+    host = workloads.make(args.config, 0, rows=args.rows)
+    sampler = ts.Sampler(0, host["cap"])
+    if args.path:
+        sampler.set_option(ts.TS_OPT_PATH, args.path)
+    batch = ts.DeviceBatch(host, "cuda")
+    for _ in range(args.profile):
+        sampler.sample(batch)
+        ts.ts_advance_steps(batch.step)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": args.config, "rows": int(host["n_rows"]), "launches": args.profile,
+                      "plan": sampler.plan(batch), "status": sampler.read_status()}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -317,12 +336,19 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
+                    help="force the kernel family (0 = automatic, 1 = warp, 2 = CTA/cluster)")
+    ap.add_argument("--profile", type=int, default=0, metavar="N",
+                    help="profiling mode: N plain launches of one step, no timing (for ncu)")
     args = ap.parse_args()
     if args.config == "stress" and args.rows is None:
         args.rows = 512
     world, rank, local = dist_env()
     if args.warmup < 3:
         args.warmup = 3
+    if args.profile:
+        profile_launches(args)
+        return
 
     desc = DESCRIPTIONS[args.config].format(rows=args.rows)
     host0 = workloads.make(args.config, 0, rows=args.rows)

@@ -29,7 +29,7 @@ constexpr int kSliceMaxBF16 = 20480;
 constexpr int kSliceMaxF32 = 10240;
 
 struct ClusterLayout {
-  uint32_t keys, hist_a, hist_b, cand_key, cand_idx, misc, total;
+  uint32_t keys, hist_a, hist_b, cand, misc, total;
 };
 
 __host__ __device__ inline uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -44,10 +44,8 @@ __host__ __device__ inline ClusterLayout cluster_layout(int slice, int cap, int 
   o += kHistWords * 4;
   l.hist_b = o;
   o += kHistWords * 4;
-  l.cand_key = o;
-  o += align16(static_cast<uint32_t>(cap) * 4u);
-  l.cand_idx = o;
-  o += align16(static_cast<uint32_t>(cap) * 4u);
+  l.cand = o;  // (key, index) pairs
+  o += align16(static_cast<uint32_t>(cap) * 8u);
   l.misc = o;
   o += 1024;
   l.total = o;
@@ -121,15 +119,28 @@ __device__ void merged_select(const uint32_t *h, int nbins, uint32_t kk, uint32_
                               uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
   uint32_t hb[4] = {0u, 0u, 0u, 0u};
+  if (4 * t < nbins) {  // nbins is a multiple of 4
+    if constexpr (G == 1) {
+      const uint4 v = reinterpret_cast<const uint4 *>(h)[t];
+      hb[0] = v.x;
+      hb[1] = v.y;
+      hb[2] = v.z;
+      hb[3] = v.w;
+    } else {
+      uint4 v[G];
+      const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(&h[4 * t]));
 #pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const int bin = 4 * t + b;
-    if (bin < nbins) {
-      if constexpr (G == 1) {
-        hb[b] = h[bin];
-      } else {
+      for (int c = 0; c < G; ++c) {
+        uint32_t ra;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(c));
+        v[c] = dsmem_ld_v4(ra);
+      }
 #pragma unroll
-        for (int c = 0; c < G; ++c) hb[b] += dsmem_ld_u32(dsmem_addr(&h[bin], c));
+      for (int c = 0; c < G; ++c) {
+        hb[0] += v[c].x;
+        hb[1] += v[c].y;
+        hb[2] += v[c].z;
+        hb[3] += v[c].w;
       }
     }
   }
@@ -156,13 +167,19 @@ __device__ void merged_select(const uint32_t *h, int nbins, uint32_t kk, uint32_
 
 // Radix descent over offsets (max key - key) of the kept set with exact
 // fixed-point masses.  cut_mode: first position whose cumulative mass
-// reaches `cut` (a double); else first position whose cumulative mass
+// reaches `cut` (i.e. is >= cut); else first position whose cumulative mass
 // exceeds `target`.  Returns the key of that position's group and writes the
 // mass of all keys above that group to *above_out.
+//
+// Levels take 10 offset bits each.  At the last level a bin is one key, so
+// its mass is (count x weight of that key); above it a bin mixes keys and
+// its mass is kept as three 32-bit partial sums (weight bits 0-12, 13-25 and
+// 26+), so only native 32-bit shared-memory atomics are used.
 template <class K>
-__device__ uint32_t mass_descent(const uint32_t *ckey, int kq, uint32_t maxk, uint32_t range,
-                                 float m, float temp, bool cut_mode, double cut, uint64_t target,
-                                 uint64_t *mh, uint32_t *misc, uint64_t *scratch,
+__device__ uint32_t mass_descent(const uint2 *cand, int kq, uint32_t maxk, uint32_t range,
+                                 float m, float temp, float inv_temp, bool cut_mode, uint64_t cut,
+                                 uint64_t target,
+                                 uint32_t *h, uint32_t *misc, uint64_t *scratch,
                                  uint64_t *above_out) {
   const int t = static_cast<int>(threadIdx.x);
   const int bits = range ? 32 - __clz(range) : 0;
@@ -172,24 +189,45 @@ __device__ uint32_t mass_descent(const uint32_t *ckey, int kq, uint32_t maxk, ui
   uint64_t above = 0;
   uint64_t *wide = reinterpret_cast<uint64_t *>(misc + kMiscWide);
   for (;;) {
+    const bool exact = shift == 0;
     __syncthreads();
-    for (int i = t; i < kMassBins; i += kClusterThreads) mh[i] = 0ull;
+    for (int i = t; i < (exact ? kMassBins : 3 * kMassBins); i += kClusterThreads) h[i] = 0u;
     __syncthreads();
     for (int i = t; i < kq; i += kClusterThreads) {
-      const uint32_t key = ckey[i];
+      const uint32_t key = cand[i].x;
       const uint32_t off = maxk - key;
       if (off >= off_lo && static_cast<uint64_t>(off - off_lo) < (1ull << span)) {
-        const uint64_t f = to_fixed(kept_weight(K::value(key), m, temp));
-        if (f) atomicAdd(reinterpret_cast<unsigned long long *>(&mh[(off - off_lo) >> shift]),
-                         static_cast<unsigned long long>(f));
+        const uint32_t d = (off - off_lo) >> shift;
+        if (exact) {
+          atomicAdd(&h[d], 1u);
+        } else {
+          const uint64_t f = to_fixed(kept_weight(K::value(key), m, temp, inv_temp));
+          if (f) {
+            atomicAdd(&h[d], static_cast<uint32_t>(f & 0x1FFFu));
+            atomicAdd(&h[kMassBins + d], static_cast<uint32_t>((f >> 13) & 0x1FFFu));
+            atomicAdd(&h[2 * kMassBins + d], static_cast<uint32_t>(f >> 26));
+          }
+        }
       }
     }
     __syncthreads();
-    const uint64_t a = mh[2 * t], b = mh[2 * t + 1];
+    uint64_t ab[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const uint32_t d = static_cast<uint32_t>(2 * t + x);
+      if (exact) {
+        const uint32_t n = h[d];
+        ab[x] = n ? n * to_fixed(kept_weight(K::value(maxk - off_lo - d), m, temp, inv_temp)) : 0ull;
+      } else {
+        ab[x] = (static_cast<uint64_t>(h[2 * kMassBins + d]) << 26) +
+                (static_cast<uint64_t>(h[kMassBins + d]) << 13) + h[d];
+      }
+    }
+    const uint64_t a = ab[0], b = ab[1];
     uint64_t tot;
     const uint64_t excl = block_excl_scan_u64(a + b, scratch, &tot);
     auto reached = [&](uint64_t cum) {
-      return cut_mode ? static_cast<double>(cum) >= cut : cum > target;
+      return cut_mode ? cum >= cut : cum > target;
     };
     const uint64_t p0 = above + excl, p1 = p0 + a, p2 = p1 + b;
     if (!reached(p0) && reached(p1)) {
@@ -212,20 +250,20 @@ __device__ uint32_t mass_descent(const uint32_t *ckey, int kq, uint32_t maxk, ui
 
 // Index (token id) of the `rank`-th kept token, in index order, among those
 // with key == key_sel.  Candidates are stored in index order within each key.
-__device__ int32_t rank_select(const uint32_t *ckey, const uint32_t *cidx, int kq, uint32_t key_sel,
-                               uint64_t rank, uint32_t *misc, uint64_t *scratch) {
+__device__ int32_t rank_select(const uint2 *cand, int kq, uint32_t key_sel, uint64_t rank,
+                               uint32_t *misc, uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
   const int per = (kq + kClusterThreads - 1) / kClusterThreads;
   const int lo = min(t * per, kq), hi = min(lo + per, kq);
   uint32_t c = 0;
-  for (int i = lo; i < hi; ++i) c += ckey[i] == key_sel;
+  for (int i = lo; i < hi; ++i) c += cand[i].x == key_sel;
   uint64_t tot;
   const uint64_t excl = block_excl_scan_u64(c, scratch, &tot);
   if (rank >= excl && rank < excl + c) {
     uint64_t seen = excl;
     for (int i = lo; i < hi; ++i) {
-      if (ckey[i] == key_sel) {
-        if (seen == rank) misc[kMiscId] = cidx[i];
+      if (cand[i].x == key_sel) {
+        if (seen == rank) misc[kMiscId] = cand[i].y;
         ++seen;
       }
     }
@@ -235,7 +273,7 @@ __device__ int32_t rank_select(const uint32_t *ckey, const uint32_t *cidx, int k
 }
 
 template <class K, int G>
-__global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(const Params p) {
+__global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(const Params p) {
   constexpr int EPC = K::kPerChunk;
   constexpr int NPASS = K::kBits == 16 ? 2 : 3;
   using KT = typename std::conditional<K::kBits == 16, uint16_t, uint32_t>::type;
@@ -244,14 +282,14 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
   KT *kbuf = reinterpret_cast<KT *>(smem + lay.keys);
   uint32_t *hist_a = reinterpret_cast<uint32_t *>(smem + lay.hist_a);
   uint32_t *hist_b = reinterpret_cast<uint32_t *>(smem + lay.hist_b);
-  uint32_t *ckey = reinterpret_cast<uint32_t *>(smem + lay.cand_key);
-  uint32_t *cidx = reinterpret_cast<uint32_t *>(smem + lay.cand_idx);
+  uint2 *cand = reinterpret_cast<uint2 *>(smem + lay.cand);
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + lay.misc);
   uint64_t *scratch = reinterpret_cast<uint64_t *>(misc + kMiscScratch);
 
   const uint32_t rank = G > 1 ? cluster_rank() : 0u;
   const int r = G > 1 ? static_cast<int>(cluster_index()) : static_cast<int>(blockIdx.x);
   const int tid = static_cast<int>(threadIdx.x);
+  pdl_wait_and_release();
   if (r >= p.n_rows) return;  // whole cluster (grid is sized exactly)
   const Row w = load_row(p, r);
   if (w.err) {  // identical in every CTA of the cluster: all leave before any barrier
@@ -274,12 +312,13 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
 
   // ---- stream the slice in; keys to smem; first radix histogram ----
   constexpr int kShift0 = K::kBits - 11;
+  const uint64_t pol = l2_evict_first();
   uint32_t nbad = 0, nfin = 0;
   for (int m = tid; m < nq; m += kClusterThreads) {
     uint32_t cw[4];
     const bool interior = m * EPC >= pad && (m + 1) * EPC <= sc + pad;
     if (interior) {
-      const uint4 v = ld_stream_v4(cbase + static_cast<size_t>(m) * 16);
+      const uint4 v = ld_stream_v4(cbase + static_cast<size_t>(m) * 16, pol);
       cw[0] = K::key_word(v.x);
       cw[1] = K::key_word(v.y);
       cw[2] = K::key_word(v.z);
@@ -419,14 +458,18 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
   __syncthreads();
   if constexpr (G > 1) {
     cluster_sync_all();
-    if (tid == 0) {
+    if (tid < 32) {  // lane c < rank reads CTA c's totals
       uint32_t bg = 0, be = 0;
-      for (uint32_t c = 0; c < rank; ++c) {
-        bg += dsmem_ld_u32(dsmem_addr(&misc[kMiscTotGt], c));
-        be += dsmem_ld_u32(dsmem_addr(&misc[kMiscTotEq], c));
+      if (static_cast<uint32_t>(tid) < rank) {
+        bg = dsmem_ld_u32(dsmem_addr(&misc[kMiscTotGt], tid));
+        be = dsmem_ld_u32(dsmem_addr(&misc[kMiscTotEq], tid));
       }
-      misc[kMiscBaseGt] = bg;
-      misc[kMiscBaseEq] = be;
+      bg = __reduce_add_sync(0xFFFFFFFFu, bg);
+      be = __reduce_add_sync(0xFFFFFFFFu, be);
+      if (tid == 0) {
+        misc[kMiscBaseGt] = bg;
+        misc[kMiscBaseEq] = be;
+      }
     }
   } else if (tid == 0) {
     misc[kMiscBaseGt] = 0;
@@ -435,11 +478,8 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
   __syncthreads();
   const uint32_t base_gt = misc[kMiscBaseGt], base_eq = misc[kMiscBaseEq];
   const uint32_t idx_base = static_cast<uint32_t>(s_begin - pad);
-  uint32_t ckey_remote = 0, cidx_remote = 0;
-  if constexpr (G > 1) {
-    ckey_remote = dsmem_addr(ckey, 0);
-    cidx_remote = dsmem_addr(cidx, 0);
-  }
+  uint32_t cand_remote = 0;
+  if constexpr (G > 1) cand_remote = dsmem_addr(cand, 0);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const int m = tid + j * kClusterThreads;
@@ -461,11 +501,9 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
         if (pos < static_cast<uint32_t>(p.cap)) {
           const uint32_t idx = idx_base + static_cast<uint32_t>(m * EPC + e);
           if constexpr (G == 1) {
-            ckey[pos] = k;
-            cidx[pos] = idx;
+            cand[pos] = make_uint2(k, idx);
           } else {
-            dsmem_st_u32(ckey_remote + 4u * pos, k);
-            dsmem_st_u32(cidx_remote + 4u * pos, idx);
+            dsmem_st_v2(cand_remote + 8u * pos, k, idx);
           }
         }
       }
@@ -478,19 +516,19 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
   // ---- leader: weights, nucleus cutoff and draw over the k_eff candidates ----
   const int kq = w.k_eff;
   uint32_t mloc = 0;
-  for (int i = tid; i < kq; i += kClusterThreads) mloc = max(mloc, ckey[i]);
+  for (int i = tid; i < kq; i += kClusterThreads) mloc = max(mloc, cand[i].x);
   const uint32_t maxk = block_max_u32(mloc, scratch);
   const float mval = K::value(maxk);
-  uint64_t *mh = reinterpret_cast<uint64_t *>(hist_a);
+  uint32_t *mh = hist_a;  // mass histograms (hist_a is free again)
   int32_t id;
   int n_p = 1;
   uint64_t s_k = 0;
   if (w.greedy) {
-    id = rank_select(ckey, cidx, kq, maxk, 0, misc, scratch);
+    id = rank_select(cand, kq, maxk, 0, misc, scratch);
   } else {
     uint64_t part = 0;
     for (int i = tid; i < kq; i += kClusterThreads)
-      part += to_fixed(kept_weight(K::value(ckey[i]), mval, w.temp));
+      part += to_fixed(kept_weight(K::value(cand[i].x), mval, w.temp, w.inv_temp));
     block_excl_scan_u64(part, scratch, &s_k);
     const uint32_t range = maxk - thr;
     uint64_t s_p;
@@ -499,26 +537,19 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
       s_p = s_k;
     } else if (!(w.top_p > 0.0f)) {
       n_p = 1;
-      s_p = to_fixed(kept_weight(mval, mval, w.temp));
+      s_p = to_fixed(kept_weight(mval, mval, w.temp, w.inv_temp));
     } else {
-      const double cut = static_cast<double>(w.top_p) * static_cast<double>(s_k);
+      const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
       uint64_t above;
-      const uint32_t key_c = mass_descent<K>(ckey, kq, maxk, range, mval, w.temp, true, cut, 0,
-                                             mh, misc, scratch, &above);
-      const uint64_t wc = to_fixed(kept_weight(K::value(key_c), mval, w.temp));
-      // smallest n >= 1 with above + n * wc >= cut, compared exactly (the
-      // crossing group has positive mass; the bounds only guard the loops)
-      uint64_t n_c = 1;
-      if (wc > 0) {
-        const double est = ceil((cut - static_cast<double>(above)) / static_cast<double>(wc));
-        n_c = est < 1.0 ? 1 : (est > static_cast<double>(kq) ? static_cast<uint64_t>(kq)
-                                                              : static_cast<uint64_t>(est));
-        while (n_c > 1 && static_cast<double>(above + (n_c - 1) * wc) >= cut) --n_c;
-        while (n_c < static_cast<uint64_t>(kq) && static_cast<double>(above + n_c * wc) < cut)
-          ++n_c;
-      }
+      const uint32_t key_c = mass_descent<K>(cand, kq, maxk, range, mval, w.temp, w.inv_temp, true,
+                                             cut, 0, mh, misc, scratch, &above);
+      const uint64_t wc = to_fixed(kept_weight(K::value(key_c), mval, w.temp, w.inv_temp));
+      // smallest n >= 1 with above + n * wc >= cut (above < cut; the crossing
+      // group has positive mass, the guard only protects the division)
+      uint64_t n_c = wc > 0 ? (cut - above + wc - 1) / wc : 1;
+      if (n_c < 1) n_c = 1;
       uint32_t gt_loc = 0;
-      for (int i = tid; i < kq; i += kClusterThreads) gt_loc += ckey[i] > key_c;
+      for (int i = tid; i < kq; i += kClusterThreads) gt_loc += cand[i].x > key_c;
       uint64_t n_above;
       block_excl_scan_u64(gt_loc, scratch, &n_above);
       n_p = static_cast<int>(n_above + n_c);
@@ -529,21 +560,21 @@ __global__ void __launch_bounds__(kClusterThreads, 1) cluster_sampler_kernel(con
                                     static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
     const uint64_t target = scale_u24(u24, s_p);
     uint64_t above_d;
-    const uint32_t key_d = mass_descent<K>(ckey, kq, maxk, range, mval, w.temp, false, 0.0,
-                                           target, mh, misc, scratch, &above_d);
-    const uint64_t wd = to_fixed(kept_weight(K::value(key_d), mval, w.temp));
-    id = rank_select(ckey, cidx, kq, key_d, wd > 0 ? (target - above_d) / wd : 0, misc, scratch);
+    const uint32_t key_d = mass_descent<K>(cand, kq, maxk, range, mval, w.temp, w.inv_temp, false,
+                                           0, target, mh, misc, scratch, &above_d);
+    const uint64_t wd = to_fixed(kept_weight(K::value(key_d), mval, w.temp, w.inv_temp));
+    id = rank_select(cand, kq, key_d, wd > 0 ? (target - above_d) / wd : 0, misc, scratch);
   }
   if (tid == 0) finish_row(p, r, w, id, 0u);
   if (p.kept_ids) {
     const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
     const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
     for (int i = tid; i < kq && i < p.max_keep; i += kClusterThreads) {
-      const int32_t tok = static_cast<int32_t>(cidx[i]);
+      const int32_t tok = static_cast<int32_t>(cand[i].y);
       p.kept_ids[rb + i] = tok;
       p.kept_probs[rb + i] =
           w.greedy ? (tok == id ? 1.f : 0.f)
-                   : __fdiv_rn(kept_weight(K::value(ckey[i]), mval, w.temp), s_real);
+                   : __fdiv_rn(kept_weight(K::value(cand[i].x), mval, w.temp, w.inv_temp), s_real);
     }
     if (tid == 0) {
       p.n_kept[r] = kq;

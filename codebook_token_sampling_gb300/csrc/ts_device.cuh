@@ -127,21 +127,21 @@ __device__ __forceinline__ uint32_t philox_u24(uint64_t seed, uint64_t request,
 }
 
 // ---------------------------------------------------------------------------
-// Kept-set weight w = exp((v - m) / T) for v <= m, T > 0.  The argument is
-// carried as a float pair (exact difference by two-sum, exact division
-// remainder by fma) so that its rounding does not grow with |v - m|:
-// exp(x_hi + x_lo) = exp(x_hi) * (1 + x_lo) to first order.
+// Kept-set weight w = exp((v - m) / T) for v <= m, T > 0 (inv_t = 1 / T).
+// The argument is carried as a float pair (exact difference by two-sum, the
+// quotient's remainder by fma) so that its rounding does not grow with
+// |v - m|: exp(x_hi + x_lo) = exp(x_hi) * (1 + x_lo) to first order.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float kept_weight(float v, float m, float t) {
+__device__ __forceinline__ float kept_weight(float v, float m, float t, float inv_t) {
   if (v == -INFINITY) return 0.0f;
   const float d = v - m;
   const float bv = d - v;
   const float d_err = (v - (d - bv)) + (-m - bv);
-  const float x = __fdiv_rn(d, t);
+  const float x = d * inv_t;
   const float e = expf(x);
   if (e == 0.0f) return 0.0f;
   const float rem = fmaf(-x, t, d);
-  const float x_lo = __fdiv_rn(rem + d_err, t);
+  const float x_lo = (rem + d_err) * inv_t;
   return fmaf(e, x_lo, e);
 }
 
@@ -149,6 +149,34 @@ __device__ __forceinline__ float kept_weight(float v, float m, float t) {
 // weights stay below 2^53, so every prefix sum is exact and order-free.
 __device__ __forceinline__ uint64_t to_fixed(float w) {
   return __float2ull_rn(w * 1099511627776.0f);
+}
+
+// ceil(p * s) for an fp32 0 < p < 1 and s < 2^53, exact (128-bit product).
+// A prefix mass C (an integer) reaches top_p * S exactly when C >= this.
+__device__ __forceinline__ uint64_t ceil_mul_p(float p, uint64_t s) {
+  const uint32_t bits = __float_as_uint(p);
+  const int biased = static_cast<int>((bits >> 23) & 0xFFu);
+  uint64_t mant = bits & 0x7FFFFFu;
+  int sh;  // p = mant * 2^-sh
+  if (biased == 0) {
+    sh = 149;
+  } else {
+    mant |= 0x800000u;
+    sh = 150 - biased;
+  }
+  const uint64_t lo = mant * s, hi = __umul64hi(mant, s);
+  if (sh >= 128) return (hi | lo) ? 1ull : 0ull;
+  uint64_t q;
+  bool rem;
+  if (sh >= 64) {
+    const int k = sh - 64;
+    q = k == 0 ? hi : (hi >> k);
+    rem = lo != 0 || (k != 0 && (hi & ((1ull << k) - 1)) != 0);
+  } else {  // sh >= 24 here because p < 1
+    q = (lo >> sh) | (hi << (64 - sh));
+    rem = (lo & ((1ull << sh) - 1)) != 0;
+  }
+  return q + (rem ? 1ull : 0ull);
 }
 
 // floor(u24 * s / 2^24), exact for s < 2^53.
@@ -161,15 +189,32 @@ __device__ __forceinline__ uint64_t scale_u24(uint32_t u24, uint64_t s) {
 // ---------------------------------------------------------------------------
 // Memory helpers.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 ld_stream_v4(const void *p) {
+// An L2 policy that evicts the streamed logits first, so that the small
+// per-row parameter arrays stay resident from step to step.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint4 ld_stream_v4(const void *p, uint64_t pol) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+               : "l"(p), "l"(pol));
   return v;
 }
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
+
+// Programmatic dependent launch: the next kernel in the stream may be
+// scheduled as soon as every block of this one has started; this kernel in
+// turn waits for its predecessor's completion (and memory) before it reads
+// anything.  Without a programmatic predecessor the wait returns at once.
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+}
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -202,14 +247,25 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank)
   return r;
 }
 
+// Loads and stores to a peer CTA's shared memory.  They are ordered with
+// respect to the cluster barriers (which carry the memory clobber) and do not
+// themselves force a wait, so a thread can have several loads in flight.
 __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
   uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 
-__device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ uint4 dsmem_ld_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void dsmem_st_v2(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b));
 }
 
 // ---------------------------------------------------------------------------
@@ -221,7 +277,9 @@ struct Row {
   int32_t k_eff;
   int32_t stream;
   int32_t slot;
+  int32_t eos;
   float temp;
+  float inv_temp;
   float top_p;
   uint32_t err;
   bool greedy;
@@ -235,6 +293,7 @@ __device__ __forceinline__ Row load_row(const Params &p, int r) {
   w.top_p = p.top_p[r];
   w.stream = p.row_stream[r];
   w.slot = p.feedback_buf ? p.feedback_slot[r] : -1;
+  w.eos = p.eos_id ? p.eos_id[r] : -1;
   uint32_t e = 0;
   if (w.vocab <= 0 || w.vocab > p.max_row_vocab || w.off < 0 ||
       w.off > p.logits_len - static_cast<int64_t>(w.vocab))
@@ -248,6 +307,7 @@ __device__ __forceinline__ Row load_row(const Params &p, int r) {
   k = min(k, w.vocab);
   w.k_eff = k;
   w.greedy = !(w.temp > 0.0f) || k == 1;
+  w.inv_temp = w.greedy ? 1.0f : 1.0f / w.temp;
   w.err = e;
   return w;
 }
@@ -265,8 +325,7 @@ __device__ __forceinline__ void finish_row(const Params &p, int r, const Row &w,
     return;
   }
   p.out_ids[r] = id;
-  const int32_t eos = p.eos_id ? p.eos_id[r] : -1;
-  p.out_eos[r] = static_cast<uint8_t>(eos >= 0 && id == eos);
+  p.out_eos[r] = static_cast<uint8_t>(w.eos >= 0 && id == w.eos);
   if (w.slot >= 0) p.feedback_buf[w.slot] = id;
 }
 

@@ -20,6 +20,7 @@ struct ts_sampler {
   int num_sms;
   int force_path;     // 0 auto, 1 warp per row, 2 CTA/cluster per row
   int force_cluster;  // 0 auto, else CTAs per row
+  int pdl;            // launch with programmatic stream serialization
   uint32_t *status;   // device word
 };
 
@@ -63,11 +64,11 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
   pl->path = path;
   if (path == 1) {
     const int epc = bf16 ? 8 : 4;
-    const int per_lane = (vmax + 32 * epc - 1) / (32 * epc);
-    pl->nch = per_lane <= 4 ? 4 : (per_lane <= 8 ? 8 : 16);
-    pl->threads = ts::kWarpRowsPerBlock * 32;
-    pl->smem = ts::kWarpRowsPerBlock * pl->nch * 32 * 16;  // staged keys, one buffer per warp
-    pl->grid = (b->n_rows + ts::kWarpRowsPerBlock - 1) / ts::kWarpRowsPerBlock;
+    const int per_thread = (vmax + ts::kRowThreads * epc - 1) / (ts::kRowThreads * epc);
+    pl->nch = per_thread <= 1 ? 1 : (per_thread <= 2 ? 2 : 4);
+    pl->threads = ts::kRowThreads;
+    pl->smem = 0;  // static shared memory only
+    pl->grid = b->n_rows;
     return TS_OK;
   }
   const int slice_max = bf16 ? ts::kSliceMaxBF16 : ts::kSliceMaxF32;
@@ -143,9 +144,9 @@ ts::Params make_params(const ts_sampler *s, const ts_batch *b) {
 
 template <class K>
 void *warp_kernel_for(int nch) {
-  if (nch == 4) return reinterpret_cast<void *>(ts::warp_sampler_kernel<K, 4>);
-  if (nch == 8) return reinterpret_cast<void *>(ts::warp_sampler_kernel<K, 8>);
-  return reinterpret_cast<void *>(ts::warp_sampler_kernel<K, 16>);
+  if (nch == 1) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 1>);
+  if (nch == 2) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 2>);
+  return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 4>);
 }
 
 template <class K>
@@ -169,7 +170,7 @@ ts_status set_attributes(int device) {
     fns[n++] = cluster_kernel_for<ts::KeyBF16>(gs[i]);
     fns[n++] = cluster_kernel_for<ts::KeyF32>(gs[i]);
   }
-  const int nchs[3] = {4, 8, 16};
+  const int nchs[3] = {1, 2, 4};
   for (int i = 0; i < 3; ++i) {
     fns[n++] = warp_kernel_for<ts::KeyBF16>(nchs[i]);
     fns[n++] = warp_kernel_for<ts::KeyF32>(nchs[i]);
@@ -204,15 +205,20 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   cfg.blockDim = dim3(static_cast<unsigned>(pl.threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = s->pdl ? 1 : 0;
+  ++na;
   if (pl.path == 2 && pl.g > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.g);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(pl.g);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
   void *args[] = {&p};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return cuda_fail(e, "sampler launch");
@@ -220,6 +226,7 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
 }
 
 __global__ void advance_steps_kernel(int64_t *step, int32_t n) {
+  ts::pdl_wait_and_release();
   const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
   if (i < n) step[i] += 1;
 }
@@ -250,6 +257,7 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->cap = cap;
   s->force_path = 0;
   s->force_cluster = 0;
+  s->pdl = 1;
   s->status = nullptr;
   ts_status rc = TS_OK;
   e = cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, device);
@@ -313,9 +321,17 @@ ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream) {
   if (n_streams < 0 || (n_streams > 0 && !step)) return TS_ERR_INVALID_ARG;
   if (n_streams == 0) return TS_OK;
   const int threads = 256;
-  advance_steps_kernel<<<(n_streams + threads - 1) / threads, threads, 0,
-                         static_cast<cudaStream_t>(stream)>>>(step, n_streams);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>((n_streams + threads - 1) / threads));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, advance_steps_kernel, step, n_streams);
   return e == cudaSuccess ? TS_OK : cuda_fail(e, "advance_steps launch");
 }
 
@@ -342,6 +358,11 @@ ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value) {
     if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
       return TS_ERR_INVALID_ARG;
     s->force_cluster = value;
+    return TS_OK;
+  }
+  if (option == TS_OPT_PDL) {
+    if (value != 0 && value != 1) return TS_ERR_INVALID_ARG;
+    s->pdl = value;
     return TS_OK;
   }
   return TS_ERR_INVALID_ARG;

@@ -3,21 +3,65 @@
 // under the default cap 64, Drama 3 article sections "测试口径" and
 // "能跑通的命令，和文档写明的边界").
 //
-// One warp owns one row.  The row is read once with 16-byte streaming loads
-// (lane l issues chunks l, l+32, ..., all in flight at once), turned into
-// order-preserving keys in a per-warp shared-memory buffer, and the k-th
-// largest key is found by 8-bit radix select over a per-warp histogram (no
-// sort of the row).  The
-// k_eff <= 64 survivors (ties at the threshold taken by lowest index) are
-// bitonic-sorted across the warp by (key desc, index asc); the warp then
-// forms fixed-point weights, scans them, cuts the nucleus and draws.
+// One block of 128 threads owns one row.  Fast path (every realistic row):
+//   1. the row is read once with 16-byte streaming loads (thread t issues
+//      chunks t, t+128, ..., all in flight at once); the Philox draw is
+//      computed while they are in flight;
+//   2. keys stay in registers (and are staged in shared memory for the slow
+//      path) and feed a 1024-bin histogram of their top 10 bits (sign,
+//      exponent and one mantissa bit: half-binade bins);
+//   3. warp 0 finds the bin holding the k_eff-th largest key by a two-level
+//      suffix scan; bins 0, 1022 and 1023 hold only NaN / +inf keys and bin 1
+//      only -inf / NaN keys, so the same histogram validates the row; a
+//      second 64-bin histogram over the next 6 key bits of that bin narrows
+//      the threshold (for bf16 to the exact k_eff-th largest key);
+//   4. every key at or above the threshold (k_eff plus any ties) is packed
+//      with its index into one word (key high, inverted index low) and warp
+//      0 bitonic-sorts the words: the first k_eff are the top-k set in
+//      (logit desc, index asc) order, ties included;
+//   5. warp 0 forms fixed-point weights, scans them, cuts the nucleus and
+//      draws (the Philox draw itself is computed by warp 1 while warp 0
+//      searches the histogram).
+// Rows whose threshold would leave more than 128 candidates (huge ties) or
+// whose threshold is -inf take an exact slow path on warp 0: 8-bit radix
+// select over the staged keys with index-ordered tie ranking, then the same
+// sort and tail.
 #pragma once
 
 #include "ts_device.cuh"
 
 namespace ts {
 
-constexpr int kWarpRowsPerBlock = 8;
+constexpr int kWarpHistBins = 1024;
+constexpr int kWarpCandMax = 128;
+
+// Sort word: key in the high part, bit-inverted row index in the low part, so
+// that descending word order is (key desc, index asc).  A zero word sorts
+// after every real key (real keys are >= the -inf key).
+template <class K>
+struct SortWord;
+
+template <>
+struct SortWord<KeyBF16> {  // rows of at most 65536 tokens
+  using T = uint32_t;
+  __device__ __forceinline__ static T make(uint32_t key, uint32_t idx) {
+    return (key << 16) | (0xFFFFu - idx);
+  }
+  __device__ __forceinline__ static uint32_t key(T w) { return w >> 16; }
+  __device__ __forceinline__ static uint32_t idx(T w) { return 0xFFFFu - (w & 0xFFFFu); }
+};
+
+template <>
+struct SortWord<KeyF32> {
+  using T = unsigned long long;
+  __device__ __forceinline__ static T make(uint32_t key, uint32_t idx) {
+    return (static_cast<T>(key) << 32) | (0xFFFFFFFFu - idx);
+  }
+  __device__ __forceinline__ static uint32_t key(T w) { return static_cast<uint32_t>(w >> 32); }
+  __device__ __forceinline__ static uint32_t idx(T w) {
+    return 0xFFFFFFFFu - static_cast<uint32_t>(w);
+  }
+};
 
 // Warp inclusive scan of a 64-bit value.
 __device__ __forceinline__ uint64_t warp_incl_scan_u64(uint64_t v) {
@@ -42,63 +86,141 @@ __device__ __forceinline__ uint32_t warp_excl_scan_u32(uint32_t v, uint32_t *tot
   return x - v;
 }
 
-// Descending bitonic sort of one 64-bit value per lane.
-__device__ __forceinline__ uint64_t bitonic32_desc(uint64_t v) {
+// Inclusive suffix sum over lanes (lane l gets the sum over lanes >= l).
+__device__ __forceinline__ uint32_t warp_incl_suffix_u32(uint32_t v) {
   const uint32_t lane = lane_id();
 #pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int j = size >> 1; j > 0; j >>= 1) {
-      const uint64_t o = __shfl_xor_sync(0xFFFFFFFFu, v, j);
-      const bool lower = (lane & j) == 0;
-      const bool desc = (lane & size) == 0;
-      v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, v, o);
+    if (lane + o < 32) v += t;
   }
   return v;
 }
 
-// Descending bitonic sort of 64 values: v0 at position lane, v1 at lane + 32.
-__device__ __forceinline__ void bitonic64_desc(uint64_t &v0, uint64_t &v1) {
+// Descending bitonic sort of 32*R words held as v[i] = element i*32 + lane.
+template <class T, int R>
+__device__ __forceinline__ void bitonic_desc(T (&v)[R]) {
   const uint32_t lane = lane_id();
 #pragma unroll
-  for (int size = 2; size <= 64; size <<= 1) {
+  for (int size = 2; size <= 32 * R; size <<= 1) {
 #pragma unroll
     for (int j = size >> 1; j > 0; j >>= 1) {
-      if (j == 32) {
-        const uint64_t hi = v0 > v1 ? v0 : v1, lo = v0 > v1 ? v1 : v0;
-        v0 = hi;
-        v1 = lo;
+      if (j >= 32) {
+        const int jj = j >> 5;
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          if ((i & jj) == 0) {
+            const bool desc = ((i * 32) & size) == 0;
+            const T a = v[i], b = v[i | jj];
+            const T hi = a > b ? a : b, lo = a > b ? b : a;
+            v[i] = desc ? hi : lo;
+            v[i | jj] = desc ? lo : hi;
+          }
+        }
       } else {
-        const uint64_t o0 = __shfl_xor_sync(0xFFFFFFFFu, v0, j);
-        const uint64_t o1 = __shfl_xor_sync(0xFFFFFFFFu, v1, j);
-        const bool lower = (lane & j) == 0;
-        const bool d0 = (lane & size) == 0;
-        const bool d1 = ((lane + 32) & size) == 0;
-        v0 = (lower == d0) ? (v0 > o0 ? v0 : o0) : (v0 < o0 ? v0 : o0);
-        v1 = (lower == d1) ? (v1 > o1 ? v1 : o1) : (v1 < o1 ? v1 : o1);
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          const T o = __shfl_xor_sync(0xFFFFFFFFu, v[i], j);
+          const bool lower = (lane & j) == 0;
+          const bool desc = ((static_cast<uint32_t>(i * 32) + lane) & size) == 0;
+          v[i] = (lower == desc) ? (v[i] > o ? v[i] : o) : (v[i] < o ? v[i] : o);
+        }
       }
     }
   }
 }
 
-// Candidate word: key in the high half, bit-inverted index in the low half,
-// so that a descending order is (key desc, index asc).
-__device__ __forceinline__ uint64_t cand_word(uint32_t key, uint32_t idx) {
-  return (static_cast<uint64_t>(key) << 32) | (0xFFFFFFFFu - idx);
+// Nucleus cutoff and draw over the sorted top-k set (positions lane and
+// lane + 32 hold s0 and s1; k_eff = kq <= 64), then the outputs.
+template <class K>
+__device__ __forceinline__ void warp_tail(const Params &p, int r, const Row &w,
+                                          typename SortWord<K>::T s0,
+                                          typename SortWord<K>::T s1, int kq, uint32_t u24) {
+  using SW = SortWord<K>;
+  const uint32_t lane = lane_id();
+  const float m = K::value(SW::key(__shfl_sync(0xFFFFFFFFu, s0, 0)));
+  const bool has1 = kq > 32;
+  const int p0 = static_cast<int>(lane), p1 = static_cast<int>(lane) + 32;
+  float w0 = 0.f, w1 = 0.f;
+  if (!w.greedy) {
+    if (p0 < kq) w0 = kept_weight(K::value(SW::key(s0)), m, w.temp, w.inv_temp);
+    if (has1 && p1 < kq) w1 = kept_weight(K::value(SW::key(s1)), m, w.temp, w.inv_temp);
+  }
+  // prefix masses in 2^-40 units, as four interleaved 32-bit scans of the
+  // 20-bit halves (sums of 64 halves stay below 2^27)
+  const uint64_t f0 = to_fixed(w0), f1 = to_fixed(w1);
+  uint32_t h0 = static_cast<uint32_t>(f0 >> 20), l0 = static_cast<uint32_t>(f0 & 0xFFFFFu);
+  uint32_t h1 = static_cast<uint32_t>(f1 >> 20), l1 = static_cast<uint32_t>(f1 & 0xFFFFFu);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, h0, o), b = __shfl_up_sync(0xFFFFFFFFu, l0, o);
+    const uint32_t cc = __shfl_up_sync(0xFFFFFFFFu, h1, o), d = __shfl_up_sync(0xFFFFFFFFu, l1, o);
+    if (lane >= static_cast<uint32_t>(o)) {
+      h0 += a;
+      l0 += b;
+      h1 += cc;
+      l1 += d;
+    }
+  }
+  const uint64_t c0 = (static_cast<uint64_t>(h0) << 20) + l0;
+  const uint64_t tot0 = __shfl_sync(0xFFFFFFFFu, c0, 31);
+  const uint64_t c1 = (static_cast<uint64_t>(h1) << 20) + l1 + tot0;
+  const uint64_t s_k = __shfl_sync(0xFFFFFFFFu, c1, 31);
+
+  int n_p = 1, pick = 0;
+  if (!w.greedy) {
+    if (w.top_p >= 1.0f) {
+      n_p = kq;
+    } else if (w.top_p > 0.0f) {
+      const uint64_t cut_i = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut_i
+      const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, p0 < kq && c0 < cut_i);
+      const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, p1 < kq && c1 < cut_i);
+      n_p = min(__popc(b0) + __popc(b1) + 1, kq);
+    }
+    const int last = n_p - 1;
+    const uint64_t s_p = last < 32 ? __shfl_sync(0xFFFFFFFFu, c0, last)
+                                   : __shfl_sync(0xFFFFFFFFu, c1, last - 32);
+    const uint64_t target = scale_u24(u24, s_p);
+    const uint32_t le0 = __ballot_sync(0xFFFFFFFFu, p0 < n_p && c0 <= target);
+    const uint32_t le1 = __ballot_sync(0xFFFFFFFFu, p1 < n_p && c1 <= target);
+    pick = __popc(le0) + __popc(le1);
+  }
+  const typename SW::T pw = pick < 32 ? __shfl_sync(0xFFFFFFFFu, s0, pick)
+                                      : __shfl_sync(0xFFFFFFFFu, s1, pick - 32);
+  if (lane == 0) finish_row(p, r, w, static_cast<int32_t>(SW::idx(pw)), 0u);
+
+  if (p.kept_ids) {
+    const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
+    const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
+    if (p0 < kq && p0 < p.max_keep) {
+      p.kept_ids[rb + p0] = static_cast<int32_t>(SW::idx(s0));
+      p.kept_probs[rb + p0] = w.greedy ? (p0 == 0 ? 1.f : 0.f) : __fdiv_rn(w0, s_real);
+    }
+    if (has1 && p1 < kq && p1 < p.max_keep) {
+      p.kept_ids[rb + p1] = static_cast<int32_t>(SW::idx(s1));
+      p.kept_probs[rb + p1] = w.greedy ? 0.f : __fdiv_rn(w1, s_real);
+    }
+    if (lane == 0) {
+      p.n_kept[r] = kq;
+      p.n_nucleus[r] = n_p;
+    }
+  }
 }
 
-// Radix select, top-k collection, sort, nucleus and draw for one row whose
-// keys sit in `keys` (nq full chunks; head/tail element ekey at index eidx).
+// Exact slow path for rows the fast path declines (threshold at -inf, or a
+// threshold bin with more than kWarpCandMax keys): 8-bit radix select over the
+// staged keys, then the top-k set collected in index order (keys equal to
+// the threshold taken by lowest index), sorted, and the common tail.
 template <class K>
-__device__ __noinline__ void warp_select_and_draw(const Params &p, int r, const Row &w,
-                                                  uint32_t *hist, uint64_t *cand,
-                                                  const uint4 *keys, int nq, int rounds,
-                                                  int head, int tail, int eidx, uint32_t ekey) {
+__device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w, uint32_t *hist,
+                                            typename SortWord<K>::T *cand, const uint4 *keys,
+                                            int nq, int head, int tail, int eidx, uint32_t ekey,
+                                            uint32_t u24) {
+  using SW = SortWord<K>;
   constexpr int EPC = K::kPerChunk;
   const uint32_t lane = lane_id();
+  const int rounds = (nq + 31) >> 5;
 
-  // ---- radix select of the k_eff-th largest key, 8 bits per pass ----
   uint32_t prefix = 0, pmask = 0;
   uint32_t kk = static_cast<uint32_t>(w.k_eff);
 #pragma unroll 1
@@ -107,7 +229,7 @@ __device__ __noinline__ void warp_select_and_draw(const Params &p, int r, const 
     reinterpret_cast<uint4 *>(hist)[lane * 2] = make_uint4(0u, 0u, 0u, 0u);
     reinterpret_cast<uint4 *>(hist)[lane * 2 + 1] = make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
-#pragma unroll 4
+#pragma unroll 1
     for (int q = static_cast<int>(lane); q < nq; q += 32) {
       const uint4 v = keys[q];
       const uint32_t c[4] = {v.x, v.y, v.z, v.w};
@@ -117,22 +239,16 @@ __device__ __noinline__ void warp_select_and_draw(const Params &p, int r, const 
         if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 0xFFu], 1u);
       }
     }
-    if ((ekey & pmask) == prefix) atomicAdd(&hist[(ekey >> shift) & 0xFFu], 1u);
+    if (eidx < w.vocab && (ekey & pmask) == prefix)
+      atomicAdd(&hist[(ekey >> shift) & 0xFFu], 1u);
     __syncwarp();
-    // lane l owns bins 8l .. 8l+7; find the bin where the count from the top
-    // reaches kk
     const uint4 h0 = reinterpret_cast<const uint4 *>(hist)[lane * 2];
     const uint4 h1 = reinterpret_cast<const uint4 *>(hist)[lane * 2 + 1];
     const uint32_t hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
     uint32_t s = 0;
 #pragma unroll
     for (int b = 0; b < 8; ++b) s += hb[b];
-    uint32_t suf = s;  // sum over lanes >= this lane
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_down_sync(0xFFFFFFFFu, suf, o);
-      if (lane + o < 32) suf += t;
-    }
+    const uint32_t suf = warp_incl_suffix_u32(s);
     const uint32_t owner = 31 - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk));
     uint32_t run = suf - s, dsel = 0, asel = 0;
     bool found = false;
@@ -154,19 +270,19 @@ __device__ __noinline__ void warp_select_and_draw(const Params &p, int r, const 
     __syncwarp();
   }
   const uint32_t thr = prefix;  // k_eff-th largest key
-  const uint32_t need = kk;     // how many keys equal to thr are kept
+  const uint32_t need = kk;     // keys equal to thr that are kept
 
-  // ---- collect the top-k set in index order: head, chunks, tail ----
   uint32_t base = 0, eq_base = 0;
   const uint32_t lt = lanemask_lt();
+  const bool has_e = eidx < w.vocab;
   {  // head elements (indices 0 .. head-1 live in lanes 0 .. head-1)
-    const bool in = static_cast<int>(lane) < head;
+    const bool in = has_e && static_cast<int>(lane) < head;
     const bool gt = in && ekey > thr, eq = in && ekey == thr;
     const uint32_t eqm = __ballot_sync(0xFFFFFFFFu, eq);
     const bool take = gt || (eq && eq_base + __popc(eqm & lt) < need);
     const uint32_t sm = __ballot_sync(0xFFFFFFFFu, take);
     const uint32_t at = base + __popc(sm & lt);
-    if (take && at < 64) cand[at] = cand_word(ekey, static_cast<uint32_t>(eidx));
+    if (take && at < 64) cand[at] = SW::make(ekey, static_cast<uint32_t>(eidx));
     base += __popc(sm);
     eq_base += __popc(eqm);
   }
@@ -205,7 +321,7 @@ __device__ __noinline__ void warp_select_and_draw(const Params &p, int r, const 
         ++er;
       }
       if (take) {
-        if (pos < 64) cand[pos] = cand_word(k, idx0 + e);
+        if (pos < 64) cand[pos] = SW::make(k, idx0 + e);
         ++pos;
       }
     }
@@ -213,102 +329,282 @@ __device__ __noinline__ void warp_select_and_draw(const Params &p, int r, const 
     eq_base += eq_tot;
   }
   {  // tail elements, in lane order after the chunks
-    const bool in = static_cast<int>(lane) >= head && static_cast<int>(lane) < head + tail;
+    const bool in = has_e && static_cast<int>(lane) >= head && static_cast<int>(lane) < head + tail;
     const bool gt = in && ekey > thr, eq = in && ekey == thr;
     const uint32_t eqm = __ballot_sync(0xFFFFFFFFu, eq);
     const bool take = gt || (eq && eq_base + __popc(eqm & lt) < need);
     const uint32_t sm = __ballot_sync(0xFFFFFFFFu, take);
     const uint32_t at = base + __popc(sm & lt);
-    if (take && at < 64) cand[at] = cand_word(ekey, static_cast<uint32_t>(eidx));
-    base += __popc(sm);
+    if (take && at < 64) cand[at] = SW::make(ekey, static_cast<uint32_t>(eidx));
   }
   __syncwarp();
-
-  // ---- sort the <= 64 survivors by (key desc, index asc) ----
-  const int kq = w.k_eff;  // == base
-  uint64_t v0, v1 = 0;
+  const int kq = w.k_eff;
+  typename SW::T s[2];
+  s[0] = static_cast<int>(lane) < kq ? cand[lane] : 0;
+  s[1] = static_cast<int>(lane) + 32 < kq ? cand[lane + 32] : 0;
+  __syncwarp();
   if (kq <= 32) {
-    v0 = static_cast<int>(lane) < kq ? cand[lane] : 0ull;
-    v0 = bitonic32_desc(v0);
+    typename SW::T one[1] = {s[0]};
+    bitonic_desc<typename SW::T, 1>(one);
+    s[0] = one[0];
   } else {
-    v0 = cand[lane];
-    v1 = static_cast<int>(lane) + 32 < kq ? cand[lane + 32] : 0ull;
-    bitonic64_desc(v0, v1);
+    bitonic_desc<typename SW::T, 2>(s);
   }
-  __syncwarp();
-
-  // ---- weights, prefix masses, nucleus and draw ----
-  const uint32_t top_key = static_cast<uint32_t>(__shfl_sync(0xFFFFFFFFu, v0, 0) >> 32);
-  const float m = K::value(top_key);
-  const bool has1 = kq > 32;
-  const int p0 = static_cast<int>(lane), p1 = static_cast<int>(lane) + 32;
-  float w0 = 0.f, w1 = 0.f;
-  if (!w.greedy) {
-    if (p0 < kq) w0 = kept_weight(K::value(static_cast<uint32_t>(v0 >> 32)), m, w.temp);
-    if (has1 && p1 < kq) w1 = kept_weight(K::value(static_cast<uint32_t>(v1 >> 32)), m, w.temp);
-  }
-  const uint64_t f0 = to_fixed(w0), f1 = to_fixed(w1);
-  const uint64_t c0 = warp_incl_scan_u64(f0);
-  const uint64_t tot0 = __shfl_sync(0xFFFFFFFFu, c0, 31);
-  const uint64_t c1 = has1 ? warp_incl_scan_u64(f1) + tot0 : tot0;
-  const uint64_t s_k = has1 ? __shfl_sync(0xFFFFFFFFu, c1, 31) : tot0;
-
-  int n_p = 1, pick = 0;
-  if (!w.greedy) {
-    if (w.top_p >= 1.0f) {
-      n_p = kq;
-    } else {
-      const double cut = static_cast<double>(w.top_p) * static_cast<double>(s_k);
-      const uint32_t below0 = __ballot_sync(0xFFFFFFFFu, p0 < kq && static_cast<double>(c0) < cut);
-      const uint32_t below1 = __ballot_sync(0xFFFFFFFFu, p1 < kq && static_cast<double>(c1) < cut);
-      n_p = min(__popc(below0) + __popc(below1) + 1, kq);
-    }
-    const int last = n_p - 1;
-    const uint64_t s_p = last < 32 ? __shfl_sync(0xFFFFFFFFu, c0, last)
-                                   : __shfl_sync(0xFFFFFFFFu, c1, last - 32);
-    const uint32_t u24 = philox_u24(p.seed[r], p.request[r],
-                                    static_cast<uint64_t>(p.step[w.stream]),
-                                    static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
-    const uint64_t target = scale_u24(u24, s_p);
-    const uint32_t le0 = __ballot_sync(0xFFFFFFFFu, p0 < n_p && c0 <= target);
-    const uint32_t le1 = __ballot_sync(0xFFFFFFFFu, p1 < n_p && c1 <= target);
-    pick = __popc(le0) + __popc(le1);
-  }
-  const uint64_t pw = pick < 32 ? __shfl_sync(0xFFFFFFFFu, v0, pick)
-                                : __shfl_sync(0xFFFFFFFFu, v1, pick - 32);
-  const int32_t id = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(pw));
-  if (lane == 0) finish_row(p, r, w, id, 0u);
-
-  if (p.kept_ids) {
-    const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
-    const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
-    if (p0 < kq && p0 < p.max_keep) {
-      p.kept_ids[rb + p0] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(v0));
-      p.kept_probs[rb + p0] = w.greedy ? (p0 == 0 ? 1.f : 0.f) : __fdiv_rn(w0, s_real);
-    }
-    if (has1 && p1 < kq && p1 < p.max_keep) {
-      p.kept_ids[rb + p1] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(v1));
-      p.kept_probs[rb + p1] = w.greedy ? 0.f : __fdiv_rn(w1, s_real);
-    }
-    if (lane == 0) {
-      p.n_kept[r] = kq;
-      p.n_nucleus[r] = n_p;
-    }
-  }
+  warp_tail<K>(p, r, w, s[0], s[1], kq, u24);
 }
 
-// NCH = most 16-byte chunks per lane (the row holds at most
-// NCH * 32 * kPerChunk elements).  `keys` is this warp's staging buffer of
-// NCH * 32 chunks.
-template <class K, int NCH>
-__device__ void warp_row(const Params &p, int r, uint32_t *hist, uint64_t *cand, uint4 *keys) {
-  constexpr int EPC = K::kPerChunk;
+// Sorts the n (<= 32 * R) candidate words in `cand` and runs the tail.
+template <class K, int R>
+__device__ __forceinline__ void warp_sort_and_tail(const Params &p, int r, const Row &w,
+                                                   const typename SortWord<K>::T *cand, int n,
+                                                   uint32_t u24) {
+  using T = typename SortWord<K>::T;
   const uint32_t lane = lane_id();
-  const Row w = load_row(p, r);
-  if (w.err) {
-    if (lane == 0) finish_row(p, r, w, -1, w.err);
+  T v[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const int e = i * 32 + static_cast<int>(lane);
+    v[i] = e < n ? cand[e] : T(0);
+  }
+  bitonic_desc<T, R>(v);
+  T second = T(0);
+  if constexpr (R > 1) second = v[1];
+  warp_tail<K>(p, r, w, v[0], second, w.k_eff, u24);
+}
+
+// Histogram bin b lives at b + b / 32, so that a lane reading 32 consecutive
+// bins touches 32 different banks.
+__device__ __forceinline__ uint32_t hist_slot(uint32_t b) { return b + (b >> 5); }
+constexpr int kRowHistWords = kWarpHistBins + kWarpHistBins / 32;
+
+// Shared state of one row in a block.
+constexpr int kSubBins = 64;  // second-level histogram: the next 6 key bits
+template <class K>
+struct RowShared {
+  using T = typename SortWord<K>::T;
+  uint32_t hist[kRowHistWords];
+  uint32_t sub[kSubBins];
+  T cand[kWarpCandMax];
+  uint32_t n_cand;
+  uint32_t b1;
+  uint32_t above1;  // keys in bins above b1
+  uint32_t thr;     // candidate threshold key after the second level
+  uint32_t n_sel;   // keys >= thr
+  uint32_t u24;
+};
+
+// One block of kRowThreads threads per row.
+constexpr int kRowThreads = 128;
+
+// The row body for rows of at most NCH 16-byte chunks per thread.
+template <class K, int NCH>
+__device__ __forceinline__ void row_body(const Params &p, int r, const Row &w, int64_t step,
+                                         RowShared<K> &sh, uint4 *keys, int head, int nq,
+                                         int tail, const char *rowp) {
+  using SW = SortWord<K>;
+  using T = typename SW::T;
+  constexpr int EPC = K::kPerChunk;
+  constexpr int kShift = K::kBits - 10;  // top 10 key bits select the bin
+  constexpr int kShift2 = kShift - 6;    // the next 6 select the sub-bin
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t lane = lane_id();
+  const int warp = t >> 5;
+  const int V = w.vocab;
+  const char *body = rowp + head * K::kElemBytes;
+  const uint64_t pol = l2_evict_first();
+
+  // ---- issue every load of the row (thread t: chunks t, t+128, ...) ----
+  uint4 v[NCH];
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int q = t + kRowThreads * j;
+    v[j] = make_uint4(0u, 0u, 0u, 0u);
+    if (q < nq) v[j] = ld_stream_v4(body + static_cast<size_t>(q) * 16, pol);
+  }
+  int eidx = 0x7FFFFFFF;  // head / tail elements live in the first threads
+  if (t < head)
+    eidx = t;
+  else if (t < head + tail)
+    eidx = nq * EPC + t;
+  uint32_t ebits = 0;
+  if (eidx < V) ebits = K::load_one(rowp, eidx);
+  __syncthreads();  // histograms cleared
+
+  // ---- keys: to registers (packed) and shared memory; 10-bit histogram ----
+  uint32_t c[NCH][4];
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int q = t + kRowThreads * j;
+    c[j][0] = K::key_word(v[j].x);
+    c[j][1] = K::key_word(v[j].y);
+    c[j][2] = K::key_word(v[j].z);
+    c[j][3] = K::key_word(v[j].w);
+    if (q < nq) {
+      keys[q] = make_uint4(c[j][0], c[j][1], c[j][2], c[j][3]);
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) atomicAdd(&sh.hist[hist_slot(K::elem(c[j], e) >> kShift)], 1u);
+    }
+  }
+  const uint32_t ekey = eidx < V ? K::key(ebits) : 0u;
+  if (eidx < V) atomicAdd(&sh.hist[hist_slot(ekey >> kShift)], 1u);
+  __syncthreads();
+
+  // ---- validity: bins 0, 1022, 1023 hold only NaN/+inf keys; bin 1 holds
+  // -inf and negative NaNs ----
+  const uint32_t h_nan = sh.hist[hist_slot(0)] + sh.hist[hist_slot(kWarpHistBins - 2)] +
+                         sh.hist[hist_slot(kWarpHistBins - 1)];
+  const uint32_t h_ninf = sh.hist[hist_slot(1)];
+  bool bad = h_nan != 0;
+  if (!bad && h_ninf != 0) {  // uniform branch
+    bool nan = false;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      if (t + kRowThreads * j < nq) {
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) nan |= K::elem(c[j], e) < K::kNegInf;
+      }
+    }
+    if (eidx < V) nan |= ekey < K::kNegInf;
+    bad = __syncthreads_or(nan) != 0;
+  }
+  if (bad || static_cast<uint32_t>(V) == h_ninf) {
+    if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
     return;
   }
+
+  // ---- warp 0: the bin of the k_eff-th largest key; warp 1: the draw ----
+  const uint32_t kk = static_cast<uint32_t>(w.k_eff);
+  if (warp == 0) {
+    const uint32_t *hb = &sh.hist[lane * 33];
+    uint32_t part[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) part[i & 3] += hb[i];
+    const uint32_t s = part[0] + part[1] + part[2] + part[3];
+    const uint32_t suf = warp_incl_suffix_u32(s);
+    const uint32_t big = 31 - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk));
+    const uint32_t above_lane = __shfl_sync(0xFFFFFFFFu, suf - s, big);
+    const uint32_t cb = sh.hist[big * 33 + lane];
+    const uint32_t suf2 = warp_incl_suffix_u32(cb) + above_lane;
+    const uint32_t sub = 31 - __clz(__ballot_sync(0xFFFFFFFFu, suf2 >= kk));
+    const uint32_t above1 = __shfl_sync(0xFFFFFFFFu, suf2 - cb, sub);
+    if (lane == 0) {
+      sh.b1 = big * 32 + sub;
+      sh.above1 = above1;
+    }
+  } else if (warp == 1 && lane == 0) {
+    sh.u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(step),
+                        static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
+  }
+  __syncthreads();
+  const uint32_t b1 = sh.b1;
+  if (b1 < 2) {  // threshold at -inf: exact slow path
+    if (warp == 0)
+      warp_slow_path<K>(p, r, w, sh.hist, sh.cand, keys, nq, head, tail, eidx, ekey, sh.u24);
+    return;
+  }
+
+  // ---- second level inside bin b1: the next 6 key bits ----
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    if (t + kRowThreads * j < nq) {
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) {
+        const uint32_t k = K::elem(c[j], e);
+        if ((k >> kShift) == b1) atomicAdd(&sh.sub[(k >> kShift2) & (kSubBins - 1)], 1u);
+      }
+    }
+  }
+  if (eidx < V && (ekey >> kShift) == b1)
+    atomicAdd(&sh.sub[(ekey >> kShift2) & (kSubBins - 1)], 1u);
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t kk2 = kk - sh.above1;  // ranks still needed inside bin b1
+    const uint32_t lo = sh.sub[2 * lane], hi = sh.sub[2 * lane + 1];
+    const uint32_t s = lo + hi;
+    const uint32_t suf = warp_incl_suffix_u32(s);
+    const uint32_t own = 31 - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk2));
+    const uint32_t above_lane = suf - s;  // counts in sub-bins above this lane's pair
+    // within the owning lane: sub-bin 2*own+1 first, then 2*own
+    const bool top = above_lane + hi >= kk2;
+    const uint32_t b2 = 2 * lane + (top ? 1u : 0u);
+    const uint32_t n_sel = sh.above1 + (top ? above_lane + hi : suf);
+    if (lane == own) {
+      sh.thr = ((b1 << 6) | b2) << kShift2;
+      sh.n_sel = n_sel;
+    }
+  }
+  __syncthreads();
+  const uint32_t tkey = sh.thr, n_sel = sh.n_sel;
+  if (n_sel > static_cast<uint32_t>(kWarpCandMax)) {  // huge ties: exact slow path
+    if (warp == 0)
+      warp_slow_path<K>(p, r, w, sh.hist, sh.cand, keys, nq, head, tail, eidx, ekey, sh.u24);
+    return;
+  }
+
+  // ---- every key >= tkey joins the candidates (any order: sorted next) ----
+  uint32_t mine = 0;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    if (t + kRowThreads * j < nq) {
+#pragma unroll
+      for (int e = 0; e < EPC; ++e) mine += K::elem(c[j], e) >= tkey;
+    }
+  }
+  const bool e_in = eidx < V && ekey >= tkey;
+  mine += e_in;
+  if (mine) {
+    uint32_t pos = atomicAdd(&sh.n_cand, mine);
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int q = t + kRowThreads * j;
+      if (q < nq) {
+#pragma unroll
+        for (int e = 0; e < EPC; ++e) {
+          const uint32_t k = K::elem(c[j], e);
+          if (k >= tkey) {
+            if (pos < static_cast<uint32_t>(kWarpCandMax))
+              sh.cand[pos] = SW::make(k, static_cast<uint32_t>(head + q * EPC + e));
+            ++pos;
+          }
+        }
+      }
+    }
+    if (e_in && pos < static_cast<uint32_t>(kWarpCandMax))
+      sh.cand[pos] = SW::make(ekey, static_cast<uint32_t>(eidx));
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const int nc = static_cast<int>(n_sel);
+  if (nc <= 32)
+    warp_sort_and_tail<K, 1>(p, r, w, sh.cand, nc, sh.u24);
+  else if (nc <= 64)
+    warp_sort_and_tail<K, 2>(p, r, w, sh.cand, nc, sh.u24);
+  else
+    warp_sort_and_tail<K, 4>(p, r, w, sh.cand, nc, sh.u24);
+}
+
+// MAXNCH = most 16-byte chunks per thread of any row in the launch; each row
+// runs the body sized for its own width.
+template <class K, int MAXNCH>
+__global__ void __launch_bounds__(kRowThreads, 10) row_sampler_kernel(const Params p) {
+  constexpr int EPC = K::kPerChunk;
+  __shared__ __align__(16) RowShared<K> sh;
+  __shared__ __align__(16) uint4 keys[MAXNCH * kRowThreads];
+  const int r = static_cast<int>(blockIdx.x);
+  const int t = static_cast<int>(threadIdx.x);
+  pdl_wait_and_release();
+  if (r >= p.n_rows) return;
+
+  for (int i = t; i < kRowHistWords; i += kRowThreads) sh.hist[i] = 0u;
+  if (t < kSubBins) sh.sub[t] = 0u;
+  if (t == 0) sh.n_cand = 0;
+
+  const Row w = load_row(p, r);
+  if (w.err) {
+    if (t == 0) finish_row(p, r, w, -1, w.err);
+    return;
+  }
+  const int64_t step = (t >> 5) == 1 ? p.step[w.stream] : 0;  // for the draw (warp 1)
   const int V = w.vocab;
   const char *rowp = static_cast<const char *>(p.logits) + w.off * K::kElemBytes;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
@@ -316,68 +612,12 @@ __device__ void warp_row(const Params &p, int r, uint32_t *hist, uint64_t *cand,
   head = min(head, V);
   const int nq = (V - head) / EPC;
   const int tail = V - head - nq * EPC;
-  const char *body = rowp + head * K::kElemBytes;
-  const int rounds = (nq + 31) >> 5;  // warp-uniform chunk rounds
-
-  // ---- load: interior chunks by 16-byte loads (all in flight), head/tail by
-  // single loads; keys go to this warp's shared buffer ----
-  {
-    uint4 v[NCH];
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int q = static_cast<int>(lane) + 32 * j;
-      v[j] = make_uint4(0u, 0u, 0u, 0u);
-      if (q < nq) v[j] = ld_stream_v4(body + static_cast<size_t>(q) * 16);
-    }
-    bool bad = false, finite = false;
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int q = static_cast<int>(lane) + 32 * j;
-      if (q < nq) {
-        const uint32_t c[4] = {K::key_word(v[j].x), K::key_word(v[j].y), K::key_word(v[j].z),
-                               K::key_word(v[j].w)};
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) {
-          const uint32_t k = K::elem(c, e);
-          bad |= (k < K::kNegInf) | (k >= K::kPosInf);
-          finite |= k > K::kNegInf;
-        }
-        keys[q] = make_uint4(c[0], c[1], c[2], c[3]);
-      }
-    }
-    // the head/tail element of this lane, if any
-    int eidx = 0x7FFFFFFF;
-    if (static_cast<int>(lane) < head)
-      eidx = static_cast<int>(lane);
-    else if (static_cast<int>(lane) < head + tail)
-      eidx = nq * EPC + static_cast<int>(lane);
-    uint32_t ekey = 0;
-    if (eidx < V) {
-      ekey = K::key(K::load_one(rowp, eidx));
-      bad |= (ekey < K::kNegInf) | (ekey >= K::kPosInf);
-      finite |= ekey > K::kNegInf;
-    }
-    bad = __any_sync(0xFFFFFFFFu, bad);
-    finite = __any_sync(0xFFFFFFFFu, finite);
-    if (bad || !finite) {
-      if (lane == 0) finish_row(p, r, w, -1, kRowNonFinite);
-      return;
-    }
-    __syncwarp();
-    warp_select_and_draw<K>(p, r, w, hist, cand, keys, nq, rounds, head, tail, eidx, ekey);
-  }
-}
-
-template <class K, int NCH>
-__global__ void __launch_bounds__(kWarpRowsPerBlock * 32)
-    warp_sampler_kernel(const Params p) {
-  __shared__ __align__(16) uint32_t hist[kWarpRowsPerBlock][256];
-  __shared__ __align__(16) uint64_t cand[kWarpRowsPerBlock][64];
-  extern __shared__ __align__(16) uint4 warp_keys[];
-  const int wid = static_cast<int>(threadIdx.x >> 5);
-  const int r = static_cast<int>(blockIdx.x) * kWarpRowsPerBlock + wid;
-  if (r >= p.n_rows) return;
-  warp_row<K, NCH>(p, r, hist[wid], cand[wid], warp_keys + wid * NCH * 32);
+  if (MAXNCH == 1 || nq <= kRowThreads)
+    row_body<K, 1>(p, r, w, step, sh, keys, head, nq, tail, rowp);
+  else if (MAXNCH == 2 || nq <= 2 * kRowThreads)
+    row_body<K, (MAXNCH >= 2 ? 2 : 1)>(p, r, w, step, sh, keys, head, nq, tail, rowp);
+  else
+    row_body<K, MAXNCH>(p, r, w, step, sh, keys, head, nq, tail, rowp);
 }
 
 }  // namespace ts

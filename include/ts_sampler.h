@@ -150,12 +150,18 @@ ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream);
  * Synchronises `stream`: for tests and debugging, not for the decode loop. */
 ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
 
-/* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = warp per row
- * (requires cap <= 64 and max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or
- * cluster per row.  TS_OPT_CLUSTER: 0 = automatic, else the CTAs per row of
- * the CTA/cluster path (1, 2, 4 or 8).  Results never depend on either. */
+/* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = one 128-thread
+ * block per row with a bounded candidate set (requires cap <= 64 and
+ * max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row.
+ * TS_OPT_CLUSTER: 0 = automatic, else the CTAs per row of the CTA/cluster
+ * path (1, 2, 4 or 8).  TS_OPT_PDL: 1 (default) launches with programmatic
+ * dependent launch, so that a step's kernel is scheduled while the previous
+ * kernel in the stream drains (each kernel still waits for its predecessor
+ * before touching memory); 0 launches plainly.  Results never depend on any
+ * option. */
 #define TS_OPT_PATH 1
 #define TS_OPT_CLUSTER 2
+#define TS_OPT_PDL 3
 ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value);
 
 /* Describes the kernel that ts_sample would launch for `b` (path 1 or 2,

@@ -113,11 +113,13 @@ def test_geometry_independence(ts):
         assert np.array_equal(o["n_nucleus"], outs[0]["n_nucleus"])
     d = workloads.make("drama3", 4)
     ids = []
-    for path in (1, 2):
+    for path, pdl in ((1, 1), (2, 1), (1, 0), (2, 0)):
         s = make_sampler(ts, 64, path=path)
+        s.set_option(ts.TS_OPT_PDL, pdl)
         ids.append(run_gpu(s, d)["ids"])
         s.close()
-    assert np.array_equal(ids[0], ids[1])
+    for other in ids[1:]:
+        assert np.array_equal(ids[0], other)
 
 
 # ---------------------------------------------------------------------------
