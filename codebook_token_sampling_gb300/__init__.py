@@ -36,6 +36,7 @@ TS_ROW_BAD_SLOT = 8
 TS_OPT_PATH = 1
 TS_OPT_CLUSTER = 2
 TS_OPT_PDL = 3
+TS_OPT_WIDE_EXACT = 4
 TS_MAX_VOCAB_BF16 = 163840
 TS_MAX_VOCAB_F32 = 81920
 

@@ -44,14 +44,17 @@ struct Params {
   float *kept_probs;
   int32_t *n_kept;
   int32_t *n_nucleus;
-  // CTA/cluster path: elements of a row held by one CTA
+  // CTA/cluster and wide paths: elements of a row held by one CTA
   int32_t slice;
+  // wide path: 1 = always take the exact (re-reading) path (testing)
+  int32_t wide_exact;
 };
 
 // ---------------------------------------------------------------------------
 // Order-preserving keys.  A float's bit pattern becomes an unsigned integer
 // whose order is the float order: negative values have every bit flipped,
-// non-negative ones only the sign bit.  -inf maps to kNegInf, +inf to kPosInf;
+// non-negative ones only the sign bit; -0 is first made +0, so that equal
+// values always have equal keys (ties then go by token index).  -inf maps to kNegInf, +inf to kPosInf;
 // a NaN maps below kNegInf or above kPosInf.
 // ---------------------------------------------------------------------------
 struct KeyBF16 {
@@ -60,15 +63,21 @@ struct KeyBF16 {
   static constexpr int kPerChunk = 8;  // elements per 16-byte chunk
   static constexpr uint32_t kNegInf = 0x007Fu;
   static constexpr uint32_t kPosInf = 0xFF80u;
+  // -0 and +0 are equal values, so -0 takes the key of +0.
   __device__ __forceinline__ static uint32_t key(uint32_t bits) {
+    if (bits == 0x8000u) bits = 0u;
     return bits ^ ((bits & 0x8000u) ? 0xFFFFu : 0x8000u);
   }
   __device__ __forceinline__ static float value(uint32_t k) {
     uint32_t bits = k ^ ((k & 0x8000u) ? 0x8000u : 0xFFFFu);
     return __uint_as_float(bits << 16);
   }
-  // Two packed bf16 values -> two packed keys, no branch.
+  // Two packed bf16 values -> two packed keys, no branch.  A zero half
+  // loses its sign first: the mask keeps the sign bit only where the
+  // magnitude is non-zero (its sum with 0x7FFF carries into bit 15).
   __device__ __forceinline__ static uint32_t key_word(uint32_t w) {
+    const uint32_t mag = w & 0x7FFF7FFFu;
+    w &= (mag + 0x7FFF7FFFu) | 0x7FFF7FFFu;
     uint32_t neg = (w >> 15) & 0x00010001u;
     return w ^ ((neg * 0x7FFFu) | 0x80008000u);
   }
@@ -86,7 +95,9 @@ struct KeyF32 {
   static constexpr int kPerChunk = 4;
   static constexpr uint32_t kNegInf = 0x007FFFFFu;
   static constexpr uint32_t kPosInf = 0xFF800000u;
+  // -0 and +0 are equal values, so -0 takes the key of +0.
   __device__ __forceinline__ static uint32_t key(uint32_t bits) {
+    if (bits == 0x80000000u) bits = 0u;
     return bits ^ ((bits & 0x80000000u) ? 0xFFFFFFFFu : 0x80000000u);
   }
   __device__ __forceinline__ static float value(uint32_t k) {

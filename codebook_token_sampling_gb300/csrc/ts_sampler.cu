@@ -13,14 +13,16 @@
 #include "ts_cluster.cuh"
 #include "ts_device.cuh"
 #include "ts_warp.cuh"
+#include "ts_wide.cuh"
 
 struct ts_sampler {
   int device;
   int cap;
   int num_sms;
-  int force_path;     // 0 auto, 1 warp per row, 2 CTA/cluster per row
+  int force_path;     // 0 auto, 1 block per row, 2 CTA/cluster per row, 3 wide
   int force_cluster;  // 0 auto, else CTAs per row
   int pdl;            // launch with programmatic stream serialization
+  int wide_exact;     // wide path: always take the exact path (testing)
   uint32_t *status;   // device word
 };
 
@@ -41,12 +43,14 @@ int cap_of(int requested) {
 
 constexpr int kWarpMaxBF16 = 4096;
 constexpr int kWarpMaxF32 = 2048;
+// bf16 rows wider than this take the single-pass wide kernel
+constexpr int kWideMinVocab = 32768;
 
 struct Plan {
-  int path;   // 1 warp, 2 cluster
-  int nch;    // warp path: 16-byte chunks per lane
-  int g;      // cluster path: CTAs per row
-  int slice;  // cluster path: elements per CTA
+  int path;   // 1 block per row, 2 cluster, 3 wide
+  int nch;    // block-per-row path: 16-byte chunks per thread
+  int g;      // cluster and wide paths: CTAs per row
+  int slice;  // cluster and wide paths: elements per CTA
   int threads;
   int smem;
   int grid;
@@ -58,10 +62,31 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
   if (vmax > (bf16 ? TS_MAX_VOCAB_BF16 : TS_MAX_VOCAB_F32)) return TS_ERR_UNSUPPORTED;
   const int warp_max = bf16 ? kWarpMaxBF16 : kWarpMaxF32;
   const bool warp_ok = s->cap <= 64 && vmax <= warp_max;
-  int path = s->force_path ? s->force_path : (warp_ok ? 1 : 2);
+  int path = s->force_path ? s->force_path : (warp_ok ? 1 : (bf16 && vmax > kWideMinVocab ? 3 : 2));
   if (path == 1 && !warp_ok) return TS_ERR_INVALID_ARG;
+  if (path == 3 && !bf16) return TS_ERR_INVALID_ARG;
   std::memset(pl, 0, sizeof *pl);
   pl->path = path;
+  if (path == 3) {
+    int g = 1;
+    if (s->force_cluster) {
+      g = s->force_cluster;
+    } else {
+      while ((vmax + g - 1) / g > ts::kWideSliceMax) g *= 2;
+      // few rows: spread each row over more SMs
+      while (g < 8 && static_cast<long long>(b->n_rows) * g < 2LL * s->num_sms) g *= 2;
+    }
+    if (g != 1 && g != 2 && g != 4 && g != 8) return TS_ERR_INVALID_ARG;
+    int slice = (vmax + g - 1) / g;
+    slice = (slice + 7) / 8 * 8;
+    if (slice > ts::kWideSliceMax) return TS_ERR_UNSUPPORTED;
+    pl->g = g;
+    pl->slice = slice;
+    pl->threads = ts::kWideThreads;
+    pl->smem = static_cast<int>(ts::kWideSmemBytes);
+    pl->grid = b->n_rows * g;
+    return TS_OK;
+  }
   if (path == 1) {
     const int epc = bf16 ? 8 : 4;
     const int per_thread = (vmax + ts::kRowThreads * epc - 1) / (ts::kRowThreads * epc);
@@ -149,6 +174,13 @@ void *warp_kernel_for(int nch) {
   return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 4>);
 }
 
+void *wide_kernel_for(int g) {
+  if (g == 1) return reinterpret_cast<void *>(ts::wide_sampler_kernel<1>);
+  if (g == 2) return reinterpret_cast<void *>(ts::wide_sampler_kernel<2>);
+  if (g == 4) return reinterpret_cast<void *>(ts::wide_sampler_kernel<4>);
+  return reinterpret_cast<void *>(ts::wide_sampler_kernel<8>);
+}
+
 template <class K>
 void *cluster_kernel_for(int g) {
   if (g == 1) return reinterpret_cast<void *>(ts::cluster_sampler_kernel<K, 1>);
@@ -163,12 +195,13 @@ ts_status set_attributes(int device) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  void *fns[14];
+  void *fns[18];
   int n = 0;
   const int gs[4] = {1, 2, 4, 8};
   for (int i = 0; i < 4; ++i) {
     fns[n++] = cluster_kernel_for<ts::KeyBF16>(gs[i]);
     fns[n++] = cluster_kernel_for<ts::KeyF32>(gs[i]);
+    fns[n++] = wide_kernel_for(gs[i]);
   }
   const int nchs[3] = {1, 2, 4};
   for (int i = 0; i < 3; ++i) {
@@ -192,10 +225,13 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   if (rc != TS_OK) return rc;
   ts::Params p = base;
   p.slice = pl.slice;
+  p.wide_exact = s->wide_exact;
   const bool bf16 = b->dtype == TS_DTYPE_BF16;
   void *fn = nullptr;
   if (pl.path == 1) {
     fn = bf16 ? warp_kernel_for<ts::KeyBF16>(pl.nch) : warp_kernel_for<ts::KeyF32>(pl.nch);
+  } else if (pl.path == 3) {
+    fn = wide_kernel_for(pl.g);
   } else {
     fn = bf16 ? cluster_kernel_for<ts::KeyBF16>(pl.g) : cluster_kernel_for<ts::KeyF32>(pl.g);
   }
@@ -210,7 +246,7 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[na].val.programmaticStreamSerializationAllowed = s->pdl ? 1 : 0;
   ++na;
-  if (pl.path == 2 && pl.g > 1) {
+  if (pl.path >= 2 && pl.g > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
     attr[na].val.clusterDim.x = static_cast<unsigned>(pl.g);
     attr[na].val.clusterDim.y = 1;
@@ -258,6 +294,7 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->force_path = 0;
   s->force_cluster = 0;
   s->pdl = 1;
+  s->wide_exact = 0;
   s->status = nullptr;
   ts_status rc = TS_OK;
   e = cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, device);
@@ -350,7 +387,7 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream) {
 ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value) {
   if (!s) return TS_ERR_INVALID_ARG;
   if (option == TS_OPT_PATH) {
-    if (value < 0 || value > 2) return TS_ERR_INVALID_ARG;
+    if (value < 0 || value > 3) return TS_ERR_INVALID_ARG;
     s->force_path = value;
     return TS_OK;
   }
@@ -363,6 +400,11 @@ ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value) {
   if (option == TS_OPT_PDL) {
     if (value != 0 && value != 1) return TS_ERR_INVALID_ARG;
     s->pdl = value;
+    return TS_OK;
+  }
+  if (option == TS_OPT_WIDE_EXACT) {
+    if (value != 0 && value != 1) return TS_ERR_INVALID_ARG;
+    s->wide_exact = value;
     return TS_OK;
   }
   return TS_ERR_INVALID_ARG;

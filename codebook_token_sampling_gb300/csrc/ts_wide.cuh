@@ -1,0 +1,999 @@
+// ts_wide.cuh -- single-pass sampler for wide bf16 rows (backbone vocabularies
+// such as 151,936 tokens) under any top-k cap up to 4096 (Drama 3 article,
+// section "能跑通的命令，和文档写明的边界": the cap may be any power of two in
+// [32, 4096]).
+//
+// A row is split into G contiguous slices, one CTA each, forming a
+// thread-block cluster.  The row is read from HBM exactly once:
+//
+//  1. Threshold estimate.  Every CTA reads the same evenly spaced sample of
+//     the row (1024 16-byte chunks; these lines stay in L2 for the pass that
+//     follows) and takes, by an exact two-level radix select, the sample's
+//     r-th largest key t with r sized so that about 1.4 k_eff row elements
+//     are expected at or above t.  This is the sampling step of Floyd and
+//     Rivest's selection algorithm ("Expected time bounds for selection",
+//     CACM 18(3), 1975): only its speed depends on the sample, never its
+//     result.  Rows no wider than the candidate buffer skip it (t = lowest key).
+//  2. Filter.  Each CTA streams its slice with 16-byte loads, compares eight
+//     logits per chunk against t with packed bf16 compares (an unordered
+//     compare, so a NaN is flagged too), stages the flagged chunks per warp
+//     and appends every element >= t as (key << 16 | slice index) to its own
+//     candidate buffer in shared memory.
+//  3. Check and gather.  After a cluster barrier every CTA reads all
+//     candidate counts through distributed shared memory.  If the row holds a
+//     NaN or +inf it is an error.  If the candidates number at least k_eff
+//     (so they hold the whole top-k set and every key tied with its last
+//     member) and fit the leader's buffer, each CTA copies its candidates
+//     into the leader CTA and leaves.  Otherwise (an unlucky or adversarial
+//     sample) the cluster runs an exact radix select over the slice again
+//     and collects exactly the top-k set, ties taken by lowest index.
+//  4. Leader tail, order-free.  The leader finds the threshold key and the
+//     number of kept tokens tied at it by radix select over the candidates,
+//     sums 2^-40 fixed-point weights (which depend only on the key), finds
+//     the nucleus cutoff and the draw by a radix descent over (max key - key)
+//     with exact masses, and picks the token inside the drawn key group by a
+//     radix select on the token index.  No step depends on the order in
+//     which candidates were appended, so the result is the same for every
+//     cluster size and equal to the other kernels' bit for bit.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ts_device.cuh"
+
+namespace ts {
+
+constexpr int kWideThreads = 256;
+constexpr int kWideWarps = kWideThreads / 32;
+constexpr int kWideCandMax = 8192;        // candidate entries per CTA (32 KB)
+constexpr int kWideU = 4;                 // 16-byte chunks per lane per iteration
+constexpr int kWideStage = 32 * kWideU;   // staged chunks per warp per iteration
+constexpr int kWideSampleChunks = 1024;   // 8,192 sampled logits
+constexpr int kWideSliceMax = 65536;      // slice index fits 16 bits
+constexpr int kWideMaxG = 16;
+constexpr uint32_t kWideWorkBytes = kWideWarps * kWideStage * (16 + 4);  // 20 KB
+constexpr uint32_t kWideMiscWords = 256;
+constexpr uint32_t kWideSmemBytes = kWideCandMax * 4 + kWideWorkBytes + kWideMiscWords * 4;
+
+// misc word slots
+constexpr int kWN = 0;        // local candidate count (may exceed the buffer)
+constexpr int kWBad = 1;      // NaN / +inf seen in this slice
+constexpr int kWTKey = 2;     // threshold key t
+constexpr int kWU24 = 3;      // the row's draw (leader)
+constexpr int kWTotal = 4;    // candidates over the cluster
+constexpr int kWFast = 5;     // 1: fast path, 2: row error, 0: exact path
+constexpr int kWDigit = 8, kWAbove = 9, kWCount = 10, kWId = 11;
+constexpr int kWFin = 12;     // finite logits in this slice (exact path)
+constexpr int kWEq = 13;      // keys equal to the threshold in this slice (exact path)
+constexpr int kWTake = 14;    // ... of which this slice keeps (exact path)
+constexpr int kWMaxK = 15;
+constexpr int kWWide = 16;    // 2 x u64 (words 16..19)
+constexpr int kWSeg = 24;     // G + 1 segment offsets (words 24..40)
+constexpr int kWHist2 = 64;   // 32-bin second-level histogram (words 64..95)
+constexpr int kWScan = 128;   // block-scan scratch: u64 x (kWideWarps + 1)
+
+// Keys of the wide path are KeyBF16's (-0 takes the key of +0).
+__device__ __forceinline__ uint32_t wkey(uint32_t bits16) { return KeyBF16::key(bits16); }
+__device__ __forceinline__ uint32_t wkey_word(uint32_t w) { return KeyBF16::key_word(w); }
+
+// bf16 bits of the value whose key is k (k = 0 stands for "every element":
+// -inf, so that an unordered compare flags every logit).
+__device__ __forceinline__ uint32_t wkey_bits(uint32_t k) {
+  if (k == 0u) return 0xFF80u;
+  return k ^ ((k & 0x8000u) ? 0x8000u : 0xFFFFu);
+}
+
+__device__ __forceinline__ uint32_t hgeu_mask(uint32_t w, uint32_t t2) {
+  return __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w),
+                      *reinterpret_cast<const __nv_bfloat162 *>(&t2));
+}
+
+// Cluster barrier preceded by a block barrier, so that every warp arrives
+// converged (the cluster barrier is the warp-aligned form).
+__device__ __forceinline__ void wide_cluster_sync() {
+  __syncthreads();
+  cluster_sync_all();
+}
+
+// ---------------------------------------------------------------------------
+// Block primitives for kWideThreads threads.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t wide_excl_scan_u64(uint64_t v, uint64_t *scratch,
+                                                       uint64_t *total) {
+  const uint32_t lane = lane_id(), wid = threadIdx.x >> 5;
+  uint64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t t = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= static_cast<uint32_t>(o)) x += t;
+  }
+  __syncthreads();  // scratch may still be read by a previous call
+  if (lane == 31) scratch[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    const uint64_t s = lane < kWideWarps ? scratch[lane] : 0ull;
+    uint64_t inc = s;
+#pragma unroll
+    for (int o = 1; o < kWideWarps; o <<= 1) {
+      const uint64_t t = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+      if (lane >= static_cast<uint32_t>(o)) inc += t;
+    }
+    if (lane < kWideWarps) scratch[lane] = inc - s;
+    if (lane == kWideWarps - 1) scratch[kWideWarps] = inc;
+  }
+  __syncthreads();
+  *total = scratch[kWideWarps];
+  return scratch[wid] + x - v;
+}
+
+__device__ __forceinline__ uint32_t wide_max_u32(uint32_t v, uint64_t *scratch) {
+  const uint32_t x = __reduce_max_sync(0xFFFFFFFFu, v);
+  const uint32_t lane = lane_id(), wid = threadIdx.x >> 5;
+  __syncthreads();
+  if (lane == 0) scratch[wid] = x;
+  __syncthreads();
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < kWideWarps; ++i) r = max(r, static_cast<uint32_t>(scratch[i]));
+  return r;
+}
+
+// Selects, from a histogram of PER * kWideThreads bins in ascending key
+// order (thread t owns bins [t*PER, t*PER + PER)), the bin holding the kk-th
+// largest element (1-based).  Writes the bin, the count above it and its
+// count to misc.  `h` may live in another CTA of the cluster when G > 1
+// (distributed shared memory, summed over the G CTAs).
+template <int PER, int G>
+__device__ void wide_select_top(const uint32_t *h, uint32_t kk, uint32_t *misc,
+                                uint64_t *scratch) {
+  const int t = static_cast<int>(threadIdx.x);
+  uint32_t hb[PER];
+#pragma unroll
+  for (int b = 0; b < PER; ++b) hb[b] = 0u;
+  if constexpr (G == 1) {
+#pragma unroll
+    for (int b = 0; b < PER; ++b) hb[b] = h[t * PER + b];
+  } else {
+#pragma unroll
+    for (int c = 0; c < G; ++c) {
+#pragma unroll
+      for (int b = 0; b < PER; ++b) hb[b] += dsmem_ld_u32(dsmem_addr(&h[t * PER + b], c));
+    }
+  }
+  uint32_t s = 0;
+#pragma unroll
+  for (int b = 0; b < PER; ++b) s += hb[b];
+  uint64_t tot64;
+  const uint32_t excl = static_cast<uint32_t>(wide_excl_scan_u64(s, scratch, &tot64));
+  const uint32_t above_me = static_cast<uint32_t>(tot64) - excl - s;
+  if (s != 0 && above_me < kk && above_me + s >= kk) {
+    uint32_t run = above_me;
+#pragma unroll
+    for (int b = PER - 1; b >= 0; --b) {
+      if (run < kk && run + hb[b] >= kk) {
+        misc[kWDigit] = static_cast<uint32_t>(t * PER + b);
+        misc[kWAbove] = run;
+        misc[kWCount] = hb[b];
+      }
+      run += hb[b];
+    }
+  }
+  __syncthreads();
+}
+
+// Position p of the leader's candidate buffer came from CTA seg_of(p); the
+// segments are contiguous and in CTA order.
+__device__ __forceinline__ uint32_t wide_gidx(uint32_t e, int c, int S) {
+  return static_cast<uint32_t>(c * S) + (e & 0xFFFFu);
+}
+
+// The rho-th smallest (0-based) token index among candidates with key
+// `key_sel`, by a two-level radix select on the 18-bit token index (512 bins
+// per level).  Order-free.
+__device__ uint32_t wide_rank_select(const uint32_t *cand, int n, const uint32_t *seg, int G,
+                                     int S, uint32_t key_sel, uint32_t rho, uint32_t *h,
+                                     uint32_t *misc, uint64_t *scratch) {
+  const int t = static_cast<int>(threadIdx.x);
+  uint32_t b1 = 0, below = 0;
+#pragma unroll 1
+  for (int level = 0; level < 2; ++level) {
+    __syncthreads();
+    for (int i = t; i < 512; i += kWideThreads) h[i] = 0u;
+    __syncthreads();
+    int c = 0;
+    for (int i = t; i < n; i += kWideThreads) {
+      while (c + 1 < G && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
+      const uint32_t e = cand[i];
+      if ((e >> 16) != key_sel) continue;
+      const uint32_t g = wide_gidx(e, c, S);
+      if (level == 0)
+        atomicAdd(&h[g >> 9], 1u);
+      else if ((g >> 9) == b1)
+        atomicAdd(&h[g & 511u], 1u);
+    }
+    __syncthreads();
+    // ascending select: the bin where the running count first exceeds rho'
+    const uint32_t want = rho - below;
+    const uint32_t h0 = h[2 * t], h1 = h[2 * t + 1];
+    uint64_t tot;
+    const uint32_t ex = static_cast<uint32_t>(wide_excl_scan_u64(h0 + h1, scratch, &tot));
+    if (ex <= want && want < ex + h0) {
+      misc[kWDigit] = 2 * t;
+      misc[kWAbove] = ex;
+    } else if (ex + h0 <= want && want < ex + h0 + h1) {
+      misc[kWDigit] = 2 * t + 1;
+      misc[kWAbove] = ex + h0;
+    }
+    __syncthreads();
+    if (level == 0) {
+      b1 = misc[kWDigit];
+      below += misc[kWAbove];
+    } else {
+      return (b1 << 9) | misc[kWDigit];
+    }
+  }
+  return 0;
+}
+
+// Radix descent over offsets (maxk - key) of the kept set with exact 2^-40
+// fixed-point masses: every candidate with key > thr is kept; the group at
+// thr contributes `need` tokens (the lowest-index ones; which ones does not
+// matter for masses).  cut_mode: the group whose cumulative mass first
+// reaches `cut` (>= cut); else the group whose cumulative mass first exceeds
+// `target`.  Returns that group's key; *above_out = mass of all groups above.
+// Levels take 10 offset bits; at the last level a bin is one key, whose mass
+// is count x weight; above it a bin's mass is summed per token as three
+// 32-bit partials (bits 0-12, 13-25, 26+), so only 32-bit shared atomics are
+// used.
+__device__ uint32_t wide_mass_descent(const uint32_t *cand, int n, uint32_t maxk, uint32_t thr,
+                                      uint32_t need, float m, float temp, float inv_temp,
+                                      bool cut_mode, uint64_t cut, uint64_t target, uint32_t *h,
+                                      uint32_t *misc, uint64_t *scratch, uint64_t *above_out) {
+  constexpr int kBins = 1024;
+  constexpr int kPer = kBins / kWideThreads;
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t range = maxk - thr;
+  const int bits = range ? 32 - __clz(range) : 0;
+  int span = bits;
+  int shift = bits > 10 ? bits - 10 : 0;
+  uint32_t off_lo = 0;
+  uint64_t above = 0;
+  uint64_t *wide = reinterpret_cast<uint64_t *>(misc + kWWide);
+  for (;;) {
+    const bool exact = shift == 0;
+    __syncthreads();
+    for (int i = t; i < (exact ? kBins : 3 * kBins); i += kWideThreads) h[i] = 0u;
+    if (t == 0) {
+      misc[kWDigit] = 0;
+      wide[0] = above;
+    }
+    __syncthreads();
+    auto add = [&](uint32_t key, uint32_t cnt) {
+      const uint32_t off = maxk - key;
+      if (off < off_lo || static_cast<uint64_t>(off - off_lo) >= (1ull << span)) return;
+      const uint32_t d = (off - off_lo) >> shift;
+      if (exact) {
+        atomicAdd(&h[d], cnt);
+      } else {
+        const uint64_t f = cnt * to_fixed(kept_weight(KeyBF16::value(key), m, temp, inv_temp));
+        if (f) {
+          atomicAdd(&h[d], static_cast<uint32_t>(f & 0x1FFFu));
+          atomicAdd(&h[kBins + d], static_cast<uint32_t>((f >> 13) & 0x1FFFu));
+          atomicAdd(&h[2 * kBins + d], static_cast<uint32_t>(f >> 26));
+        }
+      }
+    };
+    for (int i = t; i < n; i += kWideThreads) {
+      const uint32_t key = cand[i] >> 16;
+      if (key > thr) add(key, 1u);
+    }
+    if (t == 0 && need) add(thr, need);
+    __syncthreads();
+    uint64_t ab[kPer];
+    uint64_t s = 0;
+#pragma unroll
+    for (int x = 0; x < kPer; ++x) {
+      const uint32_t d = static_cast<uint32_t>(kPer * t + x);
+      if (exact) {
+        const uint32_t cnt = h[d];
+        ab[x] = cnt ? cnt * to_fixed(kept_weight(KeyBF16::value(maxk - off_lo - d), m, temp, inv_temp))
+                    : 0ull;
+      } else {
+        ab[x] = (static_cast<uint64_t>(h[2 * kBins + d]) << 26) +
+                (static_cast<uint64_t>(h[kBins + d]) << 13) + h[d];
+      }
+      s += ab[x];
+    }
+    uint64_t tot;
+    uint64_t cum = above + wide_excl_scan_u64(s, scratch, &tot);
+#pragma unroll
+    for (int x = 0; x < kPer; ++x) {
+      const uint64_t nxt = cum + ab[x];
+      const bool r0 = cut_mode ? cum >= cut : cum > target;
+      const bool r1 = cut_mode ? nxt >= cut : nxt > target;
+      if (!r0 && r1) {
+        misc[kWDigit] = static_cast<uint32_t>(kPer * t + x);
+        wide[0] = cum;
+      }
+      cum = nxt;
+    }
+    __syncthreads();
+    off_lo += misc[kWDigit] << shift;
+    above = wide[0];
+    if (shift == 0) break;
+    span = shift;
+    shift = shift > 10 ? shift - 10 : 0;
+  }
+  *above_out = above;
+  return maxk - off_lo;
+}
+
+// Exact r-th largest canonical key of an evenly spaced sample of the row
+// (every CTA of the cluster computes the same value from the same sample).
+// Returns 0 ("every element") when the sample cannot give a useful bound.
+__device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, uint32_t *hist,
+                                          uint32_t *misc, uint64_t *scratch) {
+  const int t = static_cast<int>(threadIdx.x);
+  const int head_r =
+      min(V, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / 2u));
+  const int nq_r = (V - head_r) / 8;
+  const int n_chunks = min(nq_r, kWideSampleChunks);
+  const int n_s = 8 * n_chunks;
+  if (n_chunks <= 0) return 0u;
+  // r such that about 1.4 k_eff row elements are expected at or above it
+  const long long want = (14ll * k_eff * n_s + 10ll * V - 1) / (10ll * V);
+  const int r = static_cast<int>(max(32ll, want));
+  if (r > n_s) return 0u;
+  const char *body = rowp + 2 * head_r;
+  constexpr int kPerT = kWideSampleChunks / kWideThreads;
+  for (int i = t; i < 2048; i += kWideThreads) hist[i] = 0u;
+  if (t < 32) misc[kWHist2 + t] = 0u;
+  __syncthreads();
+  uint32_t kw[kPerT][4];
+#pragma unroll
+  for (int i = 0; i < kPerT; ++i) {
+    const int j = t + i * kWideThreads;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j < n_chunks) {
+      const long long q = static_cast<long long>(j) * nq_r / n_chunks;
+      v = __ldg(reinterpret_cast<const uint4 *>(body + 16 * q));
+    }
+    kw[i][0] = wkey_word(v.x);
+    kw[i][1] = wkey_word(v.y);
+    kw[i][2] = wkey_word(v.z);
+    kw[i][3] = wkey_word(v.w);
+  }
+#pragma unroll
+  for (int i = 0; i < kPerT; ++i) {
+    if (t + i * kWideThreads < n_chunks) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        atomicAdd(&hist[(kw[i][x] & 0xFFFFu) >> 5], 1u);
+        atomicAdd(&hist[kw[i][x] >> 21], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  wide_select_top<8, 1>(hist, static_cast<uint32_t>(r), misc, scratch);
+  const uint32_t b1 = misc[kWDigit];
+  const uint32_t above = misc[kWAbove];
+#pragma unroll
+  for (int i = 0; i < kPerT; ++i) {
+    if (t + i * kWideThreads < n_chunks) {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const uint32_t lo = kw[i][x] & 0xFFFFu, hi = kw[i][x] >> 16;
+        if ((lo >> 5) == b1) atomicAdd(&misc[kWHist2 + (lo & 31u)], 1u);
+        if ((hi >> 5) == b1) atomicAdd(&misc[kWHist2 + (hi & 31u)], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  // 32 bins: threads 0..31 own one bin each (PER = 1 over the first 32 threads)
+  uint32_t d2 = 0;
+  if (t < 32) {
+    const uint32_t kk = static_cast<uint32_t>(r) - above;
+    const uint32_t c = misc[kWHist2 + t];
+    // suffix count over bins >= t
+    uint32_t suf = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+      if (t + o < 32) suf += x;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, suf >= kk);
+    d2 = 31u - __clz(hit);
+  }
+  __syncthreads();  // everyone has read misc before it is reused
+  uint32_t tk = (b1 << 5) | d2;
+  if (t >= 32) tk = 0;  // only warp 0 holds d2; broadcast below
+  if (t == 0) misc[kWTKey] = tk;
+  __syncthreads();
+  tk = misc[kWTKey];
+  if (tk < KeyBF16::kNegInf || tk >= KeyBF16::kPosInf) tk = 0u;
+  return tk;
+}
+
+// Appends (key << 16 | slice index) to this CTA's candidate buffer for the
+// flagged elements of `n` staged chunks (lane l handles staged chunk
+// base + l); returns through *bad whether a NaN / +inf key was met.
+__device__ __forceinline__ void wide_append_staged(const uint4 *stage, const uint32_t *stage_q,
+                                                   int base, int n, uint32_t t_key, int head,
+                                                   uint32_t *cand, uint32_t *counter,
+                                                   uint32_t &bad) {
+  const uint32_t lane = lane_id();
+  const int i = base + static_cast<int>(lane);
+  uint32_t k[8];
+  uint32_t flags = 0, cnt = 0, idx0 = 0;
+  if (i < n) {
+    const uint4 c = stage[i];
+    idx0 = static_cast<uint32_t>(head) + 8u * stage_q[i];
+    const uint32_t wds[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t kw = wkey_word(wds[x]);
+      k[2 * x] = kw & 0xFFFFu;
+      k[2 * x + 1] = kw >> 16;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const bool nonfinite = k[e] < KeyBF16::kNegInf || k[e] >= KeyBF16::kPosInf;
+      bad |= nonfinite;
+      if (!nonfinite && k[e] >= t_key) {
+        flags |= 1u << e;
+        ++cnt;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) k[e] = 0u;
+  }
+  uint32_t incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= static_cast<uint32_t>(o)) incl += x;
+  }
+  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  if (total == 0) return;
+  uint32_t pos = 0;
+  if (lane == 31) pos = atomicAdd(counter, total);
+  pos = __shfl_sync(0xFFFFFFFFu, pos, 31) + incl - cnt;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    if (flags & (1u << e)) {
+      if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = (k[e] << 16) | (idx0 + e);
+      ++pos;
+    }
+  }
+}
+
+// One element of a slice's unaligned head or tail.
+__device__ __forceinline__ void wide_append_one(const char *sp, int idx, uint32_t t_key,
+                                                uint32_t *cand, uint32_t *counter, uint32_t &bad) {
+  const uint32_t k = wkey(KeyBF16::load_one(sp, idx));
+  const bool nonfinite = k < KeyBF16::kNegInf || k >= KeyBF16::kPosInf;
+  bad |= nonfinite;
+  if (!nonfinite && k >= t_key) {
+    const uint32_t pos = atomicAdd(counter, 1u);
+    if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = (k << 16) | static_cast<uint32_t>(idx);
+  }
+}
+
+// Appends one entry; the count keeps growing past the buffer (callers
+// compare it with kWideCandMax), the entry is dropped.
+__device__ __forceinline__ void wide_put(uint32_t *cand, uint32_t *counter, uint32_t e) {
+  const uint32_t pos = atomicAdd(counter, 1u);
+  if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = e;
+}
+
+// Exact path of a cluster (rare: the sample's threshold left fewer than
+// k_eff candidates or more than the buffer holds): radix select over the
+// slices re-read from global memory (11 + 5 key bits, histograms merged
+// through distributed shared memory), then the exact top-k set collected
+// into each CTA's candidate buffer: every key above the threshold, and the
+// lowest-index keys equal to it (ranked in index order across the cluster).
+// Returns false when the row has no finite logit or holds a NaN / +inf
+// (the caller reports the error), true otherwise.
+template <int G>
+__device__ bool wide_exact_collect(const char *sp, int head, int nq, int tail, uint32_t rank,
+                                   uint32_t k_eff, uint32_t *cand, uint32_t *hist,
+                                   uint32_t *misc, uint64_t *scratch) {
+  const int t = static_cast<int>(threadIdx.x);
+  const char *body = sp + 2 * head;
+  for (int i = t; i < 2048; i += kWideThreads) hist[i] = 0u;
+  if (t < 32) misc[kWHist2 + t] = 0u;
+  if (t == 0) {
+    misc[kWBad] = 0u;
+    misc[kWFin] = 0u;
+  }
+  __syncthreads();
+  // pass 1: 11-bit histogram, NaN / +inf and finite counts
+  uint32_t nbad = 0, nfin = 0;
+  auto count1 = [&](uint32_t k) {
+    nbad += (k < KeyBF16::kNegInf) | (k >= KeyBF16::kPosInf);
+    nfin += k > KeyBF16::kNegInf;
+    atomicAdd(&hist[k >> 5], 1u);
+  };
+  for (int m = t; m < nq; m += kWideThreads) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(body + 16 * static_cast<size_t>(m)));
+    const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t kw = wkey_word(wds[x]);
+      count1(kw & 0xFFFFu);
+      count1(kw >> 16);
+    }
+  }
+  if (t < head + tail) {
+    const int idx = t < head ? t : head + 8 * nq + (t - head);
+    count1(wkey(KeyBF16::load_one(sp, idx)));
+  }
+  nbad = __reduce_add_sync(0xFFFFFFFFu, nbad);
+  nfin = __reduce_add_sync(0xFFFFFFFFu, nfin);
+  if (lane_id() == 0) {
+    if (nbad) atomicAdd(&misc[kWBad], nbad);
+    if (nfin) atomicAdd(&misc[kWFin], nfin);
+  }
+  __syncthreads();
+  if constexpr (G > 1) wide_cluster_sync();
+  uint32_t bad = 0, fin = 0;
+#pragma unroll
+  for (int c = 0; c < G; ++c) {
+    if constexpr (G == 1) {
+      bad += misc[kWBad];
+      fin += misc[kWFin];
+    } else {
+      bad += dsmem_ld_u32(dsmem_addr(&misc[kWBad], c));
+      fin += dsmem_ld_u32(dsmem_addr(&misc[kWFin], c));
+    }
+  }
+  wide_select_top<8, G>(hist, k_eff, misc, scratch);
+  if (bad != 0 || fin == 0) {
+    if constexpr (G > 1) wide_cluster_sync();  // peers may still read our histogram
+    return false;
+  }
+  const uint32_t b1 = misc[kWDigit];
+  uint32_t kk = k_eff - misc[kWAbove];
+  // pass 2: the low 5 key bits inside bin b1
+  auto count2 = [&](uint32_t k) {
+    if ((k >> 5) == b1) atomicAdd(&misc[kWHist2 + (k & 31u)], 1u);
+  };
+  for (int m = t; m < nq; m += kWideThreads) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(body + 16 * static_cast<size_t>(m)));
+    const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t kw = wkey_word(wds[x]);
+      count2(kw & 0xFFFFu);
+      count2(kw >> 16);
+    }
+  }
+  if (t < head + tail) {
+    const int idx = t < head ? t : head + 8 * nq + (t - head);
+    count2(wkey(KeyBF16::load_one(sp, idx)));
+  }
+  __syncthreads();
+  if constexpr (G > 1) wide_cluster_sync();
+  // merged 32-bin select by warp 0
+  if (t < 32) {
+    uint32_t c = 0;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if constexpr (G == 1)
+        c += misc[kWHist2 + t];
+      else
+        c += dsmem_ld_u32(dsmem_addr(&misc[kWHist2 + t], g));
+    }
+    uint32_t suf = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+      if (t + o < 32) suf += x;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, suf >= kk);
+    const uint32_t d2 = 31u - __clz(hit);
+    const uint32_t above2 = __shfl_sync(0xFFFFFFFFu, suf - c, d2);
+    // keys equal to the threshold in lower-ranked CTAs (index order)
+    uint32_t eq_before = 0;
+    if (t < static_cast<int>(rank)) {
+      if constexpr (G > 1) eq_before = dsmem_ld_u32(dsmem_addr(&misc[kWHist2 + d2], t));
+    }
+    eq_before = __reduce_add_sync(0xFFFFFFFFu, eq_before);
+    if (t == 0) {
+      const uint32_t need = kk - above2;  // keys equal to the threshold that are kept
+      const uint32_t mine = misc[kWHist2 + d2];
+      const uint32_t take = need > eq_before ? min(need - eq_before, mine) : 0u;
+      misc[kWTKey] = (b1 << 5) | d2;
+      misc[kWTake] = take;
+      misc[kWN] = 0u;
+    }
+  }
+  __syncthreads();
+  if constexpr (G > 1) wide_cluster_sync();  // peers are done reading our histograms
+  const uint32_t thr = misc[kWTKey];
+  const uint32_t take = misc[kWTake];
+  uint32_t *counter = &misc[kWN];
+  // pass 3: collect.  Keys above thr in any order; keys equal to thr in
+  // index order until `take` of them.  Head elements first (thread 0, in
+  // order), then the body in rounds of kWideThreads chunks, then the tail.
+  uint32_t eq_seen = 0;  // uniform: equal keys already met in this slice
+  if (t == 0) {
+    for (int idx = 0; idx < head; ++idx) {
+      const uint32_t k = wkey(KeyBF16::load_one(sp, idx));
+      bool keep = k > thr;
+      if (k == thr) keep = eq_seen++ < take;
+      if (keep) wide_put(cand, counter, (k << 16) | static_cast<uint32_t>(idx));
+    }
+    misc[kWEq] = eq_seen;
+  }
+  __syncthreads();
+  eq_seen = misc[kWEq];
+  const int rounds = (nq + kWideThreads - 1) / kWideThreads;
+#pragma unroll 1
+  for (int j = 0; j < rounds; ++j) {
+    const int m = j * kWideThreads + t;
+    uint32_t k[8];
+    uint32_t ne = 0;
+    if (m < nq) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(body + 16 * static_cast<size_t>(m)));
+      const uint32_t wds[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const uint32_t kw = wkey_word(wds[x]);
+        k[2 * x] = kw & 0xFFFFu;
+        k[2 * x + 1] = kw >> 16;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ne += k[e] == thr;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) k[e] = 0u;
+    }
+    uint64_t tot;
+    uint32_t er = eq_seen + static_cast<uint32_t>(wide_excl_scan_u64(ne, scratch, &tot));
+    if (m < nq) {
+      const uint32_t idx0 = static_cast<uint32_t>(head) + 8u * static_cast<uint32_t>(m);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        bool keep = k[e] > thr;
+        if (k[e] == thr) keep = er++ < take;
+        if (keep) wide_put(cand, counter, (k[e] << 16) | (idx0 + e));
+      }
+    }
+    eq_seen += static_cast<uint32_t>(tot);
+  }
+  __syncthreads();
+  if (t == 0) {
+    for (int j = 0; j < tail; ++j) {
+      const int idx = head + 8 * nq + j;
+      const uint32_t k = wkey(KeyBF16::load_one(sp, idx));
+      bool keep = k > thr;
+      if (k == thr) keep = eq_seen++ < take;
+      if (keep) wide_put(cand, counter, (k << 16) | static_cast<uint32_t>(idx));
+    }
+  }
+  __syncthreads();
+  return true;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint32_t *cand = reinterpret_cast<uint32_t *>(smem);
+  unsigned char *work = smem + kWideCandMax * 4;
+  uint32_t *misc = reinterpret_cast<uint32_t *>(work + kWideWorkBytes);
+  uint64_t *scratch = reinterpret_cast<uint64_t *>(misc + kWScan);
+  uint32_t *hist = reinterpret_cast<uint32_t *>(work);  // aliases the staging area
+
+  const uint32_t rank = G > 1 ? cluster_rank() : 0u;
+  const int r = G > 1 ? static_cast<int>(cluster_index()) : static_cast<int>(blockIdx.x);
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t lane = lane_id();
+  const int warp = t >> 5;
+  pdl_wait_and_release();
+  if (r >= p.n_rows) return;  // whole cluster (grid is sized exactly)
+  const Row w = load_row(p, r);
+  if (w.err) {  // identical in every CTA of the cluster: all leave before any barrier
+    if (rank == 0 && t == 0) finish_row(p, r, w, -1, w.err);
+    return;
+  }
+  if (rank == 0 && t == 32) {  // the draw, off the critical path
+    misc[kWU24] = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
+                             static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
+  }
+
+  // ---- slice geometry ----
+  const int V = w.vocab;
+  const int S = p.slice;
+  const int s_begin = static_cast<int>(rank) * S;
+  const int sc = max(0, min(S, V - s_begin));
+  const char *rowp = static_cast<const char *>(p.logits) + w.off * 2;
+  const char *sp = rowp + 2 * static_cast<int64_t>(s_begin);
+  const int head =
+      min(sc, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(sp) & 15u)) & 15u) / 2u));
+  const int nq = (sc - head) / 8;
+  const int tail = sc - head - 8 * nq;
+  const char *body = sp + 2 * head;
+  const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
+
+  // ---- first loads of the slice in flight before the threshold estimate ----
+  const uint64_t pol = l2_evict_first();
+  constexpr int kPerIter = kWideThreads * kWideU;
+  const int n_it = (nq + kPerIter - 1) / kPerIter;
+  uint4 cur[kWideU];
+#pragma unroll
+  for (int u = 0; u < kWideU; ++u) {
+    const int m = u * kWideThreads + t;
+    cur[u] = m < nq ? ld_stream_v4(body + 16 * static_cast<size_t>(m), pol)
+                    : make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  uint32_t t_key = 0;
+  if (V > kWideCandMax && !p.wide_exact)
+    t_key = wide_sample_threshold(rowp, V, w.k_eff, hist, misc, scratch);
+  if (t == 0) {
+    misc[kWN] = 0u;
+    misc[kWBad] = 0u;
+  }
+  __syncthreads();  // the staging area (hist) is free; counters are clear
+
+  // ---- filter: every element with key >= t_key becomes a candidate ----
+  uint32_t bad = 0;
+  if (!p.wide_exact) {
+    const uint32_t tb = wkey_bits(t_key);
+    const uint32_t t2 = tb | (tb << 16);
+    uint4 *stage = reinterpret_cast<uint4 *>(work) + warp * kWideStage;
+    uint32_t *stage_q =
+        reinterpret_cast<uint32_t *>(work + kWideWarps * kWideStage * 16) + warp * kWideStage;
+    const uint32_t lt = lanemask_lt();
+#pragma unroll 1
+    for (int it = 0; it < n_it; ++it) {
+      uint4 nxt[kWideU];
+#pragma unroll
+      for (int u = 0; u < kWideU; ++u) {
+        const int m = (it + 1) * kPerIter + u * kWideThreads + t;
+        nxt[u] = m < nq ? ld_stream_v4(body + 16 * static_cast<size_t>(m), pol)
+                        : make_uint4(0u, 0u, 0u, 0u);
+      }
+      int n_st = 0;
+#pragma unroll
+      for (int u = 0; u < kWideU; ++u) {
+        const int m = it * kPerIter + u * kWideThreads + t;
+        bool f = false;
+        if (m < nq) {
+          const uint32_t mk = hgeu_mask(cur[u].x, t2) | hgeu_mask(cur[u].y, t2) |
+                              hgeu_mask(cur[u].z, t2) | hgeu_mask(cur[u].w, t2);
+          f = mk != 0u;
+        }
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, f);
+        if (f) {
+          const int pos = n_st + __popc(bal & lt);
+          stage[pos] = cur[u];
+          stage_q[pos] = static_cast<uint32_t>(m);
+        }
+        n_st += __popc(bal);
+      }
+      __syncwarp();
+      for (int b = 0; b < n_st; b += 32)
+        wide_append_staged(stage, stage_q, b, n_st, t_key, head, cand, &misc[kWN], bad);
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < kWideU; ++u) cur[u] = nxt[u];
+    }
+    if (t < head + tail) {
+      const int idx = t < head ? t : head + 8 * nq + (t - head);
+      wide_append_one(sp, idx, t_key, cand, &misc[kWN], bad);
+    }
+    if (bad) atomicOr(&misc[kWBad], 1u);
+  }
+  __syncthreads();
+  if constexpr (G > 1) wide_cluster_sync();
+
+  // ---- check: counts and flags of every CTA; segment offsets ----
+  if (t < 32) {
+    uint32_t n = 0, b = 0;
+    if (t < G) {
+      if constexpr (G == 1) {
+        n = misc[kWN];
+        b = misc[kWBad];
+      } else {
+        n = dsmem_ld_u32(dsmem_addr(&misc[kWN], t));
+        b = dsmem_ld_u32(dsmem_addr(&misc[kWBad], t));
+      }
+    }
+    uint32_t incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= static_cast<uint32_t>(o)) incl += x;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    const bool any_bad = __any_sync(0xFFFFFFFFu, b != 0);
+    if (t <= G) misc[kWSeg + t] = incl - n;  // exclusive offsets; entry G = total
+    if (t == 0) {
+      misc[kWTotal] = total;
+      misc[kWFast] = p.wide_exact ? 0u
+                                  : (any_bad ? 2u : ((total >= k_eff && total <= kWideCandMax) ? 1u : 0u));
+    }
+  }
+  __syncthreads();
+  const uint32_t mode = misc[kWFast];
+  if (mode == 2u) {
+    if constexpr (G > 1) wide_cluster_sync();  // peers may still read our counters
+    if (rank == 0 && t == 0) finish_row(p, r, w, -1, kRowNonFinite);
+    return;
+  }
+  if (mode == 0u) {
+    if constexpr (G > 1) wide_cluster_sync();  // peers may still read our counters
+    const bool ok = wide_exact_collect<G>(sp, head, nq, tail, rank, k_eff, cand, hist, misc,
+                                          scratch);
+    if (!ok) {
+      if (rank == 0 && t == 0) finish_row(p, r, w, -1, kRowNonFinite);
+      return;
+    }
+    // new counts and offsets
+    if constexpr (G > 1) wide_cluster_sync();
+    if (t < 32) {
+      uint32_t n = 0;
+      if (t < G) {
+        if constexpr (G == 1)
+          n = misc[kWN];
+        else
+          n = dsmem_ld_u32(dsmem_addr(&misc[kWN], t));
+      }
+      uint32_t incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= static_cast<uint32_t>(o)) incl += x;
+      }
+      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);  // every lane of warp 0
+      if (t <= G) misc[kWSeg + t] = incl - n;
+      if (t == 0) misc[kWTotal] = total;
+    }
+    __syncthreads();
+  }
+
+  // ---- gather into the leader ----
+  const int n_all = min(static_cast<int>(misc[kWTotal]), kWideCandMax);
+  if constexpr (G > 1) {
+    if (rank != 0) {
+      const uint32_t off = misc[kWSeg + rank];
+      const int n_mine = min(static_cast<int>(misc[kWSeg + rank + 1] - off),
+                             kWideCandMax - static_cast<int>(min(off, static_cast<uint32_t>(kWideCandMax))));
+      const uint32_t dst = dsmem_addr(cand, 0) + 4u * off;
+      for (int i = t; i < n_mine; i += kWideThreads)
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst + 4u * i), "r"(cand[i]));
+    }
+    wide_cluster_sync();
+    if (rank != 0) return;
+  }
+
+  // ---- leader tail ----
+  const uint32_t *seg = &misc[kWSeg];
+  uint32_t kmax = 0;
+  for (int i = t; i < n_all; i += kWideThreads) kmax = max(kmax, cand[i] >> 16);
+  const uint32_t maxk = wide_max_u32(kmax, scratch);
+  if (maxk <= KeyBF16::kNegInf) {  // no finite logit among the candidates: none in the row
+    if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
+    return;
+  }
+  // threshold key (the k_eff-th largest) and the kept count tied at it
+  for (int i = t; i < 2048; i += kWideThreads) hist[i] = 0u;
+  if (t < 32) misc[kWHist2 + t] = 0u;
+  __syncthreads();
+  for (int i = t; i < n_all; i += kWideThreads) atomicAdd(&hist[cand[i] >> 21], 1u);
+  __syncthreads();
+  wide_select_top<8, 1>(hist, k_eff, misc, scratch);
+  const uint32_t b1 = misc[kWDigit];
+  const uint32_t above1 = misc[kWAbove];
+  for (int i = t; i < n_all; i += kWideThreads) {
+    const uint32_t key = cand[i] >> 16;
+    if ((key >> 5) == b1) atomicAdd(&misc[kWHist2 + (key & 31u)], 1u);
+  }
+  __syncthreads();
+  uint32_t thr = 0, need = 0;
+  {
+    const uint32_t kk = k_eff - above1;
+    uint32_t c = 0, suf = 0, d2 = 0, above2 = 0;
+    if (t < 32) {
+      c = misc[kWHist2 + t];
+      suf = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+        if (t + o < 32) suf += x;
+      }
+      d2 = 31u - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk));
+      above2 = __shfl_sync(0xFFFFFFFFu, suf - c, d2);
+      if (t == 0) {
+        misc[kWTKey] = (b1 << 5) | d2;
+        misc[kWTake] = kk - above2;
+      }
+    }
+    __syncthreads();
+    thr = misc[kWTKey];
+    need = misc[kWTake];
+  }
+  const float mval = KeyBF16::value(maxk);
+  const uint32_t u24 = misc[kWU24];
+  uint32_t *mh = hist;  // mass / rank histograms (hist is free again)
+  int32_t id;
+  int n_p = 1;
+  uint64_t s_k = 0;
+  if (w.greedy) {
+    id = static_cast<int32_t>(wide_rank_select(cand, n_all, seg, G, S, maxk, 0u, mh, misc, scratch));
+  } else {
+    uint64_t part = 0;
+    for (int i = t; i < n_all; i += kWideThreads) {
+      const uint32_t key = cand[i] >> 16;
+      if (key > thr) part += to_fixed(kept_weight(KeyBF16::value(key), mval, w.temp, w.inv_temp));
+    }
+    if (t == 0) part += need * to_fixed(kept_weight(KeyBF16::value(thr), mval, w.temp, w.inv_temp));
+    wide_excl_scan_u64(part, scratch, &s_k);
+    uint64_t s_p;
+    if (w.top_p >= 1.0f) {
+      n_p = static_cast<int>(k_eff);
+      s_p = s_k;
+    } else if (!(w.top_p > 0.0f)) {
+      n_p = 1;
+      s_p = to_fixed(kept_weight(mval, mval, w.temp, w.inv_temp));
+    } else {
+      const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
+      uint64_t above;
+      const uint32_t key_c = wide_mass_descent(cand, n_all, maxk, thr, need, mval, w.temp,
+                                               w.inv_temp, true, cut, 0, mh, misc, scratch, &above);
+      const uint64_t wc = to_fixed(kept_weight(KeyBF16::value(key_c), mval, w.temp, w.inv_temp));
+      uint64_t n_c = wc > 0 ? (cut - above + wc - 1) / wc : 1;
+      if (n_c < 1) n_c = 1;
+      uint32_t gt_loc = 0;
+      for (int i = t; i < n_all; i += kWideThreads) gt_loc += (cand[i] >> 16) > key_c;
+      uint64_t n_above;
+      wide_excl_scan_u64(gt_loc, scratch, &n_above);
+      n_p = static_cast<int>(n_above + n_c);
+      s_p = above + n_c * wc;
+    }
+    const uint64_t target = scale_u24(u24, s_p);
+    uint64_t above_d;
+    const uint32_t key_d = wide_mass_descent(cand, n_all, maxk, thr, need, mval, w.temp,
+                                             w.inv_temp, false, 0, target, mh, misc, scratch,
+                                             &above_d);
+    const uint64_t wd = to_fixed(kept_weight(KeyBF16::value(key_d), mval, w.temp, w.inv_temp));
+    const uint32_t rho = wd > 0 ? static_cast<uint32_t>((target - above_d) / wd) : 0u;
+    id = static_cast<int32_t>(wide_rank_select(cand, n_all, seg, G, S, key_d, rho, mh, misc, scratch));
+  }
+  if (t == 0) finish_row(p, r, w, id, 0u);
+  if (p.kept_ids) {
+    // the kept set: keys above thr, and the `need` lowest-index keys at thr
+    const uint32_t idx_cut =
+        need ? wide_rank_select(cand, n_all, seg, G, S, thr, need - 1, mh, misc, scratch) : 0u;
+    if (t == 0) misc[kWN] = 0u;
+    __syncthreads();
+    const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
+    const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
+    int c = 0;
+    for (int i = t; i < n_all; i += kWideThreads) {
+      while (c + 1 < G && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
+      const uint32_t e = cand[i];
+      const uint32_t key = e >> 16;
+      const uint32_t g = wide_gidx(e, c, S);
+      if (key > thr || (key == thr && need && g <= idx_cut)) {
+        const uint32_t pos = atomicAdd(&misc[kWN], 1u);
+        if (pos < static_cast<uint32_t>(p.max_keep)) {
+          p.kept_ids[rb + pos] = static_cast<int32_t>(g);
+          p.kept_probs[rb + pos] =
+              w.greedy ? (static_cast<int32_t>(g) == id ? 1.f : 0.f)
+                       : __fdiv_rn(kept_weight(KeyBF16::value(key), mval, w.temp, w.inv_temp),
+                                   s_real);
+        }
+      }
+    }
+    if (t == 0) {
+      p.n_kept[r] = static_cast<int32_t>(k_eff);
+      p.n_nucleus[r] = n_p;
+    }
+  }
+}
+
+}  // namespace ts

@@ -152,19 +152,24 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
 
 /* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = one 128-thread
  * block per row with a bounded candidate set (requires cap <= 64 and
- * max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row.
- * TS_OPT_CLUSTER: 0 = automatic, else the CTAs per row of the CTA/cluster
- * path (1, 2, 4 or 8).  TS_OPT_PDL: 1 (default) launches with programmatic
- * dependent launch, so that a step's kernel is scheduled while the previous
- * kernel in the stream drains (each kernel still waits for its predecessor
- * before touching memory); 0 launches plainly.  Results never depend on any
+ * max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row that
+ * holds the row in shared memory, 3 = the single-pass wide-row path (bf16
+ * only; automatic for bf16 rows wider than 32,768).  TS_OPT_CLUSTER: 0 =
+ * automatic, else the CTAs per row of paths 2 and 3 (1, 2, 4 or 8; path 3
+ * needs max_row_vocab / CTAs <= 65,536).  TS_OPT_PDL: 1 (default) launches
+ * with programmatic dependent launch, so that a step's kernel is scheduled
+ * while the previous kernel in the stream drains (each kernel still waits
+ * for its predecessor before touching memory); 0 launches plainly.
+ * TS_OPT_WIDE_EXACT: 1 makes path 3 skip its sampled threshold and always
+ * take its exact re-reading select (for tests).  Results never depend on any
  * option. */
 #define TS_OPT_PATH 1
 #define TS_OPT_CLUSTER 2
 #define TS_OPT_PDL 3
+#define TS_OPT_WIDE_EXACT 4
 ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value);
 
-/* Describes the kernel that ts_sample would launch for `b` (path 1 or 2,
+/* Describes the kernel that ts_sample would launch for `b` (path 1, 2 or 3,
  * CTAs per row, threads per CTA, dynamic shared memory bytes, grid size).
  * Any output pointer may be NULL. */
 ts_status ts_plan(const ts_sampler *s, const ts_batch *b, int32_t *path,

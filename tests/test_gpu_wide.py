@@ -1,0 +1,201 @@
+"""The single-pass wide-row kernel (path 3) vs the CPU oracle, through the C ABI.
+
+Covers the 151,936-wide stress rows on its sampled-threshold path and with
+the exact re-reading path forced, every cluster size, rows whose sample
+misleads the threshold (overflow, too few candidates), ties, signed zeros,
+non-finite values, degenerate parameters, and the narrower workloads forced
+onto the path (all-candidates mode).  Results must also equal the other
+kernel families' bit for bit.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from parity import compare, run_gpu, sub_batch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ts():
+    import codebook_token_sampling_gb300 as mod
+    return mod
+
+
+def make_sampler(ts, cap, path=3, cluster=0, exact=0):
+    s = ts.Sampler(0, cap)
+    s.set_option(ts.TS_OPT_PATH, path)
+    if cluster:
+        s.set_option(ts.TS_OPT_CLUSTER, cluster)
+    if exact:
+        s.set_option(ts.TS_OPT_WIDE_EXACT, 1)
+    return s
+
+
+def batch_from_rows(rows, *, cap, seed=0, gaps=True):
+    """rows: list of (float32 values, temp, top_k, top_p); bf16 logits packed
+    with random misaligned gaps."""
+    rng = np.random.default_rng(seed)
+    n = len(rows)
+    offs, parts, pos = [], [], 0
+    for vals, *_ in rows:
+        g = int(rng.integers(0, 7)) if gaps else 0
+        parts.append(np.zeros(g, np.float32))
+        pos += g
+        offs.append(pos)
+        parts.append(vals)
+        pos += vals.size
+    flat = np.concatenate(parts)
+    logits = workloads.to_bf16_bits(flat)
+    logits[np.isnan(flat)] = 0x7FC0
+    host = {
+        "dtype": "bf16", "logits": logits, "n_rows": n, "n_streams": n, "n_codebooks": 1,
+        "row_vocab": np.array([r[0].size for r in rows], np.int32),
+        "row_offsets": np.array(offs, np.int64),
+        "temp": np.array([r[1] for r in rows], np.float32),
+        "top_k": np.array([r[2] for r in rows], np.int32),
+        "top_p": np.array([r[3] for r in rows], np.float32),
+        "seed": np.arange(n, dtype=np.uint64) * np.uint64(7919) + np.uint64(seed),
+        "request": np.arange(n, dtype=np.uint64),
+        "codebook": np.zeros(n, np.int32), "row_stream": np.arange(n, dtype=np.int32),
+        "step": np.full(n, 3 + seed, np.int64), "eos_id": np.full(n, 5, np.int32),
+        "feedback_slot": np.arange(n, dtype=np.int32), "feedback_len": n, "cap": cap,
+    }
+    host["max_row_vocab"] = int(host["row_vocab"].max())
+    return host
+
+
+# ---------------------------------------------------------------------------
+# the stress shape: sampled threshold and forced exact path, all cluster sizes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("exact", [0, 1])
+@pytest.mark.parametrize("rows,cluster", [(1, 0), (8, 0), (32, 4), (6, 8)])
+def test_stress_wide(ts, rows, cluster, exact):
+    host = workloads.make("stress", 2, rows=rows)
+    ref = oracle.sample(host, max_keep=4096, n_threads=8)
+    s = make_sampler(ts, 4096, cluster=cluster, exact=exact)
+    gpu = run_gpu(s, host, debug_keep=4096)
+    compare(host, gpu, ref, label=f"wide stress{rows} g{cluster} exact{exact}")
+    s.close()
+
+
+def test_stress_512_default_plan_is_wide(ts):
+    host = workloads.make("stress", 0, rows=512)
+    s = ts.Sampler(0, 4096)
+    batch = ts.DeviceBatch(host, "cuda")
+    assert s.plan(batch)["path"] == 3
+    s.close()
+
+
+# ---------------------------------------------------------------------------
+# adversarial and degenerate wide rows
+# ---------------------------------------------------------------------------
+def _wide_rows(rng):
+    V = 20000
+    rows = []
+    nrm = lambda n, sd=3.0: rng.normal(0, sd, n).astype(np.float32)
+    for k, p, t in ((1, 0.9, 1.0), (30, 0.9, 1.0), (64, 0.5, 0.7), (700, 0.95, 1.3),
+                    (4096, 0.9, 1.0), (0, 0.9, 1.0), (4096, 1.0, 1.0), (30, 0.0, 1.0),
+                    (30, 0.9, 0.0), (30, 0.9, -2.0), (64, 0.99, 0.05), (64, 0.99, 25.0)):
+        rows.append((nrm(V), t, k, p))
+    rows.append((np.full(V, 1.5, np.float32), 1.0, 64, 0.9))                      # all tied
+    rows.append((rng.choice([0.0, 0.5, 1.0], V).astype(np.float32), 1.0, 4096, 0.9))  # huge ties
+    y = np.full(V, -np.inf, np.float32)
+    y[[7, 5000, 19999]] = [0.0, 1.0, 0.5]
+    rows.append((y, 1.0, 30, 1.0))                                                 # -inf in top-k
+    z = nrm(V)
+    z[12345] = np.nan
+    rows.append((z, 1.0, 30, 0.9))                                                 # NaN
+    z = nrm(V)
+    z[3] = np.inf
+    rows.append((z, 1.0, 30, 0.9))                                                 # +inf
+    rows.append((np.full(V, -np.inf, np.float32), 1.0, 30, 0.9))                  # no finite
+    sz = rng.choice([-0.0, 0.0], V).astype(np.float32)
+    sz[rng.choice(V, 20, replace=False)] = 0.25
+    rows.append((sz, 1.0, 64, 0.9))                                                # signed-zero ties
+    rows.append((np.sort(nrm(V)), 1.0, 4096, 0.9))                                 # sorted row
+    # the sample sees only the bulk: the top values sit between sampled chunks
+    adv = nrm(V, 1.0)
+    q = np.arange(V // 8)
+    sampled = np.unique((np.arange(1024) * (V // 8) // 1024))
+    free = np.setdiff1d(q, sampled)
+    hot = rng.choice(free, 1000, replace=False)
+    for c in hot:
+        adv[8 * c: 8 * c + 8] += 20.0
+    rows.append((adv, 1.0, 4096, 0.9))
+    rows.append((adv, 1.0, 30, 0.9))
+    # a sample that overestimates: the sampled chunks hold the largest values
+    over = nrm(V, 1.0)
+    for c in sampled:
+        over[8 * c: 8 * c + 8] += 30.0
+    rows.append((over, 1.0, 4096, 0.9))
+    # values crossing zero in the kept set (wide key range)
+    rows.append((rng.standard_t(3, V).astype(np.float32), 1.0, 4096, 0.6))
+    return rows
+
+
+@pytest.mark.parametrize("exact", [0, 1])
+@pytest.mark.parametrize("cluster", [1, 2, 4])
+def test_wide_edge_rows(ts, cluster, exact):
+    rng = np.random.default_rng(41)
+    host = batch_from_rows(_wide_rows(rng), cap=4096, seed=cluster)
+    ref = oracle.sample(host, max_keep=4096, n_threads=8)
+    assert np.any(ref["err"] == 4) and np.any(ref["err"] == 0)
+    s = make_sampler(ts, 4096, cluster=cluster, exact=exact)
+    gpu = run_gpu(s, host, debug_keep=4096)
+    compare(host, gpu, ref, label=f"wide edge g{cluster} exact{exact}")
+    s.close()
+
+
+@pytest.mark.parametrize("path", [1, 2, 3])
+def test_signed_zero_ties_every_path(ts, path):
+    """-0 and +0 are the same value: ties between them go by token index."""
+    rng = np.random.default_rng(8)
+    rows = []
+    for v in (40, 777, 2000):
+        x = rng.choice([-0.0, 0.0], v).astype(np.float32)
+        x[rng.choice(v, 5, replace=False)] = rng.normal(0, 1, 5)
+        rows.append((x, 1.0, 30, 0.9))
+        rows.append((x, 0.0, 30, 0.9))
+    host = batch_from_rows(rows, cap=64, seed=3)
+    ref = oracle.sample(host, max_keep=64)
+    s = make_sampler(ts, 64, path=path)
+    gpu = run_gpu(s, host, debug_keep=64)
+    compare(host, gpu, ref, label=f"signed zeros path{path}")
+    s.close()
+
+
+# ---------------------------------------------------------------------------
+# narrower workloads forced onto the wide path (all-candidates mode)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("name", ["mixed", "drama3", "qwen3tts"])
+def test_workloads_on_wide_path(ts, name):
+    host = workloads.make(name, 5)
+    cap = host["cap"]
+    ref = oracle.sample(host, max_keep=cap, n_threads=8)
+    s = make_sampler(ts, cap)
+    gpu = run_gpu(s, host, debug_keep=cap)
+    compare(host, gpu, ref, label=f"{name} wide")
+    s.close()
+
+
+def test_wide_matches_other_paths_bit_for_bit(ts):
+    rng = np.random.default_rng(17)
+    v, rows = 40000, 5
+    x = workloads.to_bf16_bits(rng.normal(0, 3, v * rows).astype(np.float32))
+    host = workloads.make("mixed", 0)
+    host = sub_batch(host, np.arange(rows))
+    host.update(logits=x, row_vocab=np.full(rows, v, np.int32),
+                row_offsets=np.arange(rows, dtype=np.int64) * v, max_row_vocab=v,
+                top_k=np.array([1, 30, 700, 4096, 0], np.int32))
+    outs = []
+    for path, g, exact in ((2, 0, 0), (3, 1, 0), (3, 2, 0), (3, 4, 0), (3, 8, 0), (3, 4, 1)):
+        s = make_sampler(ts, 4096, path=path, cluster=g, exact=exact)
+        outs.append(run_gpu(s, host, debug_keep=4096))
+        s.close()
+    ref = oracle.sample(host, max_keep=4096)
+    compare(host, outs[1], ref, label="wide g1")
+    for o in outs[1:]:
+        assert np.array_equal(o["ids"], outs[0]["ids"])
+        assert np.array_equal(o["n_nucleus"], outs[0]["n_nucleus"])
