@@ -156,10 +156,23 @@ __device__ __forceinline__ float kept_weight(float v, float m, float t, float in
   return fmaf(e, x_lo, e);
 }
 
-// Fixed-point mass: w * 2^40 rounded to an integer.  Sums of up to 4096
-// weights stay below 2^53, so every prefix sum is exact and order-free.
+// Fixed-point mass: w * 2^40 rounded to the nearest integer, ties to even,
+// for a finite w in [0, 2^23).  Sums of up to 4096 weights <= 1 stay below
+// 2^53, so every prefix sum is exact and order-free.  Computed from the IEEE
+// fields with integer operations: w = m * 2^(e - 150) for a normal w with
+// significand m (24 bits) and biased exponent e, so w * 2^40 = m * 2^sh with
+// sh = e - 110; a right shift by s = -sh rounds on the s discarded bits.
 __device__ __forceinline__ uint64_t to_fixed(float w) {
-  return __float2ull_rn(w * 1099511627776.0f);
+  const uint32_t b = __float_as_uint(w);
+  const int e = static_cast<int>(b >> 23);
+  if (e == 0) return 0ull;  // zero or subnormal: w * 2^40 < 2^-86
+  const uint64_t m = (b & 0x7FFFFFu) | 0x800000u;
+  const int sh = e - 110;
+  if (sh >= 0) return m << sh;
+  if (sh < -25) return 0ull;  // below 1/4
+  const int s = -sh;          // 1 <= s <= 25
+  const uint64_t q = m >> s, rem = m & ((1ull << s) - 1ull), half = 1ull << (s - 1);
+  return q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull);
 }
 
 // ceil(p * s) for an fp32 0 < p < 1 and s < 2^53, exact (128-bit product).

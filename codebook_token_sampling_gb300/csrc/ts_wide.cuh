@@ -47,11 +47,18 @@ constexpr int kWideThreads = 256;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideCandMax = 8192;        // candidate entries per CTA (32 KB)
 constexpr int kWideU = 4;                 // 16-byte chunks per lane per iteration
-constexpr int kWideStage = 32 * kWideU;   // staged chunks per warp per iteration
-constexpr int kWideSampleChunks = 1024;   // 8,192 sampled logits
+constexpr int kWideRing = 64;             // staged words per warp (a ring)
+constexpr int kWideSampleChunks = 512;    // 4,096 sampled logits
 constexpr int kWideSliceMax = 65536;      // slice index fits 16 bits
+constexpr int kWideBins = 2048;           // per-key counts: keys t .. t + 2047
 constexpr int kWideMaxG = 16;
-constexpr uint32_t kWideWorkBytes = kWideWarps * kWideStage * (16 + 4);  // 20 KB
+// work area: [staging rings 4 KB][per-key counts, packed 16-bit pairs 4 KB]
+//            [merge / sample histogram 8 KB][spare 4 KB]; the exact path
+//            reuses all of it from offset 0 once the fast path is abandoned
+constexpr uint32_t kWideRingBytes = kWideWarps * kWideRing * 8;
+constexpr uint32_t kWideLhOff = kWideRingBytes;
+constexpr uint32_t kWideMhOff = kWideLhOff + kWideBins * 2;
+constexpr uint32_t kWideWorkBytes = 20480;
 constexpr uint32_t kWideMiscWords = 256;
 constexpr uint32_t kWideSmemBytes = kWideCandMax * 4 + kWideWorkBytes + kWideMiscWords * 4;
 
@@ -59,9 +66,10 @@ constexpr uint32_t kWideSmemBytes = kWideCandMax * 4 + kWideWorkBytes + kWideMis
 constexpr int kWN = 0;        // local candidate count (may exceed the buffer)
 constexpr int kWBad = 1;      // NaN / +inf seen in this slice
 constexpr int kWTKey = 2;     // threshold key t
-constexpr int kWU24 = 3;      // the row's draw (leader)
+constexpr int kWU24 = 3;      // the row's draw
 constexpr int kWTotal = 4;    // candidates over the cluster
-constexpr int kWFast = 5;     // 1: fast path, 2: row error, 0: exact path
+constexpr int kWFast = 5;     // 1: per-key tail, 3: gathered tail, 2: row error, 0: exact path
+constexpr int kWRange = 6;    // a candidate key beyond t + kWideBins - 1
 constexpr int kWDigit = 8, kWAbove = 9, kWCount = 10, kWId = 11;
 constexpr int kWFin = 12;     // finite logits in this slice (exact path)
 constexpr int kWEq = 13;      // keys equal to the threshold in this slice (exact path)
@@ -70,6 +78,9 @@ constexpr int kWMaxK = 15;
 constexpr int kWWide = 16;    // 2 x u64 (words 16..19)
 constexpr int kWSeg = 24;     // G + 1 segment offsets (words 24..40)
 constexpr int kWHist2 = 64;   // 32-bin second-level histogram (words 64..95)
+constexpr int kWThrB = 96, kWNeed = 97, kWNp = 98, kWDrawB = 99, kWRho = 100;
+constexpr int kWOwner = 101, kWRho2 = 102, kWKept = 103, kWSelIdx = 104, kWMaxB = 105;
+constexpr int kWSp = 106;     // u64 (words 106..107)
 constexpr int kWScan = 128;   // block-scan scratch: u64 x (kWideWarps + 1)
 
 // Keys of the wide path are KeyBF16's (-0 takes the key of +0).
@@ -235,104 +246,11 @@ __device__ uint32_t wide_rank_select(const uint32_t *cand, int n, const uint32_t
   return 0;
 }
 
-// Radix descent over offsets (maxk - key) of the kept set with exact 2^-40
-// fixed-point masses: every candidate with key > thr is kept; the group at
-// thr contributes `need` tokens (the lowest-index ones; which ones does not
-// matter for masses).  cut_mode: the group whose cumulative mass first
-// reaches `cut` (>= cut); else the group whose cumulative mass first exceeds
-// `target`.  Returns that group's key; *above_out = mass of all groups above.
-// Levels take 10 offset bits; at the last level a bin is one key, whose mass
-// is count x weight; above it a bin's mass is summed per token as three
-// 32-bit partials (bits 0-12, 13-25, 26+), so only 32-bit shared atomics are
-// used.
-__device__ uint32_t wide_mass_descent(const uint32_t *cand, int n, uint32_t maxk, uint32_t thr,
-                                      uint32_t need, float m, float temp, float inv_temp,
-                                      bool cut_mode, uint64_t cut, uint64_t target, uint32_t *h,
-                                      uint32_t *misc, uint64_t *scratch, uint64_t *above_out) {
-  constexpr int kBins = 1024;
-  constexpr int kPer = kBins / kWideThreads;
-  const int t = static_cast<int>(threadIdx.x);
-  const uint32_t range = maxk - thr;
-  const int bits = range ? 32 - __clz(range) : 0;
-  int span = bits;
-  int shift = bits > 10 ? bits - 10 : 0;
-  uint32_t off_lo = 0;
-  uint64_t above = 0;
-  uint64_t *wide = reinterpret_cast<uint64_t *>(misc + kWWide);
-  for (;;) {
-    const bool exact = shift == 0;
-    __syncthreads();
-    for (int i = t; i < (exact ? kBins : 3 * kBins); i += kWideThreads) h[i] = 0u;
-    if (t == 0) {
-      misc[kWDigit] = 0;
-      wide[0] = above;
-    }
-    __syncthreads();
-    auto add = [&](uint32_t key, uint32_t cnt) {
-      const uint32_t off = maxk - key;
-      if (off < off_lo || static_cast<uint64_t>(off - off_lo) >= (1ull << span)) return;
-      const uint32_t d = (off - off_lo) >> shift;
-      if (exact) {
-        atomicAdd(&h[d], cnt);
-      } else {
-        const uint64_t f = cnt * to_fixed(kept_weight(KeyBF16::value(key), m, temp, inv_temp));
-        if (f) {
-          atomicAdd(&h[d], static_cast<uint32_t>(f & 0x1FFFu));
-          atomicAdd(&h[kBins + d], static_cast<uint32_t>((f >> 13) & 0x1FFFu));
-          atomicAdd(&h[2 * kBins + d], static_cast<uint32_t>(f >> 26));
-        }
-      }
-    };
-    for (int i = t; i < n; i += kWideThreads) {
-      const uint32_t key = cand[i] >> 16;
-      if (key > thr) add(key, 1u);
-    }
-    if (t == 0 && need) add(thr, need);
-    __syncthreads();
-    uint64_t ab[kPer];
-    uint64_t s = 0;
-#pragma unroll
-    for (int x = 0; x < kPer; ++x) {
-      const uint32_t d = static_cast<uint32_t>(kPer * t + x);
-      if (exact) {
-        const uint32_t cnt = h[d];
-        ab[x] = cnt ? cnt * to_fixed(kept_weight(KeyBF16::value(maxk - off_lo - d), m, temp, inv_temp))
-                    : 0ull;
-      } else {
-        ab[x] = (static_cast<uint64_t>(h[2 * kBins + d]) << 26) +
-                (static_cast<uint64_t>(h[kBins + d]) << 13) + h[d];
-      }
-      s += ab[x];
-    }
-    uint64_t tot;
-    uint64_t cum = above + wide_excl_scan_u64(s, scratch, &tot);
-#pragma unroll
-    for (int x = 0; x < kPer; ++x) {
-      const uint64_t nxt = cum + ab[x];
-      const bool r0 = cut_mode ? cum >= cut : cum > target;
-      const bool r1 = cut_mode ? nxt >= cut : nxt > target;
-      if (!r0 && r1) {
-        misc[kWDigit] = static_cast<uint32_t>(kPer * t + x);
-        wide[0] = cum;
-      }
-      cum = nxt;
-    }
-    __syncthreads();
-    off_lo += misc[kWDigit] << shift;
-    above = wide[0];
-    if (shift == 0) break;
-    span = shift;
-    shift = shift > 10 ? shift - 10 : 0;
-  }
-  *above_out = above;
-  return maxk - off_lo;
-}
-
 // Exact r-th largest canonical key of an evenly spaced sample of the row
 // (every CTA of the cluster computes the same value from the same sample).
 // Returns 0 ("every element") when the sample cannot give a useful bound.
-__device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, uint32_t *hist,
-                                          uint32_t *misc, uint64_t *scratch) {
+__device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, int G,
+                                          uint32_t *hist, uint32_t *misc, uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
   const int head_r =
       min(V, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / 2u));
@@ -340,8 +258,10 @@ __device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, ui
   const int n_chunks = min(nq_r, kWideSampleChunks);
   const int n_s = 8 * n_chunks;
   if (n_chunks <= 0) return 0u;
-  // r such that about 1.4 k_eff row elements are expected at or above it
-  const long long want = (14ll * k_eff * n_s + 10ll * V - 1) / (10ll * V);
+  // r such that about 1.6 k_eff row elements (at most 3/4 of the cluster's
+  // candidate buffers) are expected at or above it
+  const long long expect10 = min(16ll * k_eff, 75ll * kWideCandMax * G / 10);
+  const long long want = (expect10 * n_s + 10ll * V - 1) / (10ll * V);
   const int r = static_cast<int>(max(32ll, want));
   if (r > n_s) return 0u;
   const char *body = rowp + 2 * head_r;
@@ -414,70 +334,63 @@ __device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, ui
   return tk;
 }
 
-// Appends (key << 16 | slice index) to this CTA's candidate buffer for the
-// flagged elements of `n` staged chunks (lane l handles staged chunk
-// base + l); returns through *bad whether a NaN / +inf key was met.
-__device__ __forceinline__ void wide_append_staged(const uint4 *stage, const uint32_t *stage_q,
-                                                   int base, int n, uint32_t t_key, int head,
-                                                   uint32_t *cand, uint32_t *counter,
-                                                   uint32_t &bad) {
+// One candidate: its entry (key << 16 | slice index) and its per-key count.
+// The count keeps growing past the buffer (the caller compares it with
+// kWideCandMax) and the entry is then dropped; a key beyond the counted
+// window raises `range`.
+__device__ __forceinline__ void wide_keep(uint32_t key, uint32_t idx, uint32_t pos,
+                                          uint32_t t_key, uint32_t *cand, uint32_t *lh,
+                                          uint32_t &range) {
+  if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = (key << 16) | idx;
+  const uint32_t off = key - t_key;
+  if (off < static_cast<uint32_t>(kWideBins))
+    atomicAdd(&lh[off >> 1], 1u << ((off & 1u) * 16u));
+  else
+    range = 1u;
+}
+
+// Drains n <= 32 staged words (two logits each) from a warp's ring: lane l
+// takes entry head + l; every element with key >= t_key becomes a
+// candidate.  NaN / +inf keys raise `bad`.
+__device__ __forceinline__ void wide_drain(const uint2 *ring, uint32_t head, uint32_t n,
+                                           uint32_t t_key, uint32_t *cand, uint32_t *lh,
+                                           uint32_t *counter, uint32_t &bad, uint32_t &range) {
   const uint32_t lane = lane_id();
-  const int i = base + static_cast<int>(lane);
-  uint32_t k[8];
-  uint32_t flags = 0, cnt = 0, idx0 = 0;
-  if (i < n) {
-    const uint4 c = stage[i];
-    idx0 = static_cast<uint32_t>(head) + 8u * stage_q[i];
-    const uint32_t wds[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint32_t kw = wkey_word(wds[x]);
-      k[2 * x] = kw & 0xFFFFu;
-      k[2 * x + 1] = kw >> 16;
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const bool nonfinite = k[e] < KeyBF16::kNegInf || k[e] >= KeyBF16::kPosInf;
-      bad |= nonfinite;
-      if (!nonfinite && k[e] >= t_key) {
-        flags |= 1u << e;
-        ++cnt;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) k[e] = 0u;
+  bool f0 = false, f1 = false;
+  uint32_t k0 = 0, k1 = 0, idx0 = 0;
+  if (lane < n) {
+    const uint2 e = ring[(head + lane) & (kWideRing - 1)];
+    const uint32_t kw = wkey_word(e.x);
+    k0 = kw & 0xFFFFu;
+    k1 = kw >> 16;
+    idx0 = e.y;
+    const bool nf0 = k0 < KeyBF16::kNegInf || k0 >= KeyBF16::kPosInf;
+    const bool nf1 = k1 < KeyBF16::kNegInf || k1 >= KeyBF16::kPosInf;
+    bad |= nf0 | nf1;
+    f0 = !nf0 && k0 >= t_key;
+    f1 = !nf1 && k1 >= t_key;
   }
-  uint32_t incl = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= static_cast<uint32_t>(o)) incl += x;
-  }
-  const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, f0), b1 = __ballot_sync(0xFFFFFFFFu, f1);
+  const uint32_t total = __popc(b0) + __popc(b1);
   if (total == 0) return;
-  uint32_t pos = 0;
-  if (lane == 31) pos = atomicAdd(counter, total);
-  pos = __shfl_sync(0xFFFFFFFFu, pos, 31) + incl - cnt;
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    if (flags & (1u << e)) {
-      if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = (k[e] << 16) | (idx0 + e);
-      ++pos;
-    }
-  }
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(counter, total);
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  const uint32_t lt = lanemask_lt();
+  const uint32_t pos = base + __popc(b0 & lt) + __popc(b1 & lt);
+  if (f0) wide_keep(k0, idx0, pos, t_key, cand, lh, range);
+  if (f1) wide_keep(k1, idx0 + 1u, pos + (f0 ? 1u : 0u), t_key, cand, lh, range);
 }
 
 // One element of a slice's unaligned head or tail.
 __device__ __forceinline__ void wide_append_one(const char *sp, int idx, uint32_t t_key,
-                                                uint32_t *cand, uint32_t *counter, uint32_t &bad) {
+                                                uint32_t *cand, uint32_t *lh, uint32_t *counter,
+                                                uint32_t &bad, uint32_t &range) {
   const uint32_t k = wkey(KeyBF16::load_one(sp, idx));
   const bool nonfinite = k < KeyBF16::kNegInf || k >= KeyBF16::kPosInf;
   bad |= nonfinite;
-  if (!nonfinite && k >= t_key) {
-    const uint32_t pos = atomicAdd(counter, 1u);
-    if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = (k << 16) | static_cast<uint32_t>(idx);
-  }
+  if (!nonfinite && k >= t_key)
+    wide_keep(k, static_cast<uint32_t>(idx), atomicAdd(counter, 1u), t_key, cand, lh, range);
 }
 
 // Appends one entry; the count keeps growing past the buffer (callers
@@ -677,6 +590,566 @@ __device__ bool wide_exact_collect(const char *sp, int head, int nq, int tail, u
   return true;
 }
 
+// The rho-th smallest (0-based) slice index among this CTA's candidates
+// with key `key_sel`: a two-level radix select on the 16-bit slice index
+// (256 bins per level).  Order-free.
+__device__ uint32_t wide_local_rank_select(const uint32_t *cand, int n, uint32_t key_sel,
+                                           uint32_t rho, uint32_t *h, uint32_t *misc,
+                                           uint64_t *scratch) {
+  const int t = static_cast<int>(threadIdx.x);
+  uint32_t b1 = 0, below = 0;
+#pragma unroll 1
+  for (int level = 0; level < 2; ++level) {
+    __syncthreads();
+    h[t] = 0u;  // kWideThreads == 256 bins
+    __syncthreads();
+    for (int i = t; i < n; i += kWideThreads) {
+      const uint32_t e = cand[i];
+      if ((e >> 16) != key_sel) continue;
+      const uint32_t idx = e & 0xFFFFu;
+      if (level == 0)
+        atomicAdd(&h[idx >> 8], 1u);
+      else if ((idx >> 8) == b1)
+        atomicAdd(&h[idx & 255u], 1u);
+    }
+    __syncthreads();
+    const uint32_t want = rho - below;
+    const uint32_t c = h[t];
+    uint64_t tot;
+    const uint32_t ex = static_cast<uint32_t>(wide_excl_scan_u64(c, scratch, &tot));
+    if (ex <= want && want < ex + c) {
+      misc[kWDigit] = static_cast<uint32_t>(t);
+      misc[kWAbove] = ex;
+    }
+    __syncthreads();
+    if (level == 0) {
+      b1 = misc[kWDigit];
+      below = misc[kWAbove];
+    } else {
+      return (b1 << 8) | misc[kWDigit];
+    }
+  }
+  return 0;
+}
+
+__device__ __forceinline__ uint32_t dsmem_atomic_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
+
+// Fast tail.  Every CTA of the cluster merges the G per-key candidate counts
+// (keys t .. t + kWideBins - 1) and, redundantly so that none waits for
+// another, finds the threshold key and the kept count tied at it, the
+// masses (one weight per key), the nucleus cutoff and the draw; the CTA that
+// holds the drawn token (index order = CTA order) picks it from its own
+// candidates.  Bins: thread j owns keys t + 8j .. t + 8j + 7.
+template <int G>
+__device__ void wide_fast_tail(const Params &p, int r, const Row &w, uint32_t rank, int S,
+                               uint32_t t_key, const uint32_t *cand, int n_loc,
+                               const uint32_t *lh, uint32_t *hsel, uint32_t *misc,
+                               uint64_t *scratch) {
+  constexpr int kPer = kWideBins / kWideThreads;
+  static_assert(kPer == 8, "two packed words per uint4 load");
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t lane = lane_id();
+  const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
+  uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
+
+  // ---- merged per-key counts (packed 16-bit pairs add without carries) ----
+  uint32_t c[kPer];
+  {
+    uint4 acc = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      uint4 v;
+      if constexpr (G == 1)
+        v = reinterpret_cast<const uint4 *>(lh)[t];
+      else
+        v = dsmem_ld_v4(dsmem_addr(&lh[4 * t], g));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const uint32_t wd[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      c[2 * j] = wd[j] & 0xFFFFu;
+      c[2 * j + 1] = wd[j] >> 16;
+    }
+  }
+  // ---- highest populated key, threshold key (k_eff-th largest) ----
+  uint32_t s = 0, hi = 0;
+#pragma unroll
+  for (int b = 0; b < kPer; ++b) {
+    s += c[b];
+    if (c[b]) hi = static_cast<uint32_t>(kPer * t + b) + 1u;
+  }
+  const uint32_t maxb = wide_max_u32(hi, scratch) - 1u;
+  if (t_key + maxb <= KeyBF16::kNegInf) {  // every candidate is -inf: no finite logit in the row
+    if (rank == 0 && t == 0) finish_row(p, r, w, -1, kRowNonFinite);
+    return;
+  }
+  uint64_t tot;
+  const uint32_t excl = static_cast<uint32_t>(wide_excl_scan_u64(s, scratch, &tot));
+  const uint32_t above_cnt = static_cast<uint32_t>(tot) - excl - s;  // kept above my keys
+  if (s != 0 && above_cnt < k_eff && above_cnt + s >= k_eff) {
+    uint32_t run = above_cnt;
+#pragma unroll
+    for (int b = kPer - 1; b >= 0; --b) {
+      if (run < k_eff && run + c[b] >= k_eff) {
+        misc[kWThrB] = static_cast<uint32_t>(kPer * t + b);
+        misc[kWNeed] = k_eff - run;
+      }
+      run += c[b];
+    }
+  }
+  __syncthreads();
+  const uint32_t thr_b = misc[kWThrB], need = misc[kWNeed];
+  const float m = KeyBF16::value(t_key + maxb);
+  const uint32_t u24 = misc[kWU24];
+  uint32_t draw_b = maxb, rho = 0, n_p = 1;
+  uint64_t s_k = 0;
+  if (!w.greedy) {
+    // ---- masses: count x weight of the key (the threshold key: need) ----
+    uint64_t mass[kPer];
+    uint64_t st = 0;
+#pragma unroll
+    for (int b = 0; b < kPer; ++b) {
+      const uint32_t bin = static_cast<uint32_t>(kPer * t + b);
+      const uint32_t cnt = bin > thr_b ? c[b] : (bin == thr_b ? need : 0u);
+      mass[b] = cnt ? cnt * to_fixed(kept_weight(KeyBF16::value(t_key + bin), m, w.temp,
+                                                 w.inv_temp))
+                    : 0ull;
+      st += mass[b];
+    }
+    const uint64_t ex_m = wide_excl_scan_u64(st, scratch, &s_k);
+    const uint64_t above_m = s_k - ex_m - st;  // mass above my keys
+    // ---- nucleus cutoff ----
+    uint64_t s_p;
+    if (w.top_p >= 1.0f) {
+      n_p = k_eff;
+      s_p = s_k;
+    } else if (!(w.top_p > 0.0f)) {
+      n_p = 1;
+      s_p = to_fixed(kept_weight(m, m, w.temp, w.inv_temp));
+    } else {
+      const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
+      if (st != 0 && above_m < cut && above_m + st >= cut) {
+        uint64_t cum = above_m;
+        uint32_t cnt_above = above_cnt;
+#pragma unroll
+        for (int b = kPer - 1; b >= 0; --b) {
+          if (cum < cut && cum + mass[b] >= cut) {
+            const uint32_t bin = static_cast<uint32_t>(kPer * t + b);
+            const uint64_t wb =
+                to_fixed(kept_weight(KeyBF16::value(t_key + bin), m, w.temp, w.inv_temp));
+            uint64_t n_c = (cut - cum + wb - 1) / wb;
+            if (n_c < 1) n_c = 1;
+            m64[kWSp / 2] = cum + n_c * wb;
+            misc[kWNp] = cnt_above + static_cast<uint32_t>(n_c);
+          }
+          cum += mass[b];
+          cnt_above += c[b];
+        }
+      }
+      __syncthreads();
+      s_p = m64[kWSp / 2];
+      n_p = misc[kWNp];
+    }
+    // ---- draw: the key group whose cumulative mass first exceeds target ----
+    const uint64_t target = scale_u24(u24, s_p);
+    if (st != 0 && above_m <= target && target < above_m + st) {
+      uint64_t cum = above_m;
+#pragma unroll
+      for (int b = kPer - 1; b >= 0; --b) {
+        if (cum <= target && target < cum + mass[b]) {
+          const uint32_t bin = static_cast<uint32_t>(kPer * t + b);
+          const uint64_t wb =
+              to_fixed(kept_weight(KeyBF16::value(t_key + bin), m, w.temp, w.inv_temp));
+          misc[kWDrawB] = bin;
+          misc[kWRho] = static_cast<uint32_t>((target - cum) / wb);
+        }
+        cum += mass[b];
+      }
+    }
+    __syncthreads();
+    draw_b = misc[kWDrawB];
+    rho = misc[kWRho];
+  }
+  // ---- the CTA holding the drawn token (index order = CTA order) ----
+  if (t < 32) {
+    uint32_t cnt = 0;
+    if (lane < static_cast<uint32_t>(G)) {
+      uint32_t word;
+      if constexpr (G == 1)
+        word = lh[draw_b >> 1];
+      else
+        word = dsmem_ld_u32(dsmem_addr(&lh[draw_b >> 1], lane));
+      cnt = (word >> ((draw_b & 1u) * 16u)) & 0xFFFFu;
+    }
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= static_cast<uint32_t>(o)) incl += x;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > rho && lane < static_cast<uint32_t>(G));
+    const uint32_t owner = hit ? static_cast<uint32_t>(__ffs(hit) - 1) : 0u;
+    const uint32_t before = __shfl_sync(0xFFFFFFFFu, incl - cnt, owner);
+    if (t == 0) {
+      misc[kWOwner] = owner;
+      misc[kWRho2] = rho - before;
+    }
+  }
+  __syncthreads();
+  const uint32_t owner = misc[kWOwner];
+  uint32_t sel = 0xFFFFFFFFu;
+  if (rank == owner) {
+    sel = wide_local_rank_select(cand, n_loc, t_key + draw_b, misc[kWRho2], hsel, misc, scratch);
+    if (t == 0) finish_row(p, r, w, static_cast<int32_t>(rank * S + sel), 0u);
+  }
+  if (p.kept_ids) {
+    // this CTA's share of the keys tied at the threshold: the lowest indices
+    // of the row first, and CTA order is index order
+    if (t < 32) {
+      uint32_t e = 0;
+      if (lane < rank) {
+        if constexpr (G > 1) {
+          const uint32_t word = dsmem_ld_u32(dsmem_addr(&lh[thr_b >> 1], lane));
+          e = (word >> ((thr_b & 1u) * 16u)) & 0xFFFFu;
+        }
+      }
+      const uint32_t before = __reduce_add_sync(0xFFFFFFFFu, e);
+      if (t == 0) {
+        const uint32_t mine = (lh[thr_b >> 1] >> ((thr_b & 1u) * 16u)) & 0xFFFFu;
+        misc[kWTake] = need > before ? min(need - before, mine) : 0u;
+        misc[kWEq] = mine;
+      }
+    }
+    __syncthreads();
+    const uint32_t take = misc[kWTake], mine = misc[kWEq];
+    uint32_t cut_idx = take ? 0xFFFFu : 0u;
+    if (take != 0 && take < mine)
+      cut_idx = wide_local_rank_select(cand, n_loc, t_key + thr_b, take - 1, hsel, misc, scratch);
+    const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
+    const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
+    const uint32_t kept_addr = G > 1 ? dsmem_addr(&misc[kWKept], 0) : 0u;
+    for (int i = t; i < n_loc; i += kWideThreads) {
+      const uint32_t e = cand[i];
+      const uint32_t key = e >> 16, idx = e & 0xFFFFu;
+      const uint32_t bin = key - t_key;
+      const bool keep = bin > thr_b || (bin == thr_b && take != 0 && idx <= cut_idx);
+      if (!keep) continue;
+      uint32_t pos;
+      if constexpr (G > 1)
+        pos = dsmem_atomic_add(kept_addr, 1u);
+      else
+        pos = atomicAdd(&misc[kWKept], 1u);
+      if (pos < static_cast<uint32_t>(p.max_keep)) {
+        p.kept_ids[rb + pos] = static_cast<int32_t>(rank * S + idx);
+        p.kept_probs[rb + pos] =
+            w.greedy ? ((rank == owner && idx == sel) ? 1.f : 0.f)
+                     : __fdiv_rn(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp), s_real);
+      }
+    }
+    if (rank == 0 && t == 0) {
+      p.n_kept[r] = static_cast<int32_t>(k_eff);
+      p.n_nucleus[r] = static_cast<int32_t>(n_p);
+    }
+  }
+}
+
+// Exact second level of the gathered tail: inside coarse bin `bin` (keys
+// maxk - (bin << shift) - j, j < 2^shift <= 64) counts the kept tokens per
+// key, weighs them, and finds the key where the cumulative mass (from the
+// top, starting at `above`) first reaches `goal` (cut_mode: >= goal) or first
+// exceeds it (else).  Writes the key, the mass above it and the kept count
+// above it inside the bin to misc.
+__device__ void wide_level2(const uint32_t *cand, int n, uint32_t maxk, uint32_t thr,
+                            uint32_t need, int shift, uint32_t bin, float m, float temp,
+                            float inv_temp, bool cut_mode, uint64_t goal, uint64_t above,
+                            uint32_t *l2, uint32_t *misc) {
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t lane = lane_id();
+  uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
+  __syncthreads();
+  if (t < 64) l2[t] = 0u;
+  __syncthreads();
+#pragma unroll 4
+  for (int i = t; i < n; i += kWideThreads) {
+    const uint32_t key = cand[i] >> 16;
+    const uint32_t off = maxk - key;
+    if (key > thr && (off >> shift) == bin) atomicAdd(&l2[off & ((1u << shift) - 1u)], 1u);
+  }
+  if (t == 0 && need && ((maxk - thr) >> shift) == bin)
+    atomicAdd(&l2[(maxk - thr) & ((1u << shift) - 1u)], need);
+  __syncthreads();
+  if (t < 32) {
+    const uint32_t base = maxk - (bin << shift);
+    uint64_t ms[2];
+    uint32_t cs[2];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const uint32_t j = 2 * lane + x;
+      cs[x] = j < (1u << shift) ? l2[j] : 0u;
+      ms[x] = cs[x] ? cs[x] * to_fixed(kept_weight(KeyBF16::value(base - j), m, temp, inv_temp))
+                    : 0ull;
+    }
+    uint64_t incl = ms[0] + ms[1];
+    uint32_t cincl = cs[0] + cs[1];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t a = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      const uint32_t b = __shfl_up_sync(0xFFFFFFFFu, cincl, o);
+      if (lane >= static_cast<uint32_t>(o)) {
+        incl += a;
+        cincl += b;
+      }
+    }
+    uint64_t cum = above + incl - ms[0] - ms[1];
+    uint32_t ccum = cincl - cs[0] - cs[1];
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      const uint64_t nxt = cum + ms[x];
+      const bool hit = cut_mode ? (cum < goal && nxt >= goal) : (cum <= goal && goal < nxt);
+      if (hit) {
+        misc[kWDigit] = base - (2 * lane + x);
+        m64[kWSp / 2] = cum;
+        misc[kWCount] = ccum;
+      }
+      cum = nxt;
+      ccum += cs[x];
+    }
+  }
+  __syncthreads();
+}
+
+// Gathered tail (one CTA holds every candidate; any key range): the
+// threshold key and the kept count tied at it by radix select on the keys;
+// then a coarse histogram of the kept masses over (max key - key) >> shift
+// (the only pass that evaluates exp per token), which gives S_k and the
+// coarse bins of the nucleus cutoff and of the draw; an exact second level
+// inside each of those two bins; the token by a radix select on the index.
+template <int G>
+__device__ void wide_gather_tail(const Params &p, int r, const Row &w, const uint32_t *cand,
+                                 int n, const uint32_t *seg, int S, uint32_t *hw,
+                                 uint32_t *misc, uint64_t *scratch) {
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
+  uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
+  // ---- counts by key >> 5 and the maximum key ----
+  for (int i = t; i < 2048; i += kWideThreads) hw[i] = 0u;
+  if (t < 32) misc[kWHist2 + t] = 0u;
+  __syncthreads();
+  uint32_t kmax = 0;
+#pragma unroll 4
+  for (int i = t; i < n; i += kWideThreads) {
+    const uint32_t key = cand[i] >> 16;
+    atomicAdd(&hw[key >> 5], 1u);
+    kmax = max(kmax, key);
+  }
+  const uint32_t maxk = wide_max_u32(kmax, scratch);
+  if (maxk <= KeyBF16::kNegInf) {  // every candidate is -inf: no finite logit in the row
+    if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
+    return;
+  }
+  wide_select_top<8, 1>(hw, k_eff, misc, scratch);
+  const uint32_t b1 = misc[kWDigit];
+  const uint32_t above1 = misc[kWAbove];
+#pragma unroll 4
+  for (int i = t; i < n; i += kWideThreads) {
+    const uint32_t key = cand[i] >> 16;
+    if ((key >> 5) == b1) atomicAdd(&misc[kWHist2 + (key & 31u)], 1u);
+  }
+  __syncthreads();
+  if (t < 32) {
+    const uint32_t kk = k_eff - above1;
+    const uint32_t c = misc[kWHist2 + t];
+    uint32_t suf = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
+      if (t + o < 32) suf += x;
+    }
+    const uint32_t d2 = 31u - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk));
+    const uint32_t above2 = __shfl_sync(0xFFFFFFFFu, suf - c, d2);
+    if (t == 0) {
+      misc[kWTKey] = (b1 << 5) | d2;
+      misc[kWTake] = kk - above2;
+    }
+  }
+  __syncthreads();
+  const uint32_t thr = misc[kWTKey];
+  const uint32_t need = misc[kWTake];
+  const float m = KeyBF16::value(maxk);
+  const uint32_t u24 = misc[kWU24];
+  int32_t id;
+  uint32_t n_p = 1;
+  uint64_t s_k = 0;
+  if (w.greedy) {
+    id = static_cast<int32_t>(wide_rank_select(cand, n, seg, G, S, maxk, 0u, hw, misc, scratch));
+  } else {
+    // ---- coarse kept masses and counts over (maxk - key) >> shift ----
+    const uint32_t range = maxk - thr;
+    const int bits = range ? 32 - __clz(range) : 0;
+    const int shift = bits > 10 ? bits - 10 : 0;
+    uint32_t *plo = hw, *pmid = hw + 1024, *phi = hw + 2048, *pcnt = hw + 3072;
+    __syncthreads();
+    for (int i = t; i < 4096; i += kWideThreads) hw[i] = 0u;
+    __syncthreads();
+    auto add = [&](uint32_t key, uint32_t cnt) {
+      const uint32_t d = (maxk - key) >> shift;
+      atomicAdd(&pcnt[d], cnt);
+      if (shift) {
+        const uint64_t f = cnt * to_fixed(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp));
+        if (f) {
+          atomicAdd(&plo[d], static_cast<uint32_t>(f & 0x1FFFu));
+          atomicAdd(&pmid[d], static_cast<uint32_t>((f >> 13) & 0x1FFFu));
+          atomicAdd(&phi[d], static_cast<uint32_t>(f >> 26));
+        }
+      }
+    };
+#pragma unroll 4
+    for (int i = t; i < n; i += kWideThreads) {
+      const uint32_t key = cand[i] >> 16;
+      if (key > thr) add(key, 1u);
+    }
+    if (t == 0 && need) add(thr, need);
+    __syncthreads();
+    uint64_t ms[4];
+    uint32_t cs[4];
+    uint64_t st = 0;
+    uint32_t ct = 0;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+      const uint32_t d = static_cast<uint32_t>(4 * t + x);
+      cs[x] = pcnt[d];
+      if (shift == 0)
+        ms[x] = cs[x] ? cs[x] * to_fixed(kept_weight(KeyBF16::value(maxk - d), m, w.temp, w.inv_temp))
+                      : 0ull;
+      else
+        ms[x] = (static_cast<uint64_t>(phi[d]) << 26) + (static_cast<uint64_t>(pmid[d]) << 13) +
+                plo[d];
+      st += ms[x];
+      ct += cs[x];
+    }
+    const uint64_t cum_t = wide_excl_scan_u64(st, scratch, &s_k);
+    uint64_t n_all64;
+    const uint32_t ccum_t = static_cast<uint32_t>(wide_excl_scan_u64(ct, scratch, &n_all64));
+    // ---- nucleus cutoff ----
+    uint64_t s_p;
+    if (w.top_p >= 1.0f) {
+      n_p = k_eff;
+      s_p = s_k;
+    } else if (!(w.top_p > 0.0f)) {
+      n_p = 1;
+      s_p = to_fixed(kept_weight(m, m, w.temp, w.inv_temp));
+    } else {
+      const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
+      {
+        uint64_t cum = cum_t;
+        uint32_t ccum = ccum_t;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          if (cum < cut && cum + ms[x] >= cut) {
+            misc[kWThrB] = static_cast<uint32_t>(4 * t + x);
+            m64[kWWide / 2] = cum;
+            misc[kWNeed] = ccum;
+          }
+          cum += ms[x];
+          ccum += cs[x];
+        }
+      }
+      __syncthreads();
+      const uint32_t c1 = misc[kWThrB];
+      const uint64_t above_c = m64[kWWide / 2];
+      const uint32_t cnt_c = misc[kWNeed];
+      uint32_t key_c;
+      uint64_t above_k;
+      uint32_t cnt_k;
+      if (shift == 0) {
+        key_c = maxk - c1;
+        above_k = above_c;
+        cnt_k = cnt_c;
+      } else {
+        wide_level2(cand, n, maxk, thr, need, shift, c1, m, w.temp, w.inv_temp, true, cut,
+                    above_c, hw + 4096, misc);
+        key_c = misc[kWDigit];
+        above_k = m64[kWSp / 2];
+        cnt_k = cnt_c + misc[kWCount];
+      }
+      const uint64_t wc = to_fixed(kept_weight(KeyBF16::value(key_c), m, w.temp, w.inv_temp));
+      uint64_t n_c = wc > 0 ? (cut - above_k + wc - 1) / wc : 1;
+      if (n_c < 1) n_c = 1;
+      n_p = cnt_k + static_cast<uint32_t>(n_c);
+      s_p = above_k + n_c * wc;
+      __syncthreads();  // everyone has read misc before it is reused
+    }
+    // ---- draw ----
+    const uint64_t target = scale_u24(u24, s_p);
+    {
+      uint64_t cum = cum_t;
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        if (cum <= target && target < cum + ms[x]) {
+          misc[kWDrawB] = static_cast<uint32_t>(4 * t + x);
+          m64[kWWide / 2] = cum;
+        }
+        cum += ms[x];
+      }
+    }
+    __syncthreads();
+    const uint32_t d1 = misc[kWDrawB];
+    const uint64_t above_d1 = m64[kWWide / 2];
+    uint32_t key_d;
+    uint64_t above_d;
+    if (shift == 0) {
+      key_d = maxk - d1;
+      above_d = above_d1;
+    } else {
+      wide_level2(cand, n, maxk, thr, need, shift, d1, m, w.temp, w.inv_temp, false, target,
+                  above_d1, hw + 4096, misc);
+      key_d = misc[kWDigit];
+      above_d = m64[kWSp / 2];
+    }
+    const uint64_t wd = to_fixed(kept_weight(KeyBF16::value(key_d), m, w.temp, w.inv_temp));
+    const uint32_t rho = wd > 0 ? static_cast<uint32_t>((target - above_d) / wd) : 0u;
+    id = static_cast<int32_t>(wide_rank_select(cand, n, seg, G, S, key_d, rho, hw, misc, scratch));
+  }
+  if (t == 0) finish_row(p, r, w, id, 0u);
+  if (p.kept_ids) {
+    // the kept set: keys above thr, and the `need` lowest-index keys at thr
+    const uint32_t idx_cut =
+        need ? wide_rank_select(cand, n, seg, G, S, thr, need - 1, hw, misc, scratch) : 0u;
+    if (t == 0) misc[kWN] = 0u;
+    __syncthreads();
+    const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
+    const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
+    int c = 0;
+    for (int i = t; i < n; i += kWideThreads) {
+      while (c + 1 < G && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
+      const uint32_t e = cand[i];
+      const uint32_t key = e >> 16;
+      const uint32_t g = wide_gidx(e, c, S);
+      if (key > thr || (key == thr && need && g <= idx_cut)) {
+        const uint32_t pos = atomicAdd(&misc[kWN], 1u);
+        if (pos < static_cast<uint32_t>(p.max_keep)) {
+          p.kept_ids[rb + pos] = static_cast<int32_t>(g);
+          p.kept_probs[rb + pos] =
+              w.greedy ? (static_cast<int32_t>(g) == id ? 1.f : 0.f)
+                       : __fdiv_rn(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp), s_real);
+        }
+      }
+    }
+    if (t == 0) {
+      p.n_kept[r] = static_cast<int32_t>(k_eff);
+      p.n_nucleus[r] = static_cast<int32_t>(n_p);
+    }
+  }
+}
+
 template <int G>
 __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -684,7 +1157,8 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
   unsigned char *work = smem + kWideCandMax * 4;
   uint32_t *misc = reinterpret_cast<uint32_t *>(work + kWideWorkBytes);
   uint64_t *scratch = reinterpret_cast<uint64_t *>(misc + kWScan);
-  uint32_t *hist = reinterpret_cast<uint32_t *>(work);  // aliases the staging area
+  uint32_t *lh = reinterpret_cast<uint32_t *>(work + kWideLhOff);  // per-key counts
+  uint32_t *mh = reinterpret_cast<uint32_t *>(work + kWideMhOff);  // sample / select histograms
 
   const uint32_t rank = G > 1 ? cluster_rank() : 0u;
   const int r = G > 1 ? static_cast<int>(cluster_index()) : static_cast<int>(blockIdx.x);
@@ -698,7 +1172,7 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
     if (rank == 0 && t == 0) finish_row(p, r, w, -1, w.err);
     return;
   }
-  if (rank == 0 && t == 32) {  // the draw, off the critical path
+  if (t == 32) {  // the draw, off the critical path (every CTA may need it)
     misc[kWU24] = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
                              static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
   }
@@ -731,22 +1205,24 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
 
   uint32_t t_key = 0;
   if (V > kWideCandMax && !p.wide_exact)
-    t_key = wide_sample_threshold(rowp, V, w.k_eff, hist, misc, scratch);
+    t_key = wide_sample_threshold(rowp, V, w.k_eff, G, mh, misc, scratch);
+  for (int i = t; i < kWideBins / 2; i += kWideThreads) lh[i] = 0u;
+  if (t < 16) misc[kWThrB + t] = 0u;  // fast-tail results and the kept-set counter
   if (t == 0) {
     misc[kWN] = 0u;
     misc[kWBad] = 0u;
+    misc[kWRange] = 0u;
   }
-  __syncthreads();  // the staging area (hist) is free; counters are clear
+  __syncthreads();
 
   // ---- filter: every element with key >= t_key becomes a candidate ----
-  uint32_t bad = 0;
+  uint32_t bad = 0, range = 0;
   if (!p.wide_exact) {
     const uint32_t tb = wkey_bits(t_key);
     const uint32_t t2 = tb | (tb << 16);
-    uint4 *stage = reinterpret_cast<uint4 *>(work) + warp * kWideStage;
-    uint32_t *stage_q =
-        reinterpret_cast<uint32_t *>(work + kWideWarps * kWideStage * 16) + warp * kWideStage;
+    uint2 *ring = reinterpret_cast<uint2 *>(work) + warp * kWideRing;
     const uint32_t lt = lanemask_lt();
+    uint32_t rh = 0, rt = 0;  // warp-uniform ring head (drained) and tail (staged)
 #pragma unroll 1
     for (int it = 0; it < n_it; ++it) {
       uint4 nxt[kWideU];
@@ -756,50 +1232,61 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
         nxt[u] = m < nq ? ld_stream_v4(body + 16 * static_cast<size_t>(m), pol)
                         : make_uint4(0u, 0u, 0u, 0u);
       }
-      int n_st = 0;
 #pragma unroll
       for (int u = 0; u < kWideU; ++u) {
         const int m = it * kPerIter + u * kWideThreads + t;
-        bool f = false;
+        const uint32_t wd[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+        uint32_t mk[4] = {0u, 0u, 0u, 0u};
         if (m < nq) {
-          const uint32_t mk = hgeu_mask(cur[u].x, t2) | hgeu_mask(cur[u].y, t2) |
-                              hgeu_mask(cur[u].z, t2) | hgeu_mask(cur[u].w, t2);
-          f = mk != 0u;
+#pragma unroll
+          for (int x = 0; x < 4; ++x) mk[x] = hgeu_mask(wd[x], t2);
         }
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, f);
-        if (f) {
-          const int pos = n_st + __popc(bal & lt);
-          stage[pos] = cur[u];
-          stage_q[pos] = static_cast<uint32_t>(m);
+        if (!__any_sync(0xFFFFFFFFu, (mk[0] | mk[1] | mk[2] | mk[3]) != 0u)) continue;
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const bool f = mk[x] != 0u;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, f);
+          if (f)
+            ring[(rt + __popc(bal & lt)) & (kWideRing - 1)] =
+                make_uint2(wd[x], static_cast<uint32_t>(head + 8 * m + 2 * x));
+          rt += __popc(bal);
+          if (rt - rh >= 32u) {
+            __syncwarp();
+            wide_drain(ring, rh, 32u, t_key, cand, lh, &misc[kWN], bad, range);
+            rh += 32u;
+            __syncwarp();
+          }
         }
-        n_st += __popc(bal);
       }
-      __syncwarp();
-      for (int b = 0; b < n_st; b += 32)
-        wide_append_staged(stage, stage_q, b, n_st, t_key, head, cand, &misc[kWN], bad);
-      __syncwarp();
 #pragma unroll
       for (int u = 0; u < kWideU; ++u) cur[u] = nxt[u];
     }
+    __syncwarp();
+    if (rt != rh) wide_drain(ring, rh, rt - rh, t_key, cand, lh, &misc[kWN], bad, range);
     if (t < head + tail) {
       const int idx = t < head ? t : head + 8 * nq + (t - head);
-      wide_append_one(sp, idx, t_key, cand, &misc[kWN], bad);
+      wide_append_one(sp, idx, t_key, cand, lh, &misc[kWN], bad, range);
     }
     if (bad) atomicOr(&misc[kWBad], 1u);
+    if (range) atomicOr(&misc[kWRange], 1u);
   }
-  __syncthreads();
-  if constexpr (G > 1) wide_cluster_sync();
+  if constexpr (G > 1)
+    wide_cluster_sync();
+  else
+    __syncthreads();
 
-  // ---- check: counts and flags of every CTA; segment offsets ----
+  // ---- check: counts and flags of every CTA ----
   if (t < 32) {
-    uint32_t n = 0, b = 0;
-    if (t < G) {
+    uint32_t n = 0, b = 0, rg = 0;
+    if (lane < static_cast<uint32_t>(G)) {
       if constexpr (G == 1) {
         n = misc[kWN];
         b = misc[kWBad];
+        rg = misc[kWRange];
       } else {
-        n = dsmem_ld_u32(dsmem_addr(&misc[kWN], t));
-        b = dsmem_ld_u32(dsmem_addr(&misc[kWBad], t));
+        n = dsmem_ld_u32(dsmem_addr(&misc[kWN], lane));
+        b = dsmem_ld_u32(dsmem_addr(&misc[kWBad], lane));
+        rg = dsmem_ld_u32(dsmem_addr(&misc[kWRange], lane));
       }
     }
     uint32_t incl = n;
@@ -810,11 +1297,19 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
     }
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const bool any_bad = __any_sync(0xFFFFFFFFu, b != 0);
-    if (t <= G) misc[kWSeg + t] = incl - n;  // exclusive offsets; entry G = total
+    const bool any_range = __any_sync(0xFFFFFFFFu, rg != 0);
+    const bool any_full = __any_sync(0xFFFFFFFFu, n > static_cast<uint32_t>(kWideCandMax));
     if (t == 0) {
-      misc[kWTotal] = total;
-      misc[kWFast] = p.wide_exact ? 0u
-                                  : (any_bad ? 2u : ((total >= k_eff && total <= kWideCandMax) ? 1u : 0u));
+      uint32_t mode = 0u;
+      if (!p.wide_exact) {
+        if (any_bad)
+          mode = 2u;
+        else if (total >= k_eff && total <= 65535u && !any_full && !any_range)
+          mode = 1u;
+        else if (total >= k_eff && total <= static_cast<uint32_t>(kWideCandMax))
+          mode = 3u;  // key range too wide for the per-key counts: gather instead
+      }
+      misc[kWFast] = mode;
     }
   }
   __syncthreads();
@@ -824,6 +1319,17 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
     if (rank == 0 && t == 0) finish_row(p, r, w, -1, kRowNonFinite);
     return;
   }
+  if (mode == 1u) {
+    wide_fast_tail<G>(p, r, w, rank, S, t_key, cand, static_cast<int>(misc[kWN]), lh, mh, misc,
+                      scratch);
+    if constexpr (G > 1) wide_cluster_sync();  // peers read our counts and the leader's counter
+    return;
+  }
+
+  // ---- the rest gathers a candidate set into the leader for the generic
+  // tail: the filter's candidates (mode 3), or the exact top-k set collected
+  // anew by re-reading the slice (mode 0) ----
+  uint32_t *hist = reinterpret_cast<uint32_t *>(work);
   if (mode == 0u) {
     if constexpr (G > 1) wide_cluster_sync();  // peers may still read our counters
     const bool ok = wide_exact_collect<G>(sp, head, nq, tail, rank, k_eff, cand, hist, misc,
@@ -832,30 +1338,29 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
       if (rank == 0 && t == 0) finish_row(p, r, w, -1, kRowNonFinite);
       return;
     }
-    // new counts and offsets
-    if constexpr (G > 1) wide_cluster_sync();
-    if (t < 32) {
-      uint32_t n = 0;
-      if (t < G) {
-        if constexpr (G == 1)
-          n = misc[kWN];
-        else
-          n = dsmem_ld_u32(dsmem_addr(&misc[kWN], t));
-      }
-      uint32_t incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= static_cast<uint32_t>(o)) incl += x;
-      }
-      const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);  // every lane of warp 0
-      if (t <= G) misc[kWSeg + t] = incl - n;
-      if (t == 0) misc[kWTotal] = total;
-    }
-    __syncthreads();
   }
+  if constexpr (G > 1) wide_cluster_sync();
+  if (t < 32) {
+    uint32_t n = 0;
+    if (lane < static_cast<uint32_t>(G)) {
+      if constexpr (G == 1)
+        n = misc[kWN];
+      else
+        n = dsmem_ld_u32(dsmem_addr(&misc[kWN], lane));
+    }
+    uint32_t incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= static_cast<uint32_t>(o)) incl += x;
+    }
+    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);  // every lane of warp 0
+    if (t <= G) misc[kWSeg + t] = incl - n;
+    if (t == 0) misc[kWTotal] = total;
+  }
+  __syncthreads();
 
-  // ---- gather into the leader ----
+  // gather into the leader
   const int n_all = min(static_cast<int>(misc[kWTotal]), kWideCandMax);
   if constexpr (G > 1) {
     if (rank != 0) {
@@ -870,130 +1375,7 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
     if (rank != 0) return;
   }
 
-  // ---- leader tail ----
-  const uint32_t *seg = &misc[kWSeg];
-  uint32_t kmax = 0;
-  for (int i = t; i < n_all; i += kWideThreads) kmax = max(kmax, cand[i] >> 16);
-  const uint32_t maxk = wide_max_u32(kmax, scratch);
-  if (maxk <= KeyBF16::kNegInf) {  // no finite logit among the candidates: none in the row
-    if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
-    return;
-  }
-  // threshold key (the k_eff-th largest) and the kept count tied at it
-  for (int i = t; i < 2048; i += kWideThreads) hist[i] = 0u;
-  if (t < 32) misc[kWHist2 + t] = 0u;
-  __syncthreads();
-  for (int i = t; i < n_all; i += kWideThreads) atomicAdd(&hist[cand[i] >> 21], 1u);
-  __syncthreads();
-  wide_select_top<8, 1>(hist, k_eff, misc, scratch);
-  const uint32_t b1 = misc[kWDigit];
-  const uint32_t above1 = misc[kWAbove];
-  for (int i = t; i < n_all; i += kWideThreads) {
-    const uint32_t key = cand[i] >> 16;
-    if ((key >> 5) == b1) atomicAdd(&misc[kWHist2 + (key & 31u)], 1u);
-  }
-  __syncthreads();
-  uint32_t thr = 0, need = 0;
-  {
-    const uint32_t kk = k_eff - above1;
-    uint32_t c = 0, suf = 0, d2 = 0, above2 = 0;
-    if (t < 32) {
-      c = misc[kWHist2 + t];
-      suf = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
-        if (t + o < 32) suf += x;
-      }
-      d2 = 31u - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk));
-      above2 = __shfl_sync(0xFFFFFFFFu, suf - c, d2);
-      if (t == 0) {
-        misc[kWTKey] = (b1 << 5) | d2;
-        misc[kWTake] = kk - above2;
-      }
-    }
-    __syncthreads();
-    thr = misc[kWTKey];
-    need = misc[kWTake];
-  }
-  const float mval = KeyBF16::value(maxk);
-  const uint32_t u24 = misc[kWU24];
-  uint32_t *mh = hist;  // mass / rank histograms (hist is free again)
-  int32_t id;
-  int n_p = 1;
-  uint64_t s_k = 0;
-  if (w.greedy) {
-    id = static_cast<int32_t>(wide_rank_select(cand, n_all, seg, G, S, maxk, 0u, mh, misc, scratch));
-  } else {
-    uint64_t part = 0;
-    for (int i = t; i < n_all; i += kWideThreads) {
-      const uint32_t key = cand[i] >> 16;
-      if (key > thr) part += to_fixed(kept_weight(KeyBF16::value(key), mval, w.temp, w.inv_temp));
-    }
-    if (t == 0) part += need * to_fixed(kept_weight(KeyBF16::value(thr), mval, w.temp, w.inv_temp));
-    wide_excl_scan_u64(part, scratch, &s_k);
-    uint64_t s_p;
-    if (w.top_p >= 1.0f) {
-      n_p = static_cast<int>(k_eff);
-      s_p = s_k;
-    } else if (!(w.top_p > 0.0f)) {
-      n_p = 1;
-      s_p = to_fixed(kept_weight(mval, mval, w.temp, w.inv_temp));
-    } else {
-      const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
-      uint64_t above;
-      const uint32_t key_c = wide_mass_descent(cand, n_all, maxk, thr, need, mval, w.temp,
-                                               w.inv_temp, true, cut, 0, mh, misc, scratch, &above);
-      const uint64_t wc = to_fixed(kept_weight(KeyBF16::value(key_c), mval, w.temp, w.inv_temp));
-      uint64_t n_c = wc > 0 ? (cut - above + wc - 1) / wc : 1;
-      if (n_c < 1) n_c = 1;
-      uint32_t gt_loc = 0;
-      for (int i = t; i < n_all; i += kWideThreads) gt_loc += (cand[i] >> 16) > key_c;
-      uint64_t n_above;
-      wide_excl_scan_u64(gt_loc, scratch, &n_above);
-      n_p = static_cast<int>(n_above + n_c);
-      s_p = above + n_c * wc;
-    }
-    const uint64_t target = scale_u24(u24, s_p);
-    uint64_t above_d;
-    const uint32_t key_d = wide_mass_descent(cand, n_all, maxk, thr, need, mval, w.temp,
-                                             w.inv_temp, false, 0, target, mh, misc, scratch,
-                                             &above_d);
-    const uint64_t wd = to_fixed(kept_weight(KeyBF16::value(key_d), mval, w.temp, w.inv_temp));
-    const uint32_t rho = wd > 0 ? static_cast<uint32_t>((target - above_d) / wd) : 0u;
-    id = static_cast<int32_t>(wide_rank_select(cand, n_all, seg, G, S, key_d, rho, mh, misc, scratch));
-  }
-  if (t == 0) finish_row(p, r, w, id, 0u);
-  if (p.kept_ids) {
-    // the kept set: keys above thr, and the `need` lowest-index keys at thr
-    const uint32_t idx_cut =
-        need ? wide_rank_select(cand, n_all, seg, G, S, thr, need - 1, mh, misc, scratch) : 0u;
-    if (t == 0) misc[kWN] = 0u;
-    __syncthreads();
-    const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
-    const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
-    int c = 0;
-    for (int i = t; i < n_all; i += kWideThreads) {
-      while (c + 1 < G && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
-      const uint32_t e = cand[i];
-      const uint32_t key = e >> 16;
-      const uint32_t g = wide_gidx(e, c, S);
-      if (key > thr || (key == thr && need && g <= idx_cut)) {
-        const uint32_t pos = atomicAdd(&misc[kWN], 1u);
-        if (pos < static_cast<uint32_t>(p.max_keep)) {
-          p.kept_ids[rb + pos] = static_cast<int32_t>(g);
-          p.kept_probs[rb + pos] =
-              w.greedy ? (static_cast<int32_t>(g) == id ? 1.f : 0.f)
-                       : __fdiv_rn(kept_weight(KeyBF16::value(key), mval, w.temp, w.inv_temp),
-                                   s_real);
-        }
-      }
-    }
-    if (t == 0) {
-      p.n_kept[r] = static_cast<int32_t>(k_eff);
-      p.n_nucleus[r] = n_p;
-    }
-  }
+  wide_gather_tail<G>(p, r, w, cand, n_all, &misc[kWSeg], S, hist, misc, scratch);
 }
 
 }  // namespace ts
