@@ -83,7 +83,7 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
     pl->g = g;
     pl->slice = slice;
     pl->threads = ts::kWideThreads;
-    pl->smem = static_cast<int>(ts::kWideSmemBytes);
+    pl->smem = static_cast<int>(ts::wide_smem_bytes(g));
     pl->grid = b->n_rows * g;
     return TS_OK;
   }

@@ -45,7 +45,8 @@ namespace ts {
 
 constexpr int kWideThreads = 256;
 constexpr int kWideWarps = kWideThreads / 32;
-constexpr int kWideCandMax = 8192;        // candidate entries per CTA (32 KB)
+constexpr int kWideCandMax = 8192;        // candidate entries per CTA, G <= 2 (32 KB)
+constexpr int kWideCandMaxWide = 4096;    // ... G >= 4 (16 KB)
 constexpr int kWideU = 4;                 // 16-byte chunks per lane per iteration
 constexpr int kWideRing = 64;             // staged words per warp (a ring)
 constexpr int kWideSampleChunks = 512;    // 4,096 sampled logits
@@ -53,14 +54,20 @@ constexpr int kWideSliceMax = 65536;      // slice index fits 16 bits
 constexpr int kWideBins = 2048;           // per-key counts: keys t .. t + 2047
 constexpr int kWideMaxG = 16;
 // work area: [staging rings 4 KB][per-key counts, packed 16-bit pairs 4 KB]
-//            [merge / sample histogram 8 KB][spare 4 KB]; the exact path
-//            reuses all of it from offset 0 once the fast path is abandoned
+//            [sample / rank-select histogram 8 KB][counts by key >> 8 1 KB]
+//            [spare 1 KB]; the exact path and the distributed tail reuse the
+//            first 8 KB once the filter is done with it
 constexpr uint32_t kWideRingBytes = kWideWarps * kWideRing * 8;
 constexpr uint32_t kWideLhOff = kWideRingBytes;
 constexpr uint32_t kWideMhOff = kWideLhOff + kWideBins * 2;
-constexpr uint32_t kWideWorkBytes = 20480;
+constexpr uint32_t kWidePgOff = kWideMhOff + 8192;  // candidate counts by key >> 8 (256)
+constexpr uint32_t kWideWorkBytes = 18432;
 constexpr uint32_t kWideMiscWords = 256;
-constexpr uint32_t kWideSmemBytes = kWideCandMax * 4 + kWideWorkBytes + kWideMiscWords * 4;
+// candidate entries each CTA holds; CTAs of a cluster never pool them
+__host__ __device__ constexpr int wide_cap(int g) { return g >= 4 ? kWideCandMaxWide : kWideCandMax; }
+__host__ __device__ constexpr uint32_t wide_smem_bytes(int g) {
+  return static_cast<uint32_t>(wide_cap(g)) * 4u + kWideWorkBytes + kWideMiscWords * 4u;
+}
 
 // misc word slots
 constexpr int kWN = 0;        // local candidate count (may exceed the buffer)
@@ -192,60 +199,6 @@ __device__ void wide_select_top(const uint32_t *h, uint32_t kk, uint32_t *misc,
   __syncthreads();
 }
 
-// Position p of the leader's candidate buffer came from CTA seg_of(p); the
-// segments are contiguous and in CTA order.
-__device__ __forceinline__ uint32_t wide_gidx(uint32_t e, int c, int S) {
-  return static_cast<uint32_t>(c * S) + (e & 0xFFFFu);
-}
-
-// The rho-th smallest (0-based) token index among candidates with key
-// `key_sel`, by a two-level radix select on the 18-bit token index (512 bins
-// per level).  Order-free.
-__device__ uint32_t wide_rank_select(const uint32_t *cand, int n, const uint32_t *seg, int G,
-                                     int S, uint32_t key_sel, uint32_t rho, uint32_t *h,
-                                     uint32_t *misc, uint64_t *scratch) {
-  const int t = static_cast<int>(threadIdx.x);
-  uint32_t b1 = 0, below = 0;
-#pragma unroll 1
-  for (int level = 0; level < 2; ++level) {
-    __syncthreads();
-    for (int i = t; i < 512; i += kWideThreads) h[i] = 0u;
-    __syncthreads();
-    int c = 0;
-    for (int i = t; i < n; i += kWideThreads) {
-      while (c + 1 < G && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
-      const uint32_t e = cand[i];
-      if ((e >> 16) != key_sel) continue;
-      const uint32_t g = wide_gidx(e, c, S);
-      if (level == 0)
-        atomicAdd(&h[g >> 9], 1u);
-      else if ((g >> 9) == b1)
-        atomicAdd(&h[g & 511u], 1u);
-    }
-    __syncthreads();
-    // ascending select: the bin where the running count first exceeds rho'
-    const uint32_t want = rho - below;
-    const uint32_t h0 = h[2 * t], h1 = h[2 * t + 1];
-    uint64_t tot;
-    const uint32_t ex = static_cast<uint32_t>(wide_excl_scan_u64(h0 + h1, scratch, &tot));
-    if (ex <= want && want < ex + h0) {
-      misc[kWDigit] = 2 * t;
-      misc[kWAbove] = ex;
-    } else if (ex + h0 <= want && want < ex + h0 + h1) {
-      misc[kWDigit] = 2 * t + 1;
-      misc[kWAbove] = ex + h0;
-    }
-    __syncthreads();
-    if (level == 0) {
-      b1 = misc[kWDigit];
-      below += misc[kWAbove];
-    } else {
-      return (b1 << 9) | misc[kWDigit];
-    }
-  }
-  return 0;
-}
-
 // Exact r-th largest canonical key of an evenly spaced sample of the row
 // (every CTA of the cluster computes the same value from the same sample).
 // Returns 0 ("every element") when the sample cannot give a useful bound.
@@ -260,7 +213,7 @@ __device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, in
   if (n_chunks <= 0) return 0u;
   // r such that about 1.6 k_eff row elements (at most 3/4 of the cluster's
   // candidate buffers) are expected at or above it
-  const long long expect10 = min(16ll * k_eff, 75ll * kWideCandMax * G / 10);
+  const long long expect10 = min(16ll * k_eff, 75ll * wide_cap(G) * G / 10);
   const long long want = (expect10 * n_s + 10ll * V - 1) / (10ll * V);
   const int r = static_cast<int>(max(32ll, want));
   if (r > n_s) return 0u;
@@ -334,14 +287,18 @@ __device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, in
   return tk;
 }
 
-// One candidate: its entry (key << 16 | slice index) and its per-key count.
+// One candidate: its entry (key << 16 | slice index), its per-key count, its
+// count by key >> 8 and the running maximum key.
 // The count keeps growing past the buffer (the caller compares it with
-// kWideCandMax) and the entry is then dropped; a key beyond the counted
+// the capacity) and the entry is then dropped; a key beyond the counted
 // window raises `range`.
 __device__ __forceinline__ void wide_keep(uint32_t key, uint32_t idx, uint32_t pos,
-                                          uint32_t t_key, uint32_t *cand, uint32_t *lh,
-                                          uint32_t &range) {
-  if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = (key << 16) | idx;
+                                          uint32_t t_key, uint32_t *cand, uint32_t cap,
+                                          uint32_t *lh, uint32_t *pg, uint32_t &range,
+                                          uint32_t &kmax) {
+  if (pos < cap) cand[pos] = (key << 16) | idx;
+  atomicAdd(&pg[key >> 8], 1u);
+  kmax = max(kmax, key);
   const uint32_t off = key - t_key;
   if (off < static_cast<uint32_t>(kWideBins))
     atomicAdd(&lh[off >> 1], 1u << ((off & 1u) * 16u));
@@ -353,8 +310,9 @@ __device__ __forceinline__ void wide_keep(uint32_t key, uint32_t idx, uint32_t p
 // takes entry head + l; every element with key >= t_key becomes a
 // candidate.  NaN / +inf keys raise `bad`.
 __device__ __forceinline__ void wide_drain(const uint2 *ring, uint32_t head, uint32_t n,
-                                           uint32_t t_key, uint32_t *cand, uint32_t *lh,
-                                           uint32_t *counter, uint32_t &bad, uint32_t &range) {
+                                           uint32_t t_key, uint32_t *cand, uint32_t cap,
+                                           uint32_t *lh, uint32_t *pg, uint32_t *counter,
+                                           uint32_t &bad, uint32_t &range, uint32_t &kmax) {
   const uint32_t lane = lane_id();
   bool f0 = false, f1 = false;
   uint32_t k0 = 0, k1 = 0, idx0 = 0;
@@ -378,26 +336,28 @@ __device__ __forceinline__ void wide_drain(const uint2 *ring, uint32_t head, uin
   base = __shfl_sync(0xFFFFFFFFu, base, 0);
   const uint32_t lt = lanemask_lt();
   const uint32_t pos = base + __popc(b0 & lt) + __popc(b1 & lt);
-  if (f0) wide_keep(k0, idx0, pos, t_key, cand, lh, range);
-  if (f1) wide_keep(k1, idx0 + 1u, pos + (f0 ? 1u : 0u), t_key, cand, lh, range);
+  if (f0) wide_keep(k0, idx0, pos, t_key, cand, cap, lh, pg, range, kmax);
+  if (f1) wide_keep(k1, idx0 + 1u, pos + (f0 ? 1u : 0u), t_key, cand, cap, lh, pg, range, kmax);
 }
 
 // One element of a slice's unaligned head or tail.
 __device__ __forceinline__ void wide_append_one(const char *sp, int idx, uint32_t t_key,
-                                                uint32_t *cand, uint32_t *lh, uint32_t *counter,
-                                                uint32_t &bad, uint32_t &range) {
+                                                uint32_t *cand, uint32_t cap, uint32_t *lh,
+                                                uint32_t *pg, uint32_t *counter, uint32_t &bad,
+                                                uint32_t &range, uint32_t &kmax) {
   const uint32_t k = wkey(KeyBF16::load_one(sp, idx));
   const bool nonfinite = k < KeyBF16::kNegInf || k >= KeyBF16::kPosInf;
   bad |= nonfinite;
   if (!nonfinite && k >= t_key)
-    wide_keep(k, static_cast<uint32_t>(idx), atomicAdd(counter, 1u), t_key, cand, lh, range);
+    wide_keep(k, static_cast<uint32_t>(idx), atomicAdd(counter, 1u), t_key, cand, cap, lh, pg,
+              range, kmax);
 }
 
-// Appends one entry; the count keeps growing past the buffer (callers
-// compare it with kWideCandMax), the entry is dropped.
+// Appends one entry of the exact path (at most k_eff <= 4096 per CTA, so
+// within every capacity); out-of-range positions are dropped defensively.
 __device__ __forceinline__ void wide_put(uint32_t *cand, uint32_t *counter, uint32_t e) {
   const uint32_t pos = atomicAdd(counter, 1u);
-  if (pos < static_cast<uint32_t>(kWideCandMax)) cand[pos] = e;
+  if (pos < static_cast<uint32_t>(kWideCandMaxWide)) cand[pos] = e;
 }
 
 // Exact path of a cluster (rare: the sample's threshold left fewer than
@@ -410,7 +370,7 @@ __device__ __forceinline__ void wide_put(uint32_t *cand, uint32_t *counter, uint
 // (the caller reports the error), true otherwise.
 template <int G>
 __device__ bool wide_exact_collect(const char *sp, int head, int nq, int tail, uint32_t rank,
-                                   uint32_t k_eff, uint32_t *cand, uint32_t *hist,
+                                   uint32_t k_eff, uint32_t *cand, uint32_t *hist, uint32_t *pg,
                                    uint32_t *misc, uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
   const char *body = sp + 2 * head;
@@ -522,11 +482,18 @@ __device__ bool wide_exact_collect(const char *sp, int head, int nq, int tail, u
       misc[kWN] = 0u;
     }
   }
+  pg[threadIdx.x] = 0u;  // kWideThreads == 256 page counts, rebuilt for the exact set
   __syncthreads();
   if constexpr (G > 1) wide_cluster_sync();  // peers are done reading our histograms
   const uint32_t thr = misc[kWTKey];
   const uint32_t take = misc[kWTake];
   uint32_t *counter = &misc[kWN];
+  uint32_t kmax = 0;
+  auto put = [&](uint32_t k, uint32_t idx) {
+    wide_put(cand, counter, (k << 16) | idx);
+    atomicAdd(&pg[k >> 8], 1u);
+    kmax = max(kmax, k);
+  };
   // pass 3: collect.  Keys above thr in any order; keys equal to thr in
   // index order until `take` of them.  Head elements first (thread 0, in
   // order), then the body in rounds of kWideThreads chunks, then the tail.
@@ -536,7 +503,7 @@ __device__ bool wide_exact_collect(const char *sp, int head, int nq, int tail, u
       const uint32_t k = wkey(KeyBF16::load_one(sp, idx));
       bool keep = k > thr;
       if (k == thr) keep = eq_seen++ < take;
-      if (keep) wide_put(cand, counter, (k << 16) | static_cast<uint32_t>(idx));
+      if (keep) put(k, static_cast<uint32_t>(idx));
     }
     misc[kWEq] = eq_seen;
   }
@@ -571,7 +538,7 @@ __device__ bool wide_exact_collect(const char *sp, int head, int nq, int tail, u
       for (int e = 0; e < 8; ++e) {
         bool keep = k[e] > thr;
         if (k[e] == thr) keep = er++ < take;
-        if (keep) wide_put(cand, counter, (k[e] << 16) | (idx0 + e));
+        if (keep) put(k[e], idx0 + e);
       }
     }
     eq_seen += static_cast<uint32_t>(tot);
@@ -583,9 +550,11 @@ __device__ bool wide_exact_collect(const char *sp, int head, int nq, int tail, u
       const uint32_t k = wkey(KeyBF16::load_one(sp, idx));
       bool keep = k > thr;
       if (k == thr) keep = eq_seen++ < take;
-      if (keep) wide_put(cand, counter, (k << 16) | static_cast<uint32_t>(idx));
+      if (keep) put(k, static_cast<uint32_t>(idx));
     }
   }
+  kmax = wide_max_u32(kmax, scratch);
+  if (threadIdx.x == 0) misc[kWMaxK] = kmax;
   __syncthreads();
   return true;
 }
@@ -861,21 +830,91 @@ __device__ void wide_fast_tail(const Params &p, int r, const Row &w, uint32_t ra
   }
 }
 
-// Exact second level of the gathered tail: inside coarse bin `bin` (keys
-// maxk - (bin << shift) - j, j < 2^shift <= 64) counts the kept tokens per
-// key, weighs them, and finds the key where the cumulative mass (from the
-// top, starting at `above`) first reaches `goal` (cut_mode: >= goal) or first
-// exceeds it (else).  Writes the key, the mass above it and the kept count
-// above it inside the bin to misc.
-__device__ void wide_level2(const uint32_t *cand, int n, uint32_t maxk, uint32_t thr,
-                            uint32_t need, int shift, uint32_t bin, float m, float temp,
-                            float inv_temp, bool cut_mode, uint64_t goal, uint64_t above,
-                            uint32_t *l2, uint32_t *misc) {
-  const int t = static_cast<int>(threadIdx.x);
-  const uint32_t lane = lane_id();
-  uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
+// Reads word `i` of CTA c's shared array `a` (c == this CTA when G == 1).
+template <int G>
+__device__ __forceinline__ uint32_t wide_peer_u32(const uint32_t *a, int i, int c) {
+  if constexpr (G == 1)
+    return a[i];
+  else
+    return dsmem_ld_u32(dsmem_addr(&a[i], c));
+}
+template <int G>
+__device__ __forceinline__ uint4 wide_peer_v4(const uint32_t *a, int i, int c) {
+  if constexpr (G == 1)
+    return *reinterpret_cast<const uint4 *>(&a[i]);
+  else
+    return dsmem_ld_v4(dsmem_addr(&a[i], c));
+}
+
+// Cluster barrier (or a block barrier for a single CTA).
+template <int G>
+__device__ __forceinline__ void wide_sync_all() {
+  if constexpr (G > 1)
+    wide_cluster_sync();
+  else
+    __syncthreads();
+}
+
+// Sum over the G CTAs of word i of the shared arrays a[0..N-1]; every
+// remote load is issued before any is used.
+template <int G, int N>
+__device__ __forceinline__ void wide_sum_peers(const uint32_t *const (&a)[N], int i,
+                                               uint32_t (&out)[N]) {
+  if constexpr (G == 1) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) out[j] = a[j][i];
+  } else {
+    uint32_t v[N][G];
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(&a[j][i]));
+#pragma unroll
+      for (int c = 0; c < G; ++c) {
+        uint32_t ra;
+        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(base), "r"(c));
+        v[j][c] = dsmem_ld_u32(ra);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      uint32_t sum = 0;
+#pragma unroll
+      for (int c = 0; c < G; ++c) sum += v[j][c];
+      out[j] = sum;
+    }
+  }
+}
+
+template <int G>
+__device__ __forceinline__ uint32_t wide_sum_peers1(const uint32_t *a, int i) {
+  const uint32_t *arr[1] = {a};
+  uint32_t out[1];
+  wide_sum_peers<G, 1>(arr, i, out);
+  return out[0];
+}
+
+// 256 bins in ascending key order, bin t held by thread t: the bin holding
+// the kk-th largest element (bin -> misc[kWDigit], count above it ->
+// misc[kWAbove]).  Ends with a block barrier.
+__device__ __forceinline__ void wide_select256(uint32_t c, uint32_t kk, uint32_t *misc,
+                                               uint64_t *scratch) {
+  uint64_t tot;
+  const uint32_t ex = static_cast<uint32_t>(wide_excl_scan_u64(c, scratch, &tot));
+  const uint32_t above = static_cast<uint32_t>(tot) - ex - c;
+  if (c != 0 && above < kk && above + c >= kk) {
+    misc[kWDigit] = threadIdx.x;
+    misc[kWAbove] = above;
+  }
   __syncthreads();
-  if (t < 64) l2[t] = 0u;
+}
+
+// This CTA's kept-key counts inside coarse bin `bin` (keys maxk - (bin <<
+// shift) - j, j < 2^shift <= 256; the key at thr is counted apart).
+__device__ __forceinline__ void wide_local_level2(const uint32_t *cand, int n, uint32_t maxk,
+                                                  uint32_t thr, int shift, uint32_t bin,
+                                                  uint32_t *l2) {
+  const int t = static_cast<int>(threadIdx.x);
+  l2[t] = 0u;
   __syncthreads();
 #pragma unroll 4
   for (int i = t; i < n; i += kWideThreads) {
@@ -883,161 +922,157 @@ __device__ void wide_level2(const uint32_t *cand, int n, uint32_t maxk, uint32_t
     const uint32_t off = maxk - key;
     if (key > thr && (off >> shift) == bin) atomicAdd(&l2[off & ((1u << shift) - 1u)], 1u);
   }
-  if (t == 0 && need && ((maxk - thr) >> shift) == bin)
-    atomicAdd(&l2[(maxk - thr) & ((1u << shift) - 1u)], need);
-  __syncthreads();
-  if (t < 32) {
-    const uint32_t base = maxk - (bin << shift);
-    uint64_t ms[2];
-    uint32_t cs[2];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const uint32_t j = 2 * lane + x;
-      cs[x] = j < (1u << shift) ? l2[j] : 0u;
-      ms[x] = cs[x] ? cs[x] * to_fixed(kept_weight(KeyBF16::value(base - j), m, temp, inv_temp))
-                    : 0ull;
-    }
-    uint64_t incl = ms[0] + ms[1];
-    uint32_t cincl = cs[0] + cs[1];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint64_t a = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      const uint32_t b = __shfl_up_sync(0xFFFFFFFFu, cincl, o);
-      if (lane >= static_cast<uint32_t>(o)) {
-        incl += a;
-        cincl += b;
-      }
-    }
-    uint64_t cum = above + incl - ms[0] - ms[1];
-    uint32_t ccum = cincl - cs[0] - cs[1];
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-      const uint64_t nxt = cum + ms[x];
-      const bool hit = cut_mode ? (cum < goal && nxt >= goal) : (cum <= goal && goal < nxt);
-      if (hit) {
-        misc[kWDigit] = base - (2 * lane + x);
-        m64[kWSp / 2] = cum;
-        misc[kWCount] = ccum;
-      }
-      cum = nxt;
-      ccum += cs[x];
-    }
+}
+
+// Merged second level: thread j weighs key base - j (the G CTAs' counts plus
+// the `need` kept tokens at thr); finds the key where the cumulative mass
+// from the top (starting at `above`) first reaches `goal` (cut_mode) or first
+// exceeds it.  Writes the key, the mass above it and the kept count above it
+// inside the bin to misc.  Ends with a block barrier.
+template <int G>
+__device__ void wide_merge_level2(const uint32_t *l2, uint32_t maxk, uint32_t thr, uint32_t need,
+                                  int shift, uint32_t bin, float m, float temp, float inv_temp,
+                                  bool cut_mode, uint64_t goal, uint64_t above, uint32_t *misc,
+                                  uint64_t *scratch) {
+  const uint32_t j = threadIdx.x;
+  uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
+  const uint32_t base = maxk - (bin << shift);
+  uint32_t c = 0;
+  if (j < (1u << shift)) {
+    c = wide_sum_peers1<G>(l2, static_cast<int>(j));
+    if (((maxk - thr) >> shift) == bin && j == ((maxk - thr) & ((1u << shift) - 1u))) c += need;
+  }
+  const uint64_t ms = c ? c * to_fixed(kept_weight(KeyBF16::value(base - j), m, temp, inv_temp)) : 0ull;
+  uint64_t tm, tc;
+  const uint64_t cum = above + wide_excl_scan_u64(ms, scratch, &tm);
+  const uint32_t ccum = static_cast<uint32_t>(wide_excl_scan_u64(c, scratch, &tc));
+  const uint64_t nxt = cum + ms;
+  const bool hit = cut_mode ? (cum < goal && nxt >= goal) : (cum <= goal && goal < nxt);
+  if (hit) {
+    misc[kWDigit] = base - j;
+    m64[kWSp / 2] = cum;
+    misc[kWCount] = ccum;
   }
   __syncthreads();
 }
 
-// Gathered tail (one CTA holds every candidate; any key range): the
-// threshold key and the kept count tied at it by radix select on the keys;
-// then a coarse histogram of the kept masses over (max key - key) >> shift
-// (the only pass that evaluates exp per token), which gives S_k and the
-// coarse bins of the nucleus cutoff and of the draw; an exact second level
-// inside each of those two bins; the token by a radix select on the index.
+// Distributed tail (any key range).  Every CTA of the cluster keeps its own
+// candidates (together a superset of the top-k set that holds every key
+// tied with the k_eff-th largest); each pass runs over the CTA's own
+// candidates and 256-bin histograms are merged through distributed shared
+// memory, every CTA reaching the same decisions:
+//   1. counts by key >> 8 (built during the filter) -> the threshold's page;
+//   2. the low key byte inside that page -> the threshold key thr and
+//      `need`, the kept tokens tied at it (the lowest indices of the row);
+//   3. kept masses and counts over (maxk - key) >> shift (256 coarse bins;
+//      the only pass that evaluates exp per token) -> S_k and the coarse
+//      bins of the nucleus cutoff and of the draw;
+//   4. an exact level inside each of those two bins (when shift > 0);
+//   5. the CTA holding the drawn token (index order = CTA order) picks it by
+//      a radix select on its slice index.
+// The caller ends with a cluster barrier (peers read this CTA's histograms).
 template <int G>
-__device__ void wide_gather_tail(const Params &p, int r, const Row &w, const uint32_t *cand,
-                                 int n, const uint32_t *seg, int S, uint32_t *hw,
-                                 uint32_t *misc, uint64_t *scratch) {
+__device__ void wide_dist_tail(const Params &p, int r, const Row &w, uint32_t rank, int S,
+                               const uint32_t *cand, int n, uint32_t *hw, const uint32_t *pg,
+                               uint32_t *misc, uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
+  const uint32_t lane = lane_id();
   const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
   uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
-  // ---- counts by key >> 5 and the maximum key ----
-  for (int i = t; i < 2048; i += kWideThreads) hw[i] = 0u;
-  if (t < 32) misc[kWHist2 + t] = 0u;
-  __syncthreads();
-  uint32_t kmax = 0;
-#pragma unroll 4
-  for (int i = t; i < n; i += kWideThreads) {
-    const uint32_t key = cand[i] >> 16;
-    atomicAdd(&hw[key >> 5], 1u);
-    kmax = max(kmax, key);
+  uint32_t *bB = hw;  // low key bytes inside the threshold's page
+  uint32_t *plo = hw + 256, *pmid = hw + 512, *phi = hw + 768, *pcnt = hw + 1024;
+  uint32_t *lD = hw + 1280;  // second level of the cutoff's coarse bin
+  uint32_t *lE = hw + 1536;  // second level of the draw's coarse bin
+  uint32_t *rs = hw + 1792;  // rank select
+
+  // ---- 1. the threshold's page, the maximum key ----
+  bB[t] = 0u;
+  const uint32_t cpage = wide_sum_peers1<G>(pg, t);
+  if (t < 32) {
+    uint32_t mk = 0;
+    if (lane < static_cast<uint32_t>(G)) mk = wide_peer_u32<G>(misc, kWMaxK, static_cast<int>(lane));
+    mk = __reduce_max_sync(0xFFFFFFFFu, mk);
+    if (t == 0) misc[kWMaxB] = mk;
   }
-  const uint32_t maxk = wide_max_u32(kmax, scratch);
+  wide_select256(cpage, k_eff, misc, scratch);
+  const uint32_t maxk = misc[kWMaxB];
   if (maxk <= KeyBF16::kNegInf) {  // every candidate is -inf: no finite logit in the row
-    if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
+    if (rank == 0 && t == 0) finish_row(p, r, w, -1, kRowNonFinite);
     return;
   }
-  wide_select_top<8, 1>(hw, k_eff, misc, scratch);
-  const uint32_t b1 = misc[kWDigit];
-  const uint32_t above1 = misc[kWAbove];
+  const uint32_t page = misc[kWDigit];
+  const uint32_t kk = k_eff - misc[kWAbove];
+  // ---- 2. the threshold key inside that page ----
 #pragma unroll 4
   for (int i = t; i < n; i += kWideThreads) {
     const uint32_t key = cand[i] >> 16;
-    if ((key >> 5) == b1) atomicAdd(&misc[kWHist2 + (key & 31u)], 1u);
+    if ((key >> 8) == page) atomicAdd(&bB[key & 255u], 1u);
+  }
+  wide_sync_all<G>();
+  wide_select256(wide_sum_peers1<G>(bB, t), kk, misc, scratch);
+  const uint32_t lowb = misc[kWDigit];
+  const uint32_t thr = (page << 8) | lowb;
+  const uint32_t need = kk - misc[kWAbove];
+  if (t < 32) {  // keys at thr in lower-ranked CTAs (lower token indices)
+    uint32_t eb = 0;
+    if (lane < rank) eb = wide_peer_u32<G>(bB, static_cast<int>(lowb), static_cast<int>(lane));
+    eb = __reduce_add_sync(0xFFFFFFFFu, eb);
+    if (t == 0) misc[kWEq] = eb;
   }
   __syncthreads();
-  if (t < 32) {
-    const uint32_t kk = k_eff - above1;
-    const uint32_t c = misc[kWHist2 + t];
-    uint32_t suf = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_down_sync(0xFFFFFFFFu, suf, o);
-      if (t + o < 32) suf += x;
-    }
-    const uint32_t d2 = 31u - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk));
-    const uint32_t above2 = __shfl_sync(0xFFFFFFFFu, suf - c, d2);
-    if (t == 0) {
-      misc[kWTKey] = (b1 << 5) | d2;
-      misc[kWTake] = kk - above2;
-    }
-  }
-  __syncthreads();
-  const uint32_t thr = misc[kWTKey];
-  const uint32_t need = misc[kWTake];
+  const uint32_t eq_before = misc[kWEq], eq_mine = bB[lowb];
   const float m = KeyBF16::value(maxk);
   const uint32_t u24 = misc[kWU24];
-  int32_t id;
-  uint32_t n_p = 1;
+  uint32_t key_d = maxk, rho = 0, n_p = 1;
   uint64_t s_k = 0;
-  if (w.greedy) {
-    id = static_cast<int32_t>(wide_rank_select(cand, n, seg, G, S, maxk, 0u, hw, misc, scratch));
-  } else {
-    // ---- coarse kept masses and counts over (maxk - key) >> shift ----
+  int shift = 0;
+  uint32_t d1 = 0;
+  if (!w.greedy) {
+    // ---- 3. coarse kept masses and counts over (maxk - key) >> shift ----
     const uint32_t range = maxk - thr;
     const int bits = range ? 32 - __clz(range) : 0;
-    const int shift = bits > 10 ? bits - 10 : 0;
-    uint32_t *plo = hw, *pmid = hw + 1024, *phi = hw + 2048, *pcnt = hw + 3072;
+    shift = bits > 8 ? bits - 8 : 0;
+    plo[t] = 0u;
+    pmid[t] = 0u;
+    phi[t] = 0u;
+    pcnt[t] = 0u;
     __syncthreads();
-    for (int i = t; i < 4096; i += kWideThreads) hw[i] = 0u;
-    __syncthreads();
-    auto add = [&](uint32_t key, uint32_t cnt) {
+#pragma unroll 4
+    for (int i = t; i < n; i += kWideThreads) {
+      const uint32_t key = cand[i] >> 16;
+      if (key <= thr) continue;
       const uint32_t d = (maxk - key) >> shift;
-      atomicAdd(&pcnt[d], cnt);
+      atomicAdd(&pcnt[d], 1u);
       if (shift) {
-        const uint64_t f = cnt * to_fixed(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp));
+        const uint64_t f = to_fixed(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp));
         if (f) {
           atomicAdd(&plo[d], static_cast<uint32_t>(f & 0x1FFFu));
           atomicAdd(&pmid[d], static_cast<uint32_t>((f >> 13) & 0x1FFFu));
           atomicAdd(&phi[d], static_cast<uint32_t>(f >> 26));
         }
       }
-    };
-#pragma unroll 4
-    for (int i = t; i < n; i += kWideThreads) {
-      const uint32_t key = cand[i] >> 16;
-      if (key > thr) add(key, 1u);
     }
-    if (t == 0 && need) add(thr, need);
-    __syncthreads();
-    uint64_t ms[4];
-    uint32_t cs[4];
-    uint64_t st = 0;
-    uint32_t ct = 0;
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const uint32_t d = static_cast<uint32_t>(4 * t + x);
-      cs[x] = pcnt[d];
-      if (shift == 0)
-        ms[x] = cs[x] ? cs[x] * to_fixed(kept_weight(KeyBF16::value(maxk - d), m, w.temp, w.inv_temp))
-                      : 0ull;
-      else
-        ms[x] = (static_cast<uint64_t>(phi[d]) << 26) + (static_cast<uint64_t>(pmid[d]) << 13) +
-                plo[d];
-      st += ms[x];
-      ct += cs[x];
+    wide_sync_all<G>();
+    const uint32_t dthr = (maxk - thr) >> shift;
+    uint32_t cs;
+    uint64_t ms;
+    if (shift == 0) {
+      cs = wide_sum_peers1<G>(pcnt, t) + (static_cast<uint32_t>(t) == dthr ? need : 0u);
+      ms = cs ? cs * to_fixed(kept_weight(KeyBF16::value(maxk - t), m, w.temp, w.inv_temp)) : 0ull;
+    } else {
+      const uint32_t *arr[4] = {pcnt, plo, pmid, phi};
+      uint32_t v[4];
+      wide_sum_peers<G, 4>(arr, t, v);
+      cs = v[0];
+      ms = (static_cast<uint64_t>(v[3]) << 26) + (static_cast<uint64_t>(v[2]) << 13) + v[1];
+      if (static_cast<uint32_t>(t) == dthr && need) {
+        cs += need;
+        ms += need * to_fixed(kept_weight(KeyBF16::value(thr), m, w.temp, w.inv_temp));
+      }
     }
-    const uint64_t cum_t = wide_excl_scan_u64(st, scratch, &s_k);
+    const uint64_t cum_t = wide_excl_scan_u64(ms, scratch, &s_k);
     uint64_t n_all64;
-    const uint32_t ccum_t = static_cast<uint32_t>(wide_excl_scan_u64(ct, scratch, &n_all64));
+    const uint32_t ccum_t = static_cast<uint32_t>(wide_excl_scan_u64(cs, scratch, &n_all64));
     // ---- nucleus cutoff ----
     uint64_t s_p;
     if (w.top_p >= 1.0f) {
@@ -1048,19 +1083,10 @@ __device__ void wide_gather_tail(const Params &p, int r, const Row &w, const uin
       s_p = to_fixed(kept_weight(m, m, w.temp, w.inv_temp));
     } else {
       const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
-      {
-        uint64_t cum = cum_t;
-        uint32_t ccum = ccum_t;
-#pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          if (cum < cut && cum + ms[x] >= cut) {
-            misc[kWThrB] = static_cast<uint32_t>(4 * t + x);
-            m64[kWWide / 2] = cum;
-            misc[kWNeed] = ccum;
-          }
-          cum += ms[x];
-          ccum += cs[x];
-        }
+      if (cum_t < cut && cum_t + ms >= cut) {
+        misc[kWThrB] = static_cast<uint32_t>(t);
+        m64[kWWide / 2] = cum_t;
+        misc[kWNeed] = ccum_t;
       }
       __syncthreads();
       const uint32_t c1 = misc[kWThrB];
@@ -1074,8 +1100,10 @@ __device__ void wide_gather_tail(const Params &p, int r, const Row &w, const uin
         above_k = above_c;
         cnt_k = cnt_c;
       } else {
-        wide_level2(cand, n, maxk, thr, need, shift, c1, m, w.temp, w.inv_temp, true, cut,
-                    above_c, hw + 4096, misc);
+        wide_local_level2(cand, n, maxk, thr, shift, c1, lD);
+        wide_sync_all<G>();
+        wide_merge_level2<G>(lD, maxk, thr, need, shift, c1, m, w.temp, w.inv_temp, true, cut,
+                             above_c, misc, scratch);
         key_c = misc[kWDigit];
         above_k = m64[kWSp / 2];
         cnt_k = cnt_c + misc[kWCount];
@@ -1085,65 +1113,105 @@ __device__ void wide_gather_tail(const Params &p, int r, const Row &w, const uin
       if (n_c < 1) n_c = 1;
       n_p = cnt_k + static_cast<uint32_t>(n_c);
       s_p = above_k + n_c * wc;
-      __syncthreads();  // everyone has read misc before it is reused
+      __syncthreads();  // misc is read before it is reused
     }
     // ---- draw ----
     const uint64_t target = scale_u24(u24, s_p);
-    {
-      uint64_t cum = cum_t;
-#pragma unroll
-      for (int x = 0; x < 4; ++x) {
-        if (cum <= target && target < cum + ms[x]) {
-          misc[kWDrawB] = static_cast<uint32_t>(4 * t + x);
-          m64[kWWide / 2] = cum;
-        }
-        cum += ms[x];
-      }
+    if (cum_t <= target && target < cum_t + ms) {
+      misc[kWDrawB] = static_cast<uint32_t>(t);
+      m64[kWWide / 2] = cum_t;
     }
     __syncthreads();
-    const uint32_t d1 = misc[kWDrawB];
-    const uint64_t above_d1 = m64[kWWide / 2];
-    uint32_t key_d;
-    uint64_t above_d;
+    d1 = misc[kWDrawB];
+    uint64_t above_d = m64[kWWide / 2];
     if (shift == 0) {
       key_d = maxk - d1;
-      above_d = above_d1;
     } else {
-      wide_level2(cand, n, maxk, thr, need, shift, d1, m, w.temp, w.inv_temp, false, target,
-                  above_d1, hw + 4096, misc);
+      wide_local_level2(cand, n, maxk, thr, shift, d1, lE);
+      wide_sync_all<G>();
+      wide_merge_level2<G>(lE, maxk, thr, need, shift, d1, m, w.temp, w.inv_temp, false, target,
+                           above_d, misc, scratch);
       key_d = misc[kWDigit];
       above_d = m64[kWSp / 2];
     }
     const uint64_t wd = to_fixed(kept_weight(KeyBF16::value(key_d), m, w.temp, w.inv_temp));
-    const uint32_t rho = wd > 0 ? static_cast<uint32_t>((target - above_d) / wd) : 0u;
-    id = static_cast<int32_t>(wide_rank_select(cand, n, seg, G, S, key_d, rho, hw, misc, scratch));
+    rho = wd > 0 ? static_cast<uint32_t>((target - above_d) / wd) : 0u;
   }
-  if (t == 0) finish_row(p, r, w, id, 0u);
-  if (p.kept_ids) {
-    // the kept set: keys above thr, and the `need` lowest-index keys at thr
-    const uint32_t idx_cut =
-        need ? wide_rank_select(cand, n, seg, G, S, thr, need - 1, hw, misc, scratch) : 0u;
-    if (t == 0) misc[kWN] = 0u;
+  // ---- 5. the CTA holding the drawn token ----
+  // per-CTA counts of key_d: in the threshold's page the low-byte counts;
+  // above it the coarse counts (one key per bin when shift == 0) or the
+  // draw bin's second level.  A greedy row whose maximum lies above the
+  // threshold's page counts its maximum in one more local pass.
+  const bool greedy_pass = w.greedy && (maxk >> 8) != page;
+  if (greedy_pass) {
+    if (t == 0) misc[kWCount] = 0u;
     __syncthreads();
+    uint32_t c = 0;
+    for (int i = t; i < n; i += kWideThreads) c += (cand[i] >> 16) == maxk;
+    if (c) atomicAdd(&misc[kWCount], c);
+    wide_sync_all<G>();
+  }
+  if (t < 32) {
+    uint32_t cnt = 0;
+    if (lane < static_cast<uint32_t>(G)) {
+      const int g = static_cast<int>(lane);
+      if (greedy_pass)
+        cnt = wide_peer_u32<G>(misc, kWCount, g);
+      else if ((key_d >> 8) == page && (w.greedy || key_d == thr))
+        cnt = wide_peer_u32<G>(bB, static_cast<int>(key_d & 255u), g);
+      else if (shift == 0)
+        cnt = wide_peer_u32<G>(pcnt, static_cast<int>(d1), g);
+      else
+        cnt = wide_peer_u32<G>(lE, static_cast<int>((maxk - key_d) & ((1u << shift) - 1u)), g);
+    }
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= static_cast<uint32_t>(o)) incl += x;
+    }
+    const uint32_t hit = __ballot_sync(0xFFFFFFFFu, incl > rho && lane < static_cast<uint32_t>(G));
+    const uint32_t owner = hit ? static_cast<uint32_t>(__ffs(hit) - 1) : 0u;
+    const uint32_t before = __shfl_sync(0xFFFFFFFFu, incl - cnt, owner);
+    if (t == 0) {
+      misc[kWOwner] = owner;
+      misc[kWRho2] = rho - before;
+    }
+  }
+  __syncthreads();
+  const uint32_t owner = misc[kWOwner];
+  uint32_t sel = 0xFFFFFFFFu;
+  if (rank == owner) {
+    sel = wide_local_rank_select(cand, n, key_d, misc[kWRho2], rs, misc, scratch);
+    if (t == 0) finish_row(p, r, w, static_cast<int32_t>(rank * S + sel), 0u);
+  }
+  if (p.kept_ids) {
+    // keys above thr, and this CTA's share of the `need` lowest-index keys at thr
+    const uint32_t take = need > eq_before ? min(need - eq_before, eq_mine) : 0u;
+    uint32_t cut_idx = take ? 0xFFFFu : 0u;
+    if (take != 0 && take < eq_mine)
+      cut_idx = wide_local_rank_select(cand, n, thr, take - 1, rs, misc, scratch);
     const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
     const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
-    int c = 0;
+    const uint32_t kept_addr = G > 1 ? dsmem_addr(&misc[kWKept], 0) : 0u;
     for (int i = t; i < n; i += kWideThreads) {
-      while (c + 1 < G && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
       const uint32_t e = cand[i];
-      const uint32_t key = e >> 16;
-      const uint32_t g = wide_gidx(e, c, S);
-      if (key > thr || (key == thr && need && g <= idx_cut)) {
-        const uint32_t pos = atomicAdd(&misc[kWN], 1u);
-        if (pos < static_cast<uint32_t>(p.max_keep)) {
-          p.kept_ids[rb + pos] = static_cast<int32_t>(g);
-          p.kept_probs[rb + pos] =
-              w.greedy ? (static_cast<int32_t>(g) == id ? 1.f : 0.f)
-                       : __fdiv_rn(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp), s_real);
-        }
+      const uint32_t key = e >> 16, idx = e & 0xFFFFu;
+      const bool keep = key > thr || (key == thr && take != 0 && idx <= cut_idx);
+      if (!keep) continue;
+      uint32_t pos;
+      if constexpr (G > 1)
+        pos = dsmem_atomic_add(kept_addr, 1u);
+      else
+        pos = atomicAdd(&misc[kWKept], 1u);
+      if (pos < static_cast<uint32_t>(p.max_keep)) {
+        p.kept_ids[rb + pos] = static_cast<int32_t>(rank * S + idx);
+        p.kept_probs[rb + pos] =
+            w.greedy ? ((rank == owner && idx == sel) ? 1.f : 0.f)
+                     : __fdiv_rn(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp), s_real);
       }
     }
-    if (t == 0) {
+    if (rank == 0 && t == 0) {
       p.n_kept[r] = static_cast<int32_t>(k_eff);
       p.n_nucleus[r] = static_cast<int32_t>(n_p);
     }
@@ -1152,13 +1220,15 @@ __device__ void wide_gather_tail(const Params &p, int r, const Row &w, const uin
 
 template <int G>
 __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Params p) {
+  constexpr uint32_t kCap = static_cast<uint32_t>(wide_cap(G));
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t *cand = reinterpret_cast<uint32_t *>(smem);
-  unsigned char *work = smem + kWideCandMax * 4;
+  unsigned char *work = smem + kCap * 4;
   uint32_t *misc = reinterpret_cast<uint32_t *>(work + kWideWorkBytes);
   uint64_t *scratch = reinterpret_cast<uint64_t *>(misc + kWScan);
   uint32_t *lh = reinterpret_cast<uint32_t *>(work + kWideLhOff);  // per-key counts
   uint32_t *mh = reinterpret_cast<uint32_t *>(work + kWideMhOff);  // sample / select histograms
+  uint32_t *pg = reinterpret_cast<uint32_t *>(work + kWidePgOff);  // candidate counts by key >> 8
 
   const uint32_t rank = G > 1 ? cluster_rank() : 0u;
   const int r = G > 1 ? static_cast<int>(cluster_index()) : static_cast<int>(blockIdx.x);
@@ -1203,10 +1273,12 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
                     : make_uint4(0u, 0u, 0u, 0u);
   }
 
+  // a slice no longer than the buffer keeps every element (no sample)
   uint32_t t_key = 0;
-  if (V > kWideCandMax && !p.wide_exact)
+  if (S > static_cast<int>(kCap) && !p.wide_exact)
     t_key = wide_sample_threshold(rowp, V, w.k_eff, G, mh, misc, scratch);
   for (int i = t; i < kWideBins / 2; i += kWideThreads) lh[i] = 0u;
+  pg[t] = 0u;  // kWideThreads == 256 pages
   if (t < 16) misc[kWThrB + t] = 0u;  // fast-tail results and the kept-set counter
   if (t == 0) {
     misc[kWN] = 0u;
@@ -1216,7 +1288,7 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
   __syncthreads();
 
   // ---- filter: every element with key >= t_key becomes a candidate ----
-  uint32_t bad = 0, range = 0;
+  uint32_t bad = 0, range = 0, kmax = 0;
   if (!p.wide_exact) {
     const uint32_t tb = wkey_bits(t_key);
     const uint32_t t2 = tb | (tb << 16);
@@ -1252,7 +1324,7 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
           rt += __popc(bal);
           if (rt - rh >= 32u) {
             __syncwarp();
-            wide_drain(ring, rh, 32u, t_key, cand, lh, &misc[kWN], bad, range);
+            wide_drain(ring, rh, 32u, t_key, cand, kCap, lh, pg, &misc[kWN], bad, range, kmax);
             rh += 32u;
             __syncwarp();
           }
@@ -1262,14 +1334,17 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
       for (int u = 0; u < kWideU; ++u) cur[u] = nxt[u];
     }
     __syncwarp();
-    if (rt != rh) wide_drain(ring, rh, rt - rh, t_key, cand, lh, &misc[kWN], bad, range);
+    if (rt != rh)
+      wide_drain(ring, rh, rt - rh, t_key, cand, kCap, lh, pg, &misc[kWN], bad, range, kmax);
     if (t < head + tail) {
       const int idx = t < head ? t : head + 8 * nq + (t - head);
-      wide_append_one(sp, idx, t_key, cand, lh, &misc[kWN], bad, range);
+      wide_append_one(sp, idx, t_key, cand, kCap, lh, pg, &misc[kWN], bad, range, kmax);
     }
     if (bad) atomicOr(&misc[kWBad], 1u);
     if (range) atomicOr(&misc[kWRange], 1u);
   }
+  kmax = wide_max_u32(kmax, scratch);
+  if (t == 0) misc[kWMaxK] = kmax;
   if constexpr (G > 1)
     wide_cluster_sync();
   else
@@ -1298,7 +1373,7 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
     const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
     const bool any_bad = __any_sync(0xFFFFFFFFu, b != 0);
     const bool any_range = __any_sync(0xFFFFFFFFu, rg != 0);
-    const bool any_full = __any_sync(0xFFFFFFFFu, n > static_cast<uint32_t>(kWideCandMax));
+    const bool any_full = __any_sync(0xFFFFFFFFu, n > kCap);
     if (t == 0) {
       uint32_t mode = 0u;
       if (!p.wide_exact) {
@@ -1306,8 +1381,8 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
           mode = 2u;
         else if (total >= k_eff && total <= 65535u && !any_full && !any_range)
           mode = 1u;
-        else if (total >= k_eff && total <= static_cast<uint32_t>(kWideCandMax))
-          mode = 3u;  // key range too wide for the per-key counts: gather instead
+        else if (total >= k_eff && !any_full)
+          mode = 3u;  // key range too wide for the per-key counts
       }
       misc[kWFast] = mode;
     }
@@ -1325,57 +1400,21 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
     if constexpr (G > 1) wide_cluster_sync();  // peers read our counts and the leader's counter
     return;
   }
-
-  // ---- the rest gathers a candidate set into the leader for the generic
-  // tail: the filter's candidates (mode 3), or the exact top-k set collected
-  // anew by re-reading the slice (mode 0) ----
-  uint32_t *hist = reinterpret_cast<uint32_t *>(work);
+  uint32_t *hw = reinterpret_cast<uint32_t *>(work);
   if (mode == 0u) {
+    // the exact top-k set collected anew by re-reading the slice
     if constexpr (G > 1) wide_cluster_sync();  // peers may still read our counters
-    const bool ok = wide_exact_collect<G>(sp, head, nq, tail, rank, k_eff, cand, hist, misc,
+    const bool ok = wide_exact_collect<G>(sp, head, nq, tail, rank, k_eff, cand, hw, pg, misc,
                                           scratch);
     if (!ok) {
       if (rank == 0 && t == 0) finish_row(p, r, w, -1, kRowNonFinite);
       return;
     }
   }
-  if constexpr (G > 1) wide_cluster_sync();
-  if (t < 32) {
-    uint32_t n = 0;
-    if (lane < static_cast<uint32_t>(G)) {
-      if constexpr (G == 1)
-        n = misc[kWN];
-      else
-        n = dsmem_ld_u32(dsmem_addr(&misc[kWN], lane));
-    }
-    uint32_t incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= static_cast<uint32_t>(o)) incl += x;
-    }
-    const uint32_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);  // every lane of warp 0
-    if (t <= G) misc[kWSeg + t] = incl - n;
-    if (t == 0) misc[kWTotal] = total;
-  }
-  __syncthreads();
-
-  // gather into the leader
-  const int n_all = min(static_cast<int>(misc[kWTotal]), kWideCandMax);
-  if constexpr (G > 1) {
-    if (rank != 0) {
-      const uint32_t off = misc[kWSeg + rank];
-      const int n_mine = min(static_cast<int>(misc[kWSeg + rank + 1] - off),
-                             kWideCandMax - static_cast<int>(min(off, static_cast<uint32_t>(kWideCandMax))));
-      const uint32_t dst = dsmem_addr(cand, 0) + 4u * off;
-      for (int i = t; i < n_mine; i += kWideThreads)
-        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(dst + 4u * i), "r"(cand[i]));
-    }
-    wide_cluster_sync();
-    if (rank != 0) return;
-  }
-
-  wide_gather_tail<G>(p, r, w, cand, n_all, &misc[kWSeg], S, hist, misc, scratch);
+  if (mode == 0u) wide_sync_all<G>();  // the exact set's page counts are complete everywhere
+  wide_dist_tail<G>(p, r, w, rank, S, cand, static_cast<int>(min(misc[kWN], kCap)), hw, pg, misc,
+                    scratch);
+  if constexpr (G > 1) wide_cluster_sync();  // peers read our histograms and the leader's counter
 }
 
 }  // namespace ts
