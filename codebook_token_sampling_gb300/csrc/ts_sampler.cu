@@ -89,11 +89,11 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
   }
   if (path == 1) {
     const int epc = bf16 ? 8 : 4;
-    const int per_thread = (vmax + ts::kRowThreads * epc - 1) / (ts::kRowThreads * epc);
-    pl->nch = per_thread <= 1 ? 1 : (per_thread <= 2 ? 2 : 4);
-    pl->threads = ts::kRowThreads;
+    const int per_lane = (vmax + 32 * epc - 1) / (32 * epc);  // 16-byte chunks per lane
+    pl->nch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
+    pl->threads = ts::kTowerThreads;
     pl->smem = 0;  // static shared memory only
-    pl->grid = b->n_rows;
+    pl->grid = (b->n_rows + ts::kTowerWarps - 1) / ts::kTowerWarps;
     return TS_OK;
   }
   const int slice_max = bf16 ? ts::kSliceMaxBF16 : ts::kSliceMaxF32;
@@ -171,7 +171,9 @@ template <class K>
 void *warp_kernel_for(int nch) {
   if (nch == 1) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 1>);
   if (nch == 2) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 2>);
-  return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 4>);
+  if (nch == 4) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 4>);
+  if (nch == 8) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 8>);
+  return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 16>);
 }
 
 void *wide_kernel_for(int g) {
@@ -195,7 +197,7 @@ ts_status set_attributes(int device) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  void *fns[18];
+  void *fns[22];
   int n = 0;
   const int gs[4] = {1, 2, 4, 8};
   for (int i = 0; i < 4; ++i) {
@@ -203,8 +205,8 @@ ts_status set_attributes(int device) {
     fns[n++] = cluster_kernel_for<ts::KeyF32>(gs[i]);
     fns[n++] = wide_kernel_for(gs[i]);
   }
-  const int nchs[3] = {1, 2, 4};
-  for (int i = 0; i < 3; ++i) {
+  const int nchs[5] = {1, 2, 4, 8, 16};
+  for (int i = 0; i < 5; ++i) {
     fns[n++] = warp_kernel_for<ts::KeyBF16>(nchs[i]);
     fns[n++] = warp_kernel_for<ts::KeyF32>(nchs[i]);
   }

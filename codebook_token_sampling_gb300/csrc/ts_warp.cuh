@@ -3,30 +3,18 @@
 // under the default cap 64, Drama 3 article sections "测试口径" and
 // "能跑通的命令，和文档写明的边界").
 //
-// One block of 128 threads owns one row.  Fast path (every realistic row):
-//   1. the row is read once with 16-byte streaming loads (thread t issues
-//      chunks t, t+128, ..., all in flight at once); the Philox draw is
-//      computed while they are in flight;
-//   2. keys stay in registers (and are staged in shared memory for the slow
-//      path) and feed a 1024-bin histogram of their top 10 bits (sign,
-//      exponent and one mantissa bit: half-binade bins);
-//   3. warp 0 finds the bin holding the k_eff-th largest key by a two-level
-//      suffix scan; bins 0, 1022 and 1023 hold only NaN / +inf keys and bin 1
-//      only -inf / NaN keys, so the same histogram validates the row; a
-//      second 64-bin histogram over the next 6 key bits of that bin narrows
-//      the threshold (for bf16 to the exact k_eff-th largest key);
-//   4. every key at or above the threshold (k_eff plus any ties) is packed
-//      with its index into one word (key high, inverted index low) and warp
-//      0 bitonic-sorts the words: the first k_eff are the top-k set in
-//      (logit desc, index asc) order, ties included;
-//   5. warp 0 forms fixed-point weights, scans them, cuts the nucleus and
-//      draws (the Philox draw itself is computed by warp 1 while warp 0
-//      searches the histogram).
-// Rows whose threshold would leave more than 128 candidates (huge ties) or
-// whose threshold is -inf take an exact slow path on warp 0: 8-bit radix
-// select over the staged keys with index-ordered tie ranking, then the same
-// sort and tail.
+// One warp owns one row (four rows per 128-thread block, no block barrier).
+// The row is staged in shared memory by asynchronous 16-byte copies; each
+// lane's two largest logits give, through the k_eff-th largest of the 64
+// per-lane maxima, a lower bound of the row's k_eff-th largest logit; the
+// logits at or above it (the top-k set with all its ties, about 35 words for
+// top_k 30 of 1024 gaussian logits) are bitonic-sorted by the warp as (key,
+// inverted index) words, and the warp computes the fixed-point weights, the
+// nucleus cutoff and the draw.  Rows with huge ties take an exact radix-select
+// slow path over the staged keys.
 #pragma once
+
+#include <cuda_bf16.h>
 
 #include "ts_device.cuh"
 
@@ -207,13 +195,14 @@ __device__ __forceinline__ void warp_tail(const Params &p, int r, const Row &w,
   }
 }
 
-// Exact slow path for rows the fast path declines (threshold at -inf, or a
-// threshold bin with more than kWarpCandMax keys): 8-bit radix select over the
-// staged keys, then the top-k set collected in index order (keys equal to
-// the threshold taken by lowest index), sorted, and the common tail.
-template <class K>
+// Exact slow path for rows the fast path declines (more than kWarpCandMax
+// keys at or above the candidate threshold, i.e. huge ties): 8-bit radix
+// select over the row's keys (keys(q) returns the keys of body chunk q, read
+// again from memory), then the top-k set collected in index order (keys
+// equal to the threshold taken by lowest index), sorted, and the common tail.
+template <class K, class Loader>
 __device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w, uint32_t *hist,
-                                            typename SortWord<K>::T *cand, const uint4 *keys,
+                                            typename SortWord<K>::T *cand, const Loader keys,
                                             int nq, int head, int tail, int eidx, uint32_t ekey,
                                             uint32_t u24) {
   using SW = SortWord<K>;
@@ -231,7 +220,7 @@ __device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w
     __syncwarp();
 #pragma unroll 1
     for (int q = static_cast<int>(lane); q < nq; q += 32) {
-      const uint4 v = keys[q];
+      const uint4 v = keys(q);
       const uint32_t c[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < EPC; ++e) {
@@ -290,7 +279,7 @@ __device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w
   for (int j = 0; j < rounds; ++j) {
     const int q = static_cast<int>(lane) + 32 * j;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (q < nq) v = keys[q];
+    if (q < nq) v = keys(q);
     const uint32_t c[4] = {v.x, v.y, v.z, v.w};
     uint32_t ng = 0, ne = 0;
 #pragma unroll
@@ -372,239 +361,245 @@ __device__ __forceinline__ void warp_sort_and_tail(const Params &p, int r, const
   warp_tail<K>(p, r, w, v[0], second, w.k_eff, u24);
 }
 
-// Histogram bin b lives at b + b / 32, so that a lane reading 32 consecutive
-// bins touches 32 different banks.
-__device__ __forceinline__ uint32_t hist_slot(uint32_t b) { return b + (b >> 5); }
-constexpr int kRowHistWords = kWarpHistBins + kWarpHistBins / 32;
+// Warp-per-row kernel.  Each warp owns one row (kTowerWarps rows per block,
+// no block barriers):
+//   1. the row is copied into the warp's shared-memory stage with 16-byte
+//      asynchronous copies (lane l: body chunks l, l + 32, ...), all in
+//      flight at once; the unaligned head and tail elements are read one per
+//      lane; lane 0 computes the Philox draw meanwhile;
+//   2. each lane keeps the two largest logits it has seen (packed bf16 or
+//      fp32 min / max); the k_eff-th largest of these 64 values t0 is a lower
+//      bound of the row's k_eff-th largest logit (at least k_eff of the row's
+//      logits are >= t0), so every logit >= t0 is a candidate and the
+//      candidates hold the whole top-k set with every tie at its end;
+//   3. an unordered compare with t0 (so that a NaN is flagged too) marks the
+//      chunks that hold a candidate; only those are unpacked into (key,
+//      inverted index) words, about 35 for top_k 30 of 1024 gaussian logits,
+//      which the warp bitonic-sorts: the first k_eff are the top-k set in
+//      (logit desc, index asc) order;
+//   4. the warp forms fixed-point weights, scans them, cuts the nucleus and
+//      draws.
+// Rows with more than kWarpCandMax candidates (huge ties) take the exact
+// radix-select slow path over the staged keys.
+constexpr int kTowerWarps = 4;
+constexpr int kTowerThreads = 32 * kTowerWarps;
+constexpr int kRowThreads = kTowerThreads;
 
-// Shared state of one row in a block.
-constexpr int kSubBins = 64;  // second-level histogram: the next 6 key bits
-template <class K>
-struct RowShared {
-  using T = typename SortWord<K>::T;
-  uint32_t hist[kRowHistWords];
-  uint32_t sub[kSubBins];
-  T cand[kWarpCandMax];
-  uint32_t n_cand;
-  uint32_t b1;
-  uint32_t above1;  // keys in bins above b1
-  uint32_t thr;     // candidate threshold key after the second level
-  uint32_t n_sel;   // keys >= thr
-  uint32_t u24;
-};
-
-// One block of kRowThreads threads per row.
-constexpr int kRowThreads = 128;
-
-// The row body for rows of at most NCH 16-byte chunks per thread.
-template <class K, int NCH>
-__device__ __forceinline__ void row_body(const Params &p, int r, const Row &w, int64_t step,
-                                         RowShared<K> &sh, uint4 *keys, int head, int nq,
-                                         int tail, const char *rowp) {
-  using SW = SortWord<K>;
-  using T = typename SW::T;
-  constexpr int EPC = K::kPerChunk;
-  constexpr int kShift = K::kBits - 10;  // top 10 key bits select the bin
-  constexpr int kShift2 = kShift - 6;    // the next 6 select the sub-bin
-  const int t = static_cast<int>(threadIdx.x);
-  const uint32_t lane = lane_id();
-  const int warp = t >> 5;
-  const int V = w.vocab;
-  const char *body = rowp + head * K::kElemBytes;
-  const uint64_t pol = l2_evict_first();
-
-  // ---- issue every load of the row (thread t: chunks t, t+128, ...) ----
-  uint4 v[NCH];
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    const int q = t + kRowThreads * j;
-    v[j] = make_uint4(0u, 0u, 0u, 0u);
-    if (q < nq) v[j] = ld_stream_v4(body + static_cast<size_t>(q) * 16, pol);
-  }
-  int eidx = 0x7FFFFFFF;  // head / tail elements live in the first threads
-  if (t < head)
-    eidx = t;
-  else if (t < head + tail)
-    eidx = nq * EPC + t;
-  uint32_t ebits = 0;
-  if (eidx < V) ebits = K::load_one(rowp, eidx);
-  __syncthreads();  // histograms cleared
-
-  // ---- keys: to registers (packed) and shared memory; 10-bit histogram ----
-  uint32_t c[NCH][4];
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    const int q = t + kRowThreads * j;
-    c[j][0] = K::key_word(v[j].x);
-    c[j][1] = K::key_word(v[j].y);
-    c[j][2] = K::key_word(v[j].z);
-    c[j][3] = K::key_word(v[j].w);
-    if (q < nq) {
-      keys[q] = make_uint4(c[j][0], c[j][1], c[j][2], c[j][3]);
-#pragma unroll
-      for (int e = 0; e < EPC; ++e) atomicAdd(&sh.hist[hist_slot(K::elem(c[j], e) >> kShift)], 1u);
-    }
-  }
-  const uint32_t ekey = eidx < V ? K::key(ebits) : 0u;
-  if (eidx < V) atomicAdd(&sh.hist[hist_slot(ekey >> kShift)], 1u);
-  __syncthreads();
-
-  // ---- validity: bins 0, 1022, 1023 hold only NaN/+inf keys; bin 1 holds
-  // -inf and negative NaNs ----
-  const uint32_t h_nan = sh.hist[hist_slot(0)] + sh.hist[hist_slot(kWarpHistBins - 2)] +
-                         sh.hist[hist_slot(kWarpHistBins - 1)];
-  const uint32_t h_ninf = sh.hist[hist_slot(1)];
-  bool bad = h_nan != 0;
-  if (!bad && h_ninf != 0) {  // uniform branch
-    bool nan = false;
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      if (t + kRowThreads * j < nq) {
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) nan |= K::elem(c[j], e) < K::kNegInf;
-      }
-    }
-    if (eidx < V) nan |= ekey < K::kNegInf;
-    bad = __syncthreads_or(nan) != 0;
-  }
-  if (bad || static_cast<uint32_t>(V) == h_ninf) {
-    if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
-    return;
-  }
-
-  // ---- warp 0: the bin of the k_eff-th largest key; warp 1: the draw ----
-  const uint32_t kk = static_cast<uint32_t>(w.k_eff);
-  if (warp == 0) {
-    const uint32_t *hb = &sh.hist[lane * 33];
-    uint32_t part[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 32; ++i) part[i & 3] += hb[i];
-    const uint32_t s = part[0] + part[1] + part[2] + part[3];
-    const uint32_t suf = warp_incl_suffix_u32(s);
-    const uint32_t big = 31 - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk));
-    const uint32_t above_lane = __shfl_sync(0xFFFFFFFFu, suf - s, big);
-    const uint32_t cb = sh.hist[big * 33 + lane];
-    const uint32_t suf2 = warp_incl_suffix_u32(cb) + above_lane;
-    const uint32_t sub = 31 - __clz(__ballot_sync(0xFFFFFFFFu, suf2 >= kk));
-    const uint32_t above1 = __shfl_sync(0xFFFFFFFFu, suf2 - cb, sub);
-    if (lane == 0) {
-      sh.b1 = big * 32 + sub;
-      sh.above1 = above1;
-    }
-  } else if (warp == 1 && lane == 0) {
-    sh.u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(step),
-                        static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
-  }
-  __syncthreads();
-  const uint32_t b1 = sh.b1;
-  if (b1 < 2) {  // threshold at -inf: exact slow path
-    if (warp == 0)
-      warp_slow_path<K>(p, r, w, sh.hist, sh.cand, keys, nq, head, tail, eidx, ekey, sh.u24);
-    return;
-  }
-
-  // ---- second level inside bin b1: the next 6 key bits ----
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    if (t + kRowThreads * j < nq) {
-#pragma unroll
-      for (int e = 0; e < EPC; ++e) {
-        const uint32_t k = K::elem(c[j], e);
-        if ((k >> kShift) == b1) atomicAdd(&sh.sub[(k >> kShift2) & (kSubBins - 1)], 1u);
-      }
-    }
-  }
-  if (eidx < V && (ekey >> kShift) == b1)
-    atomicAdd(&sh.sub[(ekey >> kShift2) & (kSubBins - 1)], 1u);
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t kk2 = kk - sh.above1;  // ranks still needed inside bin b1
-    const uint32_t lo = sh.sub[2 * lane], hi = sh.sub[2 * lane + 1];
-    const uint32_t s = lo + hi;
-    const uint32_t suf = warp_incl_suffix_u32(s);
-    const uint32_t own = 31 - __clz(__ballot_sync(0xFFFFFFFFu, suf >= kk2));
-    const uint32_t above_lane = suf - s;  // counts in sub-bins above this lane's pair
-    // within the owning lane: sub-bin 2*own+1 first, then 2*own
-    const bool top = above_lane + hi >= kk2;
-    const uint32_t b2 = 2 * lane + (top ? 1u : 0u);
-    const uint32_t n_sel = sh.above1 + (top ? above_lane + hi : suf);
-    if (lane == own) {
-      sh.thr = ((b1 << 6) | b2) << kShift2;
-      sh.n_sel = n_sel;
-    }
-  }
-  __syncthreads();
-  const uint32_t tkey = sh.thr, n_sel = sh.n_sel;
-  if (n_sel > static_cast<uint32_t>(kWarpCandMax)) {  // huge ties: exact slow path
-    if (warp == 0)
-      warp_slow_path<K>(p, r, w, sh.hist, sh.cand, keys, nq, head, tail, eidx, ekey, sh.u24);
-    return;
-  }
-
-  // ---- every key >= tkey joins the candidates (any order: sorted next) ----
-  uint32_t mine = 0;
-#pragma unroll
-  for (int j = 0; j < NCH; ++j) {
-    if (t + kRowThreads * j < nq) {
-#pragma unroll
-      for (int e = 0; e < EPC; ++e) mine += K::elem(c[j], e) >= tkey;
-    }
-  }
-  const bool e_in = eidx < V && ekey >= tkey;
-  mine += e_in;
-  if (mine) {
-    uint32_t pos = atomicAdd(&sh.n_cand, mine);
-#pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-      const int q = t + kRowThreads * j;
-      if (q < nq) {
-#pragma unroll
-        for (int e = 0; e < EPC; ++e) {
-          const uint32_t k = K::elem(c[j], e);
-          if (k >= tkey) {
-            if (pos < static_cast<uint32_t>(kWarpCandMax))
-              sh.cand[pos] = SW::make(k, static_cast<uint32_t>(head + q * EPC + e));
-            ++pos;
-          }
-        }
-      }
-    }
-    if (e_in && pos < static_cast<uint32_t>(kWarpCandMax))
-      sh.cand[pos] = SW::make(ekey, static_cast<uint32_t>(eidx));
-  }
-  __syncthreads();
-  if (warp != 0) return;
-  const int nc = static_cast<int>(n_sel);
-  if (nc <= 32)
-    warp_sort_and_tail<K, 1>(p, r, w, sh.cand, nc, sh.u24);
-  else if (nc <= 64)
-    warp_sort_and_tail<K, 2>(p, r, w, sh.cand, nc, sh.u24);
-  else
-    warp_sort_and_tail<K, 4>(p, r, w, sh.cand, nc, sh.u24);
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-// MAXNCH = most 16-byte chunks per thread of any row in the launch; each row
-// runs the body sized for its own width.
+// Per-dtype chunk helpers: the two largest values of a chunk folded into a
+// running pair, and the unordered >= mask of a chunk against a threshold.
+template <class K>
+struct Top2;
+
+template <>
+struct Top2<KeyBF16> {
+  using V = uint32_t;  // packed bf16x2
+  static constexpr uint32_t kInit = 0xFF80FF80u;  // -inf, -inf
+  __device__ __forceinline__ static __nv_bfloat162 b2(uint32_t x) {
+    return *reinterpret_cast<__nv_bfloat162 *>(&x);
+  }
+  __device__ __forceinline__ static uint32_t u(__nv_bfloat162 x) {
+    return *reinterpret_cast<uint32_t *>(&x);
+  }
+  __device__ __forceinline__ static void fold(uint32_t w, uint32_t &m1, uint32_t &m2) {
+    m2 = u(__hmax2(b2(m2), __hmin2(b2(m1), b2(w))));
+    m1 = u(__hmax2(b2(m1), b2(w)));
+  }
+  __device__ __forceinline__ static void fold_chunk(const uint4 &c, uint32_t &m1, uint32_t &m2) {
+    fold(c.x, m1, m2);
+    fold(c.y, m1, m2);
+    fold(c.z, m1, m2);
+    fold(c.w, m1, m2);
+  }
+  // the lane's two largest keys from the packed pair
+  __device__ __forceinline__ static void keys2(uint32_t m1, uint32_t m2, uint32_t &k1,
+                                               uint32_t &k2) {
+    const uint32_t a = KeyBF16::key(m1 & 0xFFFFu), b = KeyBF16::key(m1 >> 16);
+    const uint32_t c = KeyBF16::key(m2 & 0xFFFFu), d = KeyBF16::key(m2 >> 16);
+    k1 = max(a, b);
+    k2 = max(min(a, b), max(c, d));
+  }
+  __device__ __forceinline__ static uint32_t splat(uint32_t key) {
+    const uint32_t bits = key ^ ((key & 0x8000u) ? 0x8000u : 0xFFFFu);
+    return bits | (bits << 16);
+  }
+  __device__ __forceinline__ static bool flagged(const uint4 &c, uint32_t t2) {
+    const uint32_t m = __hgeu2_mask(b2(c.x), b2(t2)) | __hgeu2_mask(b2(c.y), b2(t2)) |
+                       __hgeu2_mask(b2(c.z), b2(t2)) | __hgeu2_mask(b2(c.w), b2(t2));
+    return m != 0u;
+  }
+};
+
+template <>
+struct Top2<KeyF32> {
+  static constexpr uint32_t kInit = 0xFF800000u;  // -inf
+  __device__ __forceinline__ static void fold(uint32_t w, uint32_t &m1, uint32_t &m2) {
+    const float x = __uint_as_float(w), a = __uint_as_float(m1), b = __uint_as_float(m2);
+    m2 = __float_as_uint(fmaxf(b, fminf(a, x)));
+    m1 = __float_as_uint(fmaxf(a, x));
+  }
+  __device__ __forceinline__ static void fold_chunk(const uint4 &c, uint32_t &m1, uint32_t &m2) {
+    fold(c.x, m1, m2);
+    fold(c.y, m1, m2);
+    fold(c.z, m1, m2);
+    fold(c.w, m1, m2);
+  }
+  __device__ __forceinline__ static void keys2(uint32_t m1, uint32_t m2, uint32_t &k1,
+                                               uint32_t &k2) {
+    k1 = KeyF32::key(m1);
+    k2 = KeyF32::key(m2);
+  }
+  __device__ __forceinline__ static uint32_t splat(uint32_t key) {
+    return key ^ ((key & 0x80000000u) ? 0x80000000u : 0xFFFFFFFFu);
+  }
+  __device__ __forceinline__ static bool flagged(const uint4 &c, uint32_t t) {
+    const float tv = __uint_as_float(t);
+    return !(__uint_as_float(c.x) < tv) || !(__uint_as_float(c.y) < tv) ||
+           !(__uint_as_float(c.z) < tv) || !(__uint_as_float(c.w) < tv);
+  }
+};
+
 template <class K, int MAXNCH>
-__global__ void __launch_bounds__(kRowThreads, 10) row_sampler_kernel(const Params p) {
+struct TowerShared {
+  using T = typename SortWord<K>::T;
+  uint4 stage[32 * MAXNCH];
+  T cand[kWarpCandMax];
+  uint32_t hist[256];
+};
+
+// The row body for rows of at most 32 * NCH body chunks.
+template <class K, int NCH, class SH>
+__device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w, uint32_t u24,
+                                           SH &sh, int head, int nq, int tail,
+                                           const char *rowp) {
+  using SW = SortWord<K>;
+  using TT = Top2<K>;
   constexpr int EPC = K::kPerChunk;
-  __shared__ __align__(16) RowShared<K> sh;
-  __shared__ __align__(16) uint4 keys[MAXNCH * kRowThreads];
-  const int r = static_cast<int>(blockIdx.x);
-  const int t = static_cast<int>(threadIdx.x);
-  pdl_wait_and_release();
-  if (r >= p.n_rows) return;
+  const uint32_t lane = lane_id();
+  const int V = w.vocab;
+  const char *body = rowp + head * K::kElemBytes;
+  // ---- the row into the stage, all copies in flight ----
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int q = static_cast<int>(lane) + 32 * j;
+    if (q < nq) cp_async16(&sh.stage[q], body + static_cast<size_t>(q) * 16);
+  }
+  // head / tail element of this lane (at most 7 + 7 of them)
+  int eidx = 0x7FFFFFFF;
+  if (static_cast<int>(lane) < head)
+    eidx = static_cast<int>(lane);
+  else if (static_cast<int>(lane) < head + tail)
+    eidx = nq * EPC + static_cast<int>(lane);
+  const bool has_e = eidx < V;
+  const uint32_t ebits = has_e ? K::load_one(rowp, eidx) : 0u;
+  const uint32_t ekey = has_e ? K::key(ebits) : 0u;
+  cp_async_wait_all();
+  __syncwarp();
 
-  for (int i = t; i < kRowHistWords; i += kRowThreads) sh.hist[i] = 0u;
-  if (t < kSubBins) sh.sub[t] = 0u;
-  if (t == 0) sh.n_cand = 0;
-
-  const Row w = load_row(p, r);
-  if (w.err) {
-    if (t == 0) finish_row(p, r, w, -1, w.err);
+  // ---- the two largest logits per lane ----
+  uint32_t m1 = TT::kInit, m2 = TT::kInit;
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int q = static_cast<int>(lane) + 32 * j;
+    if (q < nq) TT::fold_chunk(sh.stage[q], m1, m2);
+  }
+  uint32_t rep[2];
+  TT::keys2(m1, m2, rep[0], rep[1]);
+  if (has_e) {  // the lane's head / tail element joins its pair
+    rep[1] = max(rep[1], min(rep[0], ekey));
+    rep[0] = max(rep[0], ekey);
+  }
+  // ---- the k_eff-th largest of the 64 per-lane maxima: a lower bound ----
+  bitonic_desc<uint32_t, 2>(rep);
+  const int kq = w.k_eff;
+  const uint32_t top = __shfl_sync(0xFFFFFFFFu, rep[0], 0);
+  uint32_t t0 = kq <= 32 ? __shfl_sync(0xFFFFFFFFu, rep[0], kq - 1)
+                         : __shfl_sync(0xFFFFFFFFu, rep[1], kq - 33);
+  // a NaN as t0 would flag nothing (NaN rows are caught below either way)
+  if (t0 < K::kNegInf || t0 > K::kPosInf) t0 = K::kNegInf;
+  const uint32_t t2 = TT::splat(t0);
+  // ---- candidates: chunks holding a logit >= t0 (or a NaN) ----
+  uint32_t fmask = 0;  // bit j: chunk lane + 32 j is flagged
+#pragma unroll
+  for (int j = 0; j < NCH; ++j) {
+    const int q = static_cast<int>(lane) + 32 * j;
+    if (q < nq && TT::flagged(sh.stage[q], t2)) fmask |= 1u << j;
+  }
+  // keys of the flagged chunks: count, then write
+  uint32_t mine = 0, bad = 0;
+  for (uint32_t fm = fmask; fm; fm &= fm - 1u) {
+    const int q = static_cast<int>(lane) + 32 * (__ffs(fm) - 1);
+    const uint4 v = sh.stage[q];
+    const uint32_t c[4] = {K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w)};
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) {
+      const uint32_t k = K::elem(c, e);
+      bad |= (k < K::kNegInf) | (k > K::kPosInf - 1u);
+      mine += k >= t0 && k < K::kPosInf;
+    }
+  }
+  if (has_e) {
+    bad |= (ekey < K::kNegInf) | (ekey >= K::kPosInf);
+    mine += ekey >= t0 && ekey < K::kPosInf;
+  }
+  if (__any_sync(0xFFFFFFFFu, bad) || top <= K::kNegInf) {  // a NaN / +inf, or no finite logit
+    if (lane == 0) finish_row(p, r, w, -1, kRowNonFinite);
     return;
   }
-  const int64_t step = (t >> 5) == 1 ? p.step[w.stream] : 0;  // for the draw (warp 1)
+  uint32_t total;
+  uint32_t pos = warp_excl_scan_u32(mine, &total);
+  if (total > static_cast<uint32_t>(kWarpCandMax)) {
+    auto keys = [&](int q) {
+      const uint4 v = sh.stage[q];
+      return make_uint4(K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w));
+    };
+    warp_slow_path<K>(p, r, w, sh.hist, sh.cand, keys, nq, head, tail, eidx, ekey, u24);
+    return;
+  }
+  for (uint32_t fm = fmask; fm; fm &= fm - 1u) {
+    const int q = static_cast<int>(lane) + 32 * (__ffs(fm) - 1);
+    const uint4 v = sh.stage[q];
+    const uint32_t c[4] = {K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w)};
+#pragma unroll
+    for (int e = 0; e < EPC; ++e) {
+      const uint32_t k = K::elem(c, e);
+      if (k >= t0) sh.cand[pos++] = SW::make(k, static_cast<uint32_t>(head + q * EPC + e));
+    }
+  }
+  if (has_e && ekey >= t0) sh.cand[pos] = SW::make(ekey, static_cast<uint32_t>(eidx));
+  __syncwarp();
+  const int nc = static_cast<int>(total);
+  if (nc <= 32)
+    warp_sort_and_tail<K, 1>(p, r, w, sh.cand, nc, u24);
+  else if (nc <= 64)
+    warp_sort_and_tail<K, 2>(p, r, w, sh.cand, nc, u24);
+  else
+    warp_sort_and_tail<K, 4>(p, r, w, sh.cand, nc, u24);
+}
+
+// MAXNCH = most 16-byte chunks per lane of any row in the launch (1, 2, 4, 8
+// or 16); each row runs the body sized for its own width.
+template <class K, int MAXNCH>
+__global__ void __launch_bounds__(kTowerThreads) row_sampler_kernel(const Params p) {
+  constexpr int EPC = K::kPerChunk;
+  __shared__ __align__(16) TowerShared<K, MAXNCH> shared_rows[kTowerWarps];
+  const int warp = static_cast<int>(threadIdx.x) >> 5;
+  const uint32_t lane = lane_id();
+  const int r = static_cast<int>(blockIdx.x) * kTowerWarps + warp;
+  pdl_wait_and_release();
+  if (r >= p.n_rows) return;  // whole warp; the kernel has no block barrier
+  const Row w = load_row(p, r);
+  if (w.err) {
+    if (lane == 0) finish_row(p, r, w, -1, w.err);
+    return;
+  }
   const int V = w.vocab;
   const char *rowp = static_cast<const char *>(p.logits) + w.off * K::kElemBytes;
   const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
@@ -612,12 +607,23 @@ __global__ void __launch_bounds__(kRowThreads, 10) row_sampler_kernel(const Para
   head = min(head, V);
   const int nq = (V - head) / EPC;
   const int tail = V - head - nq * EPC;
-  if (MAXNCH == 1 || nq <= kRowThreads)
-    row_body<K, 1>(p, r, w, step, sh, keys, head, nq, tail, rowp);
-  else if (MAXNCH == 2 || nq <= 2 * kRowThreads)
-    row_body<K, (MAXNCH >= 2 ? 2 : 1)>(p, r, w, step, sh, keys, head, nq, tail, rowp);
+  TowerShared<K, MAXNCH> &sh = shared_rows[warp];
+  // the draw, on lane 0 (its result is needed only by the tail)
+  uint32_t u24 = 0;
+  if (lane == 0 && !w.greedy)
+    u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
+                     static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
+  u24 = __shfl_sync(0xFFFFFFFFu, u24, 0);
+  if (MAXNCH == 1 || nq <= 32)
+    tower_body<K, 1>(p, r, w, u24, sh, head, nq, tail, rowp);
+  else if (MAXNCH == 2 || nq <= 64)
+    tower_body<K, (MAXNCH >= 2 ? 2 : 1)>(p, r, w, u24, sh, head, nq, tail, rowp);
+  else if (MAXNCH == 4 || nq <= 128)
+    tower_body<K, (MAXNCH >= 4 ? 4 : 1)>(p, r, w, u24, sh, head, nq, tail, rowp);
+  else if (MAXNCH == 8 || nq <= 256)
+    tower_body<K, (MAXNCH >= 8 ? 8 : 1)>(p, r, w, u24, sh, head, nq, tail, rowp);
   else
-    row_body<K, MAXNCH>(p, r, w, step, sh, keys, head, nq, tail, rowp);
+    tower_body<K, MAXNCH>(p, r, w, u24, sh, head, nq, tail, rowp);
 }
 
 }  // namespace ts
