@@ -197,6 +197,7 @@ def run_ours(args, world, rank, local):
             base.append(src)
         bufs.append(torch.from_numpy(src.view(np_dt)).to(dev))
     sampler = ts.Sampler(local, host["cap"])
+    sampler.reserve(n_rows, int(host["max_row_vocab"]))  # workspace for the split wide path
     if args.path:
         sampler.set_option(ts.TS_OPT_PATH, args.path)
     batch = ts.DeviceBatch(host, dev)
@@ -313,6 +314,7 @@ def profile_launches(args):
     import codebook_token_sampling_gb300 as ts
     host = workloads.make(args.config, 0, rows=args.rows)
     sampler = ts.Sampler(0, host["cap"])
+    sampler.reserve(int(host["n_rows"]), int(host["max_row_vocab"]))
     if args.path:
         sampler.set_option(ts.TS_OPT_PATH, args.path)
     batch = ts.DeviceBatch(host, "cuda")
@@ -336,8 +338,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
-                    help="force the kernel family (0 = automatic, 1 = warp, 2 = CTA/cluster)")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
+                    help="force the kernel family (0 = automatic, 1 = warp per row, 2 = CTA / "
+                         "cluster per row, 3 = wide cluster, 4 = wide split)")
     ap.add_argument("--profile", type=int, default=0, metavar="N",
                     help="profiling mode: N plain launches of one step, no timing (for ncu)")
     args = ap.parse_args()

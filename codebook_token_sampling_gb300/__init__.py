@@ -5,7 +5,7 @@ of sampling runs in the CUDA kernels of ``libts_sampler.so``.  PyTorch is used
 only for device memory and streams.  The functions keep the C names:
 
     ts_create, ts_destroy, ts_max_top_k, ts_sample, ts_sample_debug,
-    ts_advance_steps, ts_read_status, ts_set_option, ts_plan,
+    ts_reserve, ts_advance_steps, ts_read_status, ts_set_option, ts_plan,
     ts_status_string, ts_last_error
 
 ``Sampler`` wraps a handle; ``DeviceBatch`` holds one step's per-row arrays on
@@ -41,7 +41,7 @@ TS_MAX_VOCAB_BF16 = 163840
 TS_MAX_VOCAB_F32 = 81920
 
 EXPORTED = ("ts_create", "ts_destroy", "ts_max_top_k", "ts_sample", "ts_sample_debug",
-            "ts_advance_steps", "ts_read_status", "ts_set_option", "ts_plan",
+            "ts_reserve", "ts_advance_steps", "ts_read_status", "ts_set_option", "ts_plan",
             "ts_status_string", "ts_last_error")
 
 
@@ -92,6 +92,7 @@ def _load(path: str):
         "ts_max_top_k": ([vp], i32),
         "ts_sample": ([vp, ctypes.POINTER(TsBatch), vp], ctypes.c_int),
         "ts_sample_debug": ([vp, ctypes.POINTER(TsBatch), i32, vp, vp, vp, vp, vp], ctypes.c_int),
+        "ts_reserve": ([vp, i32, i32], ctypes.c_int),
         "ts_advance_steps": ([vp, i32, vp], ctypes.c_int),
         "ts_read_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
         "ts_set_option": ([vp, i32, i32], ctypes.c_int),
@@ -154,6 +155,10 @@ def ts_sample_debug(handle: int, batch: "DeviceBatch", max_keep: int, kept_ids, 
     _check(_lib.ts_sample_debug(handle, ctypes.byref(batch.c), max_keep, kept_ids.data_ptr(),
                                 kept_probs.data_ptr(), n_kept.data_ptr(), n_nucleus.data_ptr(),
                                 _stream_ptr(stream)), "ts_sample_debug")
+
+
+def ts_reserve(handle: int, max_rows: int, max_row_vocab: int) -> None:
+    _check(_lib.ts_reserve(handle, max_rows, max_row_vocab), "ts_reserve")
 
 
 def ts_advance_steps(step, stream=None) -> None:
@@ -219,6 +224,9 @@ class Sampler:
 
     def read_status(self, stream=None) -> int:
         return ts_read_status(self.handle, stream)
+
+    def reserve(self, max_rows: int, max_row_vocab: int) -> None:
+        ts_reserve(self.handle, max_rows, max_row_vocab)
 
     def set_option(self, option: int, value: int) -> None:
         ts_set_option(self.handle, option, value)

@@ -48,6 +48,12 @@ struct Params {
   int32_t slice;
   // wide path: 1 = always take the exact (re-reading) path (testing)
   int32_t wide_exact;
+  // split wide path: the workspace and its layout (row and unit records),
+  // and the units (CTAs) of each row in this launch
+  void *workspace;
+  int32_t ws_rows;
+  int32_t ws_units;
+  int32_t ws_units_per_row;
 };
 
 // ---------------------------------------------------------------------------

@@ -4,6 +4,7 @@
 // sampling path, so a decode step can be captured into a CUDA graph (Drama 3
 // article, section "两阶段共享一张卡": decode steps replay as one graph, with
 // no host synchronisation between steps).
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -12,6 +13,7 @@
 #include "../../include/ts_sampler.h"
 #include "ts_cluster.cuh"
 #include "ts_device.cuh"
+#include "ts_split.cuh"
 #include "ts_warp.cuh"
 #include "ts_wide.cuh"
 
@@ -24,6 +26,11 @@ struct ts_sampler {
   int pdl;            // launch with programmatic stream serialization
   int wide_exact;     // wide path: always take the exact path (testing)
   uint32_t *status;   // device word
+  void *ws;           // split wide path workspace (ts_reserve), or null
+  size_t ws_bytes;
+  int ws_rows;        // row records it holds
+  int ws_units;       // unit records it holds
+  int ws_vocab;       // widest row it was sized for
 };
 
 namespace {
@@ -43,8 +50,21 @@ int cap_of(int requested) {
 
 constexpr int kWarpMaxBF16 = 4096;
 constexpr int kWarpMaxF32 = 2048;
-// bf16 rows wider than this take the single-pass wide kernel
+// bf16 rows wider than this take a single-pass wide path
 constexpr int kWideMinVocab = 32768;
+// split path: slices of about this many tokens at most (76 KB of bf16)
+constexpr int kSplitSliceTarget = 40000;
+
+// Units (CTAs) per row of the split path for a launch of n_rows rows of at
+// most vmax tokens: slices of at most kSplitSliceTarget tokens, at least two
+// units, and for few rows enough units to cover the GPU twice.
+int split_units(int n_rows, int vmax, int num_sms) {
+  int u = (vmax + kSplitSliceTarget - 1) / kSplitSliceTarget;
+  u = std::max(u, 2);
+  const int spread = (2 * num_sms + std::max(n_rows, 1) - 1) / std::max(n_rows, 1);
+  u = std::max(u, std::min(spread, ts::kSplitMaxUnits));
+  return std::min(u, ts::kSplitMaxUnits);
+}
 
 struct Plan {
   int path;   // 1 block per row, 2 cluster, 3 wide
@@ -62,11 +82,31 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
   if (vmax > (bf16 ? TS_MAX_VOCAB_BF16 : TS_MAX_VOCAB_F32)) return TS_ERR_UNSUPPORTED;
   const int warp_max = bf16 ? kWarpMaxBF16 : kWarpMaxF32;
   const bool warp_ok = s->cap <= 64 && vmax <= warp_max;
-  int path = s->force_path ? s->force_path : (warp_ok ? 1 : (bf16 && vmax > kWideMinVocab ? 3 : 2));
+  const int su = split_units(b->n_rows, vmax, s->num_sms);
+  const bool split_ok = bf16 && s->ws && b->n_rows <= s->ws_rows &&
+                        static_cast<long long>(b->n_rows) * su <= s->ws_units &&
+                        (vmax + su - 1) / su <= ts::kWideSliceMax;
+  int path = s->force_path;
+  if (!path) path = warp_ok ? 1 : (bf16 && vmax > kWideMinVocab ? (split_ok ? 4 : 3) : 2);
   if (path == 1 && !warp_ok) return TS_ERR_INVALID_ARG;
   if (path == 3 && !bf16) return TS_ERR_INVALID_ARG;
   std::memset(pl, 0, sizeof *pl);
   pl->path = path;
+  if (path == 4) {
+    int u = s->force_cluster ? s->force_cluster : su;
+    if (!bf16 || !s->ws || u < 2 || u > ts::kSplitMaxUnits || b->n_rows > s->ws_rows ||
+        static_cast<long long>(b->n_rows) * u > s->ws_units)
+      return TS_ERR_INVALID_ARG;
+    int slice = (vmax + u - 1) / u;
+    slice = (slice + 7) / 8 * 8;
+    if (slice > ts::kWideSliceMax) return TS_ERR_UNSUPPORTED;
+    pl->g = u;
+    pl->slice = slice;
+    pl->threads = ts::kSplitThreads;
+    pl->smem = static_cast<int>(ts::kSplitSmemBytes);
+    pl->grid = b->n_rows * u;
+    return TS_OK;
+  }
   if (path == 3) {
     int g = 1;
     if (s->force_cluster) {
@@ -197,7 +237,7 @@ ts_status set_attributes(int device) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  void *fns[22];
+  void *fns[24];
   int n = 0;
   const int gs[4] = {1, 2, 4, 8};
   for (int i = 0; i < 4; ++i) {
@@ -210,6 +250,7 @@ ts_status set_attributes(int device) {
     fns[n++] = warp_kernel_for<ts::KeyBF16>(nchs[i]);
     fns[n++] = warp_kernel_for<ts::KeyF32>(nchs[i]);
   }
+  fns[n++] = reinterpret_cast<void *>(ts::split_stream_kernel);
   for (int i = 0; i < n; ++i) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, fns[i]);
@@ -229,6 +270,30 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   p.slice = pl.slice;
   p.wide_exact = s->wide_exact;
   const bool bf16 = b->dtype == TS_DTYPE_BF16;
+  if (pl.path == 4) {
+    p.workspace = s->ws;
+    p.ws_rows = s->ws_rows;
+    p.ws_units = s->ws_units;
+    p.ws_units_per_row = pl.g;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = s->pdl ? 1 : 0;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cfg.stream = st;
+    cfg.blockDim = dim3(ts::kSplitThreads);
+    cfg.gridDim = dim3(static_cast<unsigned>(b->n_rows));
+    void *args[] = {&p};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_threshold_kernel), args);
+    if (e != cudaSuccess) return cuda_fail(e, "split threshold launch");
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+    cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_stream_kernel), args);
+    if (e != cudaSuccess) return cuda_fail(e, "split stream launch");
+    return TS_OK;
+  }
   void *fn = nullptr;
   if (pl.path == 1) {
     fn = bf16 ? warp_kernel_for<ts::KeyBF16>(pl.nch) : warp_kernel_for<ts::KeyF32>(pl.nch);
@@ -298,6 +363,11 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->pdl = 1;
   s->wide_exact = 0;
   s->status = nullptr;
+  s->ws = nullptr;
+  s->ws_bytes = 0;
+  s->ws_rows = 0;
+  s->ws_units = 0;
+  s->ws_vocab = 0;
   ts_status rc = TS_OK;
   e = cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) rc = cuda_fail(e, "cudaDeviceGetAttribute");
@@ -327,6 +397,10 @@ ts_status ts_destroy(ts_sampler *s) {
   cudaGetDevice(&prev);
   cudaSetDevice(s->device);
   cudaError_t e = cudaFree(s->status);
+  if (s->ws) {
+    const cudaError_t e2 = cudaFree(s->ws);
+    if (e == cudaSuccess) e = e2;
+  }
   cudaSetDevice(prev);
   delete s;
   return e == cudaSuccess ? TS_OK : cuda_fail(e, "cudaFree");
@@ -354,6 +428,46 @@ ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep, in
   p.n_kept = n_kept;
   p.n_nucleus = n_nucleus;
   return launch(s, b, p, static_cast<cudaStream_t>(stream));
+}
+
+ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab) {
+  if (!s || max_rows < 0 || max_row_vocab < 0) return TS_ERR_INVALID_ARG;
+  if (max_row_vocab > TS_MAX_VOCAB_BF16) return TS_ERR_UNSUPPORTED;
+  int units = 0;
+  for (int rows = 1; rows <= max_rows; ++rows)
+    units = std::max(units, rows * split_units(rows, std::max(max_row_vocab, 1), s->num_sms));
+  if (max_rows > 0 && max_rows <= s->ws_rows && units <= s->ws_units) return TS_OK;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaError_t e = cudaSetDevice(s->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  if (s->ws) {
+    e = cudaFree(s->ws);
+    s->ws = nullptr;
+    s->ws_bytes = 0;
+    s->ws_rows = 0;
+    s->ws_units = 0;
+    if (e != cudaSuccess) {
+      cudaSetDevice(prev);
+      return cuda_fail(e, "cudaFree");
+    }
+  }
+  ts_status rc = TS_OK;
+  if (max_rows > 0) {
+    const size_t bytes = ts::split_workspace_bytes(max_rows, units);
+    e = cudaMalloc(&s->ws, bytes);
+    if (e != cudaSuccess) {
+      s->ws = nullptr;
+      rc = e == cudaErrorMemoryAllocation ? TS_ERR_NO_MEMORY : cuda_fail(e, "cudaMalloc");
+    } else {
+      s->ws_bytes = bytes;
+      s->ws_rows = max_rows;
+      s->ws_units = units;
+      s->ws_vocab = max_row_vocab;
+    }
+  }
+  cudaSetDevice(prev);
+  return rc;
 }
 
 ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream) {
@@ -389,13 +503,12 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream) {
 ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value) {
   if (!s) return TS_ERR_INVALID_ARG;
   if (option == TS_OPT_PATH) {
-    if (value < 0 || value > 3) return TS_ERR_INVALID_ARG;
+    if (value < 0 || value > 4) return TS_ERR_INVALID_ARG;
     s->force_path = value;
     return TS_OK;
   }
-  if (option == TS_OPT_CLUSTER) {
-    if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8)
-      return TS_ERR_INVALID_ARG;
+  if (option == TS_OPT_CLUSTER) {  // paths 2 / 3: 1, 2, 4 or 8; path 4: 2 .. 16 (checked at launch)
+    if (value < 0 || value > ts::kSplitMaxUnits) return TS_ERR_INVALID_ARG;
     s->force_cluster = value;
     return TS_OK;
   }

@@ -114,8 +114,9 @@ typedef struct {
 
 /* Creates a sampler on CUDA device `device`.  max_top_k: 0 selects the
  * default cap 64; otherwise a power of two in [32, 4096] (else
- * TS_ERR_INVALID_ARG).  Allocates a 4-byte device status word (the only
- * allocation the library makes).  Safe to call before any stream capture. */
+ * TS_ERR_INVALID_ARG).  Allocates a 4-byte device status word (besides the
+ * workspace of ts_reserve, the only allocation the library makes).  Call it
+ * before any stream capture. */
 ts_status ts_create(int device, int max_top_k, ts_sampler **out);
 
 /* Frees the sampler and its status word.  NULL is accepted. */
@@ -142,6 +143,17 @@ ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep,
                           int32_t *kept_ids, float *kept_probs, int32_t *n_kept,
                           int32_t *n_nucleus, void *stream);
 
+/* Sizes the sampler's workspace for calls of up to max_rows rows no wider
+ * than max_row_vocab (bf16).  The workspace lets wide rows (more than 32,768
+ * tokens) take the split path: a threshold kernel, then a streaming kernel
+ * whose CTAs hand their candidates over through it, the last CTA of each row
+ * finishing the row.  Without it (or when a call exceeds it) wide rows take
+ * the cluster path, which needs no workspace.  Allocates device memory
+ * (about 17 KB per CTA of the largest launch), so call it before any stream
+ * capture and not concurrently with work on the sampler; 0 rows frees the
+ * workspace.  Smaller requests than the current size keep it. */
+ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
+
 /* step[i] += 1 for i < n_streams, on the device (graph-capturable).  Call it
  * after the step's ts_sample so that sibling rows of one stream share a step. */
 ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream);
@@ -150,13 +162,15 @@ ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream);
  * Synchronises `stream`: for tests and debugging, not for the decode loop. */
 ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
 
-/* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = one 128-thread
- * block per row with a bounded candidate set (requires cap <= 64 and
- * max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row that
- * holds the row in shared memory, 3 = the single-pass wide-row path (bf16
- * only; automatic for bf16 rows wider than 32,768).  TS_OPT_CLUSTER: 0 =
+/* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = one warp per
+ * row with a bounded candidate set (requires cap <= 64 and max_row_vocab <=
+ * 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row that holds the row in
+ * shared memory, 3 = the single-pass wide-row cluster path (bf16 only;
+ * automatic for bf16 rows wider than 32,768 without a workspace), 4 = the
+ * split wide-row path (bf16 only; needs ts_reserve; automatic for bf16 rows
+ * wider than 32,768 when the workspace fits).  TS_OPT_CLUSTER: 0 =
  * automatic, else the CTAs per row of paths 2 and 3 (1, 2, 4 or 8; path 3
- * needs max_row_vocab / CTAs <= 65,536).  TS_OPT_PDL: 1 (default) launches
+ * needs max_row_vocab / CTAs <= 65,536) or of path 4 (2 .. 16).  TS_OPT_PDL: 1 (default) launches
  * with programmatic dependent launch, so that a step's kernel is scheduled
  * while the previous kernel in the stream drains (each kernel still waits
  * for its predecessor before touching memory); 0 launches plainly.
@@ -169,7 +183,7 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
 #define TS_OPT_WIDE_EXACT 4
 ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value);
 
-/* Describes the kernel that ts_sample would launch for `b` (path 1, 2 or 3,
+/* Describes the kernel that ts_sample would launch for `b` (path 1 .. 4,
  * CTAs per row, threads per CTA, dynamic shared memory bytes, grid size).
  * Any output pointer may be NULL. */
 ts_status ts_plan(const ts_sampler *s, const ts_batch *b, int32_t *path,

@@ -1,11 +1,13 @@
-"""The single-pass wide-row kernel (path 3) vs the CPU oracle, through the C ABI.
+"""The wide-row paths vs the CPU oracle, through the C ABI: the cluster
+kernel (path 3) and the split threshold + streaming kernels over a workspace
+(path 4).
 
-Covers the 151,936-wide stress rows on its sampled-threshold path and with
-the exact re-reading path forced, every cluster size, rows whose sample
-misleads the threshold (overflow, too few candidates), ties, signed zeros,
-non-finite values, degenerate parameters, and the narrower workloads forced
-onto the path (all-candidates mode).  Results must also equal the other
-kernel families' bit for bit.
+Covers the 151,936-wide stress rows on the sampled-threshold path and with
+the exact re-reading path forced, every cluster size / unit count, rows whose
+sample misleads the threshold (overflow, too few candidates), ties, signed
+zeros, non-finite values, degenerate parameters, and the narrower workloads
+forced onto the paths (all-candidates mode).  Results must also equal the
+other kernel families' bit for bit.
 """
 import numpy as np
 import pytest
@@ -23,8 +25,10 @@ def ts():
     return mod
 
 
-def make_sampler(ts, cap, path=3, cluster=0, exact=0):
+def make_sampler(ts, cap, path=3, cluster=0, exact=0, host=None):
     s = ts.Sampler(0, cap)
+    if path == 4:
+        s.reserve(int(host["n_rows"]), int(host["max_row_vocab"]))
     s.set_option(ts.TS_OPT_PATH, path)
     if cluster:
         s.set_option(ts.TS_OPT_CLUSTER, cluster)
@@ -70,21 +74,42 @@ def batch_from_rows(rows, *, cap, seed=0, gaps=True):
 # the stress shape: sampled threshold and forced exact path, all cluster sizes
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("exact", [0, 1])
-@pytest.mark.parametrize("rows,cluster", [(1, 0), (8, 0), (32, 4), (6, 8)])
-def test_stress_wide(ts, rows, cluster, exact):
+@pytest.mark.parametrize("path,rows,cluster", [(3, 1, 0), (3, 8, 0), (3, 32, 4), (3, 6, 8),
+                                               (4, 1, 0), (4, 8, 0), (4, 32, 0), (4, 6, 3),
+                                               (4, 5, 16)])
+def test_stress_wide(ts, path, rows, cluster, exact):
     host = workloads.make("stress", 2, rows=rows)
     ref = oracle.sample(host, max_keep=4096, n_threads=8)
-    s = make_sampler(ts, 4096, cluster=cluster, exact=exact)
+    s = make_sampler(ts, 4096, path=path, cluster=cluster, exact=exact, host=host)
     gpu = run_gpu(s, host, debug_keep=4096)
-    compare(host, gpu, ref, label=f"wide stress{rows} g{cluster} exact{exact}")
+    compare(host, gpu, ref, label=f"wide path{path} stress{rows} g{cluster} exact{exact}")
     s.close()
 
 
-def test_stress_512_default_plan_is_wide(ts):
+def test_stress_512_default_plans(ts):
     host = workloads.make("stress", 0, rows=512)
     s = ts.Sampler(0, 4096)
     batch = ts.DeviceBatch(host, "cuda")
+    assert s.plan(batch)["path"] == 3  # no workspace: the cluster path
+    s.reserve(512, workloads.STRESS_VOCAB)
+    plan = s.plan(batch)
+    assert plan["path"] == 4 and plan["grid"] == 512 * plan["ctas_per_row"]
+    s.reserve(0, 0)
     assert s.plan(batch)["path"] == 3
+    s.close()
+
+
+def test_stress_512_rows_split_sampled(ts):
+    """The full-size stress step on the split path, as the benchmark launches
+    it; the oracle checks 24 sampled rows one by one."""
+    host = workloads.make("stress", 3, rows=512)
+    s = make_sampler(ts, 4096, path=4, host=host)
+    gpu = run_gpu(s, host)
+    assert gpu["status"] == 0
+    rows = np.random.default_rng(9).choice(512, size=24, replace=False)
+    ref = oracle.sample(sub_batch(host, rows), max_keep=4096, n_threads=8)
+    safe = ref["margin"] > 1e-5
+    assert np.array_equal(gpu["ids"][rows][safe], ref["ids"][safe])
     s.close()
 
 
@@ -136,19 +161,19 @@ def _wide_rows(rng):
 
 
 @pytest.mark.parametrize("exact", [0, 1])
-@pytest.mark.parametrize("cluster", [1, 2, 4])
-def test_wide_edge_rows(ts, cluster, exact):
+@pytest.mark.parametrize("path,cluster", [(3, 1), (3, 2), (3, 4), (4, 0), (4, 2), (4, 7)])
+def test_wide_edge_rows(ts, path, cluster, exact):
     rng = np.random.default_rng(41)
     host = batch_from_rows(_wide_rows(rng), cap=4096, seed=cluster)
     ref = oracle.sample(host, max_keep=4096, n_threads=8)
     assert np.any(ref["err"] == 4) and np.any(ref["err"] == 0)
-    s = make_sampler(ts, 4096, cluster=cluster, exact=exact)
+    s = make_sampler(ts, 4096, path=path, cluster=cluster, exact=exact, host=host)
     gpu = run_gpu(s, host, debug_keep=4096)
-    compare(host, gpu, ref, label=f"wide edge g{cluster} exact{exact}")
+    compare(host, gpu, ref, label=f"wide edge path{path} g{cluster} exact{exact}")
     s.close()
 
 
-@pytest.mark.parametrize("path", [1, 2, 3])
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
 def test_signed_zero_ties_every_path(ts, path):
     """-0 and +0 are the same value: ties between them go by token index."""
     rng = np.random.default_rng(8)
@@ -160,7 +185,7 @@ def test_signed_zero_ties_every_path(ts, path):
         rows.append((x, 0.0, 30, 0.9))
     host = batch_from_rows(rows, cap=64, seed=3)
     ref = oracle.sample(host, max_keep=64)
-    s = make_sampler(ts, 64, path=path)
+    s = make_sampler(ts, 64, path=path, host=host)
     gpu = run_gpu(s, host, debug_keep=64)
     compare(host, gpu, ref, label=f"signed zeros path{path}")
     s.close()
@@ -169,12 +194,13 @@ def test_signed_zero_ties_every_path(ts, path):
 # ---------------------------------------------------------------------------
 # narrower workloads forced onto the wide path (all-candidates mode)
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("path", [3, 4])
 @pytest.mark.parametrize("name", ["mixed", "drama3", "qwen3tts"])
-def test_workloads_on_wide_path(ts, name):
+def test_workloads_on_wide_path(ts, name, path):
     host = workloads.make(name, 5)
     cap = host["cap"]
     ref = oracle.sample(host, max_keep=cap, n_threads=8)
-    s = make_sampler(ts, cap)
+    s = make_sampler(ts, cap, path=path, host=host)
     gpu = run_gpu(s, host, debug_keep=cap)
     compare(host, gpu, ref, label=f"{name} wide")
     s.close()
@@ -190,8 +216,9 @@ def test_wide_matches_other_paths_bit_for_bit(ts):
                 row_offsets=np.arange(rows, dtype=np.int64) * v, max_row_vocab=v,
                 top_k=np.array([1, 30, 700, 4096, 0], np.int32))
     outs = []
-    for path, g, exact in ((2, 0, 0), (3, 1, 0), (3, 2, 0), (3, 4, 0), (3, 8, 0), (3, 4, 1)):
-        s = make_sampler(ts, 4096, path=path, cluster=g, exact=exact)
+    for path, g, exact in ((2, 0, 0), (3, 1, 0), (3, 2, 0), (3, 4, 0), (3, 8, 0), (3, 4, 1),
+                           (4, 0, 0), (4, 3, 0), (4, 16, 0), (4, 2, 1)):
+        s = make_sampler(ts, 4096, path=path, cluster=g, exact=exact, host=host)
         outs.append(run_gpu(s, host, debug_keep=4096))
         s.close()
     ref = oracle.sample(host, max_keep=4096)
