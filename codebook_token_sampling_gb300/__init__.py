@@ -5,8 +5,8 @@ of sampling runs in the CUDA kernels of ``libts_sampler.so``.  PyTorch is used
 only for device memory and streams.  The functions keep the C names:
 
     ts_create, ts_destroy, ts_max_top_k, ts_sample, ts_sample_debug,
-    ts_reserve, ts_advance_steps, ts_read_status, ts_set_option, ts_plan,
-    ts_status_string, ts_last_error
+    ts_reserve, ts_sample_noalloc, ts_advance_steps, ts_read_status,
+    ts_set_option, ts_plan, ts_status_string, ts_last_error
 
 ``Sampler`` wraps a handle; ``DeviceBatch`` holds one step's per-row arrays on
 the GPU with a prebuilt ``ts_batch`` so that repeated calls marshal nothing.
@@ -39,9 +39,11 @@ TS_OPT_PDL = 3
 TS_OPT_WIDE_EXACT = 4
 TS_MAX_VOCAB_BF16 = 163840
 TS_MAX_VOCAB_F32 = 81920
+TS_NOALLOC_SCRATCH_BYTES = 4194304
+TS_NOALLOC_MAX_ROWS = 64
 
 EXPORTED = ("ts_create", "ts_destroy", "ts_max_top_k", "ts_sample", "ts_sample_debug",
-            "ts_reserve", "ts_advance_steps", "ts_read_status", "ts_set_option", "ts_plan",
+            "ts_reserve", "ts_sample_noalloc", "ts_advance_steps", "ts_read_status", "ts_set_option", "ts_plan",
             "ts_status_string", "ts_last_error")
 
 
@@ -93,6 +95,7 @@ def _load(path: str):
         "ts_sample": ([vp, ctypes.POINTER(TsBatch), vp], ctypes.c_int),
         "ts_sample_debug": ([vp, ctypes.POINTER(TsBatch), i32, vp, vp, vp, vp, vp], ctypes.c_int),
         "ts_reserve": ([vp, i32, i32], ctypes.c_int),
+        "ts_sample_noalloc": ([i32, ctypes.POINTER(TsBatch), vp, vp], ctypes.c_int),
         "ts_advance_steps": ([vp, i32, vp], ctypes.c_int),
         "ts_read_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
         "ts_set_option": ([vp, i32, i32], ctypes.c_int),
@@ -159,6 +162,20 @@ def ts_sample_debug(handle: int, batch: "DeviceBatch", max_keep: int, kept_ids, 
 
 def ts_reserve(handle: int, max_rows: int, max_row_vocab: int) -> None:
     _check(_lib.ts_reserve(handle, max_rows, max_row_vocab), "ts_reserve")
+
+
+def ts_sample_noalloc(batch: "DeviceBatch", max_top_k: int = 0, status=None,
+                      stream=None) -> None:
+    """Samples ``batch`` without any allocation, for callers whose memory is
+    all owned by their own pool (the workspace is the library's static scratch
+    array).  ``status``: a one-element int32 device tensor that collects the
+    row error bits, or None."""
+    st = _lib.ts_sample_noalloc(max_top_k, ctypes.byref(batch.c),
+                                status.data_ptr() if status is not None else None,
+                                _stream_ptr(stream))
+    if st == TS_ERR_UNSUPPORTED:
+        raise SamplerError(st, f"ts_sample_noalloc ({ts_last_error()})")
+    _check(st, "ts_sample_noalloc")
 
 
 def ts_advance_steps(step, stream=None) -> None:

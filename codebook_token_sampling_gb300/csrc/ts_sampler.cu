@@ -7,6 +7,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <type_traits>
 
@@ -32,6 +33,13 @@ struct ts_sampler {
   int ws_units;       // unit records it holds
   int ws_vocab;       // widest row it was sized for
 };
+
+// Scratch of ts_sample_noalloc, for callers that cannot allocate device
+// memory: the split path's workspace, after a 256-byte slot that takes the row
+// error bits of calls made without a status word.  Every device that loads this
+// library holds it until the process exits.  In host code the name stands for
+// the array; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TS_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
@@ -328,6 +336,54 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   return TS_OK;
 }
 
+// ---------------------------------------------------------------------------
+// ts_sample_noalloc: per-device set-up and geometry
+// ---------------------------------------------------------------------------
+constexpr size_t kNoallocWsOff = 256;  // the workspace follows the status slot
+constexpr int kNoallocMaxDevices = 64;
+
+struct NoallocDevice {
+  void *scratch;  // device address of g_noalloc_scratch; null until set up
+  int num_sms;
+};
+
+std::mutex g_noalloc_mu;
+NoallocDevice g_noalloc_dev[kNoallocMaxDevices];
+
+ts_status noalloc_reject(const char *what) {
+  std::snprintf(g_last_error, sizeof g_last_error, "ts_sample_noalloc: %s", what);
+  return TS_ERR_UNSUPPORTED;
+}
+
+// Once per device, with the device current: the scratch array's address and
+// the streaming kernel's dynamic shared-memory limit (the value ts_create
+// sets).  Neither allocates.
+ts_status noalloc_setup(int device, NoallocDevice *out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoallocDevice &d = g_noalloc_dev[device];
+  if (!d.scratch) {
+    int sms = 0, optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e == cudaSuccess)
+      e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    const void *fn = reinterpret_cast<const void *>(ts::split_stream_kernel);
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - static_cast<int>(fa.sharedSizeBytes));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    void *ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress");
+    d.num_sms = sms;
+    d.scratch = ptr;
+  }
+  *out = d;
+  return TS_OK;
+}
+
 __global__ void advance_steps_kernel(int64_t *step, int32_t n) {
   ts::pdl_wait_and_release();
   const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
@@ -468,6 +524,50 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab) {
   }
   cudaSetDevice(prev);
   return rc;
+}
+
+ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *status,
+                            void *stream) {
+  const int cap = cap_of(max_top_k);
+  if (cap < 0) return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK) return rc;
+  if (b->dtype != TS_DTYPE_BF16) return noalloc_reject("bf16 logits only");
+  if (b->n_rows > TS_NOALLOC_MAX_ROWS) return noalloc_reject("more than 64 rows");
+  if (b->n_rows > 0 && b->max_row_vocab > TS_MAX_VOCAB_BF16)
+    return noalloc_reject("max_row_vocab above TS_MAX_VOCAB_BF16");
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (device < 0 || device >= kNoallocMaxDevices) return noalloc_reject("device index above 63");
+  NoallocDevice d;
+  rc = noalloc_setup(device, &d);
+  if (rc != TS_OK || b->n_rows == 0) return rc;
+
+  // The split path's CTAs per row, fewer (down to what the widest slice
+  // allows) while the workspace would outgrow the scratch.
+  const int n = b->n_rows, vmax = b->max_row_vocab;
+  const int u_min = std::max(2, (vmax + ts::kWideSliceMax - 1) / ts::kWideSliceMax);
+  const size_t room = TS_NOALLOC_SCRATCH_BYTES - kNoallocWsOff;
+  int u = split_units(n, vmax, d.num_sms);
+  while (u > u_min && ts::split_workspace_bytes(n, n * u) > room) --u;
+  if (ts::split_workspace_bytes(n, n * u) > room) return noalloc_reject("scratch too small");
+
+  ts_sampler s;
+  std::memset(&s, 0, sizeof s);
+  s.device = device;
+  s.cap = cap;
+  s.num_sms = d.num_sms;
+  s.force_path = 4;
+  s.force_cluster = u;
+  s.pdl = 1;
+  s.status = status ? status : static_cast<uint32_t *>(d.scratch);
+  s.ws = static_cast<char *>(d.scratch) + kNoallocWsOff;
+  s.ws_bytes = room;
+  s.ws_rows = n;
+  s.ws_units = n * u;
+  s.ws_vocab = vmax;
+  return launch(&s, b, make_params(&s, b), static_cast<cudaStream_t>(stream));
 }
 
 ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream) {

@@ -154,6 +154,56 @@ ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep,
  * workspace.  Smaller requests than the current size keep it. */
 ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
 
+/* Scratch size and row limit of ts_sample_noalloc. */
+#define TS_NOALLOC_SCRATCH_BYTES 4194304
+#define TS_NOALLOC_MAX_ROWS 64
+
+/* The method's sources describe nothing like this call; it exists for callers
+ * that cannot allocate device memory.  An engine that reserves almost all of
+ * the GPU's memory for weights and KV cache at start-up and hands out memory
+ * only from its own pool cannot let a library call cudaMalloc: the call would
+ * fail, or take memory the pool does not know about.  cudaFree also waits
+ * for the whole device, which stalls every other stream of such an engine.
+ * Such callers can use neither ts_create (it allocates the status word) nor
+ * ts_reserve (it allocates the workspace).
+ *
+ * ts_sample_noalloc samples every row of `b` on `stream` exactly as
+ * ts_sample on a sampler of cap max_top_k would (the same ids, EOS flags and
+ * write-back; results never depend on the kernel geometry).  It runs the
+ * split kernels (a threshold kernel, then a streaming kernel whose last CTA
+ * per row finishes the row), and their workspace is a static device array of
+ * TS_NOALLOC_SCRATCH_BYTES (4 MiB) inside this library: every GPU that loads
+ * the library holds those 4 MiB until the process exits, used or not.  The
+ * call allocates nothing and frees nothing, on the host or the device.
+ *
+ * max_top_k: as in ts_create (0 = 64, else a power of two in [32, 4096]).
+ * b: as in ts_sample; bf16 logits only, at most TS_NOALLOC_MAX_ROWS (64) rows,
+ *   max_row_vocab <= TS_MAX_VOCAB_BF16.  Larger requests, and fp32 logits,
+ *   return TS_ERR_UNSUPPORTED and launch nothing; ts_last_error then names the
+ *   limit.  Within them the scratch always suffices (a row takes fewer CTAs
+ *   when many rows share the scratch).
+ * status: a device word owned by the caller; each row error ORs its bits into
+ *   it (it is never cleared here).  NULL drops the bits; rows with errors
+ *   still get out_ids = -1.
+ * stream: a cudaStream_t (NULL = legacy default stream); the call is
+ *   asynchronous.
+ *
+ * Set-up: the first call on a device (the current one) looks up the array's
+ * device address and raises the streaming kernel's shared-memory limit on
+ * that device; later calls reuse both.  Make that first call, which may have
+ * n_rows = 0 and then does only the set-up, before any stream capture.  The
+ * set-up is thread-safe; a failure returns TS_ERR_CUDA and is retried by the
+ * next call.
+ *
+ * Sharing: all calls on a device use the one array, which keeps what the last
+ * call left in it.  Each call's first kernel clears the per-row arrival
+ * counters that must start at zero, and the rest is written before it is
+ * read.  Calls whose kernels may overlap on the GPU (on unordered streams, or
+ * from several host threads without ordering) race on the array and give
+ * wrong results: order them on one stream or with events. */
+ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *status,
+                            void *stream);
+
 /* step[i] += 1 for i < n_streams, on the device (graph-capturable).  Call it
  * after the step's ts_sample so that sibling rows of one stream share a step. */
 ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream);
@@ -190,7 +240,8 @@ ts_status ts_plan(const ts_sampler *s, const ts_batch *b, int32_t *path,
                   int32_t *ctas_per_row, int32_t *threads, int32_t *smem_bytes,
                   int32_t *grid);
 
-/* Static strings; ts_last_error describes the last TS_ERR_CUDA of this thread. */
+/* Static strings; ts_last_error describes the last TS_ERR_CUDA of this thread,
+ * or the limit that its last rejected ts_sample_noalloc call exceeded. */
 const char *ts_status_string(ts_status st);
 const char *ts_last_error(void);
 
