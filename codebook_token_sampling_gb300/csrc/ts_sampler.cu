@@ -111,7 +111,7 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
     pl->g = u;
     pl->slice = slice;
     pl->threads = ts::kSplitThreads;
-    pl->smem = static_cast<int>(ts::kSplitSmemBytes);
+    pl->smem = static_cast<int>(ts::kStreamSmemBytes);
     pl->grid = b->n_rows * u;
     return TS_OK;
   }
@@ -245,7 +245,7 @@ ts_status set_attributes(int device) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  void *fns[24];
+  void *fns[25];
   int n = 0;
   const int gs[4] = {1, 2, 4, 8};
   for (int i = 0; i < 4; ++i) {
@@ -259,6 +259,7 @@ ts_status set_attributes(int device) {
     fns[n++] = warp_kernel_for<ts::KeyF32>(nchs[i]);
   }
   fns[n++] = reinterpret_cast<void *>(ts::split_stream_kernel);
+  fns[n++] = reinterpret_cast<void *>(ts::split_tail_kernel);
   for (int i = 0; i < n; ++i) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, fns[i]);
@@ -300,6 +301,10 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
     cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_stream_kernel), args);
     if (e != cudaSuccess) return cuda_fail(e, "split stream launch");
+    cfg.gridDim = dim3(static_cast<unsigned>(b->n_rows));
+    cfg.dynamicSmemBytes = ts::kTailSmemBytes;
+    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_tail_kernel), args);
+    if (e != cudaSuccess) return cuda_fail(e, "split tail launch");
     return TS_OK;
   }
   void *fn = nullptr;
@@ -356,7 +361,7 @@ ts_status noalloc_reject(const char *what) {
 }
 
 // Once per device, with the device current: the scratch array's address and
-// the streaming kernel's dynamic shared-memory limit (the value ts_create
+// the split kernels' dynamic shared-memory limits (the values ts_create
 // sets).  Neither allocates.
 ts_status noalloc_setup(int device, NoallocDevice *out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
@@ -367,13 +372,16 @@ ts_status noalloc_setup(int device, NoallocDevice *out) {
     if (e == cudaSuccess)
       e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    const void *fn = reinterpret_cast<const void *>(ts::split_stream_kernel);
-    cudaFuncAttributes fa;
-    e = cudaFuncGetAttributes(&fa, fn);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             optin - static_cast<int>(fa.sharedSizeBytes));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    const void *fns[2] = {reinterpret_cast<const void *>(ts::split_stream_kernel),
+                          reinterpret_cast<const void *>(ts::split_tail_kernel)};
+    for (const void *fn : fns) {
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, fn);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               optin - static_cast<int>(fa.sharedSizeBytes));
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    }
     void *ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess || !ptr) return cuda_fail(e, "cudaGetSymbolAddress");

@@ -1,28 +1,32 @@
-// ts_split.cuh -- the wide-row sampler as two kernels over a workspace (bf16
-// rows such as the 151,936-token backbone vocabulary, any top-k cap up to
-// 4096: Drama 3 article, section "能跑通的命令，和文档写明的边界").
+// ts_split.cuh -- the wide-row sampler as three kernels over a workspace
+// (bf16 rows such as the 151,936-token backbone vocabulary, any top-k cap up
+// to 4096: Drama 3 article, section "能跑通的命令，和文档写明的边界").
 //
 // Kernel A (one CTA per row) reads an evenly spaced sample of the row and
 // stores the threshold key t (the sampling step of Floyd and Rivest's
-// selection, "Expected time bounds for selection", CACM 18(3), 1975); it
-// also resets the row's arrival counter.
+// selection, "Expected time bounds for selection", CACM 18(3), 1975).
 //
 // Kernel B (U CTAs per row, one contiguous slice each) streams its slice
 // once with 16-byte loads and keeps every logit >= t: candidates (key << 16 |
 // slice index), their counts by key >> 8, the maximum key and a NaN / +inf
-// flag go to the workspace.  A CTA that is not the last of its row to arrive
-// leaves at once, so the streaming CTAs never wait for one another.  The
-// last one gathers the row's candidates (a few thousand, from L2) and runs
-// the row's tail alone:
-//   - the threshold key thr (the k_eff-th largest) and `need`, the kept
-//     tokens tied at it, from the page counts and one 256-bin pass;
-//   - the kept masses (2^-40 fixed point, depending only on the key) over
-//     256 coarse bins of (max key - key) >> shift, then an exact level inside
-//     the bins of the nucleus cutoff and of the draw;
-//   - the drawn token by a radix select on the token index.
+// flag go to the workspace.  It does nothing else, so the streaming CTAs
+// never wait for one another or hold an SM for a row's tail.
+//
+// Kernel C (one CTA per row) gathers the row's candidates (a few thousand,
+// from L2) and runs the row's tail:
+//   - the threshold key's page from the page counts, issued while the
+//     candidate loads are in flight, and the candidates counted per key as
+//     they arrive;
+//   - the keys that occur, compacted in key order, so that one block scan
+//     over them gives the threshold key thr (the k_eff-th largest) and
+//     `need`, the kept tokens tied at it, and one more the kept masses (2^-40
+//     fixed point, depending only on the key), the nucleus cutoff and the
+//     draw;
+//   - the drawn token: the rho-th lowest token index among the candidates
+//     that share the drawn key.
 // If the sample misled t (fewer than k_eff candidates, or more than the
-// buffers hold) the last CTA re-reads the row and selects exactly.  Nothing
-// waits on another CTA: the only cross-CTA step is an atomic counter.
+// buffers hold) kernel C re-reads the row and selects exactly.  Candidates
+// spread over too many keys take a coarse-bin tail instead.
 #pragma once
 
 #include "ts_wide.cuh"
@@ -34,23 +38,36 @@ constexpr int kSplitUnitCap = 4096;     // candidates one CTA may hand over
 constexpr int kSplitRowCap = 8192;      // candidates the last CTA gathers
 constexpr int kSplitMaxUnits = 16;
 constexpr int kSplitU = 4;              // 16-byte chunks per lane per iteration
-// dynamic shared memory: the gathered candidates (32 KB; the streaming phase
-// keeps its own candidates and staging rings there), the tail's histograms
-// (20 KB), page counts and bookkeeping
-constexpr uint32_t kSplitCandOff = 0;
-constexpr uint32_t kSplitRingOff = kSplitUnitCap * 4;                       // streaming only
 constexpr int kSplitKeyPages = 32;       // per-key counts for up to 32 pages of 256 keys
-constexpr uint32_t kSplitHwOff = kSplitRowCap * 4;                          // 20 KB
-constexpr uint32_t kSplitPgOff = kSplitHwOff + 20480;                       // 256 words
-constexpr uint32_t kSplitSegOff = kSplitPgOff + 1024;                       // 32 words
-constexpr uint32_t kSplitMiscOff = kSplitSegOff + 128;                      // 256 words
-constexpr uint32_t kSplitSmemBytes = kSplitMiscOff + kWideMiscWords * 4;
+constexpr int kSplitListCap = 1024;      // distinct candidate keys the compact tail takes
+static_assert(kSplitThreads == kWideThreads, "the block scans assume 8 warps");
+
+// Kernel B's dynamic shared memory: the unit's candidates, the warps'
+// staging rings, page counts and bookkeeping (22 KB).
+constexpr uint32_t kStreamCandOff = 0;
+constexpr uint32_t kStreamRingOff = kSplitUnitCap * 4;
+constexpr uint32_t kStreamPgOff = kStreamRingOff + kWideWarps * kWideRing * 8;
+constexpr uint32_t kStreamMiscOff = kStreamPgOff + 1024;
+constexpr uint32_t kStreamSmemBytes = kStreamMiscOff + kWideMiscWords * 4;
+
+// Kernel C's: the gathered candidates (32 KB), a 16 KB work area (per-key
+// counts, then the coarse-bin tail, the exact path's histogram or the rank
+// lists), the compacted key list, page counts, page <-> slot maps, unit
+// segments and bookkeeping (55.25 KB: four CTAs per SM).
+constexpr uint32_t kTailCandOff = 0;
+constexpr uint32_t kTailHwOff = kSplitRowCap * 4;
+constexpr uint32_t kTailListOff = kTailHwOff + 16384;
+constexpr uint32_t kTailPgOff = kTailListOff + kSplitListCap * 4;
+constexpr uint32_t kTailPageSlotOff = kTailPgOff + 1024;
+constexpr uint32_t kTailSlotPageOff = kTailPageSlotOff + 1024;
+constexpr uint32_t kTailSegOff = kTailSlotPageOff + kSplitKeyPages * 4;
+constexpr uint32_t kTailMiscOff = kTailSegOff + 128;
+constexpr uint32_t kTailSmemBytes = kTailMiscOff + kWideMiscWords * 4;
 
 // Workspace layout, in 4-byte words (every region 16-byte aligned).
 struct SplitRowMeta {
   uint32_t t_key;
-  uint32_t arrived;
-  uint32_t pad[2];
+  uint32_t pad[3];
 };
 struct SplitUnitMeta {
   uint32_t n;     // candidates of the unit (may exceed kSplitUnitCap)
@@ -89,7 +106,7 @@ __device__ __forceinline__ SplitWs split_ws(void *base, int max_rows, int max_un
 }
 
 // ---------------------------------------------------------------------------
-// Kernel A: the row's threshold key from its sample; resets the counter.
+// Kernel A: the row's threshold key from its sample.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Params p) {
   __shared__ __align__(16) uint32_t hist[2048];
@@ -109,10 +126,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Pa
       t_key = wide_sample_threshold(rowp, w.vocab, w.k_eff, 1, hist, misc,
                                     reinterpret_cast<uint64_t *>(misc + kWScan));
   }
-  if (t == 0) {
-    ws.row[r].t_key = t_key;
-    ws.row[r].arrived = 0u;
-  }
+  if (t == 0) ws.row[r].t_key = t_key;
 }
 
 // One candidate of the streaming phase: its entry, its page count and the
@@ -155,6 +169,17 @@ __device__ __forceinline__ void split_drain(const uint2 *ring, uint32_t head, ui
   if (f1) split_keep(k1, idx0 + 1u, pos + (f0 ? 1u : 0u), cand, pg, kmax);
 }
 
+// The unit whose segment holds flattened entry i, for nondecreasing seg[0 ..
+// U] with seg[0] = 0 <= i < seg[U] and U <= 16: a binary search of four fixed
+// steps (no data-dependent loop, so the lanes of a warp stay converged).
+__device__ __forceinline__ int split_unit_of(const uint32_t *seg, int U, uint32_t i) {
+  int c = 0;
+#pragma unroll
+  for (int step = 8; step >= 1; step >>= 1)
+    if (c + step < U && i >= seg[c + step]) c += step;
+  return c;
+}
+
 // The rho-th smallest (0-based) token index among the gathered candidates
 // with key `key_sel`; segment c of the array came from unit c, whose slice
 // starts at token c * S.  Two-level radix select on the 18-bit index.
@@ -169,16 +194,17 @@ __device__ uint32_t split_rank_select(const uint32_t *cand, int n, const uint32_
     h[2 * t] = 0u;
     h[2 * t + 1] = 0u;
     __syncthreads();
-    int c = 0;
-    for (int i = t; i < n; i += kSplitThreads) {
-      while (c + 1 < U && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
-      const uint32_t e = cand[i];
-      if ((e >> 16) != key_sel) continue;
-      const uint32_t g = static_cast<uint32_t>(c * S) + (e & 0xFFFFu);
-      if (level == 0)
-        atomicAdd(&h[g >> 9], 1u);
-      else if ((g >> 9) == b1)
-        atomicAdd(&h[g & 511u], 1u);
+#pragma unroll 4
+    for (int base = 0; base < n; base += kSplitThreads) {
+      const int i = base + t;
+      const uint32_t e = i < n ? cand[i] : 0u;
+      if (i < n && (e >> 16) == key_sel) {
+        const uint32_t g = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
+        if (level == 0)
+          atomicAdd(&h[g >> 9], 1u);
+        else if ((g >> 9) == b1)
+          atomicAdd(&h[g & 511u], 1u);
+      }
     }
     __syncthreads();
     const uint32_t want = rho - below;
@@ -357,12 +383,10 @@ __device__ void split_row_tail(const Params &p, int r, const Row &w, const uint3
     __syncthreads();
     const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
     const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
-    int c = 0;
     for (int i = t; i < n; i += kSplitThreads) {
-      while (c + 1 < U && static_cast<uint32_t>(i) >= seg[c + 1]) ++c;
       const uint32_t e = cand[i];
       const uint32_t key = e >> 16;
-      const uint32_t g = static_cast<uint32_t>(c * S) + (e & 0xFFFFu);
+      const uint32_t g = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
       if (key > thr || (key == thr && need && g <= idx_cut)) {
         const uint32_t pos = atomicAdd(&misc[kWKept], 1u);
         if (pos < static_cast<uint32_t>(p.max_keep)) {
@@ -380,24 +404,15 @@ __device__ void split_row_tail(const Params &p, int r, const Row &w, const uint3
   }
 }
 
-// The row's tail from per-key counts: every page (256 keys, key >> 8) at or
-// above the threshold's page that holds a candidate gets a slot of 256
-// packed 16-bit counts; one pass counts the candidates per key, and block
-// scans over those keys (in key order) give the threshold key and `need`,
-// S_k, the nucleus cutoff and the draw, with one weight evaluation per key
-// that occurs.  Returns false (nothing written) when more than
-// kSplitKeyPages pages are occupied; the caller then runs split_row_tail.
-__device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint32_t *cand, int n,
-                               const uint32_t *seg, int U, int S, const uint32_t *pgc,
-                               uint32_t maxk, uint32_t *hw, uint32_t *misc, uint64_t *scratch) {
+// The threshold key's page (the page holding the k_eff-th largest candidate,
+// from the counts by key >> 8) and a slot of 256 packed 16-bit per-key counts
+// for each occupied page at or above it, cleared.  Returns the number of
+// such pages; above kSplitKeyPages nothing is cleared and the caller takes
+// the coarse-bin tail.  misc[kWDigit] = the page.
+__device__ int split_key_setup(const uint32_t *pgc, uint32_t k_eff, uint32_t *kc,
+                               uint32_t *page_slot, uint32_t *slot_page, uint32_t *misc,
+                               uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
-  const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
-  uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
-  uint32_t *kc = hw;                           // [slot][128] packed counts (16 KB)
-  uint32_t *page_slot = hw + kSplitKeyPages * 128;
-  uint32_t *slot_page = page_slot + 256;       // 32
-  uint32_t *rs = slot_page + 32;               // rank select (512)
-  // ---- the threshold's page; slots for the occupied pages at or above it ----
   const uint32_t c = pgc[t];
   wide_select256(c, k_eff, misc, scratch);
   const uint32_t page = misc[kWDigit];
@@ -405,71 +420,182 @@ __device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint3
   uint64_t n_occ;
   const uint32_t slot = static_cast<uint32_t>(wide_excl_scan_u64(occ ? 1u : 0u, scratch, &n_occ));
   const int up = static_cast<int>(n_occ);
-  if (up > kSplitKeyPages) return false;
-  page_slot[t] = occ ? slot : 0xFFFFFFFFu;
+  if (up > kSplitKeyPages) return up;
+  page_slot[t] = occ ? slot : 0u;
   if (occ) slot_page[slot] = static_cast<uint32_t>(t);
   for (int i = t; i < up * 128; i += kSplitThreads) kc[i] = 0u;
   __syncthreads();
-#pragma unroll 4
-  for (int i = t; i < n; i += kSplitThreads) {
-    const uint32_t key = cand[i] >> 16;
-    if ((key >> 8) < page) continue;
-    const uint32_t sl = page_slot[key >> 8];
-    atomicAdd(&kc[sl * 128 + ((key & 255u) >> 1)], 1u << ((key & 1u) * 16u));
+  return up;
+}
+
+// Counts one candidate key (at or above the threshold's page) in its slot.
+__device__ __forceinline__ void split_key_count(uint32_t key, uint32_t page,
+                                                const uint32_t *page_slot, uint32_t *kc) {
+  if ((key >> 8) >= page)
+    atomicAdd(&kc[page_slot[key >> 8] * 128u + ((key & 255u) >> 1)], 1u << ((key & 1u) * 16u));
+}
+
+// Exclusive block scans of two values at once (one pass of barriers).
+__device__ __forceinline__ void split_excl_scan2(uint64_t a, uint32_t b, uint64_t *scratch,
+                                                 uint64_t *ex_a, uint64_t *tot_a, uint32_t *ex_b,
+                                                 uint32_t *tot_b) {
+  const uint32_t lane = lane_id(), wid = threadIdx.x >> 5;
+  uint64_t x = a;
+  uint32_t y = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t tx = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    const uint32_t ty = __shfl_up_sync(0xFFFFFFFFu, y, o);
+    if (lane >= static_cast<uint32_t>(o)) {
+      x += tx;
+      y += ty;
+    }
+  }
+  __syncthreads();  // scratch may still be read by a previous scan
+  if (lane == 31) {
+    scratch[wid] = x;
+    scratch[16 + wid] = y;
   }
   __syncthreads();
-  // bins in key order: bin b = slot b >> 8, low byte b & 255; thread t owns
-  // bins [t * up, t * up + up)
-  auto bin_key = [&](int b) { return (slot_page[b >> 8] << 8) | static_cast<uint32_t>(b & 255); };
-  auto bin_cnt = [&](int b) {
-    return (kc[(b >> 8) * 128 + ((b & 255) >> 1)] >> ((b & 1) * 16)) & 0xFFFFu;
-  };
+  if (wid == 0) {
+    const uint64_t sa = lane < kWideWarps ? scratch[lane] : 0ull;
+    const uint64_t sb = lane < kWideWarps ? scratch[16 + lane] : 0ull;
+    uint64_t ia = sa, ib = sb;
+#pragma unroll
+    for (int o = 1; o < kWideWarps; o <<= 1) {
+      const uint64_t ta = __shfl_up_sync(0xFFFFFFFFu, ia, o);
+      const uint64_t tb = __shfl_up_sync(0xFFFFFFFFu, ib, o);
+      if (lane >= static_cast<uint32_t>(o)) {
+        ia += ta;
+        ib += tb;
+      }
+    }
+    if (lane < kWideWarps) {
+      scratch[lane] = ia - sa;
+      scratch[16 + lane] = ib - sb;
+    }
+    if (lane == kWideWarps - 1) {
+      scratch[kWideWarps] = ia;
+      scratch[16 + kWideWarps] = ib;
+    }
+  }
+  __syncthreads();
+  *ex_a = scratch[wid] + x - a;
+  *tot_a = scratch[kWideWarps];
+  *ex_b = static_cast<uint32_t>(scratch[16 + wid]) + y - b;
+  *tot_b = static_cast<uint32_t>(scratch[16 + kWideWarps]);
+}
+
+// The rho-th smallest token index among the n_key candidates with key `key`
+// (n_key <= kSplitThreads): the indices are collected, and the one with
+// exactly rho smaller ones is it.  rl: n_key words of scratch.
+__device__ uint32_t split_small_rank(const uint32_t *cand, int n, const uint32_t *seg, int U,
+                                     int S, uint32_t key, uint32_t n_key, uint32_t rho,
+                                     uint32_t *rl, uint32_t *misc) {
+  const int t = static_cast<int>(threadIdx.x);
+  if (t == 0) misc[kWN] = 0u;
+  __syncthreads();
+#pragma unroll 4
+  for (int base = 0; base < n; base += kSplitThreads) {
+    const int i = base + t;
+    const uint32_t e = i < n ? cand[i] : 0u;
+    if (i < n && (e >> 16) == key) {
+      const uint32_t pos = atomicAdd(&misc[kWN], 1u);
+      if (pos < n_key)
+        rl[pos] = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
+    }
+  }
+  __syncthreads();
+  if (static_cast<uint32_t>(t) < n_key) {
+    const uint32_t g = rl[t];
+    uint32_t below = 0;
+    for (uint32_t j = 0; j < n_key; ++j) below += rl[j] < g ? 1u : 0u;
+    if (below == rho) misc[kWSelIdx] = g;
+  }
+  __syncthreads();
+  return misc[kWSelIdx];
+}
+
+// The row's tail from the per-key counts of split_key_setup: the occupied
+// keys are compacted in key order (one entry, key << 16 | count, per key
+// that occurs), and each thread takes up to four consecutive entries in
+// descending key order, so that block scans over the entries give the
+// threshold key and `need`, S_k, the nucleus cutoff and the draw, with one
+// weight evaluation per key.  Returns false (nothing written) when more than
+// kSplitListCap keys occur; the caller then runs split_row_tail.
+__device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint32_t *cand, int n,
+                               const uint32_t *seg, int U, int S, uint32_t maxk, int up,
+                               uint32_t u24, uint32_t *kc, uint32_t *list,
+                               const uint32_t *slot_page, uint32_t *misc, uint64_t *scratch) {
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
+  uint64_t *m64 = reinterpret_cast<uint64_t *>(misc);
+  auto bin_cnt = [&](int b) { return (kc[b >> 1] >> ((b & 1) * 16)) & 0xFFFFu; };
+  // ---- the keys that occur, in ascending order (thread t owns bins
+  // [t * up, t * up + up), bin b = slot b >> 8, low byte b & 255) ----
   const int b0 = t * up;
+  uint32_t occ = 0;
+#pragma unroll 8
+  for (int j = 0; j < up; ++j) occ += bin_cnt(b0 + j) != 0u ? 1u : 0u;
+  uint64_t n_list;
+  uint32_t pos = static_cast<uint32_t>(wide_excl_scan_u64(occ, scratch, &n_list));
+  const int L = static_cast<int>(n_list);
+  if (L > kSplitListCap) return false;
+#pragma unroll 8
+  for (int j = 0; j < up; ++j) {
+    const int b = b0 + j;
+    const uint32_t c = bin_cnt(b);
+    if (c) list[pos++] = (((slot_page[b >> 8] << 8) | static_cast<uint32_t>(b & 255)) << 16) | c;
+  }
+  __syncthreads();
+  // ---- entries j0 .. j0 + E - 1 in descending key order ----
+  const int E = (L + kSplitThreads - 1) / kSplitThreads;  // <= 4
+  const int j0 = t * E;
+  uint32_t ek[4], ec[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = j0 + q;
+    const uint32_t e = q < E && j < L ? list[L - 1 - j] : 0u;
+    ek[q] = e >> 16;
+    ec[q] = e & 0xFFFFu;
+  }
   // ---- threshold key (k_eff-th largest) and `need` ----
-  uint32_t s = 0;
-  for (int b = b0; b < b0 + up; ++b) s += bin_cnt(b);
+  const uint32_t s = ec[0] + ec[1] + ec[2] + ec[3];
   uint64_t tot;
-  uint32_t ex = static_cast<uint32_t>(wide_excl_scan_u64(s, scratch, &tot));
-  uint32_t above = static_cast<uint32_t>(tot) - ex - s;
+  const uint32_t above = static_cast<uint32_t>(wide_excl_scan_u64(s, scratch, &tot));
   if (s != 0 && above < k_eff && above + s >= k_eff) {
     uint32_t run = above;
-    for (int b = b0 + up - 1; b >= b0; --b) {
-      const uint32_t cb = bin_cnt(b);
-      if (run < k_eff && run + cb >= k_eff) {
-        misc[kWTKey] = bin_key(b);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (ec[q] && run < k_eff && run + ec[q] >= k_eff) {
+        misc[kWTKey] = ek[q];
         misc[kWTake] = k_eff - run;
       }
-      run += cb;
+      run += ec[q];
     }
   }
   __syncthreads();
   const uint32_t thr = misc[kWTKey];
   const uint32_t need = misc[kWTake];
   const float m = KeyBF16::value(maxk);
-  const uint32_t u24 = misc[kWU24];
   uint32_t key_d = maxk, rho = 0, n_p = 1;
+  uint32_t c_d = list[L - 1] & 0xFFFFu;  // candidates with the largest key
   uint64_t s_k = 0;
   if (!w.greedy) {
-    auto kept = [&](int b, uint32_t key) {
-      return key > thr ? bin_cnt(b) : (key == thr ? need : 0u);
-    };
-    auto weight = [&](uint32_t key) {
-      return to_fixed(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp));
-    };
+    uint32_t kq[4];
+    uint64_t wq[4];
     uint64_t st = 0;
     uint32_t ct = 0;
-    for (int b = b0; b < b0 + up; ++b) {
-      const uint32_t key = bin_key(b), cnt = kept(b, key);
-      if (cnt) {
-        st += cnt * weight(key);
-        ct += cnt;
-      }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      kq[q] = ec[q] == 0u ? 0u : ek[q] > thr ? ec[q] : ek[q] == thr ? need : 0u;
+      wq[q] = kq[q] ? to_fixed(kept_weight(KeyBF16::value(ek[q]), m, w.temp, w.inv_temp)) : 0ull;
+      st += kq[q] * wq[q];
+      ct += kq[q];
     }
-    const uint64_t ex_m = wide_excl_scan_u64(st, scratch, &s_k);
-    const uint64_t above_m = s_k - ex_m - st;
-    uint64_t n_kept;
-    const uint32_t ex_c = static_cast<uint32_t>(wide_excl_scan_u64(ct, scratch, &n_kept));
-    const uint32_t above_c = static_cast<uint32_t>(n_kept) - ex_c - ct;
+    uint64_t ex_m;
+    uint32_t ex_c, n_kept;
+    split_excl_scan2(st, ct, scratch, &ex_m, &s_k, &ex_c, &n_kept);
     // ---- nucleus cutoff ----
     uint64_t s_p;
     if (w.top_p >= 1.0f) {
@@ -480,21 +606,20 @@ __device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint3
       s_p = to_fixed(kept_weight(m, m, w.temp, w.inv_temp));
     } else {
       const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
-      if (st != 0 && above_m < cut && above_m + st >= cut) {
-        uint64_t cum = above_m;
-        uint32_t ccum = above_c;
-        for (int b = b0 + up - 1; b >= b0; --b) {
-          const uint32_t key = bin_key(b), cnt = kept(b, key);
-          if (!cnt) continue;
-          const uint64_t wb = weight(key), mb = cnt * wb;
-          if (cum < cut && cum + mb >= cut) {
-            uint64_t n_c = wb > 0 ? (cut - cum + wb - 1) / wb : 1;
+      if (st != 0 && ex_m < cut && ex_m + st >= cut) {
+        uint64_t cum = ex_m;
+        uint32_t ccum = ex_c;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t mb = kq[q] * wq[q];
+          if (mb && cum < cut && cum + mb >= cut) {
+            uint64_t n_c = (cut - cum + wq[q] - 1) / wq[q];
             if (n_c < 1) n_c = 1;
-            m64[kWSp / 2] = cum + n_c * wb;
+            m64[kWSp / 2] = cum + n_c * wq[q];
             misc[kWNp] = ccum + static_cast<uint32_t>(n_c);
           }
           cum += mb;
-          ccum += cnt;
+          ccum += kq[q];
         }
       }
       __syncthreads();
@@ -503,15 +628,15 @@ __device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint3
     }
     // ---- draw ----
     const uint64_t target = scale_u24(u24, s_p);
-    if (st != 0 && above_m <= target && target < above_m + st) {
-      uint64_t cum = above_m;
-      for (int b = b0 + up - 1; b >= b0; --b) {
-        const uint32_t key = bin_key(b), cnt = kept(b, key);
-        if (!cnt) continue;
-        const uint64_t wb = weight(key), mb = cnt * wb;
-        if (cum <= target && target < cum + mb) {
-          misc[kWDrawB] = key;
-          misc[kWRho] = static_cast<uint32_t>((target - cum) / wb);
+    if (st != 0 && ex_m <= target && target < ex_m + st) {
+      uint64_t cum = ex_m;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t mb = kq[q] * wq[q];
+        if (mb && cum <= target && target < cum + mb) {
+          misc[kWDrawB] = ek[q];
+          misc[kWRho] = static_cast<uint32_t>((target - cum) / wq[q]);
+          misc[kWCount] = ec[q];
         }
         cum += mb;
       }
@@ -519,28 +644,30 @@ __device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint3
     __syncthreads();
     key_d = misc[kWDrawB];
     rho = misc[kWRho];
+    c_d = misc[kWCount];
   }
-  const uint32_t id = split_rank_select(cand, n, seg, U, S, key_d, rho, rs, misc, scratch);
+  // ---- the drawn token (kc is free once the list is built) ----
+  const uint32_t id = c_d <= static_cast<uint32_t>(kSplitThreads)
+                          ? split_small_rank(cand, n, seg, U, S, key_d, c_d, rho, kc, misc)
+                          : split_rank_select(cand, n, seg, U, S, key_d, rho, kc, misc, scratch);
   if (t == 0) finish_row(p, r, w, static_cast<int32_t>(id), 0u);
   if (p.kept_ids) {
     // keys above thr, and the `need` lowest-index keys at thr
     const uint32_t idx_cut =
-        need ? split_rank_select(cand, n, seg, U, S, thr, need - 1, rs, misc, scratch) : 0u;
+        need ? split_rank_select(cand, n, seg, U, S, thr, need - 1, kc, misc, scratch) : 0u;
     if (t == 0) misc[kWKept] = 0u;
     __syncthreads();
     const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
     const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
-    int cs = 0;
     for (int i = t; i < n; i += kSplitThreads) {
-      while (cs + 1 < U && static_cast<uint32_t>(i) >= seg[cs + 1]) ++cs;
       const uint32_t e = cand[i];
       const uint32_t key = e >> 16;
-      const uint32_t g = static_cast<uint32_t>(cs * S) + (e & 0xFFFFu);
+      const uint32_t g = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
       if (key > thr || (key == thr && need && g <= idx_cut)) {
-        const uint32_t pos = atomicAdd(&misc[kWKept], 1u);
-        if (pos < static_cast<uint32_t>(p.max_keep)) {
-          p.kept_ids[rb + pos] = static_cast<int32_t>(g);
-          p.kept_probs[rb + pos] =
+        const uint32_t at = atomicAdd(&misc[kWKept], 1u);
+        if (at < static_cast<uint32_t>(p.max_keep)) {
+          p.kept_ids[rb + at] = static_cast<int32_t>(g);
+          p.kept_probs[rb + at] =
               w.greedy ? (g == id ? 1.f : 0.f)
                        : __fdiv_rn(kept_weight(KeyBF16::value(key), m, w.temp, w.inv_temp), s_real);
         }
@@ -554,7 +681,7 @@ __device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint3
   return true;
 }
 
-// Exact fallback of the last CTA: the whole row read again, the k_eff-th
+// Exact fallback of kernel C: the whole row read again, the k_eff-th
 // largest key by radix select (11 + 5 bits), and the exact top-k set
 // collected in token order, ties at the threshold by lowest index, as
 // (key << 16 | slice index) entries grouped by unit (unit c's entries are
@@ -691,16 +818,14 @@ __device__ bool split_exact(const char *rowp, int V, int U, int S, uint32_t k_ef
 }
 
 // ---------------------------------------------------------------------------
-// Kernel B: stream, hand over, and (last CTA of the row) the tail.
+// Kernel B: stream the slice once and hand its candidates over.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
-  uint32_t *cand = reinterpret_cast<uint32_t *>(smem + kSplitCandOff);
-  uint2 *rings = reinterpret_cast<uint2 *>(smem + kSplitRingOff);
-  uint32_t *hw = reinterpret_cast<uint32_t *>(smem + kSplitHwOff);
-  uint32_t *pg = reinterpret_cast<uint32_t *>(smem + kSplitPgOff);
-  uint32_t *seg = reinterpret_cast<uint32_t *>(smem + kSplitSegOff);
-  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kSplitMiscOff);
+  uint32_t *cand = reinterpret_cast<uint32_t *>(smem + kStreamCandOff);
+  uint2 *rings = reinterpret_cast<uint2 *>(smem + kStreamRingOff);
+  uint32_t *pg = reinterpret_cast<uint32_t *>(smem + kStreamPgOff);
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kStreamMiscOff);
   uint64_t *scratch = reinterpret_cast<uint64_t *>(misc + kWScan);
 
   const int U = p.ws_units_per_row;
@@ -714,9 +839,8 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
     return;
   }
   const Row w = load_row(p, r);
-  if (w.err) {
+  if (w.err) {  // kernel C reports it
     pdl_wait_and_release();
-    if (u == 0 && t == 0) finish_row(p, r, w, -1, w.err);
     return;
   }
   // ---- slice geometry; the first loads go out before the threshold arrives
@@ -744,9 +868,6 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
   }
   pg[t] = 0u;  // kSplitThreads == 256 pages
   if (t == 0) misc[kWN] = 0u;
-  if (t == 32 && !w.greedy)
-    misc[kWU24] = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
-                             static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
   pdl_wait_and_release();  // the threshold kernel has finished
   SplitWs ws = split_ws(p.workspace, p.ws_rows, p.ws_units);
   const uint32_t t_key = __ldcg(&ws.row[r].t_key);
@@ -826,16 +947,53 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
     mt.pad = 0u;
     __stcg(reinterpret_cast<uint4 *>(&ws.unit[ui]), *reinterpret_cast<uint4 *>(&mt));
   }
-  __threadfence();
-  __syncthreads();
-  if (t == 0) misc[kWFast] = atomicAdd(&ws.row[r].arrived, 1u) == static_cast<uint32_t>(U - 1);
-  __syncthreads();
-  if (!misc[kWFast]) return;
-  __threadfence();
+}
 
-  // ---- last CTA of the row: gather and tail (every load of a step is issued
-  // before any is used: the units' records are independent) ----
+// ---------------------------------------------------------------------------
+// Kernel C: one CTA per row gathers the units' candidates and runs the tail.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kSplitThreads, 4) split_tail_kernel(const Params p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  uint32_t *cand = reinterpret_cast<uint32_t *>(smem + kTailCandOff);
+  uint32_t *hw = reinterpret_cast<uint32_t *>(smem + kTailHwOff);
+  uint32_t *list = reinterpret_cast<uint32_t *>(smem + kTailListOff);
+  uint32_t *pgc = reinterpret_cast<uint32_t *>(smem + kTailPgOff);
+  uint32_t *page_slot = reinterpret_cast<uint32_t *>(smem + kTailPageSlotOff);
+  uint32_t *slot_page = reinterpret_cast<uint32_t *>(smem + kTailSlotPageOff);
+  uint32_t *seg = reinterpret_cast<uint32_t *>(smem + kTailSegOff);
+  uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kTailMiscOff);
+  uint64_t *scratch = reinterpret_cast<uint64_t *>(misc + kWScan);
+
+  const int r = static_cast<int>(blockIdx.x);
+  const int t = static_cast<int>(threadIdx.x);
+  const uint32_t lane = lane_id();
+  if (r >= p.n_rows) {
+    pdl_wait_and_release();
+    return;
+  }
+  // the inputs were complete before the threshold kernel started
+  const Row w = load_row(p, r);
+  if (t == 32 && !w.err && !w.greedy)
+    misc[kWU24] = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
+                             static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
+  pdl_wait_and_release();  // the streaming kernel has finished
+  if (w.err) {
+    if (t == 0) finish_row(p, r, w, -1, w.err);
+    return;
+  }
+  const int U = p.ws_units_per_row;
+  const int S = p.slice;
+  const int V = w.vocab;
+  const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
+  SplitWs ws = split_ws(p.workspace, p.ws_rows, p.ws_units);
   const size_t u0 = static_cast<size_t>(r) * U;
+
+  // ---- the units' records (warp 0) and page counts (every thread), in one
+  // round of loads ----
+  uint32_t pv[kSplitMaxUnits];
+#pragma unroll
+  for (int c = 0; c < kSplitMaxUnits; ++c)
+    pv[c] = c < U ? __ldcg(&ws.pg[(u0 + c) * 256 + t]) : 0u;
   if (t < 32) {
     uint4 mt = make_uint4(0u, 0u, 0u, 0u);
     if (t < U) mt = __ldcg(reinterpret_cast<const uint4 *>(&ws.unit[u0 + t]));
@@ -857,49 +1015,57 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
       misc[kWRange] = fl ? 1u : 0u;
     }
   }
+  uint32_t psum = 0;
+#pragma unroll
+  for (int c = 0; c < kSplitMaxUnits; ++c) psum += pv[c];
+  pgc[t] = psum;
   __syncthreads();
   const uint32_t total = misc[kWTotal], any_bad = misc[kWBad], full = misc[kWRange];
+  const uint32_t u24 = misc[kWU24];
   uint32_t maxk = misc[kWMaxB];
   if (any_bad) {
     if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
     return;
   }
-  uint32_t *pgc = pg;  // merged page counts
-  int n = 0;
-  const uint32_t k_eff = static_cast<uint32_t>(w.k_eff);
+  int n = 0, up = 0;
   if (!p.wide_exact && !full && total >= k_eff && total <= static_cast<uint32_t>(kSplitRowCap)) {
-    uint32_t v[kSplitMaxUnits];
-#pragma unroll
-    for (int c = 0; c < kSplitMaxUnits; ++c)
-      v[c] = c < U ? __ldcg(&ws.pg[(u0 + c) * 256 + t]) : 0u;
-    uint32_t sum = 0;
-#pragma unroll
-    for (int c = 0; c < kSplitMaxUnits; ++c) sum += v[c];
-    pgc[t] = sum;
-    // the candidates, flattened over the units: entry i of the row is entry
-    // i - seg[c] of unit c (seg is increasing in i for each thread)
+    // ---- gather: entry i of the row is entry i - seg[c] of unit c; the
+    // first half of the loads is in flight while the threshold's page is
+    // found, and every entry is counted by key as it is stored ----
+    n = static_cast<int>(total);
     const uint32_t *src0 = ws.cand + u0 * kSplitUnitCap;
-    constexpr int kBatch = 8;
-    int c = 0;
-    for (uint32_t base = t; base < total; base += kBatch * kSplitThreads) {
-      uint32_t val[kBatch];
-      uint32_t dst[kBatch];
+    constexpr int kHalf = kSplitRowCap / kSplitThreads / 2;  // 16
+    uint32_t va[kHalf], vb[kHalf];
+    auto load_half = [&](uint32_t *v, int h0) {
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        const uint32_t i = base + j * kSplitThreads;
-        dst[j] = i;
-        val[j] = 0u;
+      for (int j = 0; j < kHalf; ++j) {
+        const uint32_t i = static_cast<uint32_t>((h0 + j) * kSplitThreads + t);
+        v[j] = 0u;
         if (i < total) {
-          while (c + 1 < U && i >= seg[c + 1]) ++c;
-          val[j] = __ldcg(&src0[static_cast<size_t>(c) * kSplitUnitCap + (i - seg[c])]);
+          const int c = split_unit_of(seg, U, i);
+          v[j] = __ldcg(&src0[static_cast<size_t>(c) * kSplitUnitCap + (i - seg[c])]);
         }
       }
+    };
+    load_half(va, 0);
+    up = split_key_setup(pgc, k_eff, hw, page_slot, slot_page, misc, scratch);
+    load_half(vb, kHalf);
+    const uint32_t page = misc[kWDigit];
+    const bool keyed = up <= kSplitKeyPages;
+    auto store_half = [&](const uint32_t *v, int h0) {
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j)
-        if (dst[j] < total) cand[dst[j]] = val[j];
-    }
-    n = static_cast<int>(total);
+      for (int j = 0; j < kHalf; ++j) {
+        const uint32_t i = static_cast<uint32_t>((h0 + j) * kSplitThreads + t);
+        if (i < total) {
+          cand[i] = v[j];
+          if (keyed) split_key_count(v[j] >> 16, page, page_slot, hw);
+        }
+      }
+    };
+    store_half(va, 0);
+    store_half(vb, kHalf);
   } else {
+    const char *rowp = static_cast<const char *>(p.logits) + w.off * 2;
     uint32_t *mk = &misc[kWMaxK];
     if (!split_exact(rowp, V, U, S, k_eff, cand, seg, pgc, mk, hw, misc, scratch)) {
       if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
@@ -907,13 +1073,21 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
     }
     maxk = *mk;
     n = static_cast<int>(min(seg[U], static_cast<uint32_t>(kSplitRowCap)));
+    up = split_key_setup(pgc, k_eff, hw, page_slot, slot_page, misc, scratch);
+    if (up <= kSplitKeyPages) {
+      const uint32_t page = misc[kWDigit];
+#pragma unroll 4
+      for (int i = t; i < n; i += kSplitThreads) split_key_count(cand[i] >> 16, page, page_slot, hw);
+    }
   }
   __syncthreads();
   if (maxk <= KeyBF16::kNegInf) {  // every candidate is -inf: no finite logit in the row
     if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
     return;
   }
-  if (!split_key_tail(p, r, w, cand, n, seg, U, S, pgc, maxk, hw, misc, scratch)) {
+  if (up > kSplitKeyPages ||
+      !split_key_tail(p, r, w, cand, n, seg, U, S, maxk, up, u24, hw, list, slot_page, misc,
+                      scratch)) {
     __syncthreads();
     split_row_tail(p, r, w, cand, n, seg, U, S, pgc, maxk, hw, misc, scratch);
   }

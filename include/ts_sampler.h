@@ -145,9 +145,9 @@ ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep,
 
 /* Sizes the sampler's workspace for calls of up to max_rows rows no wider
  * than max_row_vocab (bf16).  The workspace lets wide rows (more than 32,768
- * tokens) take the split path: a threshold kernel, then a streaming kernel
- * whose CTAs hand their candidates over through it, the last CTA of each row
- * finishing the row.  Without it (or when a call exceeds it) wide rows take
+ * tokens) take the split path: a threshold kernel, a streaming kernel whose
+ * CTAs hand their candidates over through it, and a tail kernel with one CTA
+ * per row that finishes the row.  Without it (or when a call exceeds it) wide rows take
  * the cluster path, which needs no workspace.  Allocates device memory
  * (about 17 KB per CTA of the largest launch), so call it before any stream
  * capture and not concurrently with work on the sampler; 0 rows frees the
@@ -170,8 +170,8 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
  * ts_sample_noalloc samples every row of `b` on `stream` exactly as
  * ts_sample on a sampler of cap max_top_k would (the same ids, EOS flags and
  * write-back; results never depend on the kernel geometry).  It runs the
- * split kernels (a threshold kernel, then a streaming kernel whose last CTA
- * per row finishes the row), and their workspace is a static device array of
+ * split kernels (a threshold kernel, a streaming kernel, then a tail kernel
+ * with one CTA per row), and their workspace is a static device array of
  * TS_NOALLOC_SCRATCH_BYTES (4 MiB) inside this library: every GPU that loads
  * the library holds those 4 MiB until the process exits, used or not.  The
  * call allocates nothing and frees nothing, on the host or the device.
@@ -196,9 +196,9 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
  * next call.
  *
  * Sharing: all calls on a device use the one array, which keeps what the last
- * call left in it.  Each call's first kernel clears the per-row arrival
- * counters that must start at zero, and the rest is written before it is
- * read.  Calls whose kernels may overlap on the GPU (on unordered streams, or
+ * call left in it.  Nothing in it has to start at zero: each call's kernels
+ * write every record of the array that they read, before they read it.
+ * Calls whose kernels may overlap on the GPU (on unordered streams, or
  * from several host threads without ordering) race on the array and give
  * wrong results: order them on one stream or with events. */
 ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *status,
