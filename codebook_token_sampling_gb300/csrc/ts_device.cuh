@@ -241,6 +241,16 @@ __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 // scheduled as soon as every block of this one has started; this kernel in
 // turn waits for its predecessor's completion (and memory) before it reads
 // anything.  Without a programmatic predecessor the wait returns at once.
+// 16-byte asynchronous global -> shared copies (both addresses 16-byte
+// aligned) and the wait for all of this thread's copies.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 __device__ __forceinline__ void pdl_wait_and_release() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");

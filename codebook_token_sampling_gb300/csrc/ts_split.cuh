@@ -4,19 +4,23 @@
 //
 // Kernel A (one CTA per row) reads an evenly spaced sample of the row and
 // stores the threshold key t (the sampling step of Floyd and Rivest's
-// selection, "Expected time bounds for selection", CACM 18(3), 1975).
+// selection, "Expected time bounds for selection", CACM 18(3), 1975); it
+// also clears the row's candidate counter.
 //
 // Kernel B (U CTAs per row, one contiguous slice each) streams its slice
-// once with 16-byte loads and keeps every logit >= t: candidates (key << 16 |
-// slice index), their counts by key >> 8, the maximum key and a NaN / +inf
-// flag go to the workspace.  It does nothing else, so the streaming CTAs
-// never wait for one another or hold an SM for a row's tail.
+// once with 16-byte loads and keeps every logit that compares >= t or is a
+// NaN, as raw entries (bf16 bits << 16 | slice index): each warp compacts
+// the flags of four chunks per lane at once, and the CTA appends its entries
+// to the row's candidate array with one atomic on the row's counter.  It
+// does nothing else, so the streaming CTAs never wait for one another or
+// hold an SM for a row's tail.
 //
-// Kernel C (one CTA per row) gathers the row's candidates (a few thousand,
-// from L2) and runs the row's tail:
-//   - the threshold key's page from the page counts, issued while the
-//     candidate loads are in flight, and the candidates counted per key as
-//     they arrive;
+// Kernel C (one CTA per row) copies the row's candidate array (a few
+// thousand entries, from L2) into shared memory in the same round of loads
+// as the units' records, and runs the row's tail:
+//   - keys, page counts, the maximum and the NaN / +inf check of the
+//     candidates; the threshold key's page from the page counts and the
+//     candidates counted per key;
 //   - the keys that occur, compacted in key order, so that one block scan
 //     over them gives the threshold key thr (the k_eff-th largest) and
 //     `need`, the kept tokens tied at it, and one more the kept masses (2^-40
@@ -35,25 +39,25 @@ namespace ts {
 
 constexpr int kSplitThreads = 256;
 constexpr int kSplitUnitCap = 4096;     // candidates one CTA may hand over
-constexpr int kSplitRowCap = 8192;      // candidates the last CTA gathers
+constexpr int kSplitRowCap = 8192;      // candidates the tail CTA gathers
 constexpr int kSplitMaxUnits = 16;
 constexpr int kSplitU = 4;              // 16-byte chunks per lane per iteration
 constexpr int kSplitKeyPages = 32;       // per-key counts for up to 32 pages of 256 keys
 constexpr int kSplitListCap = 1024;      // distinct candidate keys the compact tail takes
 static_assert(kSplitThreads == kWideThreads, "the block scans assume 8 warps");
 
-// Kernel B's dynamic shared memory: the unit's candidates, the warps'
-// staging rings, page counts and bookkeeping (22 KB).
+// Kernel B's dynamic shared memory: the unit's candidates, each thread's
+// last four chunks (for the element lookups of the compaction) and
+// bookkeeping (33 KB).
 constexpr uint32_t kStreamCandOff = 0;
-constexpr uint32_t kStreamRingOff = kSplitUnitCap * 4;
-constexpr uint32_t kStreamPgOff = kStreamRingOff + kWideWarps * kWideRing * 8;
-constexpr uint32_t kStreamMiscOff = kStreamPgOff + 1024;
+constexpr uint32_t kStreamStageOff = kSplitUnitCap * 4;
+constexpr uint32_t kStreamMiscOff = kStreamStageOff + kSplitU * kSplitThreads * 16;
 constexpr uint32_t kStreamSmemBytes = kStreamMiscOff + kWideMiscWords * 4;
 
 // Kernel C's: the gathered candidates (32 KB), a 16 KB work area (per-key
 // counts, then the coarse-bin tail, the exact path's histogram or the rank
 // lists), the compacted key list, page counts, page <-> slot maps, unit
-// segments and bookkeeping (55.25 KB: four CTAs per SM).
+// segments and their units, and bookkeeping (55.4 KB: four CTAs per SM).
 constexpr uint32_t kTailCandOff = 0;
 constexpr uint32_t kTailHwOff = kSplitRowCap * 4;
 constexpr uint32_t kTailListOff = kTailHwOff + 16384;
@@ -61,34 +65,33 @@ constexpr uint32_t kTailPgOff = kTailListOff + kSplitListCap * 4;
 constexpr uint32_t kTailPageSlotOff = kTailPgOff + 1024;
 constexpr uint32_t kTailSlotPageOff = kTailPageSlotOff + 1024;
 constexpr uint32_t kTailSegOff = kTailSlotPageOff + kSplitKeyPages * 4;
-constexpr uint32_t kTailMiscOff = kTailSegOff + 128;
+constexpr uint32_t kTailMiscOff = kTailSegOff + 256;
 constexpr uint32_t kTailSmemBytes = kTailMiscOff + kWideMiscWords * 4;
 
-// Workspace layout, in 4-byte words (every region 16-byte aligned).
+// Workspace layout (every region 16-byte aligned).
 struct SplitRowMeta {
   uint32_t t_key;
-  uint32_t pad[3];
+  uint32_t count;  // candidate entries appended so far (cleared by kernel A)
+  uint32_t pad[2];
 };
 struct SplitUnitMeta {
-  uint32_t n;     // candidates of the unit (may exceed kSplitUnitCap)
-  uint32_t maxk;  // largest candidate key
-  uint32_t bad;   // a NaN / +inf was met
-  uint32_t pad;
+  uint32_t n;     // entries the unit kept (may exceed kSplitUnitCap)
+  uint32_t base;  // where its run starts in the row's candidate array
+  uint32_t pad[2];
 };
 
-// Row records for max_rows rows, then unit records for max_units units (a
-// launch's CTAs: unit r * U + u is slice u of row r).
+// Row records for max_rows rows, unit records for max_units units (a
+// launch's CTAs: unit r * U + u is slice u of row r), then each row's
+// candidate array of kSplitRowCap entries.
 __host__ __device__ inline size_t split_workspace_bytes(int max_rows, int max_units) {
   const size_t rows = static_cast<size_t>(max_rows), units = static_cast<size_t>(max_units);
-  return rows * sizeof(SplitRowMeta) + units * sizeof(SplitUnitMeta) + units * 256 * 4 +
-         units * kSplitUnitCap * 4;
+  return rows * sizeof(SplitRowMeta) + units * sizeof(SplitUnitMeta) + rows * kSplitRowCap * 4;
 }
 
 struct SplitWs {
   SplitRowMeta *row;
   SplitUnitMeta *unit;
-  uint32_t *pg;    // [unit][256]
-  uint32_t *cand;  // [unit][kSplitUnitCap]
+  uint32_t *cand;  // [row][kSplitRowCap]
 };
 
 __device__ __forceinline__ SplitWs split_ws(void *base, int max_rows, int max_units) {
@@ -99,14 +102,12 @@ __device__ __forceinline__ SplitWs split_ws(void *base, int max_rows, int max_un
   b += rows * sizeof(SplitRowMeta);
   ws.unit = reinterpret_cast<SplitUnitMeta *>(b);
   b += units * sizeof(SplitUnitMeta);
-  ws.pg = reinterpret_cast<uint32_t *>(b);
-  b += units * 256 * 4;
   ws.cand = reinterpret_cast<uint32_t *>(b);
   return ws;
 }
 
 // ---------------------------------------------------------------------------
-// Kernel A: the row's threshold key from its sample.
+// Kernel A: the row's threshold key from its sample; clears its counter.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Params p) {
   __shared__ __align__(16) uint32_t hist[2048];
@@ -126,7 +127,10 @@ __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Pa
       t_key = wide_sample_threshold(rowp, w.vocab, w.k_eff, 1, hist, misc,
                                     reinterpret_cast<uint64_t *>(misc + kWScan));
   }
-  if (t == 0) ws.row[r].t_key = t_key;
+  if (t == 0) {
+    ws.row[r].t_key = t_key;
+    ws.row[r].count = 0u;
+  }
 }
 
 // One candidate of the streaming phase: its entry, its page count and the
@@ -169,15 +173,26 @@ __device__ __forceinline__ void split_drain(const uint2 *ring, uint32_t head, ui
   if (f1) split_keep(k1, idx0 + 1u, pos + (f0 ? 1u : 0u), cand, pg, kmax);
 }
 
-// The unit whose segment holds flattened entry i, for nondecreasing seg[0 ..
-// U] with seg[0] = 0 <= i < seg[U] and U <= 16: a binary search of four fixed
-// steps (no data-dependent loop, so the lanes of a warp stay converged).
+// Candidate entries are grouped in segments, one per unit: segment k is
+// entries seg[k] .. seg[k + 1] - 1 and came from unit seg[kSplitUmapOff + k]
+// (their low 16 bits index that unit's slice).
+constexpr int kSplitUmapOff = kSplitMaxUnits + 1;
+
+// The segment holding entry i, for nondecreasing seg[0 .. U] with seg[0] = 0
+// <= i < seg[U] and U <= 16: a binary search of four fixed steps (no
+// data-dependent loop, so the lanes of a warp stay converged).
 __device__ __forceinline__ int split_unit_of(const uint32_t *seg, int U, uint32_t i) {
   int c = 0;
 #pragma unroll
   for (int step = 8; step >= 1; step >>= 1)
     if (c + step < U && i >= seg[c + step]) c += step;
   return c;
+}
+
+// The token index of entry e, the i-th candidate.
+__device__ __forceinline__ uint32_t split_gidx(const uint32_t *seg, int U, int S, uint32_t i,
+                                               uint32_t e) {
+  return seg[kSplitUmapOff + split_unit_of(seg, U, i)] * static_cast<uint32_t>(S) + (e & 0xFFFFu);
 }
 
 // The rho-th smallest (0-based) token index among the gathered candidates
@@ -199,7 +214,7 @@ __device__ uint32_t split_rank_select(const uint32_t *cand, int n, const uint32_
       const int i = base + t;
       const uint32_t e = i < n ? cand[i] : 0u;
       if (i < n && (e >> 16) == key_sel) {
-        const uint32_t g = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
+        const uint32_t g = split_gidx(seg, U, S, static_cast<uint32_t>(i), e);
         if (level == 0)
           atomicAdd(&h[g >> 9], 1u);
         else if ((g >> 9) == b1)
@@ -386,7 +401,7 @@ __device__ void split_row_tail(const Params &p, int r, const Row &w, const uint3
     for (int i = t; i < n; i += kSplitThreads) {
       const uint32_t e = cand[i];
       const uint32_t key = e >> 16;
-      const uint32_t g = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
+      const uint32_t g = split_gidx(seg, U, S, static_cast<uint32_t>(i), e);
       if (key > thr || (key == thr && need && g <= idx_cut)) {
         const uint32_t pos = atomicAdd(&misc[kWKept], 1u);
         if (pos < static_cast<uint32_t>(p.max_keep)) {
@@ -502,7 +517,7 @@ __device__ uint32_t split_small_rank(const uint32_t *cand, int n, const uint32_t
     if (i < n && (e >> 16) == key) {
       const uint32_t pos = atomicAdd(&misc[kWN], 1u);
       if (pos < n_key)
-        rl[pos] = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
+        rl[pos] = split_gidx(seg, U, S, static_cast<uint32_t>(i), e);
     }
   }
   __syncthreads();
@@ -662,7 +677,7 @@ __device__ bool split_key_tail(const Params &p, int r, const Row &w, const uint3
     for (int i = t; i < n; i += kSplitThreads) {
       const uint32_t e = cand[i];
       const uint32_t key = e >> 16;
-      const uint32_t g = static_cast<uint32_t>(split_unit_of(seg, U, i) * S) + (e & 0xFFFFu);
+      const uint32_t g = split_gidx(seg, U, S, static_cast<uint32_t>(i), e);
       if (key > thr || (key == thr && need && g <= idx_cut)) {
         const uint32_t at = atomicAdd(&misc[kWKept], 1u);
         if (at < static_cast<uint32_t>(p.max_keep)) {
@@ -692,6 +707,7 @@ __device__ bool split_exact(const char *rowp, int V, int U, int S, uint32_t k_ef
                             uint32_t *seg, uint32_t *pgc, uint32_t *maxk_out, uint32_t *hist,
                             uint32_t *misc, uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
+  if (t < kSplitMaxUnits) seg[kSplitUmapOff + t] = static_cast<uint32_t>(t);  // units in order
   const int head = min(V, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / 2u));
   const int nq = (V - head) / 8;
   const int tail = V - head - 8 * nq;
@@ -823,17 +839,14 @@ __device__ bool split_exact(const char *rowp, int V, int U, int S, uint32_t k_ef
 __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Params p) {
   extern __shared__ __align__(16) unsigned char smem[];
   uint32_t *cand = reinterpret_cast<uint32_t *>(smem + kStreamCandOff);
-  uint2 *rings = reinterpret_cast<uint2 *>(smem + kStreamRingOff);
-  uint32_t *pg = reinterpret_cast<uint32_t *>(smem + kStreamPgOff);
+  uint4 *stage = reinterpret_cast<uint4 *>(smem + kStreamStageOff);
   uint32_t *misc = reinterpret_cast<uint32_t *>(smem + kStreamMiscOff);
-  uint64_t *scratch = reinterpret_cast<uint64_t *>(misc + kWScan);
 
   const int U = p.ws_units_per_row;
   const int r = static_cast<int>(blockIdx.x) / U;
   const int u = static_cast<int>(blockIdx.x) - r * U;
   const int t = static_cast<int>(threadIdx.x);
   const uint32_t lane = lane_id();
-  const int warp = t >> 5;
   if (r >= p.n_rows) {
     pdl_wait_and_release();
     return;
@@ -866,21 +879,20 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
     cur[j] = m < nq ? ld_stream_v4(body + 16 * static_cast<size_t>(m), pol)
                     : make_uint4(0u, 0u, 0u, 0u);
   }
-  pg[t] = 0u;  // kSplitThreads == 256 pages
   if (t == 0) misc[kWN] = 0u;
   pdl_wait_and_release();  // the threshold kernel has finished
   SplitWs ws = split_ws(p.workspace, p.ws_rows, p.ws_units);
   const uint32_t t_key = __ldcg(&ws.row[r].t_key);
   __syncthreads();
 
-  // ---- filter: every logit with key >= t_key becomes a candidate ----
-  uint32_t bad = 0, kmax = 0;
+  // ---- filter: every logit that compares >= t (NaN included) is kept as
+  // a raw entry; a lane's flags for its four chunks of an iteration form one
+  // 32-bit mask, and the warp compacts them once per iteration ----
   if (!p.wide_exact) {
     const uint32_t tb = wkey_bits(t_key);
     const uint32_t t2 = tb | (tb << 16);
-    uint2 *ring = rings + warp * kWideRing;
     const uint32_t lt = lanemask_lt();
-    uint32_t rh = 0, rt = 0;
+    const uint16_t *st16 = reinterpret_cast<const uint16_t *>(stage);
 #pragma unroll 1
     for (int it = 0; it < n_it; ++it) {
       uint4 nxt[kSplitU];
@@ -890,61 +902,80 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
         nxt[j] = m < nq ? ld_stream_v4(body + 16 * static_cast<size_t>(m), pol)
                         : make_uint4(0u, 0u, 0u, 0u);
       }
+      uint32_t f = 0;  // bit 8 j + e: element e of chunk j
 #pragma unroll
       for (int j = 0; j < kSplitU; ++j) {
         const int m = it * kPerIter + j * kSplitThreads + t;
-        const uint32_t wd[4] = {cur[j].x, cur[j].y, cur[j].z, cur[j].w};
-        uint32_t mk[4] = {0u, 0u, 0u, 0u};
         if (m < nq) {
-#pragma unroll
-          for (int x = 0; x < 4; ++x) mk[x] = hgeu_mask(wd[x], t2);
+          const uint32_t m0 = hgeu_mask(cur[j].x, t2), m1 = hgeu_mask(cur[j].y, t2);
+          const uint32_t m2 = hgeu_mask(cur[j].z, t2), m3 = hgeu_mask(cur[j].w, t2);
+          const uint32_t fj = (m0 & 1u) | ((m0 >> 30) & 2u) | ((m1 & 1u) << 2) |
+                              ((m1 >> 28) & 8u) | ((m2 & 1u) << 4) | ((m2 >> 26) & 32u) |
+                              ((m3 & 1u) << 6) | ((m3 >> 24) & 128u);
+          f |= fj << (8 * j);
         }
-        if (!__any_sync(0xFFFFFFFFu, (mk[0] | mk[1] | mk[2] | mk[3]) != 0u)) continue;
+      }
+      const uint32_t c = __popc(f);
+      const uint32_t wsum = __reduce_add_sync(0xFFFFFFFFu, c);
+      if (wsum != 0u) {
+        if (f) {  // the lane's chunks, for its own element lookups below
 #pragma unroll
-        for (int x = 0; x < 4; ++x) {
-          const bool f = mk[x] != 0u;
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, f);
-          if (f)
-            ring[(rt + __popc(bal & lt)) & (kWideRing - 1)] =
-                make_uint2(wd[x], static_cast<uint32_t>(head + 8 * m + 2 * x));
-          rt += __popc(bal);
-          if (rt - rh >= 32u) {
-            __syncwarp();
-            split_drain(ring, rh, 32u, t_key, cand, pg, &misc[kWN], bad, kmax);
-            rh += 32u;
-            __syncwarp();
+          for (int j = 0; j < kSplitU; ++j) stage[j * kSplitThreads + t] = cur[j];
+        }
+        // exclusive prefix of c over the warp's lanes, from its six bits
+        uint32_t pre = 0;
+#pragma unroll
+        for (int bb = 0; bb < 6; ++bb)
+          pre += static_cast<uint32_t>(__popc(__ballot_sync(0xFFFFFFFFu, (c >> bb) & 1u) & lt))
+                 << bb;
+        uint32_t base = 0;
+        if (lane == 0) base = atomicAdd(&misc[kWN], wsum);
+        uint32_t pos = __shfl_sync(0xFFFFFFFFu, base, 0) + pre;
+        const uint32_t cmax = __reduce_max_sync(0xFFFFFFFFu, c);
+        for (uint32_t q = 0; q < cmax; ++q) {  // the same trip count in every lane
+          if (f) {
+            const uint32_t e = static_cast<uint32_t>(__ffs(f) - 1);
+            f &= f - 1u;
+            const uint32_t j = e >> 3, k8 = e & 7u;
+            const uint32_t bits = st16[(j * kSplitThreads + t) * 8u + k8];
+            const uint32_t idx =
+                static_cast<uint32_t>(head + 8 * (it * kPerIter + static_cast<int>(j) * kSplitThreads + t)) + k8;
+            if (pos < static_cast<uint32_t>(kSplitUnitCap)) cand[pos] = (bits << 16) | idx;
+            ++pos;
           }
         }
       }
 #pragma unroll
       for (int j = 0; j < kSplitU; ++j) cur[j] = nxt[j];
     }
-    __syncwarp();
-    if (rt != rh) split_drain(ring, rh, rt - rh, t_key, cand, pg, &misc[kWN], bad, kmax);
     if (t < head + tail) {
       const int idx = t < head ? t : head + 8 * nq + (t - head);
-      const uint32_t k = KeyBF16::key(KeyBF16::load_one(sp, idx));
-      const bool nf = k < KeyBF16::kNegInf || k >= KeyBF16::kPosInf;
-      bad |= nf;
-      if (!nf && k >= t_key) split_keep(k, static_cast<uint32_t>(idx), atomicAdd(&misc[kWN], 1u),
-                                        cand, pg, kmax);
+      const uint32_t bits = KeyBF16::load_one(sp, idx);
+      const uint32_t k = KeyBF16::key(bits);
+      if (k >= t_key || k < KeyBF16::kNegInf || k >= KeyBF16::kPosInf) {
+        const uint32_t pos = atomicAdd(&misc[kWN], 1u);
+        if (pos < static_cast<uint32_t>(kSplitUnitCap)) cand[pos] = (bits << 16) | static_cast<uint32_t>(idx);
+      }
     }
   }
-  kmax = wide_max_u32(kmax, scratch);
-  // ---- hand the unit's results over ----
+  __syncthreads();
+  // ---- hand over: the unit's entries go to the row's candidate array at a
+  // run reserved with one atomic ----
   const size_t ui = static_cast<size_t>(r) * U + u;  // == blockIdx.x
   const uint32_t n_loc = misc[kWN];
-  const int n_copy = static_cast<int>(min(n_loc, static_cast<uint32_t>(kSplitUnitCap)));
-  uint32_t *gc = ws.cand + ui * kSplitUnitCap;
-  for (int i = t; i < n_copy; i += kSplitThreads) __stcg(&gc[i], cand[i]);
-  __stcg(&ws.pg[ui * 256 + t], pg[t]);
-  const uint32_t bad_any = __syncthreads_or(bad != 0u);
+  const uint32_t n_copy = min(n_loc, static_cast<uint32_t>(kSplitUnitCap));
+  if (t == 0) misc[kWFast] = atomicAdd(&ws.row[r].count, n_copy);
+  __syncthreads();
+  const uint32_t base = misc[kWFast];
+  uint32_t *gc = ws.cand + static_cast<size_t>(r) * kSplitRowCap;
+  for (uint32_t i = static_cast<uint32_t>(t); i < n_copy; i += kSplitThreads)
+    if (base + i < static_cast<uint32_t>(kSplitRowCap)) __stcg(&gc[base + i], cand[i]);
   if (t == 0) {
     SplitUnitMeta mt;
     mt.n = n_loc;
-    mt.maxk = kmax;
-    mt.bad = bad_any;
-    mt.pad = 0u;
+    mt.base = base;
+    mt.pad[0] = 0u;
+    mt.pad[1] = 0u;
     __stcg(reinterpret_cast<uint4 *>(&ws.unit[ui]), *reinterpret_cast<uint4 *>(&mt));
   }
 }
@@ -988,82 +1019,70 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_tail_kernel(const Para
   SplitWs ws = split_ws(p.workspace, p.ws_rows, p.ws_units);
   const size_t u0 = static_cast<size_t>(r) * U;
 
-  // ---- the units' records (warp 0) and page counts (every thread), in one
-  // round of loads ----
-  uint32_t pv[kSplitMaxUnits];
+  // ---- one round of loads: the row's whole candidate array, whatever its
+  // count, copied straight into shared memory, and the units' records ----
+  if (!p.wide_exact) {
+    const uint32_t *src = ws.cand + static_cast<size_t>(r) * kSplitRowCap;
 #pragma unroll
-  for (int c = 0; c < kSplitMaxUnits; ++c)
-    pv[c] = c < U ? __ldcg(&ws.pg[(u0 + c) * 256 + t]) : 0u;
+    for (int j = 0; j < kSplitRowCap / (4 * kSplitThreads); ++j) {
+      const int q = j * kSplitThreads + t;
+      cp_async16(&cand[4 * q], &src[4 * q]);
+    }
+  }
+  pgc[t] = 0u;
   if (t < 32) {
     uint4 mt = make_uint4(0u, 0u, 0u, 0u);
     if (t < U) mt = __ldcg(reinterpret_cast<const uint4 *>(&ws.unit[u0 + t]));
-    uint32_t incl = mt.x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t x = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-      if (lane >= static_cast<uint32_t>(o)) incl += x;
-    }
-    const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
-    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, mt.y);
-    const bool bd = __any_sync(0xFFFFFFFFu, mt.z != 0u);
+    const uint32_t nc = min(mt.x, static_cast<uint32_t>(kSplitUnitCap));  // entries written
+    const uint32_t tot = __reduce_add_sync(0xFFFFFFFFu, nc);
     const bool fl = __any_sync(0xFFFFFFFFu, mt.x > static_cast<uint32_t>(kSplitUnitCap));
-    if (t <= U) seg[t] = incl - mt.x;  // exclusive offsets; seg[U] = total
+    // segments: the units that wrote entries, in the order of their runs
+    const bool has = t < U && nc != 0u;
+    const uint32_t bkey = has ? mt.y : 0xFFFFFFFFu;
+    uint32_t rank = 0;
+#pragma unroll
+    for (int o = 0; o < kSplitMaxUnits; ++o) rank += __shfl_sync(0xFFFFFFFFu, bkey, o) < bkey ? 1u : 0u;
+    const uint32_t n_has = static_cast<uint32_t>(__popc(__ballot_sync(0xFFFFFFFFu, has)));
+    if (has) {
+      seg[rank] = mt.y;
+      seg[kSplitUmapOff + rank] = static_cast<uint32_t>(t);
+    }
+    if (static_cast<uint32_t>(t) >= n_has && t <= U) seg[t] = tot;
     if (t == 0) {
       misc[kWTotal] = tot;
-      misc[kWMaxB] = mk;
-      misc[kWBad] = bd ? 1u : 0u;
       misc[kWRange] = fl ? 1u : 0u;
     }
   }
-  uint32_t psum = 0;
-#pragma unroll
-  for (int c = 0; c < kSplitMaxUnits; ++c) psum += pv[c];
-  pgc[t] = psum;
+  cp_async_wait_all();
   __syncthreads();
-  const uint32_t total = misc[kWTotal], any_bad = misc[kWBad], full = misc[kWRange];
+  const uint32_t total = misc[kWTotal], full = misc[kWRange];
   const uint32_t u24 = misc[kWU24];
-  uint32_t maxk = misc[kWMaxB];
-  if (any_bad) {
-    if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
-    return;
-  }
+  uint32_t maxk = 0;
   int n = 0, up = 0;
   if (!p.wide_exact && !full && total >= k_eff && total <= static_cast<uint32_t>(kSplitRowCap)) {
-    // ---- gather: entry i of the row is entry i - seg[c] of unit c; the
-    // first half of the loads is in flight while the threshold's page is
-    // found, and every entry is counted by key as it is stored ----
+    // ---- keys, page counts, maximum and the NaN / +inf check ----
     n = static_cast<int>(total);
-    const uint32_t *src0 = ws.cand + u0 * kSplitUnitCap;
-    constexpr int kHalf = kSplitRowCap / kSplitThreads / 2;  // 16
-    uint32_t va[kHalf], vb[kHalf];
-    auto load_half = [&](uint32_t *v, int h0) {
-#pragma unroll
-      for (int j = 0; j < kHalf; ++j) {
-        const uint32_t i = static_cast<uint32_t>((h0 + j) * kSplitThreads + t);
-        v[j] = 0u;
-        if (i < total) {
-          const int c = split_unit_of(seg, U, i);
-          v[j] = __ldcg(&src0[static_cast<size_t>(c) * kSplitUnitCap + (i - seg[c])]);
-        }
-      }
-    };
-    load_half(va, 0);
+    uint32_t nbad = 0, kmax = 0;
+#pragma unroll 4
+    for (int i = t; i < n; i += kSplitThreads) {
+      const uint32_t e = cand[i];
+      const uint32_t k = KeyBF16::key(e >> 16);
+      nbad |= (k < KeyBF16::kNegInf || k >= KeyBF16::kPosInf) ? 1u : 0u;
+      kmax = max(kmax, k);
+      cand[i] = (k << 16) | (e & 0xFFFFu);
+      atomicAdd(&pgc[k >> 8], 1u);
+    }
+    if (__syncthreads_or(nbad != 0u)) {
+      if (t == 0) finish_row(p, r, w, -1, kRowNonFinite);
+      return;
+    }
+    maxk = wide_max_u32(kmax, scratch);
     up = split_key_setup(pgc, k_eff, hw, page_slot, slot_page, misc, scratch);
-    load_half(vb, kHalf);
-    const uint32_t page = misc[kWDigit];
-    const bool keyed = up <= kSplitKeyPages;
-    auto store_half = [&](const uint32_t *v, int h0) {
-#pragma unroll
-      for (int j = 0; j < kHalf; ++j) {
-        const uint32_t i = static_cast<uint32_t>((h0 + j) * kSplitThreads + t);
-        if (i < total) {
-          cand[i] = v[j];
-          if (keyed) split_key_count(v[j] >> 16, page, page_slot, hw);
-        }
-      }
-    };
-    store_half(va, 0);
-    store_half(vb, kHalf);
+    if (up <= kSplitKeyPages) {
+      const uint32_t page = misc[kWDigit];
+#pragma unroll 4
+      for (int i = t; i < n; i += kSplitThreads) split_key_count(cand[i] >> 16, page, page_slot, hw);
+    }
   } else {
     const char *rowp = static_cast<const char *>(p.logits) + w.off * 2;
     uint32_t *mk = &misc[kWMaxK];

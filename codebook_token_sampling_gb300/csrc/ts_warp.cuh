@@ -385,13 +385,6 @@ constexpr int kTowerWarps = 4;
 constexpr int kTowerThreads = 32 * kTowerWarps;
 constexpr int kRowThreads = kTowerThreads;
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
 
 // Per-dtype chunk helpers: the two largest values of a chunk folded into a
 // running pair, and the unordered >= mask of a chunk against a threshold.

@@ -149,7 +149,7 @@ ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep,
  * CTAs hand their candidates over through it, and a tail kernel with one CTA
  * per row that finishes the row.  Without it (or when a call exceeds it) wide rows take
  * the cluster path, which needs no workspace.  Allocates device memory
- * (about 17 KB per CTA of the largest launch), so call it before any stream
+ * (32 KB per row plus 16 bytes per CTA of the largest launch), so call it before any stream
  * capture and not concurrently with work on the sampler; 0 rows frees the
  * workspace.  Smaller requests than the current size keep it. */
 ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
@@ -180,8 +180,7 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
  * b: as in ts_sample; bf16 logits only, at most TS_NOALLOC_MAX_ROWS (64) rows,
  *   max_row_vocab <= TS_MAX_VOCAB_BF16.  Larger requests, and fp32 logits,
  *   return TS_ERR_UNSUPPORTED and launch nothing; ts_last_error then names the
- *   limit.  Within them the scratch always suffices (a row takes fewer CTAs
- *   when many rows share the scratch).
+ *   limit.  Within them the scratch always suffices.
  * status: a device word owned by the caller; each row error ORs its bits into
  *   it (it is never cleared here).  NULL drops the bits; rows with errors
  *   still get out_ids = -1.
@@ -196,8 +195,9 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
  * next call.
  *
  * Sharing: all calls on a device use the one array, which keeps what the last
- * call left in it.  Nothing in it has to start at zero: each call's kernels
- * write every record of the array that they read, before they read it.
+ * call left in it.  Each call's first kernel clears the per-row counters
+ * that must start at zero, and everything else that a call uses it writes
+ * before it reads it.
  * Calls whose kernels may overlap on the GPU (on unordered streams, or
  * from several host threads without ordering) race on the array and give
  * wrong results: order them on one stream or with events. */

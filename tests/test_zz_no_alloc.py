@@ -99,7 +99,7 @@ def test_noalloc_stress_then_tower_rows(ts):
 
 def test_noalloc_edge_rows_then_widest_rows(ts):
     """Rows with errors, then 64 rows of the widest bf16 vocabulary (the
-    geometry shrinks to fit the scratch)."""
+    largest call the scratch takes)."""
     first = _edge_batch(5)
     rng = np.random.default_rng(6)
     v = ts.TS_MAX_VOCAB_BF16
