@@ -49,6 +49,107 @@ DESCRIPTIONS = {
 }
 
 
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources, to tell whether recorded ncu counters still
+    describe the kernels that run."""
+    import hashlib
+    h = hashlib.sha256()
+    src = os.path.join(ROOT, "codebook_token_sampling_gb300", "csrc")
+    for name in sorted(os.listdir(src)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(src, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config: str, rows):
+    """DRAM bytes per launch from the committed ncu record of this workload,
+    or None when there is none or the kernels changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    key = config if config != "stress" else f"stress{rows}"
+    e = rec.get(key)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def concat_steps(hosts):
+    """R steps' batches as one batch (R times the rows, streams and slots)."""
+    out = dict(hosts[0])
+    off, logits, streams = 0, [], 0
+    for k in ("row_vocab", "temp", "top_k", "top_p", "seed", "request", "codebook", "eos_id"):
+        out[k] = np.concatenate([np.asarray(h[k]) for h in hosts])
+    offs, rs, slots, steps = [], [], [], []
+    for h in hosts:
+        lg = np.asarray(h["logits"])
+        offs.append(np.asarray(h["row_offsets"]) + off)
+        logits.append(lg)
+        off += lg.size
+        rs.append(np.asarray(h["row_stream"]) + streams)
+        sl = np.asarray(h["feedback_slot"])
+        before = sum(int(x["feedback_len"]) for x in hosts[:len(slots)])
+        slots.append(np.where(sl >= 0, sl + before, sl).astype(sl.dtype))
+        steps.append(np.asarray(h["step"]))
+        streams += int(h["n_streams"])
+    out.update(logits=np.concatenate(logits), row_offsets=np.concatenate(offs),
+               row_stream=np.concatenate(rs), feedback_slot=np.concatenate(slots),
+               step=np.concatenate(steps), n_rows=sum(int(h["n_rows"]) for h in hosts),
+               n_streams=streams, feedback_len=sum(int(h["feedback_len"]) for h in hosts))
+    return out
+
+
+def multi_step(args, dev, l2, peak):
+    """R steps' rows sampled by one launch (R = 1, 8, 64), to show the
+    bandwidth bound of steps too small to fill the GPU on their own."""
+    import torch
+    import codebook_token_sampling_gb300 as ts
+    res = {}
+    for R in (1, 8, 64):
+        host = concat_steps([workloads.make(args.config, i) for i in range(R)])
+        n_rows = int(host["n_rows"])
+        sbytes = workloads.logit_bytes(host)
+        n_buf = max(2, min(64, -(-(2 * l2 + sbytes) // sbytes)))
+        np_dt = np.int16 if host["dtype"] == "bf16" else np.float32
+        base = torch.from_numpy(np.ascontiguousarray(host["logits"]).view(np_dt)).to(dev)
+        # distinct buffers: the same rows' values rotated by a row-sized stride
+        bufs = [torch.roll(base, shifts=int(i * 4099)) for i in range(n_buf)]
+        sampler = ts.Sampler(dev.index or 0, host["cap"])
+        batch = ts.DeviceBatch(host, dev)
+        stream = torch.cuda.Stream(device=dev)
+        with torch.cuda.stream(stream):
+            sampler.sample(batch, stream)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_buf):
+                batch.set_logits(bufs[i])
+                sampler.sample(batch)
+        reps = max(3, 2000 // (n_buf * R))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / (reps * n_buf)
+        if sampler.read_status(stream) != 0:
+            raise RuntimeError("row errors in the multi-step launch")
+        gbs = algorithmic_bytes(host) / t / 1e9
+        res[str(R)] = {"rows_per_launch": n_rows, "us_per_launch": 1e6 * t,
+                       "us_per_step": 1e6 * t / R, "rows_per_s": n_rows / t,
+                       "gb_per_s": gbs, "frac": gbs / peak}
+        sampler.close()
+        del bufs, base
+    return res
+
+
 def algorithmic_bytes(host) -> int:
     n = int(host["n_rows"])
     return workloads.logit_bytes(host) + n * (PARAM_BYTES_READ + PARAM_BYTES_WRITTEN)
@@ -303,7 +404,8 @@ def run_ours(args, world, rank, local):
     return {
         "host": host, "n_rows": n_rows, "t_step": t_max / k, "t_launch": t_launch,
         "t_e2e": t_e2e, "clocks": clk, "plan": plan, "n_buf": n_buf, "l2": l2,
-        "step_bytes": step_bytes, "launches": 2 * k,
+        "step_bytes": step_bytes,
+        "launches": ((3 if plan["path"] == 4 else 1) + 1) * k,
         "h2d": int(bufs[0].numel() * bufs[0].element_size()), "d2h": n_rows * 5,
     }
 
@@ -338,6 +440,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-multi-step", action="store_true",
+                    help="skip the multi-step batched figure (R steps' rows in one launch)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="force the kernel family (0 = automatic, 1 = warp per row, 2 = CTA / "
                          "cluster per row, 3 = wide cluster, 4 = wide split)")
@@ -399,6 +503,11 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     r = run_ours(args, world, rank, local)
+    peak, peak_kind = measured_peak_gbs()
+    multi = None
+    if args.config != "stress" and not args.no_multi_step and rank == 0:
+        import torch
+        multi = multi_step(args, torch.device("cuda", local), r["l2"], peak)
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
@@ -407,8 +516,8 @@ def main():
     t = r["t_step"]
     value = world * n_rows / t
     alg = algorithmic_bytes(r["host"])
-    peak, peak_kind = measured_peak_gbs()
     achieved = alg / r["t_launch"] / 1e9
+    split = r["plan"]["path"] == 4
     cpu = None
     if not args.no_cpu_baseline:
         threads = host_threads()
@@ -433,10 +542,16 @@ def main():
         "frames_per_s": world * n_streams / t,
         "gb_per_s": world * alg / t / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": recorded_traffic(args.config, args.rows),
                      "peak_source": f"{peak_kind} hbm_gbs",
+                     "launch": "one ts_sample call: split_threshold_kernel + split_stream_kernel + "
+                               "split_tail_kernel" if split else
+                               "one ts_sample call: one kernel (" +
+                               {1: "row_sampler_kernel", 2: "cluster_sampler_kernel",
+                                3: "wide_sampler_kernel"}[r["plan"]["path"]] + ")",
                      "algorithmic_bytes_per_launch": alg,
                      "us_per_launch": 1e6 * r["t_launch"]},
+        "multi_step": multi,
         "e2e": {"value": world * n_rows / r["t_e2e"], "unit": "rows/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
                 "us_per_step": 1e6 * r["t_e2e"]},
