@@ -342,11 +342,12 @@ __device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w
   warp_tail<K>(p, r, w, s[0], s[1], kq, u24);
 }
 
-// Sorts the n (<= 32 * R) candidate words in `cand` and runs the tail.
+// Sorts the n (<= 32 * R) candidate words in `cand`; s0 / s1 get the first
+// 64 in descending order (lane l holds positions l and l + 32).
 template <class K, int R>
-__device__ __forceinline__ void warp_sort_and_tail(const Params &p, int r, const Row &w,
-                                                   const typename SortWord<K>::T *cand, int n,
-                                                   uint32_t u24) {
+__device__ __forceinline__ void warp_sort_cand(const typename SortWord<K>::T *cand, int n,
+                                               typename SortWord<K>::T &s0,
+                                               typename SortWord<K>::T &s1) {
   using T = typename SortWord<K>::T;
   const uint32_t lane = lane_id();
   T v[R];
@@ -356,9 +357,9 @@ __device__ __forceinline__ void warp_sort_and_tail(const Params &p, int r, const
     v[i] = e < n ? cand[e] : T(0);
   }
   bitonic_desc<T, R>(v);
-  T second = T(0);
-  if constexpr (R > 1) second = v[1];
-  warp_tail<K>(p, r, w, v[0], second, w.k_eff, u24);
+  s0 = v[0];
+  s1 = T(0);
+  if constexpr (R > 1) s1 = v[1];
 }
 
 // Warp-per-row kernel.  Each warp owns one row (kTowerWarps rows per block,
@@ -467,11 +468,13 @@ struct TowerShared {
   uint32_t hist[256];
 };
 
-// The row body for rows of at most 32 * NCH body chunks.
-template <class K, int NCH, class SH>
+// The row body for rows of at most 32 * nch body chunks (nch <= 16).  One
+// body serves every row width, so that warps on other widths share its code
+// in the instruction cache.
+template <class K, class SH>
 __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w, uint32_t u24,
-                                           SH &sh, int head, int nq, int tail,
-                                           const char *rowp) {
+                                           SH &sh, int head, int nq, int tail, const char *rowp,
+                                           int nch) {
   using SW = SortWord<K>;
   using TT = Top2<K>;
   constexpr int EPC = K::kPerChunk;
@@ -480,7 +483,8 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
   const char *body = rowp + head * K::kElemBytes;
   // ---- the row into the stage, all copies in flight ----
 #pragma unroll
-  for (int j = 0; j < NCH; ++j) {
+  for (int j = 0; j < 16; ++j) {
+    if (j >= nch) break;
     const int q = static_cast<int>(lane) + 32 * j;
     if (q < nq) cp_async16(&sh.stage[q], body + static_cast<size_t>(q) * 16);
   }
@@ -499,7 +503,8 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
   // ---- the two largest logits per lane ----
   uint32_t m1 = TT::kInit, m2 = TT::kInit;
 #pragma unroll
-  for (int j = 0; j < NCH; ++j) {
+  for (int j = 0; j < 16; ++j) {
+    if (j >= nch) break;
     const int q = static_cast<int>(lane) + 32 * j;
     if (q < nq) TT::fold_chunk(sh.stage[q], m1, m2);
   }
@@ -521,7 +526,8 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
   // ---- candidates: chunks holding a logit >= t0 (or a NaN) ----
   uint32_t fmask = 0;  // bit j: chunk lane + 32 j is flagged
 #pragma unroll
-  for (int j = 0; j < NCH; ++j) {
+  for (int j = 0; j < 16; ++j) {
+    if (j >= nch) break;
     const int q = static_cast<int>(lane) + 32 * j;
     if (q < nq && TT::flagged(sh.stage[q], t2)) fmask |= 1u << j;
   }
@@ -569,16 +575,19 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
   if (has_e && ekey >= t0) sh.cand[pos] = SW::make(ekey, static_cast<uint32_t>(eidx));
   __syncwarp();
   const int nc = static_cast<int>(total);
+  typename SortWord<K>::T s0, s1;
   if (nc <= 32)
-    warp_sort_and_tail<K, 1>(p, r, w, sh.cand, nc, u24);
+    warp_sort_cand<K, 1>(sh.cand, nc, s0, s1);
   else if (nc <= 64)
-    warp_sort_and_tail<K, 2>(p, r, w, sh.cand, nc, u24);
+    warp_sort_cand<K, 2>(sh.cand, nc, s0, s1);
   else
-    warp_sort_and_tail<K, 4>(p, r, w, sh.cand, nc, u24);
+    warp_sort_cand<K, 4>(sh.cand, nc, s0, s1);
+  warp_tail<K>(p, r, w, s0, s1, w.k_eff, u24);
 }
 
 // MAXNCH = most 16-byte chunks per lane of any row in the launch (1, 2, 4, 8
-// or 16); each row runs the body sized for its own width.
+// or 16) sizes the shared-memory stage; every row runs the same body with
+// its own chunk count.
 template <class K, int MAXNCH>
 __global__ void __launch_bounds__(kTowerThreads) row_sampler_kernel(const Params p) {
   constexpr int EPC = K::kPerChunk;
@@ -607,16 +616,7 @@ __global__ void __launch_bounds__(kTowerThreads) row_sampler_kernel(const Params
     u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
                      static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
   u24 = __shfl_sync(0xFFFFFFFFu, u24, 0);
-  if (MAXNCH == 1 || nq <= 32)
-    tower_body<K, 1>(p, r, w, u24, sh, head, nq, tail, rowp);
-  else if (MAXNCH == 2 || nq <= 64)
-    tower_body<K, (MAXNCH >= 2 ? 2 : 1)>(p, r, w, u24, sh, head, nq, tail, rowp);
-  else if (MAXNCH == 4 || nq <= 128)
-    tower_body<K, (MAXNCH >= 4 ? 4 : 1)>(p, r, w, u24, sh, head, nq, tail, rowp);
-  else if (MAXNCH == 8 || nq <= 256)
-    tower_body<K, (MAXNCH >= 8 ? 8 : 1)>(p, r, w, u24, sh, head, nq, tail, rowp);
-  else
-    tower_body<K, MAXNCH>(p, r, w, u24, sh, head, nq, tail, rowp);
+  tower_body<K>(p, r, w, u24, sh, head, nq, tail, rowp, min((nq + 31) >> 5, MAXNCH));
 }
 
 }  // namespace ts
