@@ -2,10 +2,10 @@
 // (bf16 rows such as the 151,936-token backbone vocabulary, any top-k cap up
 // to 4096: Drama 3 article, section "能跑通的命令，和文档写明的边界").
 //
-// Kernel A (one CTA per row) reads an evenly spaced sample of the row and
-// stores the threshold key t (the sampling step of Floyd and Rivest's
-// selection, "Expected time bounds for selection", CACM 18(3), 1975); it
-// also clears the row's candidate counter.
+// Kernel A (one CTA per row) reads an evenly spaced sample of the row (64
+// runs of 64 logits) and stores the threshold key t (the sampling step of
+// Floyd and Rivest's selection, "Expected time bounds for selection", CACM
+// 18(3), 1975); it also clears the row's candidate counter.
 //
 // Kernel B (U CTAs per row, one contiguous slice each) streams its slice
 // once with 16-byte loads and keeps every logit that compares >= t or is a
@@ -44,6 +44,7 @@ constexpr int kSplitMaxUnits = 16;
 constexpr int kSplitU = 4;              // 16-byte chunks per lane per iteration
 constexpr int kSplitKeyPages = 32;       // per-key counts for up to 32 pages of 256 keys
 constexpr int kSplitListCap = 1024;      // distinct candidate keys the compact tail takes
+constexpr int kSplitSampleRun = 8;       // kernel A samples 128-byte runs of the row
 static_assert(kSplitThreads == kWideThreads, "the block scans assume 8 warps");
 
 // Kernel B's dynamic shared memory: the unit's candidates, each thread's
@@ -124,8 +125,8 @@ __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Pa
     // a row the last CTA can gather whole, in slices each CTA can hold,
     // keeps every logit (t = lowest key); others sample
     if (w.vocab > kSplitRowCap || p.slice > kSplitUnitCap)
-      t_key = wide_sample_threshold(rowp, w.vocab, w.k_eff, 1, hist, misc,
-                                    reinterpret_cast<uint64_t *>(misc + kWScan));
+      t_key = wide_sample_threshold<kSplitSampleRun>(rowp, w.vocab, w.k_eff, 1, hist, misc,
+                                                     reinterpret_cast<uint64_t *>(misc + kWScan));
   }
   if (t == 0) {
     ws.row[r].t_key = t_key;

@@ -200,15 +200,21 @@ __device__ void wide_select_top(const uint32_t *h, uint32_t kk, uint32_t *misc,
 }
 
 // Exact r-th largest canonical key of an evenly spaced sample of the row
-// (every CTA of the cluster computes the same value from the same sample).
-// Returns 0 ("every element") when the sample cannot give a useful bound.
+// (every CTA of the cluster computes the same value from the same sample):
+// up to 512 16-byte chunks, taken as runs of RUN consecutive chunks at
+// evenly spaced starts (RUN = 8: 128-byte runs, a fraction of the DRAM
+// sectors that 512 scattered chunks touch).  Returns 0 ("every element") when
+// the sample cannot give a useful bound.
+template <int RUN = 1>
 __device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, int G,
                                           uint32_t *hist, uint32_t *misc, uint64_t *scratch) {
   const int t = static_cast<int>(threadIdx.x);
   const int head_r =
       min(V, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(rowp) & 15u)) & 15u) / 2u));
   const int nq_r = (V - head_r) / 8;
-  const int n_chunks = min(nq_r, kWideSampleChunks);
+  const int n_runs = min(nq_r, kWideSampleChunks) / RUN;
+  const int n_chunks = n_runs * RUN;
+  const int stride = n_runs > 0 ? nq_r / n_runs : 0;  // >= RUN
   const int n_s = 8 * n_chunks;
   if (n_chunks <= 0) return 0u;
   // r such that about 1.6 k_eff row elements (at most 3/4 of the cluster's
@@ -228,7 +234,8 @@ __device__ uint32_t wide_sample_threshold(const char *rowp, int V, int k_eff, in
     const int j = t + i * kWideThreads;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (j < n_chunks) {
-      const long long q = static_cast<long long>(j) * nq_r / n_chunks;
+      const long long q = RUN == 1 ? static_cast<long long>(j) * nq_r / n_chunks
+                                   : static_cast<long long>(j / RUN) * stride + j % RUN;
       v = __ldg(reinterpret_cast<const uint4 *>(body + 16 * q));
     }
     kw[i][0] = wkey_word(v.x);

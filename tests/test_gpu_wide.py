@@ -155,6 +155,20 @@ def _wide_rows(rng):
     for c in sampled:
         over[8 * c: 8 * c + 8] += 30.0
     rows.append((over, 1.0, 4096, 0.9))
+    # the same two cases against the split path's sample: 64 runs of 8 chunks
+    # at evenly spaced starts (8-element margins cover a misaligned row head)
+    stride = (V // 8) // 64
+    in_run = np.zeros(V, bool)
+    for k in range(64):
+        a = 8 * k * stride
+        in_run[max(a - 8, 0):a + 72] = True
+    adv2 = nrm(V, 1.0)
+    adv2[rng.choice(np.nonzero(~in_run)[0], 8000, replace=False)] += 20.0
+    rows.append((adv2, 1.0, 4096, 0.9))   # too many candidates: the exact path
+    rows.append((adv2, 1.0, 30, 0.9))     # about 8,000 candidates, all gathered
+    over2 = nrm(V, 1.0)
+    over2[in_run] += 30.0
+    rows.append((over2, 1.0, 4096, 0.9))  # too few candidates: the exact path
     # values crossing zero in the kept set (wide key range)
     rows.append((rng.standard_t(3, V).astype(np.float32), 1.0, 4096, 0.6))
     return rows
