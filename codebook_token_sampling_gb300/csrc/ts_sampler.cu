@@ -26,6 +26,7 @@ struct ts_sampler {
   int force_cluster;  // 0 auto, else CTAs per row
   int pdl;            // launch with programmatic stream serialization
   int wide_exact;     // wide path: always take the exact path (testing)
+  int force_wpr;      // warp-per-row path: 0 auto, else warps per row (1, 2, 4)
   uint32_t *status;   // device word
   void *ws;           // split wide path workspace (ts_reserve), or null
   size_t ws_bytes;
@@ -75,8 +76,9 @@ int split_units(int n_rows, int vmax, int num_sms) {
 }
 
 struct Plan {
-  int path;   // 1 block per row, 2 cluster, 3 wide
-  int nch;    // block-per-row path: 16-byte chunks per thread
+  int path;   // 1 warp(s) per row, 2 cluster, 3 wide, 4 split
+  int nch;    // warp path: 16-byte chunks per lane
+  int wpr;    // warp path: warps per row
   int g;      // cluster and wide paths: CTAs per row
   int slice;  // cluster and wide paths: elements per CTA
   int threads;
@@ -139,9 +141,16 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
     const int epc = bf16 ? 8 : 4;
     const int per_lane = (vmax + 32 * epc - 1) / (32 * epc);  // 16-byte chunks per lane
     pl->nch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
+    // small batches share each row among several warps (a shorter chain per
+    // row while the GPU has room); large ones keep one warp per row
+    int wpr = s->force_wpr;
+    if (!wpr) wpr = b->n_rows <= 4 * s->num_sms ? 4 : b->n_rows <= 16 * s->num_sms ? 2 : 1;
+    const int rpb = ts::kTowerWarps / wpr;
+    pl->wpr = wpr;
+    pl->g = wpr;
     pl->threads = ts::kTowerThreads;
     pl->smem = 0;  // static shared memory only
-    pl->grid = (b->n_rows + ts::kTowerWarps - 1) / ts::kTowerWarps;
+    pl->grid = (b->n_rows + rpb - 1) / rpb;
     return TS_OK;
   }
   const int slice_max = bf16 ? ts::kSliceMaxBF16 : ts::kSliceMaxF32;
@@ -215,13 +224,20 @@ ts::Params make_params(const ts_sampler *s, const ts_batch *b) {
   return p;
 }
 
+template <class K, int WPR>
+void *warp_kernel_wpr(int nch) {
+  if (nch == 1) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 1, WPR>);
+  if (nch == 2) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 2, WPR>);
+  if (nch == 4) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 4, WPR>);
+  if (nch == 8) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 8, WPR>);
+  return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 16, WPR>);
+}
+
 template <class K>
-void *warp_kernel_for(int nch) {
-  if (nch == 1) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 1>);
-  if (nch == 2) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 2>);
-  if (nch == 4) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 4>);
-  if (nch == 8) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 8>);
-  return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 16>);
+void *warp_kernel_for(int nch, int wpr) {
+  if (wpr == 4) return warp_kernel_wpr<K, 4>(nch);
+  if (wpr == 2) return warp_kernel_wpr<K, 2>(nch);
+  return warp_kernel_wpr<K, 1>(nch);
 }
 
 void *wide_kernel_for(int g) {
@@ -245,7 +261,7 @@ ts_status set_attributes(int device) {
   int optin = 0;
   cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  void *fns[25];
+  void *fns[48];
   int n = 0;
   const int gs[4] = {1, 2, 4, 8};
   for (int i = 0; i < 4; ++i) {
@@ -254,9 +270,12 @@ ts_status set_attributes(int device) {
     fns[n++] = wide_kernel_for(gs[i]);
   }
   const int nchs[5] = {1, 2, 4, 8, 16};
+  const int wprs[3] = {1, 2, 4};
   for (int i = 0; i < 5; ++i) {
-    fns[n++] = warp_kernel_for<ts::KeyBF16>(nchs[i]);
-    fns[n++] = warp_kernel_for<ts::KeyF32>(nchs[i]);
+    for (int k = 0; k < 3; ++k) {
+      fns[n++] = warp_kernel_for<ts::KeyBF16>(nchs[i], wprs[k]);
+      fns[n++] = warp_kernel_for<ts::KeyF32>(nchs[i], wprs[k]);
+    }
   }
   fns[n++] = reinterpret_cast<void *>(ts::split_stream_kernel);
   fns[n++] = reinterpret_cast<void *>(ts::split_tail_kernel);
@@ -309,7 +328,8 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   }
   void *fn = nullptr;
   if (pl.path == 1) {
-    fn = bf16 ? warp_kernel_for<ts::KeyBF16>(pl.nch) : warp_kernel_for<ts::KeyF32>(pl.nch);
+    fn = bf16 ? warp_kernel_for<ts::KeyBF16>(pl.nch, pl.wpr)
+              : warp_kernel_for<ts::KeyF32>(pl.nch, pl.wpr);
   } else if (pl.path == 3) {
     fn = wide_kernel_for(pl.g);
   } else {
@@ -426,6 +446,7 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->force_cluster = 0;
   s->pdl = 1;
   s->wide_exact = 0;
+  s->force_wpr = 0;
   s->status = nullptr;
   s->ws = nullptr;
   s->ws_bytes = 0;
@@ -630,6 +651,11 @@ ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value) {
     s->wide_exact = value;
     return TS_OK;
   }
+  if (option == TS_OPT_WARPS_PER_ROW) {
+    if (value != 0 && value != 1 && value != 2 && value != 4) return TS_ERR_INVALID_ARG;
+    s->force_wpr = value;
+    return TS_OK;
+  }
   return TS_ERR_INVALID_ARG;
 }
 
@@ -642,7 +668,7 @@ ts_status ts_plan(const ts_sampler *s, const ts_batch *b, int32_t *path, int32_t
   rc = make_plan(s, b, &pl);
   if (rc != TS_OK) return rc;
   if (path) *path = pl.path;
-  if (ctas_per_row) *ctas_per_row = pl.path == 1 ? 0 : pl.g;
+  if (ctas_per_row) *ctas_per_row = pl.g;
   if (threads) *threads = pl.threads;
   if (smem_bytes) *smem_bytes = pl.smem;
   if (grid) *grid = pl.grid;

@@ -412,6 +412,12 @@ struct Top2<KeyBF16> {
     fold(c.z, m1, m2);
     fold(c.w, m1, m2);
   }
+  // (m1, m2) <- the two largest of the pairs (m1, m2) and (n1, n2), per half
+  __device__ __forceinline__ static void merge(uint32_t &m1, uint32_t &m2, uint32_t n1,
+                                               uint32_t n2) {
+    m2 = u(__hmax2(__hmin2(b2(m1), b2(n1)), __hmax2(b2(m2), b2(n2))));
+    m1 = u(__hmax2(b2(m1), b2(n1)));
+  }
   // the lane's two largest keys from the packed pair
   __device__ __forceinline__ static void keys2(uint32_t m1, uint32_t m2, uint32_t &k1,
                                                uint32_t &k2) {
@@ -445,6 +451,13 @@ struct Top2<KeyF32> {
     fold(c.z, m1, m2);
     fold(c.w, m1, m2);
   }
+  __device__ __forceinline__ static void merge(uint32_t &m1, uint32_t &m2, uint32_t n1,
+                                               uint32_t n2) {
+    const float a = __uint_as_float(m1), c = __uint_as_float(m2);
+    const float x = __uint_as_float(n1), y = __uint_as_float(n2);
+    m2 = __float_as_uint(fmaxf(fminf(a, x), fmaxf(c, y)));
+    m1 = __float_as_uint(fmaxf(a, x));
+  }
   __device__ __forceinline__ static void keys2(uint32_t m1, uint32_t m2, uint32_t &k1,
                                                uint32_t &k2) {
     k1 = KeyF32::key(m1);
@@ -466,34 +479,62 @@ struct TowerShared {
   uint4 stage[32 * MAXNCH];
   T cand[kWarpCandMax];
   uint32_t hist[256];
+  uint32_t xm1[4 * 32];  // per-lane running pairs of each warp (rows shared by warps)
+  uint32_t xm2[4 * 32];
+  uint32_t xb[4];    // the row's candidate bound and largest key
+  uint32_t xt[4];
+  uint32_t xn[4];    // per-warp candidate counts
+  uint32_t xbad[4];  // per-warp NaN / +inf flags
 };
+
+// Barrier of the WPR warps that share a row (group grp of the block).
+template <int WPR>
+__device__ __forceinline__ void row_sync(int grp) {
+  if constexpr (WPR == 1) {
+    __syncwarp();
+  } else if constexpr (WPR == 4) {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+  } else {  // two rows per block: barriers 1 and 2 (constant ids)
+    if (grp == 0)
+      asm volatile("bar.sync 1, 64;" ::: "memory");
+    else
+      asm volatile("bar.sync 2, 64;" ::: "memory");
+  }
+}
 
 // The row body for rows of at most 32 * nch body chunks (nch <= 16).  One
 // body serves every row width, so that warps on other widths share its code
-// in the instruction cache.
-template <class K, class SH>
+// in the instruction cache.  With WPR > 1 the row is shared by WPR warps:
+// warp `sub` owns the chunk columns j = sub, sub + WPR, ...; lane l's running
+// pairs of all the warps are merged, so the bound is the one a single warp
+// would find; the candidate counts are exchanged so that every warp writes
+// its candidates to its own range, and warp 0 sorts and runs the tail.
+template <class K, int WPR, class SH>
 __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w, uint32_t u24,
                                            SH &sh, int head, int nq, int tail, const char *rowp,
-                                           int nch) {
+                                           int nch, int sub, int grp) {
   using SW = SortWord<K>;
   using TT = Top2<K>;
   constexpr int EPC = K::kPerChunk;
   const uint32_t lane = lane_id();
   const int V = w.vocab;
   const char *body = rowp + head * K::kElemBytes;
-  // ---- the row into the stage, all copies in flight ----
+  // ---- this warp's columns into the stage, all copies in flight ----
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int i = 0; i < 16; ++i) {
+    const int j = sub + i * WPR;
     if (j >= nch) break;
     const int q = static_cast<int>(lane) + 32 * j;
     if (q < nq) cp_async16(&sh.stage[q], body + static_cast<size_t>(q) * 16);
   }
-  // head / tail element of this lane (at most 7 + 7 of them)
+  // head / tail element of this lane of warp 0 (at most 7 + 7 of them)
   int eidx = 0x7FFFFFFF;
-  if (static_cast<int>(lane) < head)
-    eidx = static_cast<int>(lane);
-  else if (static_cast<int>(lane) < head + tail)
-    eidx = nq * EPC + static_cast<int>(lane);
+  if (sub == 0) {
+    if (static_cast<int>(lane) < head)
+      eidx = static_cast<int>(lane);
+    else if (static_cast<int>(lane) < head + tail)
+      eidx = nq * EPC + static_cast<int>(lane);
+  }
   const bool has_e = eidx < V;
   const uint32_t ebits = has_e ? K::load_one(rowp, eidx) : 0u;
   const uint32_t ekey = has_e ? K::key(ebits) : 0u;
@@ -503,38 +544,63 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
   // ---- the two largest logits per lane ----
   uint32_t m1 = TT::kInit, m2 = TT::kInit;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int i = 0; i < 16; ++i) {
+    const int j = sub + i * WPR;
     if (j >= nch) break;
     const int q = static_cast<int>(lane) + 32 * j;
     if (q < nq) TT::fold_chunk(sh.stage[q], m1, m2);
   }
-  uint32_t rep[2];
-  TT::keys2(m1, m2, rep[0], rep[1]);
-  if (has_e) {  // the lane's head / tail element joins its pair
-    rep[1] = max(rep[1], min(rep[0], ekey));
-    rep[0] = max(rep[0], ekey);
+  if constexpr (WPR > 1) {
+    sh.xm1[sub * 32 + lane] = m1;
+    sh.xm2[sub * 32 + lane] = m2;
+    row_sync<WPR>(grp);
   }
-  // ---- the k_eff-th largest of the 64 per-lane maxima: a lower bound ----
-  bitonic_desc<uint32_t, 2>(rep);
   const int kq = w.k_eff;
-  const uint32_t top = __shfl_sync(0xFFFFFFFFu, rep[0], 0);
-  uint32_t t0 = kq <= 32 ? __shfl_sync(0xFFFFFFFFu, rep[0], kq - 1)
-                         : __shfl_sync(0xFFFFFFFFu, rep[1], kq - 33);
-  // a NaN as t0 would flag nothing (NaN rows are caught below either way)
-  if (t0 < K::kNegInf || t0 > K::kPosInf) t0 = K::kNegInf;
+  uint32_t t0 = 0, top = 0;
+  if (sub == 0) {
+    if constexpr (WPR > 1) {
+#pragma unroll
+      for (int s2 = 1; s2 < WPR; ++s2) TT::merge(m1, m2, sh.xm1[s2 * 32 + lane], sh.xm2[s2 * 32 + lane]);
+    }
+    uint32_t rep[2];
+    TT::keys2(m1, m2, rep[0], rep[1]);
+    if (has_e) {  // the lane's head / tail element joins its pair
+      rep[1] = max(rep[1], min(rep[0], ekey));
+      rep[0] = max(rep[0], ekey);
+    }
+    // ---- the k_eff-th largest of the 64 per-lane maxima: a lower bound ----
+    bitonic_desc<uint32_t, 2>(rep);
+    top = __shfl_sync(0xFFFFFFFFu, rep[0], 0);
+    t0 = kq <= 32 ? __shfl_sync(0xFFFFFFFFu, rep[0], kq - 1)
+                  : __shfl_sync(0xFFFFFFFFu, rep[1], kq - 33);
+    // a NaN as t0 would flag nothing (NaN rows are caught below either way)
+    if (t0 < K::kNegInf || t0 > K::kPosInf) t0 = K::kNegInf;
+    if constexpr (WPR > 1) {
+      if (lane == 0) {
+        sh.xb[0] = t0;
+        sh.xt[0] = top;
+      }
+    }
+  }
+  if constexpr (WPR > 1) {
+    row_sync<WPR>(grp);
+    t0 = sh.xb[0];
+    top = sh.xt[0];
+  }
   const uint32_t t2 = TT::splat(t0);
   // ---- candidates: chunks holding a logit >= t0 (or a NaN) ----
-  uint32_t fmask = 0;  // bit j: chunk lane + 32 j is flagged
+  uint32_t fmask = 0;  // bit i: chunk lane + 32 (sub + i WPR) is flagged
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
+  for (int i = 0; i < 16; ++i) {
+    const int j = sub + i * WPR;
     if (j >= nch) break;
     const int q = static_cast<int>(lane) + 32 * j;
-    if (q < nq && TT::flagged(sh.stage[q], t2)) fmask |= 1u << j;
+    if (q < nq && TT::flagged(sh.stage[q], t2)) fmask |= 1u << i;
   }
   // keys of the flagged chunks: count, then write
   uint32_t mine = 0, bad = 0;
   for (uint32_t fm = fmask; fm; fm &= fm - 1u) {
-    const int q = static_cast<int>(lane) + 32 * (__ffs(fm) - 1);
+    const int q = static_cast<int>(lane) + 32 * (sub + (__ffs(fm) - 1) * WPR);
     const uint4 v = sh.stage[q];
     const uint32_t c[4] = {K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w)};
 #pragma unroll
@@ -548,13 +614,32 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
     bad |= (ekey < K::kNegInf) | (ekey >= K::kPosInf);
     mine += ekey >= t0 && ekey < K::kPosInf;
   }
-  if (__any_sync(0xFFFFFFFFu, bad) || top <= K::kNegInf) {  // a NaN / +inf, or no finite logit
-    if (lane == 0) finish_row(p, r, w, -1, kRowNonFinite);
-    return;
-  }
   uint32_t total;
   uint32_t pos = warp_excl_scan_u32(mine, &total);
+  bool any_bad = __any_sync(0xFFFFFFFFu, bad);
+  if constexpr (WPR > 1) {
+    if (lane == 0) {
+      sh.xn[sub] = total;
+      sh.xbad[sub] = any_bad ? 1u : 0u;
+    }
+    row_sync<WPR>(grp);
+    total = 0;
+#pragma unroll
+    for (int s2 = 0; s2 < WPR; ++s2) {
+      const uint32_t n2 = sh.xn[s2];
+      if (s2 < sub) pos += n2;
+      total += n2;
+      any_bad |= sh.xbad[s2] != 0u;
+    }
+  }
+  if (any_bad || top <= K::kNegInf) {  // a NaN / +inf, or no finite logit
+    if (sub == 0 && lane == 0) finish_row(p, r, w, -1, kRowNonFinite);
+    return;
+  }
   if (total > static_cast<uint32_t>(kWarpCandMax)) {
+    // every warp of the row has staged its columns (the exchange above
+    // ordered them), so warp 0 may read the whole row
+    if (sub != 0) return;
     auto keys = [&](int q) {
       const uint4 v = sh.stage[q];
       return make_uint4(K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w));
@@ -563,7 +648,7 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
     return;
   }
   for (uint32_t fm = fmask; fm; fm &= fm - 1u) {
-    const int q = static_cast<int>(lane) + 32 * (__ffs(fm) - 1);
+    const int q = static_cast<int>(lane) + 32 * (sub + (__ffs(fm) - 1) * WPR);
     const uint4 v = sh.stage[q];
     const uint32_t c[4] = {K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w)};
 #pragma unroll
@@ -573,7 +658,8 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
     }
   }
   if (has_e && ekey >= t0) sh.cand[pos] = SW::make(ekey, static_cast<uint32_t>(eidx));
-  __syncwarp();
+  row_sync<WPR>(grp);
+  if (sub != 0) return;
   const int nc = static_cast<int>(total);
   typename SortWord<K>::T s0, s1;
   if (nc <= 32)
@@ -587,19 +673,22 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
 
 // MAXNCH = most 16-byte chunks per lane of any row in the launch (1, 2, 4, 8
 // or 16) sizes the shared-memory stage; every row runs the same body with
-// its own chunk count.
-template <class K, int MAXNCH>
+// its own chunk count.  WPR = warps per row (1, 2 or 4): a block of four
+// warps samples 4 / WPR rows.
+template <class K, int MAXNCH, int WPR>
 __global__ void __launch_bounds__(kTowerThreads) row_sampler_kernel(const Params p) {
   constexpr int EPC = K::kPerChunk;
-  __shared__ __align__(16) TowerShared<K, MAXNCH> shared_rows[kTowerWarps];
+  constexpr int RPB = kTowerWarps / WPR;
+  __shared__ __align__(16) TowerShared<K, MAXNCH> shared_rows[RPB];
   const int warp = static_cast<int>(threadIdx.x) >> 5;
+  const int grp = warp / WPR, sub = warp % WPR;
   const uint32_t lane = lane_id();
-  const int r = static_cast<int>(blockIdx.x) * kTowerWarps + warp;
+  const int r = static_cast<int>(blockIdx.x) * RPB + grp;
   pdl_wait_and_release();
-  if (r >= p.n_rows) return;  // whole warp; the kernel has no block barrier
+  if (r >= p.n_rows) return;  // every warp of the row: its barriers are not reached
   const Row w = load_row(p, r);
   if (w.err) {
-    if (lane == 0) finish_row(p, r, w, -1, w.err);
+    if (sub == 0 && lane == 0) finish_row(p, r, w, -1, w.err);
     return;
   }
   const int V = w.vocab;
@@ -609,14 +698,15 @@ __global__ void __launch_bounds__(kTowerThreads) row_sampler_kernel(const Params
   head = min(head, V);
   const int nq = (V - head) / EPC;
   const int tail = V - head - nq * EPC;
-  TowerShared<K, MAXNCH> &sh = shared_rows[warp];
-  // the draw, on lane 0 (its result is needed only by the tail)
+  TowerShared<K, MAXNCH> &sh = shared_rows[grp];
+  // the draw, on lane 0 of warp 0 (its result is needed only by the tail)
   uint32_t u24 = 0;
-  if (lane == 0 && !w.greedy)
+  if (sub == 0 && lane == 0 && !w.greedy)
     u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
                      static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
   u24 = __shfl_sync(0xFFFFFFFFu, u24, 0);
-  tower_body<K>(p, r, w, u24, sh, head, nq, tail, rowp, min((nq + 31) >> 5, MAXNCH));
+  tower_body<K, WPR>(p, r, w, u24, sh, head, nq, tail, rowp, min((nq + 31) >> 5, MAXNCH), sub,
+                     grp);
 }
 
 }  // namespace ts

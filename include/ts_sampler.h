@@ -224,17 +224,21 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
  * with programmatic dependent launch, so that a step's kernel is scheduled
  * while the previous kernel in the stream drains (each kernel still waits
  * for its predecessor before touching memory); 0 launches plainly.
- * TS_OPT_WIDE_EXACT: 1 makes path 3 skip its sampled threshold and always
- * take its exact re-reading select (for tests).  Results never depend on any
- * option. */
+ * TS_OPT_WIDE_EXACT: 1 makes paths 3 and 4 skip their sampled threshold and
+ * always take their exact re-reading select (for tests).
+ * TS_OPT_WARPS_PER_ROW: path 1's warps per row, 0 = automatic (4 for calls of
+ * up to 4 rows per SM, 2 up to 16, else 1), or 1, 2 or 4.  Results never
+ * depend on any option. */
 #define TS_OPT_PATH 1
 #define TS_OPT_CLUSTER 2
 #define TS_OPT_PDL 3
 #define TS_OPT_WIDE_EXACT 4
+#define TS_OPT_WARPS_PER_ROW 5
 ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value);
 
 /* Describes the kernel that ts_sample would launch for `b` (path 1 .. 4,
- * CTAs per row, threads per CTA, dynamic shared memory bytes, grid size).
+ * CTAs per row (path 1: warps per row), threads per CTA, dynamic shared
+ * memory bytes, grid size).
  * Any output pointer may be NULL. */
 ts_status ts_plan(const ts_sampler *s, const ts_batch *b, int32_t *path,
                   int32_t *ctas_per_row, int32_t *threads, int32_t *smem_bytes,

@@ -122,6 +122,24 @@ def test_geometry_independence(ts):
         assert np.array_equal(ids[0], other)
 
 
+@pytest.mark.parametrize("name", ["tiny", "qwen3tts", "drama3"])
+def test_warps_per_row(ts, name):
+    """Rows shared by 1, 2 or 4 warps give the oracle's results, and the
+    same ids as each other."""
+    host = workloads.make(name, 3)
+    ref = oracle.sample(host, max_keep=host["cap"], n_threads=8)
+    ids = []
+    for wpr in (1, 2, 4):
+        s = make_sampler(ts, host["cap"], path=1)
+        s.set_option(ts.TS_OPT_WARPS_PER_ROW, wpr)
+        assert s.plan(ts.DeviceBatch(host, "cuda"))["ctas_per_row"] == wpr
+        gpu = run_gpu(s, host, debug_keep=host["cap"])
+        compare(host, gpu, ref, label=f"{name} wpr{wpr}")
+        ids.append(gpu["ids"])
+        s.close()
+    assert np.array_equal(ids[0], ids[1]) and np.array_equal(ids[0], ids[2])
+
+
 # ---------------------------------------------------------------------------
 # edge cases: ragged / misaligned rows, ties, non-finite values, parameters
 # ---------------------------------------------------------------------------
@@ -174,14 +192,16 @@ def _edge_batch(dtype, rng):
     return host
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path,wpr", [(1, 1), (1, 2), (1, 4), (2, 0)])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-def test_edge_rows(ts, dtype, path):
+def test_edge_rows(ts, dtype, path, wpr):
     rng = np.random.default_rng(21)
     host = _edge_batch(dtype, rng)
     ref = oracle.sample(host, max_keep=64)
     assert np.any(ref["err"] == 4) and np.any(ref["err"] == 2)
     s = make_sampler(ts, 64, path=path)
+    if wpr:
+        s.set_option(ts.TS_OPT_WARPS_PER_ROW, wpr)
     gpu = run_gpu(s, host, debug_keep=64)
     compare(host, gpu, ref, label=f"edge {dtype} path{path}")
     # full ties: the kept set is the 30 lowest indices
