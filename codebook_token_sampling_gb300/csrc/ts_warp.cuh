@@ -484,6 +484,7 @@ struct TowerShared {
   uint32_t xb[4];    // the row's candidate bound and largest key
   uint32_t xt[4];
   uint32_t xn[4];    // per-warp candidate counts
+  uint32_t xu;       // the row's draw (computed by warp 1 when the row has several)
   uint32_t xbad[4];  // per-warp NaN / +inf flags
 };
 
@@ -513,6 +514,7 @@ template <class K, int WPR, class SH>
 __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w, uint32_t u24,
                                            SH &sh, int head, int nq, int tail, const char *rowp,
                                            int nch, int sub, int grp) {
+  // u24: the draw when WPR == 1; with several warps it arrives below
   using SW = SortWord<K>;
   using TT = Top2<K>;
   constexpr int EPC = K::kPerChunk;
@@ -537,6 +539,12 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
   }
   const bool has_e = eidx < V;
   const uint32_t ebits = has_e ? K::load_one(rowp, eidx) : 0u;
+  if constexpr (WPR > 1) {
+    // the draw, by warp 1 while its copies are in flight: off warp 0's path
+    if (sub == 1 && lane == 0 && !w.greedy)
+      sh.xu = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
+                         static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
+  }
   const uint32_t ekey = has_e ? K::key(ebits) : 0u;
   cp_async_wait_all();
   __syncwarp();
@@ -554,6 +562,7 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
     sh.xm1[sub * 32 + lane] = m1;
     sh.xm2[sub * 32 + lane] = m2;
     row_sync<WPR>(grp);
+    if (!w.greedy) u24 = sh.xu;  // written by warp 1 before this barrier
   }
   const int kq = w.k_eff;
   uint32_t t0 = 0, top = 0;
@@ -699,9 +708,10 @@ __global__ void __launch_bounds__(kTowerThreads) row_sampler_kernel(const Params
   const int nq = (V - head) / EPC;
   const int tail = V - head - nq * EPC;
   TowerShared<K, MAXNCH> &sh = shared_rows[grp];
-  // the draw, on lane 0 of warp 0 (its result is needed only by the tail)
+  // the draw, on lane 0 (its result is needed only by the tail); a row
+  // shared by several warps has warp 1 compute it inside the body
   uint32_t u24 = 0;
-  if (sub == 0 && lane == 0 && !w.greedy)
+  if (WPR == 1 && lane == 0 && !w.greedy)
     u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
                      static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
   u24 = __shfl_sync(0xFFFFFFFFu, u24, 0);
