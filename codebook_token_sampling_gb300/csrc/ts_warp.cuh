@@ -685,7 +685,7 @@ __device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w,
 // its own chunk count.  WPR = warps per row (1, 2 or 4): a block of four
 // warps samples 4 / WPR rows.
 template <class K, int MAXNCH, int WPR>
-__global__ void __launch_bounds__(kTowerThreads) row_sampler_kernel(const Params p) {
+__global__ void __launch_bounds__(kTowerThreads, WPR == 4 ? 9 : 1) row_sampler_kernel(const Params p) {
   constexpr int EPC = K::kPerChunk;
   constexpr int RPB = kTowerWarps / WPR;
   __shared__ __align__(16) TowerShared<K, MAXNCH> shared_rows[RPB];
