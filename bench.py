@@ -49,6 +49,13 @@ DESCRIPTIONS = {
 }
 
 
+def split_kernels(plan, num_sms: int, n_rows: int) -> int:
+    """Kernels per ts_sample call on the split path: the threshold kernel is
+    skipped when the streaming grid is small (its CTAs sample the row
+    themselves)."""
+    return 2 if n_rows * plan["ctas_per_row"] <= 2 * num_sms else 3
+
+
 def kernel_source_hash() -> str:
     """Hash of the CUDA sources, to tell whether recorded ncu counters still
     describe the kernels that run."""
@@ -405,7 +412,9 @@ def run_ours(args, world, rank, local):
         "host": host, "n_rows": n_rows, "t_step": t_max / k, "t_launch": t_launch,
         "t_e2e": t_e2e, "clocks": clk, "plan": plan, "n_buf": n_buf, "l2": l2,
         "step_bytes": step_bytes,
-        "launches": ((3 if plan["path"] == 4 else 1) + 1) * k,
+        "split_kernels": split_kernels(plan, props.multi_processor_count, n_rows),
+        "launches": (split_kernels(plan, props.multi_processor_count, n_rows)
+                     if plan["path"] == 4 else 1) * k + k,
         "h2d": int(bufs[0].numel() * bufs[0].element_size()), "d2h": n_rows * 5,
     }
 
@@ -544,8 +553,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(args.config, args.rows),
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "launch": "one ts_sample call: split_threshold_kernel + split_stream_kernel + "
-                               "split_tail_kernel" if split else
+                     "launch": ("one ts_sample call: split_stream_kernel (threshold inline) + "
+                                "split_tail_kernel" if r["split_kernels"] == 2 else
+                                "one ts_sample call: split_threshold_kernel + split_stream_kernel + "
+                                "split_tail_kernel") if split else
                                "one ts_sample call: one kernel (" +
                                {1: "row_sampler_kernel", 2: "cluster_sampler_kernel",
                                 3: "wide_sampler_kernel"}[r["plan"]["path"]] + ")",

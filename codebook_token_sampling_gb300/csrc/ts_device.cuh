@@ -54,6 +54,7 @@ struct Params {
   int32_t ws_rows;
   int32_t ws_units;
   int32_t ws_units_per_row;
+  int32_t split_inline;  // split path: the streaming CTAs compute the threshold themselves
 };
 
 // ---------------------------------------------------------------------------

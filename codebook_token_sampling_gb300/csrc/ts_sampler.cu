@@ -303,6 +303,8 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
     p.ws_rows = s->ws_rows;
     p.ws_units = s->ws_units;
     p.ws_units_per_row = pl.g;
+    // few CTAs: the streaming CTAs compute the threshold themselves
+    p.split_inline = static_cast<long long>(b->n_rows) * pl.g <= 2LL * s->num_sms ? 1 : 0;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cudaLaunchAttribute attr;
@@ -314,8 +316,11 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
     cfg.blockDim = dim3(ts::kSplitThreads);
     cfg.gridDim = dim3(static_cast<unsigned>(b->n_rows));
     void *args[] = {&p};
-    cudaError_t e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_threshold_kernel), args);
-    if (e != cudaSuccess) return cuda_fail(e, "split threshold launch");
+    cudaError_t e = cudaSuccess;
+    if (!p.split_inline) {
+      e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_threshold_kernel), args);
+      if (e != cudaSuccess) return cuda_fail(e, "split threshold launch");
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
     cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
     e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_stream_kernel), args);
@@ -541,6 +546,15 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab) {
   if (max_rows > 0) {
     const size_t bytes = ts::split_workspace_bytes(max_rows, units);
     e = cudaMalloc(&s->ws, bytes);
+    if (e == cudaSuccess) {
+      e = cudaMemset(s->ws, 0, bytes);  // the per-row counters start at zero
+      if (e != cudaSuccess) {
+        cudaFree(s->ws);
+        s->ws = nullptr;
+        cudaSetDevice(prev);
+        return cuda_fail(e, "cudaMemset");
+      }
+    }
     if (e != cudaSuccess) {
       s->ws = nullptr;
       rc = e == cudaErrorMemoryAllocation ? TS_ERR_NO_MEMORY : cuda_fail(e, "cudaMalloc");

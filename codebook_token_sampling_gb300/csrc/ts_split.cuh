@@ -15,6 +15,11 @@
 // does nothing else, so the streaming CTAs never wait for one another or
 // hold an SM for a row's tail.
 //
+// For launches of few CTAs, kernel A is skipped and every CTA of kernel B
+// takes the same sample itself (the threshold kernel's launch would cost
+// more than the duplicated sample).  Kernel C clears each row's counter
+// after use, so the counters are zero at the start of every call either way.
+//
 // Kernel C (one CTA per row) copies the row's candidate array (a few
 // thousand entries, from L2) into shared memory in the same round of loads
 // as the units' records, and runs the row's tail:
@@ -881,9 +886,19 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
                     : make_uint4(0u, 0u, 0u, 0u);
   }
   if (t == 0) misc[kWN] = 0u;
-  pdl_wait_and_release();  // the threshold kernel has finished
+  pdl_wait_and_release();  // the threshold kernel (if any) has finished
   SplitWs ws = split_ws(p.workspace, p.ws_rows, p.ws_units);
-  const uint32_t t_key = __ldcg(&ws.row[r].t_key);
+  uint32_t t_key = 0;
+  if (p.split_inline) {
+    // small launches: every CTA of the row takes the same sample itself
+    // (the staging area holds the histogram), saving the threshold kernel
+    if (!p.wide_exact && (V > kSplitRowCap || S > kSplitUnitCap))
+      t_key = wide_sample_threshold<kSplitSampleRun>(rowp, V, w.k_eff, 1,
+                                                     reinterpret_cast<uint32_t *>(stage), misc,
+                                                     reinterpret_cast<uint64_t *>(misc + kWScan));
+  } else {
+    t_key = __ldcg(&ws.row[r].t_key);
+  }
   __syncthreads();
 
   // ---- filter: every logit that compares >= t (NaN included) is kept as
@@ -1009,6 +1024,10 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_tail_kernel(const Para
     misc[kWU24] = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
                              static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
   pdl_wait_and_release();  // the streaming kernel has finished
+  if (t == 0) {  // the row's counter starts at zero for the next call
+    SplitWs ws0 = split_ws(p.workspace, p.ws_rows, p.ws_units);
+    ws0.row[r].count = 0u;
+  }
   if (w.err) {
     if (t == 0) finish_row(p, r, w, -1, w.err);
     return;

@@ -195,9 +195,9 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
  * next call.
  *
  * Sharing: all calls on a device use the one array, which keeps what the last
- * call left in it.  Each call's first kernel clears the per-row counters
- * that must start at zero, and everything else that a call uses it writes
- * before it reads it.
+ * call left in it.  The array starts zeroed, and each call clears the
+ * per-row counters it used before it ends (they must start at zero);
+ * everything else that a call uses it writes before it reads it.
  * Calls whose kernels may overlap on the GPU (on unordered streams, or
  * from several host threads without ordering) race on the array and give
  * wrong results: order them on one stream or with events. */
