@@ -525,7 +525,10 @@ def main():
     t = r["t_step"]
     value = world * n_rows / t
     alg = algorithmic_bytes(r["host"])
-    achieved = alg / r["t_launch"] / 1e9
+    # the sampler's launches timed inside the timed region: each step is one
+    # ts_sample call plus the step-advance kernel, so this slightly
+    # understates the sampler's own rate
+    achieved = alg / t / 1e9
     split = r["plan"]["path"] == 4
     cpu = None
     if not args.no_cpu_baseline:
@@ -561,7 +564,9 @@ def main():
                                {1: "row_sampler_kernel", 2: "cluster_sampler_kernel",
                                 3: "wide_sampler_kernel"}[r["plan"]["path"]] + ")",
                      "algorithmic_bytes_per_launch": alg,
-                     "us_per_launch": 1e6 * r["t_launch"]},
+                     "us_per_launch": 1e6 * t,
+                     "us_per_launch_measured_as": "the timed step loop (ts_sample + step advance)",
+                     "us_per_launch_back_to_back": 1e6 * r["t_launch"]},
         "multi_step": multi,
         "e2e": {"value": world * n_rows / r["t_e2e"], "unit": "rows/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
