@@ -151,7 +151,9 @@ ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep,
  * the cluster path, which needs no workspace.  Allocates device memory
  * (32 KB per row plus 16 bytes per CTA of the largest launch), so call it before any stream
  * capture and not concurrently with work on the sampler; 0 rows frees the
- * workspace.  Smaller requests than the current size keep it. */
+ * workspace.  Smaller requests than the current size keep it.  Calls that
+ * use the workspace share it: two such calls on one sampler must not
+ * overlap on the GPU (order them on one stream or with events). */
 ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
 
 /* Scratch size and row limit of ts_sample_noalloc. */

@@ -97,6 +97,18 @@ def test_noalloc_stress_then_tower_rows(ts):
     _assert_same(got[1], _existing(ts, second), "64 tower rows")
 
 
+def test_noalloc_small_then_large_stress(ts):
+    """8 rows of 151,936 logits (few CTAs: the streaming CTAs sample the rows
+    themselves, no threshold kernel), then 32 rows (the threshold kernel
+    runs): the row counters left by the first call must not leak into the
+    second."""
+    first = workloads.make("stress", 21, rows=8)
+    second = workloads.make("stress", 22, rows=32)
+    got = _noalloc_pair(ts, [first, second])
+    _assert_same(got[0], _existing(ts, first), "stress 8 rows")
+    _assert_same(got[1], _existing(ts, second), "stress 32 rows")
+
+
 def test_noalloc_edge_rows_then_widest_rows(ts):
     """Rows with errors, then 64 rows of the widest bf16 vocabulary (the
     largest call the scratch takes)."""
