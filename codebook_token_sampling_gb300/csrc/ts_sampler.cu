@@ -22,7 +22,7 @@ struct ts_sampler {
   int device;
   int cap;
   int num_sms;
-  int force_path;     // 0 auto, 1 block per row, 2 CTA/cluster per row, 3 wide
+  int force_path;     // 0 auto, 1 warps per row, 2 CTA/cluster per row, 3 wide cluster, 4 split
   int force_cluster;  // 0 auto, else CTAs per row
   int pdl;            // launch with programmatic stream serialization
   int wide_exact;     // wide path: always take the exact path (testing)

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Pa
   uint32_t t_key = 0;
   if (!w.err && !p.wide_exact) {
     const char *rowp = static_cast<const char *>(p.logits) + w.off * 2;
-    // a row the last CTA can gather whole, in slices each CTA can hold,
+    // a row the tail CTA can gather whole, in slices each CTA can hold,
     // keeps every logit (t = lowest key); others sample
     if (w.vocab > kSplitRowCap || p.slice > kSplitUnitCap)
       t_key = wide_sample_threshold<kSplitSampleRun>(rowp, w.vocab, w.k_eff, 1, hist, misc,
@@ -137,46 +137,6 @@ __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Pa
     ws.row[r].t_key = t_key;
     ws.row[r].count = 0u;
   }
-}
-
-// One candidate of the streaming phase: its entry, its page count and the
-// running maximum.
-__device__ __forceinline__ void split_keep(uint32_t key, uint32_t idx, uint32_t pos,
-                                           uint32_t *cand, uint32_t *pg, uint32_t &kmax) {
-  if (pos < static_cast<uint32_t>(kSplitUnitCap)) cand[pos] = (key << 16) | idx;
-  atomicAdd(&pg[key >> 8], 1u);
-  kmax = max(kmax, key);
-}
-
-// Drains n <= 32 staged words (two logits each) from a warp's ring.
-__device__ __forceinline__ void split_drain(const uint2 *ring, uint32_t head, uint32_t n,
-                                            uint32_t t_key, uint32_t *cand, uint32_t *pg,
-                                            uint32_t *counter, uint32_t &bad, uint32_t &kmax) {
-  const uint32_t lane = lane_id();
-  bool f0 = false, f1 = false;
-  uint32_t k0 = 0, k1 = 0, idx0 = 0;
-  if (lane < n) {
-    const uint2 e = ring[(head + lane) & (kWideRing - 1)];
-    const uint32_t kw = KeyBF16::key_word(e.x);
-    k0 = kw & 0xFFFFu;
-    k1 = kw >> 16;
-    idx0 = e.y;
-    const bool nf0 = k0 < KeyBF16::kNegInf || k0 >= KeyBF16::kPosInf;
-    const bool nf1 = k1 < KeyBF16::kNegInf || k1 >= KeyBF16::kPosInf;
-    bad |= nf0 | nf1;
-    f0 = !nf0 && k0 >= t_key;
-    f1 = !nf1 && k1 >= t_key;
-  }
-  const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, f0), b1 = __ballot_sync(0xFFFFFFFFu, f1);
-  const uint32_t total = __popc(b0) + __popc(b1);
-  if (total == 0) return;
-  uint32_t base = 0;
-  if (lane == 0) base = atomicAdd(counter, total);
-  base = __shfl_sync(0xFFFFFFFFu, base, 0);
-  const uint32_t lt = lanemask_lt();
-  const uint32_t pos = base + __popc(b0 & lt) + __popc(b1 & lt);
-  if (f0) split_keep(k0, idx0, pos, cand, pg, kmax);
-  if (f1) split_keep(k1, idx0 + 1u, pos + (f0 ? 1u : 0u), cand, pg, kmax);
 }
 
 // Candidate entries are grouped in segments, one per unit: segment k is

@@ -214,15 +214,16 @@ ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream);
  * Synchronises `stream`: for tests and debugging, not for the decode loop. */
 ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
 
-/* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = one warp per
- * row with a bounded candidate set (requires cap <= 64 and max_row_vocab <=
- * 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row that holds the row in
- * shared memory, 3 = the single-pass wide-row cluster path (bf16 only;
- * automatic for bf16 rows wider than 32,768 without a workspace), 4 = the
- * split wide-row path (bf16 only; needs ts_reserve; automatic for bf16 rows
- * wider than 32,768 when the workspace fits).  TS_OPT_CLUSTER: 0 =
- * automatic, else the CTAs per row of paths 2 and 3 (1, 2, 4 or 8; path 3
- * needs max_row_vocab / CTAs <= 65,536) or of path 4 (2 .. 16).  TS_OPT_PDL: 1 (default) launches
+/* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = one to four
+ * warps per row with a bounded candidate set (requires cap <= 64 and
+ * max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row that
+ * holds the row in shared memory, 3 = the single-pass wide-row cluster path
+ * (bf16 only; automatic for bf16 rows wider than 32,768 without a
+ * workspace), 4 = the split wide-row path (bf16 only; needs ts_reserve;
+ * automatic for bf16 rows wider than 32,768 when the workspace fits).
+ * TS_OPT_CLUSTER: 0 = automatic, else the CTAs per row of paths 2 and 3 (1,
+ * 2, 4 or 8; path 3 needs max_row_vocab / CTAs <= 65,536) or of path 4 (2 ..
+ * 16).  TS_OPT_PDL: 1 (default) launches
  * with programmatic dependent launch, so that a step's kernel is scheduled
  * while the previous kernel in the stream drains (each kernel still waits
  * for its predecessor before touching memory); 0 launches plainly.
