@@ -57,15 +57,20 @@ def split_kernels(plan, num_sms: int, n_rows: int) -> int:
 
 
 def kernel_source_hash() -> str:
-    """Hash of the CUDA sources, to tell whether recorded ncu counters still
-    describe the kernels that run."""
+    """Hash of the CUDA sources with comments and whitespace removed, to tell
+    whether recorded ncu counters still describe the kernels that run."""
     import hashlib
+    import re
     h = hashlib.sha256()
     src = os.path.join(ROOT, "codebook_token_sampling_gb300", "csrc")
     for name in sorted(os.listdir(src)):
         if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(src, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(src, name), encoding="utf-8") as f:
+                text = f.read()
+            text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+            text = re.sub(r"//[^\n]*", " ", text)
+            text = " ".join(text.split())
+            h.update(name.encode() + b"\0" + text.encode())
     return h.hexdigest()[:16]
 
 

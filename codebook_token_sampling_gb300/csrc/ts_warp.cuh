@@ -362,9 +362,10 @@ __device__ __forceinline__ void warp_sort_cand(const typename SortWord<K>::T *ca
   if constexpr (R > 1) s1 = v[1];
 }
 
-// Warp-per-row kernel.  Each warp owns one row (kTowerWarps rows per block,
-// no block barriers):
-//   1. the row is copied into the warp's shared-memory stage with 16-byte
+// Warp-path kernel.  A row is owned by one warp, or shared by 2 or 4 warps
+// (kTowerWarps / WPR rows per block; the warps of a row meet at a named
+// barrier of their own, never at a block barrier):
+//   1. the row is copied into its shared-memory stage with 16-byte
 //      asynchronous copies (lane l: body chunks l, l + 32, ...), all in
 //      flight at once; the unaligned head and tail elements are read one per
 //      lane; lane 0 computes the Philox draw meanwhile;
