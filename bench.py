@@ -536,7 +536,7 @@ def main():
     achieved = alg / t / 1e9
     split = r["plan"]["path"] == 4
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle baseline: rank 0 at N = 1 only
         threads = host_threads()
         steps_host = [workloads.make(args.config, i, rows=args.rows) for i in range(3)]
         rate, per_step, done = oracle_rate(steps_host, args.cpu_budget, threads)
