@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 import workloads  # noqa: E402
 
 METRIC = "sampled rows/s and µs/step at 128 streams×10 codebooks; HBM GB/s vs roofline"
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (about 8 TB/s)
 PARAM_BYTES_READ = 64   # per row: vocab, offset, temp, top_k, top_p, seed, request,
                         # codebook, stream, step, eos id, feedback slot
 PARAM_BYTES_WRITTEN = 9  # per row: id, eos flag, feedback slot
@@ -560,6 +561,7 @@ def main():
         "gb_per_s": world * alg / t / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": recorded_traffic(args.config, args.rows),
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "launch": ("one ts_sample call: split_stream_kernel (threshold inline) + "
                                 "split_tail_kernel" if r["split_kernels"] == 2 else

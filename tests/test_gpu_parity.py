@@ -300,6 +300,39 @@ def test_graph_capture_matches_eager(ts):
     s.close()
 
 
+def test_resume_from_a_step(ts):
+    """The sampler keeps no state between steps: restarting at step k from
+    (seed, request, step) alone reproduces the continuous run's ids, EOS flags
+    and frames from step k on."""
+    host = workloads.make("qwen3tts", 0)
+    logits = [torch.from_numpy(np.ascontiguousarray(workloads.make("qwen3tts", i)["logits"])
+                               .view(np.int16)).cuda() for i in range(4)]
+    steps, k = 60, 30
+
+    def run(first, count):
+        h = dict(host)
+        h["step"] = np.full(host["n_streams"], first, np.int64)
+        s = make_sampler(ts, host["cap"])
+        b = ts.DeviceBatch(h, "cuda")
+        ids, eos, frames = [], [], []
+        for i in range(count):
+            b.set_logits(logits[(first + i) % 4])  # the logits of absolute step first + i
+            s.sample(b)
+            ts.ts_advance_steps(b.step)
+            ids.append(b.out_ids.clone())
+            eos.append(b.out_eos.clone())
+            frames.append(b.feedback.clone())
+        torch.cuda.synchronize()
+        assert s.read_status() == 0
+        s.close()
+        return [torch.stack(x).cpu().numpy() for x in (ids, eos, frames)]
+
+    full = run(0, steps)
+    resumed = run(k, steps - k)
+    for a, b in zip(full, resumed):
+        assert np.array_equal(a[k:], b)
+
+
 @pytest.mark.parametrize("name,steps", [("tiny", 500), ("qwen3tts", 40)])
 def test_graph_loop_with_feedback(ts, name, steps):
     """`steps` decode steps captured as one graph: ts_sample then
