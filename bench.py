@@ -57,13 +57,13 @@ def split_kernels(plan, num_sms: int, n_rows: int) -> int:
     return 2 if n_rows * plan["ctas_per_row"] <= 2 * num_sms else 3
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(src: str | None = None) -> str:
     """Hash of the CUDA sources with comments and whitespace removed, to tell
     whether recorded ncu counters still describe the kernels that run."""
     import hashlib
     import re
     h = hashlib.sha256()
-    src = os.path.join(ROOT, "codebook_token_sampling_gb300", "csrc")
+    src = src or os.path.join(ROOT, "codebook_token_sampling_gb300", "csrc")
     for name in sorted(os.listdir(src)):
         if name.endswith((".cu", ".cuh")):
             with open(os.path.join(src, name), encoding="utf-8") as f:
@@ -75,10 +75,10 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config: str, rows):
+def recorded_traffic(config: str, rows, path: str | None = None, src: str | None = None):
     """DRAM bytes per launch from the committed ncu record of this workload,
     or None when there is none or the kernels changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = path or os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -86,7 +86,7 @@ def recorded_traffic(config: str, rows):
         return None
     key = config if config != "stress" else f"stress{rows}"
     e = rec.get(key)
-    if not e or e.get("source_hash") != kernel_source_hash():
+    if not e or e.get("source_hash") != kernel_source_hash(src):
         return None
     return e.get("dram_bytes_per_launch")
 
