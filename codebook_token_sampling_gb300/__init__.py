@@ -38,6 +38,7 @@ TS_OPT_CLUSTER = 2
 TS_OPT_PDL = 3
 TS_OPT_WIDE_EXACT = 4
 TS_OPT_WARPS_PER_ROW = 5
+TS_OPT_FAIL_LAUNCH = 6
 TS_MAX_VOCAB_BF16 = 163840
 TS_MAX_VOCAB_F32 = 81920
 TS_NOALLOC_SCRATCH_BYTES = 4194304

@@ -27,6 +27,7 @@ struct ts_sampler {
   int pdl;            // launch with programmatic stream serialization
   int wide_exact;     // wide path: always take the exact path (testing)
   int force_wpr;      // warp-per-row path: 0 auto, else warps per row (1, 2, 4)
+  int fail_launch;    // tests: the split path's launch of this index (2 or 3) fails once
   uint32_t *status;   // device word
   void *ws;           // split wide path workspace (ts_reserve), or null
   size_t ws_bytes;
@@ -316,6 +317,24 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
     cfg.blockDim = dim3(ts::kSplitThreads);
     cfg.gridDim = dim3(static_cast<unsigned>(b->n_rows));
     void *args[] = {&p};
+    // A launch refused after the streaming kernel was queued leaves the row
+    // counters that the tail kernel would have cleared non-zero.  The row
+    // records are then zeroed on the same stream, so that the next call on
+    // this workspace starts from clean counters (no allocation, no sync).
+    const auto fail_after_stream = [&](cudaError_t e, const char *what) {
+      const ts_status rc = cuda_fail(e, what);
+      const size_t bytes = static_cast<size_t>(b->n_rows) * sizeof(ts::SplitRowMeta);
+      const cudaError_t e2 = cudaMemsetAsync(s->ws, 0, bytes, st);
+      if (e2 != cudaSuccess) cuda_fail(e2, "split workspace reset after a failed launch");
+      return rc;
+    };
+    // the test-only injection of ts_set_option(TS_OPT_FAIL_LAUNCH): the
+    // launch is refused before anything is queued for it
+    const auto injected = [&](int which) {
+      if (s->fail_launch != which) return false;
+      const_cast<ts_sampler *>(s)->fail_launch = 0;
+      return true;
+    };
     cudaError_t e = cudaSuccess;
     if (!p.split_inline) {
       e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_threshold_kernel), args);
@@ -323,12 +342,17 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
     }
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
     cfg.dynamicSmemBytes = static_cast<size_t>(pl.smem);
-    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_stream_kernel), args);
+    e = injected(2) ? cudaErrorLaunchOutOfResources
+                    : cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_stream_kernel),
+                                          args);
+    // the threshold kernel (if it ran) cleared the counters; nothing is dirty yet
     if (e != cudaSuccess) return cuda_fail(e, "split stream launch");
     cfg.gridDim = dim3(static_cast<unsigned>(b->n_rows));
     cfg.dynamicSmemBytes = ts::kTailSmemBytes;
-    e = cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_tail_kernel), args);
-    if (e != cudaSuccess) return cuda_fail(e, "split tail launch");
+    e = injected(3) ? cudaErrorLaunchOutOfResources
+                    : cudaLaunchKernelExC(&cfg, reinterpret_cast<void *>(ts::split_tail_kernel),
+                                          args);
+    if (e != cudaSuccess) return fail_after_stream(e, "split tail launch");
     return TS_OK;
   }
   void *fn = nullptr;
@@ -371,6 +395,16 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
 // ---------------------------------------------------------------------------
 constexpr size_t kNoallocWsOff = 256;  // the workspace follows the status slot
 constexpr int kNoallocMaxDevices = 64;
+// The scratch holds a fixed layout, the same for every call: row records for
+// TS_NOALLOC_MAX_ROWS rows and unit records for that many rows at the most
+// units per row, at fixed offsets.  A row's candidate counter therefore sits
+// at the same address in every call, and the call that last used it has
+// cleared it.
+constexpr int kNoallocWsRows = TS_NOALLOC_MAX_ROWS;
+constexpr int kNoallocWsUnits = TS_NOALLOC_MAX_ROWS * ts::kSplitMaxUnits;
+static_assert(kNoallocWsOff + ts::split_workspace_bytes(kNoallocWsRows, kNoallocWsUnits) <=
+                  TS_NOALLOC_SCRATCH_BYTES,
+              "the no-alloc scratch must hold the split workspace of its largest call");
 
 struct NoallocDevice {
   void *scratch;  // device address of g_noalloc_scratch; null until set up
@@ -452,6 +486,7 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->pdl = 1;
   s->wide_exact = 0;
   s->force_wpr = 0;
+  s->fail_launch = 0;
   s->status = nullptr;
   s->ws = nullptr;
   s->ws_bytes = 0;
@@ -587,14 +622,10 @@ ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *stat
   rc = noalloc_setup(device, &d);
   if (rc != TS_OK || b->n_rows == 0) return rc;
 
-  // The split path's CTAs per row, fewer (down to what the widest slice
-  // allows) while the workspace would outgrow the scratch.
+  // The split path's CTAs per row (at most kSplitMaxUnits, which the fixed
+  // layout holds for every row).
   const int n = b->n_rows, vmax = b->max_row_vocab;
-  const int u_min = std::max(2, (vmax + ts::kWideSliceMax - 1) / ts::kWideSliceMax);
-  const size_t room = TS_NOALLOC_SCRATCH_BYTES - kNoallocWsOff;
-  int u = split_units(n, vmax, d.num_sms);
-  while (u > u_min && ts::split_workspace_bytes(n, n * u) > room) --u;
-  if (ts::split_workspace_bytes(n, n * u) > room) return noalloc_reject("scratch too small");
+  const int u = split_units(n, vmax, d.num_sms);
 
   ts_sampler s;
   std::memset(&s, 0, sizeof s);
@@ -606,9 +637,9 @@ ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *stat
   s.pdl = 1;
   s.status = status ? status : static_cast<uint32_t *>(d.scratch);
   s.ws = static_cast<char *>(d.scratch) + kNoallocWsOff;
-  s.ws_bytes = room;
-  s.ws_rows = n;
-  s.ws_units = n * u;
+  s.ws_bytes = TS_NOALLOC_SCRATCH_BYTES - kNoallocWsOff;
+  s.ws_rows = kNoallocWsRows;
+  s.ws_units = kNoallocWsUnits;
   s.ws_vocab = vmax;
   return launch(&s, b, make_params(&s, b), static_cast<cudaStream_t>(stream));
 }
@@ -668,6 +699,11 @@ ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value) {
   if (option == TS_OPT_WARPS_PER_ROW) {
     if (value != 0 && value != 1 && value != 2 && value != 4) return TS_ERR_INVALID_ARG;
     s->force_wpr = value;
+    return TS_OK;
+  }
+  if (option == TS_OPT_FAIL_LAUNCH) {
+    if (value != 0 && value != 2 && value != 3) return TS_ERR_INVALID_ARG;
+    s->fail_launch = value;
     return TS_OK;
   }
   return TS_ERR_INVALID_ARG;

@@ -89,7 +89,7 @@ struct SplitUnitMeta {
 // Row records for max_rows rows, unit records for max_units units (a
 // launch's CTAs: unit r * U + u is slice u of row r), then each row's
 // candidate array of kSplitRowCap entries.
-__host__ __device__ inline size_t split_workspace_bytes(int max_rows, int max_units) {
+__host__ __device__ constexpr size_t split_workspace_bytes(int max_rows, int max_units) {
   const size_t rows = static_cast<size_t>(max_rows), units = static_cast<size_t>(max_units);
   return rows * sizeof(SplitRowMeta) + units * sizeof(SplitUnitMeta) + rows * kSplitRowCap * 4;
 }

@@ -197,9 +197,15 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
  * next call.
  *
  * Sharing: all calls on a device use the one array, which keeps what the last
- * call left in it.  The array starts zeroed, and each call clears the
- * per-row counters it used before it ends (they must start at zero);
- * everything else that a call uses it writes before it reads it.
+ * call left in it.  Its layout is fixed, the same for every call whatever its
+ * row count: a 256-byte status slot, then 64 row records (16 bytes each),
+ * then 1024 unit records (16 bytes each, 16 per row), then 64 candidate
+ * arrays of 32 KB, each at a fixed offset (about 2 MiB of the 4 MiB in all).
+ * Row r of any call uses row record r, whose candidate counter must be zero
+ * when a call starts: the array starts zeroed, and the call that used a
+ * counter clears it before it ends (if one of its launches is refused after
+ * an earlier one was queued, the call zeroes its rows' records on the stream
+ * instead).  Everything else that a call uses it writes before it reads it.
  * Calls whose kernels may overlap on the GPU (on unordered streams, or
  * from several host threads without ordering) race on the array and give
  * wrong results: order them on one stream or with events. */
@@ -237,6 +243,13 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
 #define TS_OPT_PDL 3
 #define TS_OPT_WIDE_EXACT 4
 #define TS_OPT_WARPS_PER_ROW 5
+/* TS_OPT_FAIL_LAUNCH (tests only): 2 or 3 makes the next split-path call
+ * refuse its streaming (2) or tail (3) launch on the host, before anything is
+ * queued for it, and return TS_ERR_CUDA, as a failed cudaLaunchKernelExC
+ * would; 0 disarms it.  When the tail launch fails after the streaming kernel
+ * was queued, the call zeroes the rows' workspace records on the stream
+ * before it returns, so the next call starts from clean counters. */
+#define TS_OPT_FAIL_LAUNCH 6
 ts_status ts_set_option(ts_sampler *s, int32_t option, int32_t value);
 
 /* Describes the kernel that ts_sample would launch for `b` (path 1 .. 4,

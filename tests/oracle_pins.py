@@ -239,6 +239,62 @@ def pin_nucleus_bruteforce(orc):
                         assert abs(o["kept_probs"][0, : len(q)].sum() - 1.0) < 1e-12
 
 
+def brute_margin(values, top_k, top_p, temp, cap, u24):
+    """Distance of a row's draw from the nearest decision boundary, from its
+    definition: the smallest |prefix mass - top_p| over the sorted prefixes of
+    the top-k set (when 0 < top_p < 1), and the smallest |C_j / S_p - u| over
+    the nucleus, with C_j the inclusive sorted prefix masses (math.fsum) and
+    S_p the nucleus mass.  Greedy rows have no boundary (inf)."""
+    kept = brute_kept(values, top_k, cap)
+    if temp <= 0.0 or len(kept) == 1:
+        return math.inf
+    q = brute_probs(values, kept, temp)
+    m_cut = math.inf
+    if 0.0 < top_p < 1.0:
+        m_cut = min(abs(math.fsum(q[:n]) - top_p) for n in range(1, len(q) + 1))
+    n_p = brute_nucleus_size(q, top_p)
+    s_p = math.fsum(q[:n_p])
+    u = u24 / TWO24
+    m_draw = min(abs(math.fsum(q[:j + 1]) / s_p - u) for j in range(n_p))
+    return min(m_cut, m_draw)
+
+
+def pin_margin_bruteforce(orc):
+    """The boundary margin that decides which rows must match bit for bit,
+    against brute_margin on small rows with forced draws: random u and u set
+    right at a CDF step (a tiny margin), top_p near and far from a prefix."""
+    rng = np.random.default_rng(20)
+    cases = []
+    for v in (3, 6, 9, 16):
+        for _ in range(6):
+            x = np.round(rng.normal(0, 1.5, v) * 8) / 8
+            top_k = int(rng.integers(0, v + 1))
+            top_p = float(np.float32(rng.choice([rng.uniform(0.05, 0.99), 1.0, 0.5])))
+            temp = float(np.float32(rng.choice([1.0, 0.7, 1.6])))
+            cases.append((x, top_k, top_p, temp))
+    for x, top_k, top_p, temp in cases:
+        kept = brute_kept(x, top_k, 32)
+        q = brute_probs(x, kept, temp) if len(kept) > 1 else [1.0]
+        if near_cutoff(q, top_p, 1e-9):
+            continue  # the nucleus size itself is a rounding call here
+        n_p = brute_nucleus_size(q, top_p) if len(kept) > 1 else 1
+        s_p = math.fsum(q[:n_p])
+        us = [int(u) for u in rng.integers(0, TWO24, 6)]
+        # draws on a CDF step: the margin is below 2^-24
+        us += [min(TWO24 - 1, int(math.floor(math.fsum(q[:j + 1]) / s_p * TWO24)))
+               for j in range(n_p)]
+        b = shared_row_batch(x, n_rows=len(us), temp=temp, top_k=top_k, top_p=top_p, cap=32)
+        o = orc.sample(b, u24=us, max_keep=32)
+        assert np.all(o["err"] == 0)
+        for i, u in enumerate(us):
+            want = brute_margin(x, top_k, top_p, temp, 32, u)
+            got = float(o["margin"][i])
+            if math.isinf(want):
+                assert math.isinf(got), (x, top_k, top_p, temp, u, got)
+            else:
+                assert abs(got - want) <= 1e-12, (x, top_k, top_p, temp, u, got, want)
+
+
 def pin_draw_map_exact(orc):
     """All 2^24 draws: each nucleus token's count equals its interval on the grid."""
     cases = [
@@ -406,6 +462,7 @@ PINS = [
     pin_error_rows,
     pin_writeback_and_frame,
     pin_nucleus_bruteforce,
+    pin_margin_bruteforce,
     pin_draw_map_exact,
     pin_eos_never_drawn,
     pin_chi_square,

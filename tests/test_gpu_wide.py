@@ -109,7 +109,35 @@ def test_stress_512_rows_split_sampled(ts):
     rows = np.random.default_rng(9).choice(512, size=24, replace=False)
     ref = oracle.sample(sub_batch(host, rows), max_keep=4096, n_threads=8)
     safe = ref["margin"] > 1e-5
+    assert safe.sum() >= 0.9 * rows.size  # the boundary rule must leave most rows checked
     assert np.array_equal(gpu["ids"][rows][safe], ref["ids"][safe])
+    s.close()
+
+
+@pytest.mark.parametrize("rows", [8, 64])
+@pytest.mark.parametrize("which", [2, 3])
+def test_split_refused_launch_leaves_clean_workspace(ts, rows, which):
+    """A split-path call whose streaming (2) or tail (3) launch is refused on
+    the host returns TS_ERR_CUDA; the next call on the same workspace is still
+    oracle-exact.  The refusal is injected on the host (TS_OPT_FAIL_LAUNCH)
+    before the launch is queued: nothing faults on the device.  With 8 rows
+    the streaming CTAs sample the rows themselves (no threshold kernel clears
+    the counters), with 64 the threshold kernel runs."""
+    import torch
+    first = workloads.make("stress", 31, rows=rows)
+    s = make_sampler(ts, 4096, path=4, host=first)
+    b = ts.DeviceBatch(first, "cuda")
+    s.set_option(ts.TS_OPT_FAIL_LAUNCH, which)
+    with pytest.raises(ts.SamplerError) as e:
+        s.sample(b)
+    assert e.value.status == ts.TS_ERR_CUDA
+    torch.cuda.synchronize()
+    assert np.all(b.ids() == -2)  # no tail ran: nothing was written
+    second = workloads.make("stress", 32, rows=rows)
+    ref = oracle.sample(second, max_keep=4096, n_threads=8)
+    gpu = run_gpu(s, second, debug_keep=4096)
+    n_safe = compare(second, gpu, ref, label=f"after refused launch {which}")
+    assert n_safe >= 0.9 * rows
     s.close()
 
 

@@ -41,6 +41,10 @@ MUTANTS = {
     "cap_upper_4095": ("if (requested < 32 || requested > 4096) return -1;",
                        "if (requested < 32 || requested > 2048) return -1;"),
     "offset_check_dropped": ("off > b->logits_len - (int64_t)vocab)", "off > b->logits_len)"),
+    # the boundary margin that excuses rows from the bit-exact rule
+    "margin_draw_unnormalised": ("double d = fabs(c - u);", "double d = fabs(cum - u);"),
+    "margin_cut_exclusive_prefix": ("double d = fabs(cum - (double)top_p);",
+                                    "double d = fabs(cum - qbuf[n - 1] - (double)top_p);"),
 }
 
 

@@ -109,6 +109,26 @@ def test_noalloc_small_then_large_stress(ts):
     _assert_same(got[1], _existing(ts, second), "stress 32 rows")
 
 
+def test_noalloc_one_row_then_eight_rows(ts):
+    """1 row of 151,936 logits, then 8 rows: both calls small enough that the
+    streaming CTAs sample the rows themselves (no threshold kernel zeroes the
+    counters), and the second call uses rows the first did not.  Their
+    counters must start at zero all the same."""
+    import torch
+    first = workloads.make("stress", 23, rows=1)
+    second = workloads.make("stress", 24, rows=8)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for h in (first, second):  # the geometry that skips the threshold kernel
+        s = ts.Sampler(0, int(h["cap"]))
+        s.reserve(int(h["n_rows"]), int(h["max_row_vocab"]))
+        plan = s.plan(ts.DeviceBatch(h, "cuda"))
+        assert plan["path"] == 4 and h["n_rows"] * plan["ctas_per_row"] <= 2 * sms, plan
+        s.close()
+    got = _noalloc_pair(ts, [first, second])
+    _assert_same(got[0], _existing(ts, first), "stress 1 row")
+    _assert_same(got[1], _existing(ts, second), "stress 8 rows")
+
+
 def test_noalloc_edge_rows_then_widest_rows(ts):
     """Rows with errors, then 64 rows of the widest bf16 vocabulary (the
     largest call the scratch takes)."""
