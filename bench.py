@@ -1,13 +1,18 @@
 """Benchmark of the per-step multi-codebook token sampler.
 
-One step = one full decode-step sample: ts_sample over every (stream,
-codebook) row of the step, then ts_advance_steps, replayed from a CUDA graph
-(the decode loop of the Drama 3 article, section "两阶段共享一张卡", replays
-decode steps as one graph with no host synchronisation).  The default
+One step = one full decode-step sample: one ts_sample call over every
+(stream, codebook) row of the step with the fused step advance, replayed from
+CUDA graphs (the decode loop of the Drama 3 article, section "两阶段共享一张卡",
+replays decode steps as one graph with no host synchronisation).  The default
 workload is the 128-stream x 10-codebook step (codebook 0 V=4096, codebooks
 1-9 V=1024, bf16, temperature 1.0 / top_k 30 / top_p 0.9, cap 64).  Logits
 rotate over distinct step buffers totalling more than twice the L2, so every
-step reads from HBM.
+step reads from HBM.  The timed region is exactly --steps steps, run
+--repeats times (at least 10); the median per-step time is reported with its
+spread.  The line also carries the multi-step figure (ts_sample_steps: R
+steps in one launch), an end-to-end figure through the public API with host
+copies and a sync per step, and the same figures for every other workload
+("configs").
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config drama3]
                     [--impl ours|reference]
@@ -114,53 +119,6 @@ def concat_steps(hosts):
                step=np.concatenate(steps), n_rows=sum(int(h["n_rows"]) for h in hosts),
                n_streams=streams, feedback_len=sum(int(h["feedback_len"]) for h in hosts))
     return out
-
-
-def multi_step(args, dev, l2, peak):
-    """R steps' rows sampled by one launch (R = 1, 8, 64), to show the
-    bandwidth bound of steps too small to fill the GPU on their own."""
-    import torch
-    import codebook_token_sampling_gb300 as ts
-    res = {}
-    for R in (1, 8, 64):
-        host = concat_steps([workloads.make(args.config, i) for i in range(R)])
-        n_rows = int(host["n_rows"])
-        sbytes = workloads.logit_bytes(host)
-        n_buf = max(2, min(64, -(-(2 * l2 + sbytes) // sbytes)))
-        np_dt = np.int16 if host["dtype"] == "bf16" else np.float32
-        base = torch.from_numpy(np.ascontiguousarray(host["logits"]).view(np_dt)).to(dev)
-        # distinct buffers: the same rows' values rotated by a row-sized stride
-        bufs = [torch.roll(base, shifts=int(i * 4099)) for i in range(n_buf)]
-        sampler = ts.Sampler(dev.index or 0, host["cap"])
-        batch = ts.DeviceBatch(host, dev)
-        stream = torch.cuda.Stream(device=dev)
-        with torch.cuda.stream(stream):
-            sampler.sample(batch, stream)
-        stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(n_buf):
-                batch.set_logits(bufs[i])
-                sampler.sample(batch)
-        reps = max(3, 2000 // (n_buf * R))
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            e0.record(stream)
-            for _ in range(reps):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        t = e0.elapsed_time(e1) / 1e3 / (reps * n_buf)
-        if sampler.read_status(stream) != 0:
-            raise RuntimeError("row errors in the multi-step launch")
-        gbs = algorithmic_bytes(host) / t / 1e9
-        res[str(R)] = {"rows_per_launch": n_rows, "us_per_launch": 1e6 * t,
-                       "us_per_step": 1e6 * t / R, "rows_per_s": n_rows / t,
-                       "gb_per_s": gbs, "frac": gbs / peak}
-        sampler.close()
-        del bufs, base
-    return res
 
 
 def algorithmic_bytes(host) -> int:
@@ -290,139 +248,218 @@ def barrier(world: int):
 # --------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------
-def run_ours(args, world, rank, local):
+def rotation_unit(host) -> int:
+    """Elements of one stream's rows (one step for a single-row-stream
+    workload): rotating a step's logits by whole units keeps every row's
+    width, values and structure, only in another stream's place."""
+    q = int(host["n_codebooks"])
+    return int(np.asarray(host["row_vocab"][:q], np.int64).sum())
+
+
+def step_buffers(name, rows, dev, l2, n_gen):
+    """One step's host batch and device buffers for n_buf steps that total more
+    than twice the L2 (so that every timed step reads HBM): n_gen freshly
+    drawn steps, the rest the same steps with their streams rotated."""
     import torch
-    import codebook_token_sampling_gb300 as ts
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    props = torch.cuda.get_device_properties(local)
-    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20)) or 126 * 2**20
-    host = workloads.make(args.config, 0, rows=args.rows)
-    n_rows = int(host["n_rows"])
-    step_bytes = workloads.logit_bytes(host)
-    n_buf = max(2, min(args.max_buffers, -(-(2 * l2 + step_bytes) // step_bytes)))
-    # distinct step buffers, each a freshly drawn step of the workload
+    hosts = [workloads.make(name, i, rows=rows) for i in range(n_gen)]
+    host = hosts[0]
     np_dt = np.int16 if host["dtype"] == "bf16" else np.float32
-    base, bufs = [], []
-    for i in range(n_buf):
-        src = np.ascontiguousarray(workloads.make(args.config, i, rows=args.rows)["logits"])
-        if i < 8:
-            base.append(src)
-        bufs.append(torch.from_numpy(src.view(np_dt)).to(dev))
-    sampler = ts.Sampler(local, host["cap"])
-    sampler.reserve(n_rows, int(host["max_row_vocab"]))  # workspace for the split wide path
-    if args.path:
-        sampler.set_option(ts.TS_OPT_PATH, args.path)
-    batch = ts.DeviceBatch(host, dev)
-    plan = sampler.plan(batch)
-    stream = torch.cuda.Stream(device=dev)
+    step_elems = int(np.asarray(host["logits"]).size)
+    step_bytes = workloads.logit_bytes(host)
+    n_buf = max(3, -(-(2 * l2 + step_bytes) // step_bytes))
+    unit = rotation_unit(host)
+    units = max(1, step_elems // unit)
+    big = torch.empty(n_buf * step_elems, dtype=torch.int16 if np_dt == np.int16 else torch.float32,
+                      device=dev)
+    srcs = [torch.from_numpy(np.ascontiguousarray(h["logits"]).view(np_dt)).to(dev) for h in hosts]
+    for j in range(n_buf):
+        shift = ((j // n_gen) * 7 % units) * unit
+        big[j * step_elems:(j + 1) * step_elems] = torch.roll(srcs[j % n_gen], shifts=shift)
+    bufs = [big[j * step_elems:(j + 1) * step_elems] for j in range(n_buf)]
+    return host, hosts, big, bufs
 
-    def capture(nsteps, with_advance=True, first=0):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            sampler.sample(batch, stream)  # warm-up launch outside capture
-        stream.synchronize()
-        with torch.cuda.graph(g, stream=stream):
-            for i in range(nsteps):
-                batch.set_logits(bufs[(first + i) % n_buf])
-                sampler.sample(batch)
-                if with_advance:
-                    ts.ts_advance_steps(batch.step)
-        return g
 
-    k, w = args.steps, args.warmup
-    g_full = capture(n_buf)
-    rem = k % n_buf
-    g_rem = capture(rem) if rem else None
-
-    def run_steps(nsteps):
-        full, r = divmod(nsteps, n_buf)
-        for _ in range(full):
-            g_full.replay()
-        if r:
-            assert r == rem
-            g_rem.replay()
-
+def time_steps(sampler, batch, bufs, k, w, repeats, stream):
+    """Per-step times (s) of `repeats` timed runs of exactly k steps.  Each step
+    is one ts_sample call (with the fused step advance) on the next step
+    buffer; the k-step runs are CUDA graphs over consecutive buffers, replayed
+    in turn, so a buffer is read again only after the others."""
+    import torch
+    n_buf = len(bufs)
+    n_graph = -(-n_buf // k) if k < n_buf else 1
+    graphs = []
     with torch.cuda.stream(stream):
-        for _ in range(max(1, -(-w // n_buf))):
-            g_full.replay()
+        sampler.sample(batch, stream)  # first launch outside capture
     stream.synchronize()
-    if sampler.read_status(stream) != 0:
-        raise RuntimeError("row errors during warm-up")
-
-    clocks = ClockSampler(local) if rank == 0 else None
-    if clocks:
-        clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
+    for gi in range(n_graph):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(k):
+                batch.set_logits(bufs[(gi * k + i) % n_buf])
+                sampler.sample(batch)
+        graphs.append(g)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        run_steps(k)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    t_step = e0.elapsed_time(e1) / 1e3
-    clk = clocks.stop() if clocks else None
-    t_max = max_over_ranks(t_step, world)
+        done = 0
+        while done < max(w, k * n_graph):
+            graphs[(done // k) % n_graph].replay()
+            done += k
+    stream.synchronize()
+    times = []
+    for r in range(repeats):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graphs[r % n_graph].replay()
+            e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3 / k)
+    return times
 
-    # kernel-only pass: the sampler launches alone (for the roofline)
-    g_kern = capture(n_buf, with_advance=False)
-    with torch.cuda.stream(stream):
-        g_kern.replay()
-        e0.record(stream)
-        reps = max(1, k // n_buf)
-        for _ in range(reps):
-            g_kern.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    t_launch = e0.elapsed_time(e1) / 1e3 / (reps * n_buf)
 
-    # end to end through the C ABI from pinned host memory: per step the
-    # step's logits go host->device, the frame's ids and EOS flags come back
-    n_host = min(n_buf, 8)
-    pinned = [torch.from_numpy(np.ascontiguousarray(base[i % len(base)]).view(np_dt)).pin_memory()
-              for i in range(n_host)]
-    dev_in = [torch.empty_like(bufs[0]) for _ in range(2)]
-    ids_host = torch.empty((n_host, n_rows), dtype=torch.int32).pin_memory()
-    eos_host = torch.empty((n_host, n_rows), dtype=torch.uint8).pin_memory()
-    g_e2e = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_e2e, stream=stream):
-        for i in range(n_host):
-            d = dev_in[i % 2]
-            d.copy_(pinned[i], non_blocking=True)
-            batch.set_logits(d)
-            sampler.sample(batch)
-            ts.ts_advance_steps(batch.step)
-            ids_host[i].copy_(batch.out_ids, non_blocking=True)
-            eos_host[i].copy_(batch.out_eos, non_blocking=True)
-    with torch.cuda.stream(stream):
-        g_e2e.replay()
-    torch.cuda.synchronize()
-    e2e_reps = max(1, min(k, 20000) // n_host)
-    barrier(world)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_reps):
-            g_e2e.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3 / (e2e_reps * n_host), world)
-    status = sampler.read_status(stream)
-    if status != 0:
-        raise RuntimeError(f"row errors during the run: {status}")
+def time_multi_step(sampler, host, big, bufs, n_steps, repeats, stream, dev, l2):
+    """ts_sample_steps: n_steps steps' rows in one launch, the launches reading
+    consecutive step buffers (more than twice the L2 apart).  Per-step times."""
+    import torch
+    import codebook_token_sampling_gb300 as ts
+    n = int(host["n_rows"])
+    step_elems = bufs[0].numel()
+    step_bytes = bufs[0].numel() * bufs[0].element_size()
+    n_buf = len(bufs)
+    n_launch = max(2, -(-(2 * l2) // (n_steps * step_bytes)) + 1)
+    if n_launch * n_steps > n_buf:  # not enough buffers: a larger pool of the same steps
+        reps = -(-(n_launch * n_steps) // n_buf)
+        big = torch.cat([torch.roll(big, shifts=i * rotation_unit(host)) for i in range(reps)])
+    b = ts.DeviceBatch(host, dev, advance_steps=True)
+    out_ids = torch.empty((n_steps, n), dtype=torch.int32, device=dev)
+    out_eos = torch.empty((n_steps, n), dtype=torch.uint8, device=dev)
+    fb_len = int(host["feedback_len"])
+    frames = torch.empty((n_steps, fb_len), dtype=torch.int32, device=dev)
+    b.c.out_ids = out_ids.data_ptr()
+    b.c.out_eos = out_eos.data_ptr()
+    b.c.feedback_buf = frames.data_ptr()
+    views = [big[j * n_steps * step_elems:(j + 1) * n_steps * step_elems] for j in range(n_launch)]
 
-    return {
-        "host": host, "n_rows": n_rows, "t_step": t_max / k, "t_launch": t_launch,
-        "t_e2e": t_e2e, "clocks": clk, "plan": plan, "n_buf": n_buf, "l2": l2,
-        "step_bytes": step_bytes,
-        "split_kernels": split_kernels(plan, props.multi_processor_count, n_rows),
-        "launches": (split_kernels(plan, props.multi_processor_count, n_rows)
-                     if plan["path"] == 4 else 1) * k + k,
-        "h2d": int(bufs[0].numel() * bufs[0].element_size()), "d2h": n_rows * 5,
+    def launch(j):
+        b.set_logits(views[j % n_launch])
+        sampler.sample_steps(b, n_steps, logits_step_stride=step_elems, out_step_stride=n,
+                             feedback_step_stride=fb_len, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for j in range(2 * n_launch):
+            launch(j)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for r in range(repeats):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            launch(r)
+            e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3 / n_steps)
+    if sampler.read_status(stream) != 0:
+        raise RuntimeError("row errors in the multi-step launch")
+    return times
+
+
+def summarize(times):
+    t = sorted(times)
+    return {"us_median": 1e6 * statistics.median(t), "us_min": 1e6 * t[0], "us_max": 1e6 * t[-1],
+            "repeats": len(t)}
+
+
+def measure_config(args, name, rows, dev, l2, peak, k, w, repeats, num_sms, multi=(8, 64)):
+    """One workload's single-step and multi-step figures."""
+    import torch
+    import codebook_token_sampling_gb300 as ts
+    n_gen = 1 if name == "stress" else 4
+    host, hosts, big, bufs = step_buffers(name, rows, dev, l2, n_gen)
+    n_rows = int(host["n_rows"])
+    sampler = ts.Sampler(dev.index or 0, host["cap"])
+    sampler.reserve(n_rows, int(host["max_row_vocab"]))  # the split path's workspace
+    if args.path:
+        sampler.set_option(ts.TS_OPT_PATH, args.path)
+    if args.warps_per_row:
+        sampler.set_option(ts.TS_OPT_WARPS_PER_ROW, args.warps_per_row)
+    batch = ts.DeviceBatch(host, dev, advance_steps=True)
+    plan = sampler.plan(batch)
+    stream = torch.cuda.Stream(device=dev)
+    times = time_steps(sampler, batch, bufs, k, w, repeats, stream)
+    if sampler.read_status(stream) != 0:
+        raise RuntimeError(f"row errors in {name}")
+    alg = algorithmic_bytes(host)
+    sm = summarize(times)
+    t = sm["us_median"] / 1e6
+    launches = (split_kernels(plan, num_sms, n_rows) + 1 if plan["path"] == 4 else
+                1 if plan["path"] == 1 else 2)
+    out = {
+        "workload": DESCRIPTIONS[name].format(rows=rows), "rows_per_step": n_rows,
+        "streams": int(host["n_streams"]), "us_per_step": sm["us_median"],
+        "us_per_step_min": sm["us_min"], "us_per_step_max": sm["us_max"], "repeats": repeats,
+        "steps_per_repeat": k, "rows_per_s": n_rows / t, "frames_per_s": int(host["n_streams"]) / t,
+        "gb_per_s": alg / t / 1e9, "algorithmic_bytes_per_step": alg,
+        "frac": alg / t / 1e9 / peak, "frac_of_nominal": alg / t / 1e9 / NOMINAL_HBM_GBS,
+        "kernel": plan, "launches_per_step": launches, "dtype": host["dtype"],
+        "l2": f"{len(bufs)} step buffers ({len(bufs) * workloads.logit_bytes(host) / 2**20:.0f} MiB "
+              f"> 2x L2 {l2 / 2**20:.0f} MiB)",
     }
+    if plan["path"] == 1 and multi:
+        ms = {}
+        for r in multi:
+            mt = summarize(time_multi_step(sampler, host, big, bufs, r, repeats, stream, dev, l2))
+            tt = mt["us_median"] / 1e6
+            ms[str(r)] = {"us_per_step": mt["us_median"], "us_per_launch": mt["us_median"] * r,
+                          "rows_per_s": n_rows / tt, "gb_per_s": alg / tt / 1e9,
+                          "frac": alg / tt / 1e9 / peak}
+        out["multi_step"] = ms
+        out["multi_step_how"] = ("ts_sample_steps: R steps' rows in one launch of a resident grid "
+                                 "(fused step advance), launches over distinct buffers")
+    res = {"summary": out, "host": host, "hosts": hosts, "bufs": bufs, "big": big,
+           "sampler": sampler, "batch": batch, "stream": stream, "times": times, "plan": plan}
+    return res
+
+
+def e2e_host_calls(res, dev, k, world):
+    """End to end through the public API: per step, the step's logits go from
+    pinned host memory to the device, one ts_sample call samples them (fused
+    step advance), the ids and EOS flags come back to pinned host memory and
+    the host waits for them.  Host wall clock over k steps (at least 200)."""
+    import torch
+    import codebook_token_sampling_gb300 as ts
+    host, hosts = res["host"], res["hosts"]
+    sampler, stream = res["sampler"], res["stream"]
+    np_dt = np.int16 if host["dtype"] == "bf16" else np.float32
+    pinned = [torch.from_numpy(np.ascontiguousarray(h["logits"]).view(np_dt)).pin_memory()
+              for h in hosts]
+    n_rows = int(host["n_rows"])
+    dev_in = torch.empty_like(res["bufs"][0])
+    batch = ts.DeviceBatch(host, dev, advance_steps=True)
+    batch.set_logits(dev_in)
+    ids_host = torch.empty(n_rows, dtype=torch.int32).pin_memory()
+    eos_host = torch.empty(n_rows, dtype=torch.uint8).pin_memory()
+    n = max(200, k)
+
+    def step(i):
+        with torch.cuda.stream(stream):
+            dev_in.copy_(pinned[i % len(pinned)], non_blocking=True)
+            ts.ts_sample(sampler.handle, batch, stream)
+            ids_host.copy_(batch.out_ids, non_blocking=True)
+            eos_host.copy_(batch.out_eos, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(20):
+        step(i)
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n):
+        step(i)
+    t = (time.perf_counter() - t0) / n
+    t = max_over_ranks(t, world)
+    return {"value": world * n_rows / t, "unit": "rows/s",
+            "h2d_bytes_per_step": int(dev_in.numel() * dev_in.element_size()),
+            "d2h_bytes_per_step": n_rows * 5, "us_per_step": 1e6 * t, "steps": n,
+            "how": "host wall clock; per step: pinned H2D copy of the logits, one ts_sample "
+                   "call (fused step advance), D2H of ids and EOS flags, stream sync"}
 
 
 def profile_launches(args):
@@ -434,24 +471,47 @@ def profile_launches(args):
     sampler.reserve(int(host["n_rows"]), int(host["max_row_vocab"]))
     if args.path:
         sampler.set_option(ts.TS_OPT_PATH, args.path)
-    batch = ts.DeviceBatch(host, "cuda")
-    for _ in range(args.profile):
-        sampler.sample(batch)
-        ts.ts_advance_steps(batch.step)
+    if args.warps_per_row:
+        sampler.set_option(ts.TS_OPT_WARPS_PER_ROW, args.warps_per_row)
+    batch = ts.DeviceBatch(host, "cuda", advance_steps=True)
+    if args.profile_steps > 1:
+        hosts = [workloads.make(args.config, i, rows=args.rows) for i in range(args.profile_steps)]
+        np_dt = np.int16 if host["dtype"] == "bf16" else np.float32
+        flat = np.concatenate([np.ascontiguousarray(h["logits"]) for h in hosts]).view(np_dt)
+        buf = torch.from_numpy(flat).cuda()
+        per = int(np.asarray(host["logits"]).size)
+        n = int(host["n_rows"])
+        out = torch.empty((args.profile_steps, n), dtype=torch.int32, device="cuda")
+        eos = torch.empty((args.profile_steps, n), dtype=torch.uint8, device="cuda")
+        frames = torch.empty((args.profile_steps, int(host["feedback_len"])), dtype=torch.int32,
+                             device="cuda")
+        batch.set_logits(buf)
+        batch.c.out_ids, batch.c.out_eos = out.data_ptr(), eos.data_ptr()
+        batch.c.feedback_buf = frames.data_ptr()
+        for _ in range(args.profile):
+            sampler.sample_steps(batch, args.profile_steps, logits_step_stride=per,
+                                 out_step_stride=n, feedback_step_stride=int(host["feedback_len"]))
+    else:
+        for _ in range(args.profile):
+            sampler.sample(batch)
     torch.cuda.synchronize()
     print(json.dumps({"profile": args.config, "rows": int(host["n_rows"]), "launches": args.profile,
-                      "plan": sampler.plan(batch), "status": sampler.read_status()}))
+                      "steps_per_launch": args.profile_steps, "plan": sampler.plan(batch),
+                      "status": sampler.read_status()}))
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200000)
-    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--repeats", type=int, default=10,
+                    help="timed runs of exactly --steps steps (at least 10; the median is reported)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="drama3", choices=list(workloads.CONFIGS))
     ap.add_argument("--rows", type=int, default=None, help="rows of the stress config")
-    ap.add_argument("--max-buffers", type=int, default=160)
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads' figures (the configs object)")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -460,8 +520,12 @@ def main():
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="force the kernel family (0 = automatic, 1 = warp per row, 2 = CTA / "
                          "cluster per row, 3 = wide cluster, 4 = wide split)")
+    ap.add_argument("--warps-per-row", type=int, default=0, choices=[0, 1, 2, 4],
+                    help="the warp path's warps per row (0 = automatic)")
     ap.add_argument("--profile", type=int, default=0, metavar="N",
                     help="profiling mode: N plain launches of one step, no timing (for ncu)")
+    ap.add_argument("--profile-steps", type=int, default=1, metavar="R",
+                    help="profiling mode: each launch samples R steps (ts_sample_steps)")
     args = ap.parse_args()
     if args.config == "stress" and args.rows is None:
         args.rows = 512
@@ -517,25 +581,52 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    r = run_ours(args, world, rank, local)
+    import torch
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20)) or 126 * 2**20
+    num_sms = props.multi_processor_count
     peak, peak_kind = measured_peak_gbs()
-    multi = None
-    if args.config != "stress" and not args.no_multi_step and rank == 0:
-        import torch
-        multi = multi_step(args, torch.device("cuda", local), r["l2"], peak)
+    k, w, reps = args.steps, args.warmup, max(10, args.repeats)
+
+    # the headline workload: clocks sampled while its timed runs go
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier(world)
+    head = measure_config(args, args.config, args.rows, dev, l2, peak, k, w, reps, num_sms,
+                          multi=() if args.no_multi_step else (8, 64))
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop() if clocks else None
+    summ = head["summary"]
+    t_step = max_over_ranks(summ["us_per_step"] / 1e6, world)
+    e2e = e2e_host_calls(head, dev, k, world)
+    others = {}
+    if rank == 0 and not args.no_configs:
+        for name in [c for c in workloads.CONFIGS if c != args.config]:
+            rows = 512 if name == "stress" else None
+            res = measure_config(args, name, rows, dev, l2, peak, min(k, 200), min(w, 50), reps,
+                                 num_sms, multi=() if args.no_multi_step else (64,))
+            key = f"stress{rows}" if name == "stress" else name
+            others[key] = res["summary"]
+            res["summary"]["traffic"] = recorded_traffic(name, rows)
+            del res
+            torch.cuda.empty_cache()
     if rank != 0:
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
         return
-    t = r["t_step"]
-    value = world * n_rows / t
-    alg = algorithmic_bytes(r["host"])
-    # the sampler's launches timed inside the timed region: each step is one
-    # ts_sample call plus the step-advance kernel, so this slightly
-    # understates the sampler's own rate
-    achieved = alg / t / 1e9
-    split = r["plan"]["path"] == 4
+    host = head["host"]
+    n_rows = int(host["n_rows"])
+    n_streams = int(host["n_streams"])
+    alg = algorithmic_bytes(host)
+    achieved = alg / t_step / 1e9
+    plan = head["plan"]
+    kname = {1: "row_sampler_kernel", 2: "cluster_sampler_kernel", 3: "wide_sampler_kernel",
+             4: "split_stream_kernel"}[plan["path"]]
     cpu = None
     if not args.no_cpu_baseline and world == 1:  # the oracle baseline: rank 0 at N = 1 only
         threads = host_threads()
@@ -545,42 +636,38 @@ def main():
                "sample": f"{done} full steps of {n_rows} rows ({per_step * 1e3:.1f} ms/step), "
                          f"all {threads} host threads"}
     line = {
-        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-        if r["host"]["dtype"] == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": desc, "rows_per_step": n_rows, "streams": n_streams,
+        "metric": METRIC, "value": world * n_rows / t_step, "unit": "rows/s", "n_gpus": world,
+        "steps": k, "warmup": w, "ms_per_step": 1e3 * t_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if host["dtype"] == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": summ["workload"], "rows_per_step": n_rows, "streams": n_streams,
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                   "l2": f"inputs rotate over {r['n_buf']} distinct step buffers "
-                         f"({r['n_buf'] * r['step_bytes'] / 2**20:.0f} MiB > 2x L2 "
-                         f"{r['l2'] / 2**20:.0f} MiB)",
-                   "graph": "each step = ts_sample + ts_advance_steps, replayed from a CUDA graph",
-                   "kernel": r["plan"]},
-        "us_per_step": 1e6 * t,
-        "frames_per_s": world * n_streams / t,
-        "gb_per_s": world * alg / t / 1e9,
+                   "l2": "inputs larger than L2: " + summ["l2"],
+                   "graph": "each step = one ts_sample call with the fused step advance; "
+                            f"k-step CUDA graphs, {reps} timed runs of exactly k steps, median",
+                   "kernel": plan},
+        "us_per_step": 1e6 * t_step,
+        "timing": {"us_per_step_median": summ["us_per_step"], "us_per_step_min":
+                   summ["us_per_step_min"], "us_per_step_max": summ["us_per_step_max"],
+                   "repeats": reps, "steps_per_repeat": k},
+        "frames_per_s": world * n_streams / t_step,
+        "gb_per_s": world * alg / t_step / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": recorded_traffic(args.config, args.rows),
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(args.config, args.rows),
                      "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
-                     "peak_source": f"{peak_kind} hbm_gbs",
-                     "launch": ("one ts_sample call: split_stream_kernel (threshold inline) + "
-                                "split_tail_kernel" if r["split_kernels"] == 2 else
-                                "one ts_sample call: split_threshold_kernel + split_stream_kernel + "
-                                "split_tail_kernel") if split else
-                               "one ts_sample call: one kernel (" +
-                               {1: "row_sampler_kernel", 2: "cluster_sampler_kernel",
-                                3: "wide_sampler_kernel"}[r["plan"]["path"]] + ")",
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
+                     "kernel": kname, "launches_per_step": summ["launches_per_step"],
                      "algorithmic_bytes_per_launch": alg,
-                     "us_per_launch": 1e6 * t,
-                     "us_per_launch_measured_as": "the timed step loop (ts_sample + step advance)",
-                     "us_per_launch_back_to_back": 1e6 * r["t_launch"]},
-        "multi_step": multi,
-        "e2e": {"value": world * n_rows / r["t_e2e"], "unit": "rows/s",
-                "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"],
-                "us_per_step": 1e6 * r["t_e2e"]},
-        "gpu_launches": r["launches"],
-        "clocks": r["clocks"],
+                     "us_per_launch": 1e6 * t_step,
+                     "us_per_launch_measured_as": "median per-step time of the timed step loop "
+                                                  "(CUDA events on the launching stream)"},
+        "multi_step": summ.get("multi_step"),
+        "e2e": e2e,
+        "gpu_launches": summ["launches_per_step"] * k,
+        "clocks": clk,
         "cpu_baseline": cpu,
+        "configs": others,
     }
     print(json.dumps(line))
     if world > 1:

@@ -5,8 +5,8 @@ of sampling runs in the CUDA kernels of ``libts_sampler.so``.  PyTorch is used
 only for device memory and streams.  The functions keep the C names:
 
     ts_create, ts_destroy, ts_max_top_k, ts_sample, ts_sample_debug,
-    ts_reserve, ts_sample_noalloc, ts_advance_steps, ts_read_status,
-    ts_set_option, ts_plan, ts_status_string, ts_last_error
+    ts_sample_steps, ts_reserve, ts_sample_noalloc, ts_advance_steps,
+    ts_read_status, ts_set_option, ts_plan, ts_status_string, ts_last_error
 
 ``Sampler`` wraps a handle; ``DeviceBatch`` holds one step's per-row arrays on
 the GPU with a prebuilt ``ts_batch`` so that repeated calls marshal nothing.
@@ -33,6 +33,7 @@ TS_ROW_BAD_SHAPE = 1
 TS_ROW_BAD_PARAM = 2
 TS_ROW_NONFINITE = 4
 TS_ROW_BAD_SLOT = 8
+TS_ROW_NOT_READY = 16
 TS_OPT_PATH = 1
 TS_OPT_CLUSTER = 2
 TS_OPT_PDL = 3
@@ -45,8 +46,8 @@ TS_NOALLOC_SCRATCH_BYTES = 4194304
 TS_NOALLOC_MAX_ROWS = 64
 
 EXPORTED = ("ts_create", "ts_destroy", "ts_max_top_k", "ts_sample", "ts_sample_debug",
-            "ts_reserve", "ts_sample_noalloc", "ts_advance_steps", "ts_read_status", "ts_set_option", "ts_plan",
-            "ts_status_string", "ts_last_error")
+            "ts_sample_steps", "ts_reserve", "ts_sample_noalloc", "ts_advance_steps",
+            "ts_read_status", "ts_set_option", "ts_plan", "ts_status_string", "ts_last_error")
 
 
 class TsBatch(ctypes.Structure):
@@ -74,6 +75,19 @@ class TsBatch(ctypes.Structure):
         ("feedback_buf", ctypes.c_void_p),
         ("feedback_slot", ctypes.c_void_p),
         ("feedback_len", ctypes.c_int64),
+        ("advance_steps", ctypes.c_int32),
+    ]
+
+
+class TsSteps(ctypes.Structure):
+    """Mirror of ``ts_steps``."""
+    _fields_ = [
+        ("n_steps", ctypes.c_int32),
+        ("logits_step_stride", ctypes.c_int64),
+        ("out_step_stride", ctypes.c_int64),
+        ("feedback_step_stride", ctypes.c_int64),
+        ("ready", ctypes.c_void_p),
+        ("ready_timeout_ns", ctypes.c_uint64),
     ]
 
 
@@ -96,6 +110,8 @@ def _load(path: str):
         "ts_max_top_k": ([vp], i32),
         "ts_sample": ([vp, ctypes.POINTER(TsBatch), vp], ctypes.c_int),
         "ts_sample_debug": ([vp, ctypes.POINTER(TsBatch), i32, vp, vp, vp, vp, vp], ctypes.c_int),
+        "ts_sample_steps": ([vp, ctypes.POINTER(TsBatch), ctypes.POINTER(TsSteps), vp],
+                            ctypes.c_int),
         "ts_reserve": ([vp, i32, i32], ctypes.c_int),
         "ts_sample_noalloc": ([i32, ctypes.POINTER(TsBatch), vp, vp], ctypes.c_int),
         "ts_advance_steps": ([vp, i32, vp], ctypes.c_int),
@@ -160,6 +176,11 @@ def ts_sample_debug(handle: int, batch: "DeviceBatch", max_keep: int, kept_ids, 
     _check(_lib.ts_sample_debug(handle, ctypes.byref(batch.c), max_keep, kept_ids.data_ptr(),
                                 kept_probs.data_ptr(), n_kept.data_ptr(), n_nucleus.data_ptr(),
                                 _stream_ptr(stream)), "ts_sample_debug")
+
+
+def ts_sample_steps(handle: int, batch: "DeviceBatch", steps: TsSteps, stream=None) -> None:
+    _check(_lib.ts_sample_steps(handle, ctypes.byref(batch.c), ctypes.byref(steps),
+                                _stream_ptr(stream)), "ts_sample_steps")
 
 
 def ts_reserve(handle: int, max_rows: int, max_row_vocab: int) -> None:
@@ -241,6 +262,20 @@ class Sampler:
         return {"kept_ids": kept_ids, "kept_probs": kept_probs, "n_kept": n_kept,
                 "n_nucleus": n_nucleus}
 
+    def sample_steps(self, batch: "DeviceBatch", n_steps: int, *, logits_step_stride: int,
+                     out_step_stride: int, feedback_step_stride: int = 0, ready=None,
+                     ready_timeout_ns: int = 0, stream=None) -> None:
+        """``n_steps`` decode steps of ``batch`` in one launch (see ts_sample_steps);
+        ``ready``: a uint32/int32 tensor of per-step flags the device can read, or None."""
+        st = TsSteps()
+        st.n_steps = n_steps
+        st.logits_step_stride = logits_step_stride
+        st.out_step_stride = out_step_stride
+        st.feedback_step_stride = feedback_step_stride
+        st.ready = ready.data_ptr() if ready is not None else None
+        st.ready_timeout_ns = ready_timeout_ns
+        ts_sample_steps(self.handle, batch, st, stream)
+
     def read_status(self, stream=None) -> int:
         return ts_read_status(self.handle, stream)
 
@@ -289,7 +324,8 @@ class DeviceBatch:
     tensor of the same layout (``set_logits``), e.g. to rotate step buffers.
     """
 
-    def __init__(self, host: dict, device="cuda", feedback: bool = True):
+    def __init__(self, host: dict, device="cuda", feedback: bool = True,
+                 advance_steps: bool = False):
         import torch
         self.device = torch.device(device)
         self.dtype = TS_DTYPE_BF16 if host["dtype"] == "bf16" else TS_DTYPE_F32
@@ -316,6 +352,7 @@ class DeviceBatch:
             setattr(c, name, self.arrays[name].data_ptr())
         c.step = self.step.data_ptr()
         c.n_streams = int(host["n_streams"])
+        c.advance_steps = 1 if advance_steps else 0
         c.out_ids = self.out_ids.data_ptr()
         c.out_eos = self.out_eos.data_ptr()
         if self.feedback is not None:

@@ -12,6 +12,7 @@ constexpr uint32_t kRowBadShape = 1u;
 constexpr uint32_t kRowBadParam = 2u;
 constexpr uint32_t kRowNonFinite = 4u;
 constexpr uint32_t kRowBadSlot = 8u;
+constexpr uint32_t kRowNotReady = 16u;
 
 // Kernel parameters, passed by value (one copy per launch).
 struct Params {
@@ -55,6 +56,21 @@ struct Params {
   int32_t ws_units;
   int32_t ws_units_per_row;
   int32_t split_inline;  // split path: the streaming CTAs compute the threshold themselves
+  // multi-step launches of the warp path: steps in the launch (1 for one
+  // step), the distance from one step's logits / outputs / frame to the
+  // next's, per-step ready flags (null: all ready) and how long a warp waits
+  // for one (nanoseconds)
+  int32_t n_steps;
+  int64_t logits_step_stride;
+  int64_t out_step_stride;
+  int64_t feedback_step_stride;
+  const uint32_t *ready;
+  uint64_t ready_timeout_ns;
+  // step advance fused into the launch: after every block has read step[],
+  // the last block to finish (by an atomic ticket) adds n_steps to
+  // step_out[0 .. n_streams) and re-arms the ticket; null: no advance
+  int64_t *step_out;
+  uint32_t *ticket;
 };
 
 // ---------------------------------------------------------------------------

@@ -28,7 +28,9 @@ struct ts_sampler {
   int wide_exact;     // wide path: always take the exact path (testing)
   int force_wpr;      // warp-per-row path: 0 auto, else warps per row (1, 2, 4)
   int fail_launch;    // tests: the split path's launch of this index (2 or 3) fails once
-  uint32_t *status;   // device word
+  uint32_t *status;   // device word (first of two: the status word, then the ticket)
+  uint32_t *ticket;   // the warp path's fused step advance: blocks done so far
+  int occ_warp[2][5][3];  // resident blocks per SM of each warp-path variant
   void *ws;           // split wide path workspace (ts_reserve), or null
   size_t ws_bytes;
   int ws_rows;        // row records it holds
@@ -87,7 +89,7 @@ struct Plan {
   int grid;
 };
 
-ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
+ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl, int n_steps = 1) {
   const bool bf16 = b->dtype == TS_DTYPE_BF16;
   const int vmax = b->max_row_vocab;
   if (vmax > (bf16 ? TS_MAX_VOCAB_BF16 : TS_MAX_VOCAB_F32)) return TS_ERR_UNSUPPORTED;
@@ -144,14 +146,21 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl) {
     pl->nch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
     // small batches share each row among several warps (a shorter chain per
     // row while the GPU has room); large ones keep one warp per row
+    const long long rows = static_cast<long long>(b->n_rows) * n_steps;
+    // (measured on the 128 x 10 step: 1 warp per row 9.5 us, 2 10.2 us, 4 12.2 us)
     int wpr = s->force_wpr;
-    if (!wpr) wpr = b->n_rows <= 4 * s->num_sms ? 4 : b->n_rows <= 16 * s->num_sms ? 2 : 1;
+    if (!wpr) wpr = rows <= s->num_sms ? 4 : rows <= 4LL * s->num_sms ? 2 : 1;
     const int rpb = ts::kTowerWarps / wpr;
     pl->wpr = wpr;
     pl->g = wpr;
     pl->threads = ts::kTowerThreads;
     pl->smem = 0;  // static shared memory only
-    pl->grid = (b->n_rows + rpb - 1) / rpb;
+    // one row per row group while the grid fits on the GPU at once; beyond
+    // that a resident grid whose groups walk several rows each
+    const int ni = pl->nch == 1 ? 0 : pl->nch == 2 ? 1 : pl->nch == 4 ? 2 : pl->nch == 8 ? 3 : 4;
+    const int occ = s->occ_warp[bf16 ? 1 : 0][ni][wpr == 1 ? 0 : wpr == 2 ? 1 : 2];
+    const long long resident = static_cast<long long>(s->num_sms) * std::max(occ, 1);
+    pl->grid = static_cast<int>(std::min<long long>((rows + rpb - 1) / rpb, resident));
     return TS_OK;
   }
   const int slice_max = bf16 ? ts::kSliceMaxBF16 : ts::kSliceMaxF32;
@@ -222,6 +231,8 @@ ts::Params make_params(const ts_sampler *s, const ts_batch *b) {
   p.feedback_len = b->feedback_len;
   p.cap = s->cap;
   p.status = s->status;
+  p.n_steps = 1;
+  p.out_step_stride = b->n_rows;
   return p;
 }
 
@@ -291,13 +302,75 @@ ts_status set_attributes(int device) {
   return TS_OK;
 }
 
+__global__ void advance_steps_kernel(int64_t *step, int32_t n, int64_t by) {
+  ts::pdl_wait_and_release();
+  const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+  if (i < n) step[i] += by;
+}
+
+// step[i] += by for i < n_streams, one thread per stream.
+// Resident blocks per SM of every warp-path variant (for grids that walk
+// several rows per row group).  Done once in ts_create.
+ts_status warp_occupancy(ts_sampler *s) {
+  const int nchs[5] = {1, 2, 4, 8, 16};
+  const int wprs[3] = {1, 2, 4};
+  for (int d = 0; d < 2; ++d) {
+    for (int i = 0; i < 5; ++i) {
+      for (int k = 0; k < 3; ++k) {
+        void *fn = d ? warp_kernel_for<ts::KeyBF16>(nchs[i], wprs[k])
+                     : warp_kernel_for<ts::KeyF32>(nchs[i], wprs[k]);
+        int n = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, ts::kTowerThreads, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        s->occ_warp[d][i][k] = n;
+      }
+    }
+  }
+  return TS_OK;
+}
+
+ts_status launch_advance(int64_t *step, int32_t n_streams, int64_t by, cudaStream_t stream) {
+  if (n_streams == 0) return TS_OK;
+  const int threads = 256;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>((n_streams + threads - 1) / threads));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, advance_steps_kernel, step, n_streams, by);
+  return e == cudaSuccess ? TS_OK : cuda_fail(e, "advance_steps launch");
+}
+
+ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base, cudaStream_t st,
+                 const Plan &pl);
+
 ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base, cudaStream_t st) {
   Plan pl;
-  ts_status rc = make_plan(s, b, &pl);
+  ts_status rc = make_plan(s, b, &pl, base.n_steps);
   if (rc != TS_OK) return rc;
+  if (b->advance_steps && pl.path != 1) {
+    // the other paths advance the steps by one more small launch
+    rc = launch(s, b, base, st, pl);
+    if (rc != TS_OK) return rc;
+    return launch_advance(b->step, b->n_streams, base.n_steps, st);
+  }
+  return launch(s, b, base, st, pl);
+}
+
+ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base, cudaStream_t st,
+                 const Plan &pl) {
   ts::Params p = base;
   p.slice = pl.slice;
   p.wide_exact = s->wide_exact;
+  if (pl.path == 1 && b->advance_steps) {
+    p.step_out = b->step;
+    p.ticket = s->ticket;
+  }
   const bool bf16 = b->dtype == TS_DTYPE_BF16;
   if (pl.path == 4) {
     p.workspace = s->ws;
@@ -451,12 +524,6 @@ ts_status noalloc_setup(int device, NoallocDevice *out) {
   return TS_OK;
 }
 
-__global__ void advance_steps_kernel(int64_t *step, int32_t n) {
-  ts::pdl_wait_and_release();
-  const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
-  if (i < n) step[i] += 1;
-}
-
 }  // namespace
 
 extern "C" {
@@ -488,6 +555,8 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->force_wpr = 0;
   s->fail_launch = 0;
   s->status = nullptr;
+  s->ticket = nullptr;
+  std::memset(s->occ_warp, 0, sizeof s->occ_warp);
   s->ws = nullptr;
   s->ws_bytes = 0;
   s->ws_rows = 0;
@@ -497,15 +566,17 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   e = cudaDeviceGetAttribute(&s->num_sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) rc = cuda_fail(e, "cudaDeviceGetAttribute");
   if (rc == TS_OK) {
-    e = cudaMalloc(reinterpret_cast<void **>(&s->status), sizeof(uint32_t));
+    e = cudaMalloc(reinterpret_cast<void **>(&s->status), 2 * sizeof(uint32_t));
     if (e != cudaSuccess) rc = e == cudaErrorMemoryAllocation ? TS_ERR_NO_MEMORY
                                                               : cuda_fail(e, "cudaMalloc");
   }
   if (rc == TS_OK) {
-    e = cudaMemset(s->status, 0, sizeof(uint32_t));
+    s->ticket = s->status + 1;
+    e = cudaMemset(s->status, 0, 2 * sizeof(uint32_t));
     if (e != cudaSuccess) rc = cuda_fail(e, "cudaMemset");
   }
   if (rc == TS_OK) rc = set_attributes(device);
+  if (rc == TS_OK) rc = warp_occupancy(s);
   cudaSetDevice(prev);
   if (rc != TS_OK) {
     if (s->status) cudaFree(s->status);
@@ -552,6 +623,30 @@ ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep, in
   p.kept_probs = kept_probs;
   p.n_kept = n_kept;
   p.n_nucleus = n_nucleus;
+  return launch(s, b, p, static_cast<cudaStream_t>(stream));
+}
+
+ts_status ts_sample_steps(ts_sampler *s, const ts_batch *b, const ts_steps *st, void *stream) {
+  if (!s || !st) return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK) return rc;
+  constexpr uint64_t kMaxTimeoutNs = 10000000000ull;
+  if (st->n_steps < 1 || st->logits_step_stride < 0 || st->out_step_stride < b->n_rows ||
+      st->ready_timeout_ns > kMaxTimeoutNs ||
+      (b->feedback_buf && st->feedback_step_stride < b->feedback_len))
+    return TS_ERR_INVALID_ARG;
+  if (b->n_rows == 0) return TS_OK;
+  const bool bf16 = b->dtype == TS_DTYPE_BF16;
+  if (s->cap > 64 || b->max_row_vocab > (bf16 ? kWarpMaxBF16 : kWarpMaxF32))
+    return TS_ERR_UNSUPPORTED;
+  if (s->force_path != 0 && s->force_path != 1) return TS_ERR_INVALID_ARG;
+  ts::Params p = make_params(s, b);
+  p.n_steps = st->n_steps;
+  p.logits_step_stride = st->logits_step_stride;
+  p.out_step_stride = st->out_step_stride;
+  p.feedback_step_stride = st->feedback_step_stride;
+  p.ready = st->ready;
+  p.ready_timeout_ns = st->ready_timeout_ns ? st->ready_timeout_ns : 1000000000ull;
   return launch(s, b, p, static_cast<cudaStream_t>(stream));
 }
 
@@ -646,20 +741,7 @@ ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *stat
 
 ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream) {
   if (n_streams < 0 || (n_streams > 0 && !step)) return TS_ERR_INVALID_ARG;
-  if (n_streams == 0) return TS_OK;
-  const int threads = 256;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>((n_streams + threads - 1) / threads));
-  cfg.blockDim = dim3(threads);
-  cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, advance_steps_kernel, step, n_streams);
-  return e == cudaSuccess ? TS_OK : cuda_fail(e, "advance_steps launch");
+  return launch_advance(step, n_streams, 1, static_cast<cudaStream_t>(stream));
 }
 
 ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream) {

@@ -1,17 +1,40 @@
-// ts_warp.cuh -- warp-per-row sampler for rows of up to 4096 bf16 / 2048 fp32
+// ts_warp.cuh -- warp-path sampler for rows of up to 4096 bf16 / 2048 fp32
 // logits with a top-k cap of at most 64 (the serving configuration: top_k 30
 // under the default cap 64, Drama 3 article sections "测试口径" and
 // "能跑通的命令，和文档写明的边界").
 //
-// One warp owns one row (four rows per 128-thread block, no block barrier).
-// The row is staged in shared memory by asynchronous 16-byte copies; each
-// lane's two largest logits give, through the k_eff-th largest of the 64
-// per-lane maxima, a lower bound of the row's k_eff-th largest logit; the
-// logits at or above it (the top-k set with all its ties, about 35 words for
-// top_k 30 of 1024 gaussian logits) are bitonic-sorted by the warp as (key,
-// inverted index) words, and the warp computes the fixed-point weights, the
-// nucleus cutoff and the draw.  Rows with huge ties take an exact radix-select
-// slow path over the staged keys.
+// A row is owned by one warp, or shared by 2 or 4 warps of a 128-thread
+// block.  Per row:
+//   1. its 16-byte chunks are copied into the row's shared-memory stage by
+//      asynchronous copies, all in flight at once (the unaligned head and
+//      tail elements are read one per lane);
+//   2. every lane keeps the two largest logits of each of its two value
+//      streams (the low and high halves of its bf16 words, or the even and
+//      odd elements of its fp32 chunks): 128 sample values per row, among
+//      them the row's maximum;
+//   3. the k_eff-th largest sample value t0 is found by bisection on the
+//      order-preserving key (warp-wide counts by redux.sync).  At least k_eff
+//      logits of the row are >= t0, so the logits >= t0 (the candidates)
+//      hold the whole top-k set with all its ties; for top_k 30 of 1024
+//      gaussian logits they are about 31;
+//   4. one packed compare per word marks the candidates in a per-lane
+//      bitmap; the marked logits are written out as (key, inverted index)
+//      words and bitonic-sorted by one warp (32, 64 or 128 slots);
+//   5. the first k_eff sorted words are the top-k set in (logit desc, index
+//      asc) order: fixed-point weights, one warp scan, the nucleus cutoff and
+//      the draw, then the outputs.
+// Rows with more than kWarpCandMax candidates (huge ties) take an exact
+// radix-select slow path over the staged keys.
+//
+// The kernel walks its rows in batches of up to 32 consecutive rows: with G
+// row groups (the warps sharing a row) in the grid and B rows per batch,
+// group g takes batches g, g + G, g + 2G, ...  Lane i loads the parameters of
+// the batch's i-th row and computes its Philox draw, so these cost one round
+// of loads and one Philox evaluation per lane for up to 32 rows.  A launch may also span several decode steps (the
+// multi-step mode): row g is row g mod n_rows of step g / n_rows.  With ready
+// flags, a step's rows are sampled exactly when its flag is seen set; a warp
+// waits up to the time limit for a flag only until the first one that does
+// not come, and then looks at later flags once.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -20,8 +43,9 @@
 
 namespace ts {
 
-constexpr int kWarpHistBins = 1024;
 constexpr int kWarpCandMax = 128;
+constexpr int kTowerWarps = 4;
+constexpr int kTowerThreads = 32 * kTowerWarps;
 
 // Sort word: key in the high part, bit-inverted row index in the low part, so
 // that descending word order is (key desc, index asc).  A zero word sorts
@@ -50,6 +74,16 @@ struct SortWord<KeyF32> {
     return 0xFFFFFFFFu - static_cast<uint32_t>(w);
   }
 };
+
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) {
+  return __reduce_add_sync(0xFFFFFFFFu, v);
+}
+__device__ __forceinline__ uint32_t warp_max(uint32_t v) {
+  return __reduce_max_sync(0xFFFFFFFFu, v);
+}
+__device__ __forceinline__ uint32_t warp_min(uint32_t v) {
+  return __reduce_min_sync(0xFFFFFFFFu, v);
+}
 
 // Warp inclusive scan of a 64-bit value.
 __device__ __forceinline__ uint64_t warp_incl_scan_u64(uint64_t v) {
@@ -85,7 +119,9 @@ __device__ __forceinline__ uint32_t warp_incl_suffix_u32(uint32_t v) {
   return v;
 }
 
-// Descending bitonic sort of 32*R words held as v[i] = element i*32 + lane.
+// Descending bitonic sort of 32 * R words; lane l holds positions R*l .. R*l +
+// R - 1 in v[0 .. R-1].  Partners R or more positions apart are in another
+// lane (a shuffle); closer ones are in the same lane.
 template <class T, int R>
 __device__ __forceinline__ void bitonic_desc(T (&v)[R]) {
   const uint32_t lane = lane_id();
@@ -93,24 +129,24 @@ __device__ __forceinline__ void bitonic_desc(T (&v)[R]) {
   for (int size = 2; size <= 32 * R; size <<= 1) {
 #pragma unroll
     for (int j = size >> 1; j > 0; j >>= 1) {
-      if (j >= 32) {
-        const int jj = j >> 5;
+      if (j < R) {
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-          if ((i & jj) == 0) {
-            const bool desc = ((i * 32) & size) == 0;
-            const T a = v[i], b = v[i | jj];
+          if ((i & j) == 0) {
+            const bool desc = ((static_cast<uint32_t>(R) * lane + i) & size) == 0;
+            const T a = v[i], b = v[i | j];
             const T hi = a > b ? a : b, lo = a > b ? b : a;
             v[i] = desc ? hi : lo;
-            v[i | jj] = desc ? lo : hi;
+            v[i | j] = desc ? lo : hi;
           }
         }
       } else {
+        const int jl = j / R;
+        const bool lower = (lane & static_cast<uint32_t>(jl)) == 0;
 #pragma unroll
         for (int i = 0; i < R; ++i) {
-          const T o = __shfl_xor_sync(0xFFFFFFFFu, v[i], j);
-          const bool lower = (lane & j) == 0;
-          const bool desc = ((static_cast<uint32_t>(i * 32) + lane) & size) == 0;
+          const T o = __shfl_xor_sync(0xFFFFFFFFu, v[i], jl);
+          const bool desc = ((static_cast<uint32_t>(R) * lane + i) & size) == 0;
           v[i] = (lower == desc) ? (v[i] > o ? v[i] : o) : (v[i] < o ? v[i] : o);
         }
       }
@@ -118,42 +154,362 @@ __device__ __forceinline__ void bitonic_desc(T (&v)[R]) {
   }
 }
 
-// Nucleus cutoff and draw over the sorted top-k set (positions lane and
-// lane + 32 hold s0 and s1; k_eff = kq <= 64), then the outputs.
+// ---------------------------------------------------------------------------
+// Per-dtype lane helpers: the running top-2 of the lane's two value streams,
+// the four sample keys, and the candidate bitmap of a chunk.
+// ---------------------------------------------------------------------------
 template <class K>
-__device__ __forceinline__ void warp_tail(const Params &p, int r, const Row &w,
-                                          typename SortWord<K>::T s0,
-                                          typename SortWord<K>::T s1, int kq, uint32_t u24) {
-  using SW = SortWord<K>;
-  const uint32_t lane = lane_id();
-  const float m = K::value(SW::key(__shfl_sync(0xFFFFFFFFu, s0, 0)));
-  const bool has1 = kq > 32;
-  const int p0 = static_cast<int>(lane), p1 = static_cast<int>(lane) + 32;
-  float w0 = 0.f, w1 = 0.f;
-  if (!w.greedy) {
-    if (p0 < kq) w0 = kept_weight(K::value(SW::key(s0)), m, w.temp, w.inv_temp);
-    if (has1 && p1 < kq) w1 = kept_weight(K::value(SW::key(s1)), m, w.temp, w.inv_temp);
+struct Lane;
+
+template <>
+struct Lane<KeyBF16> {
+  // m1 >= m2 per half: the low halves of the lane's words are one stream,
+  // the high halves the other.  m1 keeps a NaN once it has met one (a NaN
+  // row is an error; m2 then no longer matters).
+  struct Acc {
+    uint32_t m1, m2;
+  };
+  static constexpr int kChunksPerMap = 4;  // a bitmap word covers 4 chunks (32 logits)
+  __device__ __forceinline__ static __nv_bfloat162 b2(uint32_t x) {
+    return *reinterpret_cast<__nv_bfloat162 *>(&x);
   }
-  // prefix masses in 2^-40 units, as four interleaved 32-bit scans of the
-  // 20-bit halves (sums of 64 halves stay below 2^27)
-  const uint64_t f0 = to_fixed(w0), f1 = to_fixed(w1);
-  uint32_t h0 = static_cast<uint32_t>(f0 >> 20), l0 = static_cast<uint32_t>(f0 & 0xFFFFFu);
-  uint32_t h1 = static_cast<uint32_t>(f1 >> 20), l1 = static_cast<uint32_t>(f1 & 0xFFFFFu);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, h0, o), b = __shfl_up_sync(0xFFFFFFFFu, l0, o);
-    const uint32_t cc = __shfl_up_sync(0xFFFFFFFFu, h1, o), d = __shfl_up_sync(0xFFFFFFFFu, l1, o);
-    if (lane >= static_cast<uint32_t>(o)) {
-      h0 += a;
-      l0 += b;
-      h1 += cc;
-      l1 += d;
+  __device__ __forceinline__ static uint32_t u(__nv_bfloat162 x) {
+    return *reinterpret_cast<uint32_t *>(&x);
+  }
+  __device__ __forceinline__ static Acc init() { return {0xFF80FF80u, 0xFF80FF80u}; }
+  __device__ __forceinline__ static void fold(uint32_t w, Acc &a) {
+    a.m2 = u(__hmax2(b2(a.m2), __hmin2(b2(a.m1), b2(w))));
+    a.m1 = u(__hmax2_nan(b2(a.m1), b2(w)));
+  }
+  __device__ __forceinline__ static void fold_chunk(const uint4 &c, Acc &a) {
+    fold(c.x, a);
+    fold(c.y, a);
+    fold(c.z, a);
+    fold(c.w, a);
+  }
+  __device__ __forceinline__ static void merge(Acc &a, const Acc &b) {
+    a.m2 = u(__hmax2(__hmin2(b2(a.m1), b2(b.m1)), __hmax2(b2(a.m2), b2(b.m2))));
+    a.m1 = u(__hmax2_nan(b2(a.m1), b2(b.m1)));
+  }
+  // a NaN among the logits folded into this lane's streams
+  __device__ __forceinline__ static bool has_nan(const Acc &a) {
+    return ((a.m1 & 0x7FFFu) > 0x7F80u) || ((a.m1 & 0x7FFF0000u) > 0x7F800000u);
+  }
+  __device__ __forceinline__ static void store(uint32_t *dst, const Acc &a) {
+    dst[0] = a.m1;
+    dst[1] = a.m2;
+  }
+  __device__ __forceinline__ static Acc load(const uint32_t *src) { return {src[0], src[1]}; }
+  __device__ __forceinline__ static void sample_keys(const Acc &a, uint32_t (&k)[4]) {
+    k[0] = KeyBF16::key(a.m1 & 0xFFFFu);
+    k[1] = KeyBF16::key(a.m1 >> 16);
+    k[2] = KeyBF16::key(a.m2 & 0xFFFFu);
+    k[3] = KeyBF16::key(a.m2 >> 16);
+  }
+  // the threshold as a packed pair of bf16 values
+  __device__ __forceinline__ static uint32_t splat(uint32_t key) {
+    const uint32_t bits = key ^ ((key & 0x8000u) ? 0x8000u : 0xFFFFu);
+    return bits | (bits << 16);
+  }
+  // bitmap bits of the logits >= t (unordered: a NaN is marked too) in chunk
+  // slot cs (0..3) of a map word: word i of the chunk is map word w = 4 cs +
+  // i, its low half at bit w and its high half at bit w + 16
+  __device__ __forceinline__ static uint32_t flags(const uint4 &c, uint32_t t2, int cs) {
+    const int w = 4 * cs;
+    return (__hgeu2_mask(b2(c.x), b2(t2)) & (0x00010001u << w)) |
+           (__hgeu2_mask(b2(c.y), b2(t2)) & (0x00010001u << (w + 1))) |
+           (__hgeu2_mask(b2(c.z), b2(t2)) & (0x00010001u << (w + 2))) |
+           (__hgeu2_mask(b2(c.w), b2(t2)) & (0x00010001u << (w + 3)));
+  }
+  // (chunk slot, element of the chunk) of a bitmap bit
+  __device__ __forceinline__ static void bit_elem(int b, int &cs, int &e) {
+    const int w = b & 15;
+    cs = w >> 2;
+    e = 2 * (w & 3) + (b >> 4);
+  }
+  // 16 times the number of the lane's four sample values whose key is >= c:
+  // two packed compares against the value of key c (the row has no NaN here)
+  __device__ __forceinline__ static uint32_t count16_ge(const Acc &a, uint32_t c) {
+    const uint32_t bits = c ^ (0xFFFFu - (c >> 15) * 0x7FFFu);
+    const uint32_t c2 = __byte_perm(bits, 0u, 0x1010);
+    return __popc(__hge2_mask(b2(a.m1), b2(c2))) + __popc(__hge2_mask(b2(a.m2), b2(c2)));
+  }
+};
+
+template <>
+struct Lane<KeyF32> {
+  // stream A: elements 0 and 2 of the lane's chunks, stream B: 1 and 3;
+  // a1 / b1 keep a NaN once they have met one
+  struct Acc {
+    uint32_t a1, a2, b1, b2;
+  };
+  __device__ __forceinline__ static float max_nan(float a, float b) {
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+  }
+  static constexpr int kChunksPerMap = 8;  // a bitmap word covers 8 chunks (32 logits)
+  __device__ __forceinline__ static Acc init() {
+    return {0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u};
+  }
+  __device__ __forceinline__ static void fold1(uint32_t w, uint32_t &m1, uint32_t &m2) {
+    const float x = __uint_as_float(w), a = __uint_as_float(m1), b = __uint_as_float(m2);
+    m2 = __float_as_uint(fmaxf(b, fminf(a, x)));
+    m1 = __float_as_uint(max_nan(a, x));
+  }
+  __device__ __forceinline__ static void fold_chunk(const uint4 &c, Acc &a) {
+    fold1(c.x, a.a1, a.a2);
+    fold1(c.y, a.b1, a.b2);
+    fold1(c.z, a.a1, a.a2);
+    fold1(c.w, a.b1, a.b2);
+  }
+  __device__ __forceinline__ static void merge2(uint32_t &m1, uint32_t &m2, uint32_t n1,
+                                                uint32_t n2) {
+    const float a = __uint_as_float(m1), c = __uint_as_float(m2);
+    const float x = __uint_as_float(n1), y = __uint_as_float(n2);
+    m2 = __float_as_uint(fmaxf(fminf(a, x), fmaxf(c, y)));
+    m1 = __float_as_uint(max_nan(a, x));
+  }
+  __device__ __forceinline__ static void merge(Acc &a, const Acc &b) {
+    merge2(a.a1, a.a2, b.a1, b.a2);
+    merge2(a.b1, a.b2, b.b1, b.b2);
+  }
+  __device__ __forceinline__ static bool has_nan(const Acc &a) {
+    return (a.a1 & 0x7FFFFFFFu) > 0x7F800000u || (a.b1 & 0x7FFFFFFFu) > 0x7F800000u;
+  }
+  __device__ __forceinline__ static void store(uint32_t *dst, const Acc &a) {
+    dst[0] = a.a1;
+    dst[1] = a.a2;
+    dst[2] = a.b1;
+    dst[3] = a.b2;
+  }
+  __device__ __forceinline__ static Acc load(const uint32_t *src) {
+    return {src[0], src[1], src[2], src[3]};
+  }
+  __device__ __forceinline__ static void sample_keys(const Acc &a, uint32_t (&k)[4]) {
+    k[0] = KeyF32::key(a.a1);
+    k[1] = KeyF32::key(a.b1);
+    k[2] = KeyF32::key(a.a2);
+    k[3] = KeyF32::key(a.b2);
+  }
+  __device__ __forceinline__ static uint32_t splat(uint32_t key) {
+    return key ^ ((key & 0x80000000u) ? 0x80000000u : 0xFFFFFFFFu);
+  }
+  // bit 4 cs + e for element e of chunk slot cs (0..7) when it is >= t
+  // (unordered: a NaN is marked too)
+  __device__ __forceinline__ static uint32_t flags(const uint4 &c, uint32_t t, int cs) {
+    const float tv = __uint_as_float(t);
+    const int b = 4 * cs;
+    return (static_cast<uint32_t>(!(__uint_as_float(c.x) < tv)) << b) |
+           (static_cast<uint32_t>(!(__uint_as_float(c.y) < tv)) << (b + 1)) |
+           (static_cast<uint32_t>(!(__uint_as_float(c.z) < tv)) << (b + 2)) |
+           (static_cast<uint32_t>(!(__uint_as_float(c.w) < tv)) << (b + 3));
+  }
+  __device__ __forceinline__ static void bit_elem(int b, int &cs, int &e) {
+    cs = b >> 2;
+    e = b & 3;
+  }
+  __device__ __forceinline__ static uint32_t count16_ge(const Acc &a, uint32_t c) {
+    uint32_t k[4];
+    sample_keys(a, k);
+    return 16u * (static_cast<uint32_t>(k[0] >= c) + static_cast<uint32_t>(k[1] >= c) +
+                  static_cast<uint32_t>(k[2] >= c) + static_cast<uint32_t>(k[3] >= c));
+  }
+};
+
+template <class K>
+__host__ __device__ constexpr int acc_words() {
+  return sizeof(typename Lane<K>::Acc) / 4;
+}
+
+// The kq-th largest of the warp's sample values (four per lane in `a`: the
+// two streams' two largest; plus `ex` on lanes that hold a head or tail
+// element), as a key, searched on the key's top 16 bits: for bf16 the exact
+// key, for fp32 that key with its low 16 bits cleared (still a lower bound).
+// The search starts from [lo, top], lo a key with at least kq sample keys >=
+// it and top the largest sample key.
+template <class K>
+__device__ __forceinline__ uint32_t sample_kth(const typename Lane<K>::Acc &a, uint32_t ex,
+                                               bool any_ex, int kq, uint32_t lo, uint32_t top) {
+  constexpr int kShift = K::kBits - 16;
+  const uint32_t lo16 = lo >> kShift, hi16 = top >> kShift;
+  const uint32_t diff = lo16 ^ hi16;
+  if (diff == 0) return lo16 << kShift;
+  int b = 31 - __clz(diff);
+  // the common prefix of lo and top, lower bits clear: <= lo
+  uint32_t t16 = hi16 & ~((2u << b) - 1u);
+  const uint32_t need = 16u * static_cast<uint32_t>(kq);
+#pragma unroll 1
+  for (; b >= 0; --b) {
+    const uint32_t c = (t16 | (1u << b)) << kShift;
+    uint32_t n = Lane<K>::count16_ge(a, c);
+    if (any_ex) n += ex >= c ? 16u : 0u;  // warp-uniform branch
+    if (warp_sum(n) >= need) t16 |= 1u << b;
+  }
+  return t16 << kShift;
+}
+
+// ---------------------------------------------------------------------------
+// One row's parameters, as one lane of the batch holds them.  The fields the
+// row body needs early (offset, width, k_eff, flags) are broadcast when the
+// row starts; the tail's (temperature, top_p, slot, EOS id) when it runs.
+// ---------------------------------------------------------------------------
+struct RowParams {
+  int64_t off;    // element offset of the row (its step's logits included)
+  int32_t r;      // row of the batch
+  int32_t s;      // step index within the launch
+  uint32_t meta;  // vocab (bits 0-17) | k_eff (18-24) | greedy (25) | error bits (26-30)
+  int32_t slot;   // write-back slot (its step's frame included), -1 = none
+  int32_t eos;
+  float temp;
+  float inv_temp;
+  float top_p;
+};
+
+__device__ __forceinline__ int meta_vocab(uint32_t m) { return static_cast<int>(m & 0x3FFFFu); }
+__device__ __forceinline__ int meta_keff(uint32_t m) { return static_cast<int>((m >> 18) & 0x7Fu); }
+__device__ __forceinline__ bool meta_greedy(uint32_t m) { return ((m >> 25) & 1u) != 0u; }
+__device__ __forceinline__ uint32_t meta_err(uint32_t m) { return m >> 26; }
+
+// The parameters of row g of the launch (row g mod n_rows of step g / n_rows).
+// Every check that the warp path needs is made here: a row whose width
+// exceeds the launch's maximum is a shape error, so width and k_eff fit their
+// fields.
+__device__ __forceinline__ RowParams load_params(const Params &p, int64_t g) {
+  RowParams w;
+  const int s = p.n_steps == 1 ? 0 : static_cast<int>(g / p.n_rows);
+  const int r = static_cast<int>(g - static_cast<int64_t>(s) * p.n_rows);
+  w.r = r;
+  w.s = s;
+  const int32_t vocab = p.row_vocab[r];
+  w.off = p.row_offsets[r];
+  w.temp = p.temp[r];
+  w.top_p = p.top_p[r];
+  const int32_t stream = p.row_stream[r];
+  const int32_t slot = p.feedback_buf ? p.feedback_slot[r] : -1;
+  w.eos = p.eos_id ? p.eos_id[r] : -1;
+  const int32_t tk = p.top_k[r];
+  uint32_t e = 0;
+  if (w.off < 0) e |= kRowBadShape;
+  w.off += static_cast<int64_t>(s) * p.logits_step_stride;
+  if (vocab <= 0 || vocab > p.max_row_vocab || w.off > p.logits_len - static_cast<int64_t>(vocab))
+    e |= kRowBadShape;
+  if (stream < 0 || stream >= p.n_streams) e |= kRowBadShape;
+  if (isnan(w.temp) || isinf(w.temp) || isnan(w.top_p)) e |= kRowBadParam;
+  if (slot >= 0 && static_cast<int64_t>(slot) >= p.feedback_len) e |= kRowBadSlot;
+  w.slot = slot >= 0 ? static_cast<int32_t>(slot + static_cast<int64_t>(s) * p.feedback_step_stride)
+                     : -1;
+  const int32_t v = e ? 1 : vocab;
+  int32_t k = tk > 0 ? tk : v;
+  k = min(k, p.cap);
+  k = min(k, v);
+  const bool greedy = !(w.temp > 0.0f) || k == 1;
+  w.inv_temp = greedy ? 1.0f : 1.0f / w.temp;
+  w.meta = static_cast<uint32_t>(v) | (static_cast<uint32_t>(k) << 18) |
+           (greedy ? (1u << 25) : 0u) | (e << 26);
+  return w;
+}
+
+// The row's outputs: id, EOS flag and write-back (its step's slots), or the
+// error marks.  `out` = the row's output index; eos / slot are used only
+// without an error.
+__device__ __forceinline__ void row_outputs(const Params &p, int r, int64_t out, int32_t eos,
+                                            int32_t slot, int32_t id, uint32_t err) {
+  if (err) {
+    p.out_ids[out] = -1;
+    p.out_eos[out] = 0;
+    atomicOr(p.status, err);
+    if (p.kept_ids) {
+      p.n_kept[r] = 0;
+      p.n_nucleus[r] = 0;
+    }
+    return;
+  }
+  p.out_ids[out] = id;
+  p.out_eos[out] = static_cast<uint8_t>(eos >= 0 && id == eos);
+  if (slot >= 0) p.feedback_buf[slot] = id;
+}
+
+// What the tail needs of a row, broadcast from the lane that loaded it.
+struct TailParams {
+  int r;
+  int64_t out;
+  int32_t slot, eos;
+  float temp, inv_temp, top_p;
+  int k_eff;
+  bool greedy;
+};
+
+__device__ __forceinline__ TailParams tail_params(const Params &p, const RowParams &a) {
+  TailParams t;
+  t.r = a.r;
+  t.out = static_cast<int64_t>(a.s) * p.out_step_stride + a.r;
+  t.slot = a.slot;
+  t.eos = a.eos;
+  t.temp = a.temp;
+  t.inv_temp = a.inv_temp;
+  t.top_p = a.top_p;
+  t.k_eff = meta_keff(a.meta);
+  t.greedy = meta_greedy(a.meta);
+  return t;
+}
+
+// Waits (lane 0, bounded) for a step's ready flag; true once it is set.  A
+// zero limit looks at the flag once.
+// The flag is read with acquire semantics at system scope, so that a flag
+// written by the host (or by a copy) orders the step's logits before the
+// loads that follow.
+__device__ __forceinline__ bool wait_ready(const uint32_t *flag, uint64_t timeout_ns) {
+  uint32_t ok = 0;
+  if (lane_id() == 0) {
+    uint64_t t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+#pragma unroll 1
+    for (uint32_t it = 0; it < (1u << 24); ++it) {
+      uint32_t v;
+      asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+      if (v) {
+        ok = 1;
+        break;
+      }
+      uint64_t t1;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t1));
+      if (t1 - t0 > timeout_ns) break;
+      __nanosleep(200);
     }
   }
-  const uint64_t c0 = (static_cast<uint64_t>(h0) << 20) + l0;
-  const uint64_t tot0 = __shfl_sync(0xFFFFFFFFu, c0, 31);
-  const uint64_t c1 = (static_cast<uint64_t>(h1) << 20) + l1 + tot0;
-  const uint64_t s_k = __shfl_sync(0xFFFFFFFFu, c1, 31);
+  return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// ---------------------------------------------------------------------------
+// The tail: the sorted top-k set (kq <= 64 positions, lane l holds positions
+// R*l .. R*l + R - 1), fixed-point weights, the nucleus cutoff and the draw.
+// ---------------------------------------------------------------------------
+template <class K, int R>
+__device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
+                                          typename SortWord<K>::T (&v)[R], int kq,
+                                          uint32_t u24) {
+  using SW = SortWord<K>;
+  using T = typename SW::T;
+  const uint32_t lane = lane_id();
+  const int pos0 = R * static_cast<int>(lane);
+  const float m = K::value(SW::key(__shfl_sync(0xFFFFFFFFu, v[0], 0)));
+  float wt[R];
+  uint64_t c[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    wt[i] = 0.f;
+    if (!w.greedy && pos0 + i < kq) wt[i] = kept_weight(K::value(SW::key(v[i])), m, w.temp, w.inv_temp);
+    c[i] = to_fixed(wt[i]);
+    if (i > 0) c[i] += c[i - 1];
+  }
+  // prefix masses in 2^-40 units: the lane's inclusive local sums plus the
+  // warp's exclusive scan of the lane totals
+  const uint64_t incl = warp_incl_scan_u64(c[R - 1]);
+  const uint64_t excl = incl - c[R - 1];
+#pragma unroll
+  for (int i = 0; i < R; ++i) c[i] += excl;
+  const uint64_t s_k = __shfl_sync(0xFFFFFFFFu, incl, 31);
 
   int n_p = 1, pick = 0;
   if (!w.greedy) {
@@ -161,57 +517,107 @@ __device__ __forceinline__ void warp_tail(const Params &p, int r, const Row &w,
       n_p = kq;
     } else if (w.top_p > 0.0f) {
       const uint64_t cut_i = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut_i
-      const uint32_t b0 = __ballot_sync(0xFFFFFFFFu, p0 < kq && c0 < cut_i);
-      const uint32_t b1 = __ballot_sync(0xFFFFFFFFu, p1 < kq && c1 < cut_i);
-      n_p = min(__popc(b0) + __popc(b1) + 1, kq);
+      uint32_t below = 0;
+#pragma unroll
+      for (int i = 0; i < R; ++i) below += (pos0 + i < kq && c[i] < cut_i) ? 1u : 0u;
+      n_p = min(static_cast<int>(warp_sum(below)) + 1, kq);
     }
     const int last = n_p - 1;
-    const uint64_t s_p = last < 32 ? __shfl_sync(0xFFFFFFFFu, c0, last)
-                                   : __shfl_sync(0xFFFFFFFFu, c1, last - 32);
+    uint64_t cl = c[0];
+#pragma unroll
+    for (int i = 1; i < R; ++i)
+      if ((last % R) == i) cl = c[i];
+    const uint64_t s_p = __shfl_sync(0xFFFFFFFFu, cl, last / R);
     const uint64_t target = scale_u24(u24, s_p);
-    const uint32_t le0 = __ballot_sync(0xFFFFFFFFu, p0 < n_p && c0 <= target);
-    const uint32_t le1 = __ballot_sync(0xFFFFFFFFu, p1 < n_p && c1 <= target);
-    pick = __popc(le0) + __popc(le1);
+    uint32_t le = 0;
+#pragma unroll
+    for (int i = 0; i < R; ++i) le += (pos0 + i < n_p && c[i] <= target) ? 1u : 0u;
+    pick = static_cast<int>(warp_sum(le));
   }
-  const typename SW::T pw = pick < 32 ? __shfl_sync(0xFFFFFFFFu, s0, pick)
-                                      : __shfl_sync(0xFFFFFFFFu, s1, pick - 32);
-  if (lane == 0) finish_row(p, r, w, static_cast<int32_t>(SW::idx(pw)), 0u);
+  T vp = v[0];
+#pragma unroll
+  for (int i = 1; i < R; ++i)
+    if ((pick % R) == i) vp = v[i];
+  const T pw = __shfl_sync(0xFFFFFFFFu, vp, pick / R);
+  if (lane == 0) row_outputs(p, w.r, w.out, w.eos, w.slot, static_cast<int32_t>(SW::idx(pw)), 0u);
 
   if (p.kept_ids) {
     const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
-    const int64_t rb = static_cast<int64_t>(r) * p.max_keep;
-    if (p0 < kq && p0 < p.max_keep) {
-      p.kept_ids[rb + p0] = static_cast<int32_t>(SW::idx(s0));
-      p.kept_probs[rb + p0] = w.greedy ? (p0 == 0 ? 1.f : 0.f) : __fdiv_rn(w0, s_real);
-    }
-    if (has1 && p1 < kq && p1 < p.max_keep) {
-      p.kept_ids[rb + p1] = static_cast<int32_t>(SW::idx(s1));
-      p.kept_probs[rb + p1] = w.greedy ? 0.f : __fdiv_rn(w1, s_real);
+    const int64_t rb = static_cast<int64_t>(w.r) * p.max_keep;
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int q = pos0 + i;
+      if (q < kq && q < p.max_keep) {
+        p.kept_ids[rb + q] = static_cast<int32_t>(SW::idx(v[i]));
+        p.kept_probs[rb + q] = w.greedy ? (q == 0 ? 1.f : 0.f) : __fdiv_rn(wt[i], s_real);
+      }
     }
     if (lane == 0) {
-      p.n_kept[r] = kq;
-      p.n_nucleus[r] = n_p;
+      p.n_kept[w.r] = kq;
+      p.n_nucleus[w.r] = n_p;
     }
   }
 }
 
-// Exact slow path for rows the fast path declines (more than kWarpCandMax
-// keys at or above the candidate threshold, i.e. huge ties): 8-bit radix
-// select over the row's keys (keys(q) returns the keys of body chunk q, read
-// again from memory), then the top-k set collected in index order (keys
-// equal to the threshold taken by lowest index), sorted, and the common tail.
+// Sorts the nc candidate words of `cand` and runs the tail on the first kq.
+template <class K, int R>
+__device__ __forceinline__ void sort_and_tail(const Params &p, const TailParams &w,
+                                              const typename SortWord<K>::T *cand, int nc,
+                                              uint32_t u24) {
+  using T = typename SortWord<K>::T;
+  const int pos0 = R * static_cast<int>(lane_id());
+  T v[R];
+#pragma unroll
+  for (int i = 0; i < R; ++i) v[i] = pos0 + i < nc ? cand[pos0 + i] : T(0);
+  if (nc > 1) bitonic_desc<T, R>(v);
+  if constexpr (R <= 2) {
+    warp_tail<K, R>(p, w, v, w.k_eff, u24);
+  } else {
+    // k_eff <= 64: the first 64 sorted positions, two per lane.  Position
+    // 2l + h lives in lane (2l + h) / R, slot (2l + h) % R; readers want
+    // different slots of one lane, so every slot is shuffled and the reader
+    // keeps its own.
+    T v2[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = 2 * static_cast<int>(lane_id()) + h;
+      T x = T(0);
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const T y = __shfl_sync(0xFFFFFFFFu, v[i], q / R);
+        if ((q % R) == i) x = y;
+      }
+      v2[h] = x;
+    }
+    warp_tail<K, 2>(p, w, v2, w.k_eff, u24);
+  }
+}
+
+// The 128-slot sort (rows with 65 to 128 candidates).
+template <class K>
+__device__ __forceinline__ void sort_and_tail_128(const Params &p, const TailParams &w,
+                                               const typename SortWord<K>::T *cand, int nc,
+                                               uint32_t u24) {
+  sort_and_tail<K, 4>(p, w, cand, nc, u24);
+}
+
+// Exact slow path for rows whose candidate count exceeds kWarpCandMax (huge
+// ties): 8-bit radix select over the row's keys (keys(q) returns the keys of
+// body chunk q, read again from the stage), then the top-k set collected in
+// index order (keys equal to the threshold taken by lowest index) into
+// cand[0 .. k_eff).
 template <class K, class Loader>
-__device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w, uint32_t *hist,
-                                            typename SortWord<K>::T *cand, const Loader keys,
-                                            int nq, int head, int tail, int eidx, uint32_t ekey,
-                                            uint32_t u24) {
+__device__ __forceinline__ void warp_slow_select(int vocab, int k_eff, uint32_t *hist,
+                                              typename SortWord<K>::T *cand, const Loader keys,
+                                              int nq, int head, int tail, int eidx,
+                                              uint32_t ekey) {
   using SW = SortWord<K>;
   constexpr int EPC = K::kPerChunk;
   const uint32_t lane = lane_id();
   const int rounds = (nq + 31) >> 5;
 
   uint32_t prefix = 0, pmask = 0;
-  uint32_t kk = static_cast<uint32_t>(w.k_eff);
+  uint32_t kk = static_cast<uint32_t>(k_eff);
 #pragma unroll 1
   for (int pass = 0; pass < K::kBits / 8; ++pass) {
     const int shift = K::kBits - 8 * (pass + 1);
@@ -228,7 +634,7 @@ __device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w
         if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & 0xFFu], 1u);
       }
     }
-    if (eidx < w.vocab && (ekey & pmask) == prefix)
+    if (eidx < vocab && (ekey & pmask) == prefix)
       atomicAdd(&hist[(ekey >> shift) & 0xFFu], 1u);
     __syncwarp();
     const uint4 h0 = reinterpret_cast<const uint4 *>(hist)[lane * 2];
@@ -263,7 +669,7 @@ __device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w
 
   uint32_t base = 0, eq_base = 0;
   const uint32_t lt = lanemask_lt();
-  const bool has_e = eidx < w.vocab;
+  const bool has_e = eidx < vocab;
   {  // head elements (indices 0 .. head-1 live in lanes 0 .. head-1)
     const bool in = has_e && static_cast<int>(lane) < head;
     const bool gt = in && ekey > thr, eq = in && ekey == thr;
@@ -327,166 +733,24 @@ __device__ __noinline__ void warp_slow_path(const Params &p, int r, const Row &w
     if (take && at < 64) cand[at] = SW::make(ekey, static_cast<uint32_t>(eidx));
   }
   __syncwarp();
-  const int kq = w.k_eff;
-  typename SW::T s[2];
-  s[0] = static_cast<int>(lane) < kq ? cand[lane] : 0;
-  s[1] = static_cast<int>(lane) + 32 < kq ? cand[lane + 32] : 0;
-  __syncwarp();
-  if (kq <= 32) {
-    typename SW::T one[1] = {s[0]};
-    bitonic_desc<typename SW::T, 1>(one);
-    s[0] = one[0];
-  } else {
-    bitonic_desc<typename SW::T, 2>(s);
-  }
-  warp_tail<K>(p, r, w, s[0], s[1], kq, u24);
 }
 
-// Sorts the n (<= 32 * R) candidate words in `cand`; s0 / s1 get the first
-// 64 in descending order (lane l holds positions l and l + 32).
-template <class K, int R>
-__device__ __forceinline__ void warp_sort_cand(const typename SortWord<K>::T *cand, int n,
-                                               typename SortWord<K>::T &s0,
-                                               typename SortWord<K>::T &s1) {
-  using T = typename SortWord<K>::T;
-  const uint32_t lane = lane_id();
-  T v[R];
-#pragma unroll
-  for (int i = 0; i < R; ++i) {
-    const int e = i * 32 + static_cast<int>(lane);
-    v[i] = e < n ? cand[e] : T(0);
-  }
-  bitonic_desc<T, R>(v);
-  s0 = v[0];
-  s1 = T(0);
-  if constexpr (R > 1) s1 = v[1];
-}
-
-// Warp-path kernel.  A row is owned by one warp, or shared by 2 or 4 warps
-// (kTowerWarps / WPR rows per block; the warps of a row meet at a named
-// barrier of their own, never at a block barrier):
-//   1. the row is copied into its shared-memory stage with 16-byte
-//      asynchronous copies (lane l: body chunks l, l + 32, ...), all in
-//      flight at once; the unaligned head and tail elements are read one per
-//      lane; lane 0 computes the Philox draw meanwhile;
-//   2. each lane keeps the two largest logits it has seen (packed bf16 or
-//      fp32 min / max); the k_eff-th largest of these 64 values t0 is a lower
-//      bound of the row's k_eff-th largest logit (at least k_eff of the row's
-//      logits are >= t0), so every logit >= t0 is a candidate and the
-//      candidates hold the whole top-k set with every tie at its end;
-//   3. an unordered compare with t0 (so that a NaN is flagged too) marks the
-//      chunks that hold a candidate; only those are unpacked into (key,
-//      inverted index) words, about 35 for top_k 30 of 1024 gaussian logits,
-//      which the warp bitonic-sorts: the first k_eff are the top-k set in
-//      (logit desc, index asc) order;
-//   4. the warp forms fixed-point weights, scans them, cuts the nucleus and
-//      draws.
-// Rows with more than kWarpCandMax candidates (huge ties) take the exact
-// radix-select slow path over the staged keys.
-constexpr int kTowerWarps = 4;
-constexpr int kTowerThreads = 32 * kTowerWarps;
-constexpr int kRowThreads = kTowerThreads;
-
-
-// Per-dtype chunk helpers: the two largest values of a chunk folded into a
-// running pair, and the unordered >= mask of a chunk against a threshold.
-template <class K>
-struct Top2;
-
-template <>
-struct Top2<KeyBF16> {
-  using V = uint32_t;  // packed bf16x2
-  static constexpr uint32_t kInit = 0xFF80FF80u;  // -inf, -inf
-  __device__ __forceinline__ static __nv_bfloat162 b2(uint32_t x) {
-    return *reinterpret_cast<__nv_bfloat162 *>(&x);
-  }
-  __device__ __forceinline__ static uint32_t u(__nv_bfloat162 x) {
-    return *reinterpret_cast<uint32_t *>(&x);
-  }
-  __device__ __forceinline__ static void fold(uint32_t w, uint32_t &m1, uint32_t &m2) {
-    m2 = u(__hmax2(b2(m2), __hmin2(b2(m1), b2(w))));
-    m1 = u(__hmax2(b2(m1), b2(w)));
-  }
-  __device__ __forceinline__ static void fold_chunk(const uint4 &c, uint32_t &m1, uint32_t &m2) {
-    fold(c.x, m1, m2);
-    fold(c.y, m1, m2);
-    fold(c.z, m1, m2);
-    fold(c.w, m1, m2);
-  }
-  // (m1, m2) <- the two largest of the pairs (m1, m2) and (n1, n2), per half
-  __device__ __forceinline__ static void merge(uint32_t &m1, uint32_t &m2, uint32_t n1,
-                                               uint32_t n2) {
-    m2 = u(__hmax2(__hmin2(b2(m1), b2(n1)), __hmax2(b2(m2), b2(n2))));
-    m1 = u(__hmax2(b2(m1), b2(n1)));
-  }
-  // the lane's two largest keys from the packed pair
-  __device__ __forceinline__ static void keys2(uint32_t m1, uint32_t m2, uint32_t &k1,
-                                               uint32_t &k2) {
-    const uint32_t a = KeyBF16::key(m1 & 0xFFFFu), b = KeyBF16::key(m1 >> 16);
-    const uint32_t c = KeyBF16::key(m2 & 0xFFFFu), d = KeyBF16::key(m2 >> 16);
-    k1 = max(a, b);
-    k2 = max(min(a, b), max(c, d));
-  }
-  __device__ __forceinline__ static uint32_t splat(uint32_t key) {
-    const uint32_t bits = key ^ ((key & 0x8000u) ? 0x8000u : 0xFFFFu);
-    return bits | (bits << 16);
-  }
-  __device__ __forceinline__ static bool flagged(const uint4 &c, uint32_t t2) {
-    const uint32_t m = __hgeu2_mask(b2(c.x), b2(t2)) | __hgeu2_mask(b2(c.y), b2(t2)) |
-                       __hgeu2_mask(b2(c.z), b2(t2)) | __hgeu2_mask(b2(c.w), b2(t2));
-    return m != 0u;
-  }
-};
-
-template <>
-struct Top2<KeyF32> {
-  static constexpr uint32_t kInit = 0xFF800000u;  // -inf
-  __device__ __forceinline__ static void fold(uint32_t w, uint32_t &m1, uint32_t &m2) {
-    const float x = __uint_as_float(w), a = __uint_as_float(m1), b = __uint_as_float(m2);
-    m2 = __float_as_uint(fmaxf(b, fminf(a, x)));
-    m1 = __float_as_uint(fmaxf(a, x));
-  }
-  __device__ __forceinline__ static void fold_chunk(const uint4 &c, uint32_t &m1, uint32_t &m2) {
-    fold(c.x, m1, m2);
-    fold(c.y, m1, m2);
-    fold(c.z, m1, m2);
-    fold(c.w, m1, m2);
-  }
-  __device__ __forceinline__ static void merge(uint32_t &m1, uint32_t &m2, uint32_t n1,
-                                               uint32_t n2) {
-    const float a = __uint_as_float(m1), c = __uint_as_float(m2);
-    const float x = __uint_as_float(n1), y = __uint_as_float(n2);
-    m2 = __float_as_uint(fmaxf(fminf(a, x), fmaxf(c, y)));
-    m1 = __float_as_uint(fmaxf(a, x));
-  }
-  __device__ __forceinline__ static void keys2(uint32_t m1, uint32_t m2, uint32_t &k1,
-                                               uint32_t &k2) {
-    k1 = KeyF32::key(m1);
-    k2 = KeyF32::key(m2);
-  }
-  __device__ __forceinline__ static uint32_t splat(uint32_t key) {
-    return key ^ ((key & 0x80000000u) ? 0x80000000u : 0xFFFFFFFFu);
-  }
-  __device__ __forceinline__ static bool flagged(const uint4 &c, uint32_t t) {
-    const float tv = __uint_as_float(t);
-    return !(__uint_as_float(c.x) < tv) || !(__uint_as_float(c.y) < tv) ||
-           !(__uint_as_float(c.z) < tv) || !(__uint_as_float(c.w) < tv);
-  }
-};
-
-template <class K, int MAXNCH>
+// Shared memory of one row group.  The slow path's histogram and the
+// candidate words are never live at once, so they share storage.
+template <class K, int MAXNCH, int WPR>
 struct TowerShared {
   using T = typename SortWord<K>::T;
   uint4 stage[32 * MAXNCH];
-  T cand[kWarpCandMax];
-  uint32_t hist[256];
-  uint32_t xm1[4 * 32];  // per-lane running pairs of each warp (rows shared by warps)
-  uint32_t xm2[4 * 32];
-  uint32_t xb[4];    // the row's candidate bound and largest key
-  uint32_t xt[4];
-  uint32_t xn[4];    // per-warp candidate counts
-  uint32_t xu;       // the row's draw (computed by warp 1 when the row has several)
-  uint32_t xbad[4];  // per-warp NaN / +inf flags
+  union {
+    T cand[kWarpCandMax];
+    uint32_t hist[256];
+  } u;
+  uint32_t xacc[(WPR > 1 ? WPR - 1 : 1) * 32 * acc_words<K>()];  // warps 1.. running pairs
+  uint32_t xu[32];    // the batch's draws
+  uint32_t xt0, xtop;
+  uint32_t xready;    // the current step's ready flag came in time
+  uint32_t xcnt;      // candidate slots taken so far
+  uint32_t xbad[1];   // the row holds a NaN or +inf
 };
 
 // Barrier of the WPR warps that share a row (group grp of the block).
@@ -496,7 +760,7 @@ __device__ __forceinline__ void row_sync(int grp) {
     __syncwarp();
   } else if constexpr (WPR == 4) {
     asm volatile("bar.sync 1, 128;" ::: "memory");
-  } else {  // two rows per block: barriers 1 and 2 (constant ids)
+  } else {  // two groups per block: barriers 1 and 2 (constant ids)
     if (grp == 0)
       asm volatile("bar.sync 1, 64;" ::: "memory");
     else
@@ -504,220 +768,276 @@ __device__ __forceinline__ void row_sync(int grp) {
   }
 }
 
-// The row body for rows of at most 32 * nch body chunks (nch <= 16).  One
-// body serves every row width, so that warps on other widths share its code
-// in the instruction cache.  With WPR > 1 the row is shared by WPR warps:
-// warp `sub` owns the chunk columns j = sub, sub + WPR, ...; lane l's running
-// pairs of all the warps are merged, so the bound is the one a single warp
-// would find; the candidate counts are exchanged so that every warp writes
-// its candidates to its own range, and warp 0 sorts and runs the tail.
-template <class K, int WPR, class SH>
-__device__ __forceinline__ void tower_body(const Params &p, int r, const Row &w, uint32_t u24,
-                                           SH &sh, int head, int nq, int tail, const char *rowp,
-                                           int nch, int sub, int grp) {
-  // u24: the draw when WPR == 1; with several warps it arrives below
-  using SW = SortWord<K>;
-  using TT = Top2<K>;
-  constexpr int EPC = K::kPerChunk;
-  const uint32_t lane = lane_id();
-  const int V = w.vocab;
-  const char *body = rowp + head * K::kElemBytes;
-  // ---- this warp's columns into the stage, all copies in flight ----
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int j = sub + i * WPR;
-    if (j >= nch) break;
-    const int q = static_cast<int>(lane) + 32 * j;
-    if (q < nq) cp_async16(&sh.stage[q], body + static_cast<size_t>(q) * 16);
+// After every block of the launch has read step[]: the last block to arrive
+// adds n_steps to step_out[0 .. n_streams) and re-arms the ticket.  No block
+// waits for another; every thread of the block must reach this call.
+__device__ __forceinline__ void advance_steps_last_block(const Params &p) {
+  __shared__ uint32_t last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(p.ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
   }
-  // head / tail element of this lane of warp 0 (at most 7 + 7 of them)
-  int eidx = 0x7FFFFFFF;
-  if (sub == 0) {
-    if (static_cast<int>(lane) < head)
-      eidx = static_cast<int>(lane);
-    else if (static_cast<int>(lane) < head + tail)
-      eidx = nq * EPC + static_cast<int>(lane);
-  }
-  const bool has_e = eidx < V;
-  const uint32_t ebits = has_e ? K::load_one(rowp, eidx) : 0u;
-  if constexpr (WPR > 1) {
-    // the draw, by warp 1 while its copies are in flight: off warp 0's path
-    if (sub == 1 && lane == 0 && !w.greedy)
-      sh.xu = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
-                         static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
-  }
-  const uint32_t ekey = has_e ? K::key(ebits) : 0u;
-  cp_async_wait_all();
-  __syncwarp();
-
-  // ---- the two largest logits per lane ----
-  uint32_t m1 = TT::kInit, m2 = TT::kInit;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int j = sub + i * WPR;
-    if (j >= nch) break;
-    const int q = static_cast<int>(lane) + 32 * j;
-    if (q < nq) TT::fold_chunk(sh.stage[q], m1, m2);
-  }
-  if constexpr (WPR > 1) {
-    sh.xm1[sub * 32 + lane] = m1;
-    sh.xm2[sub * 32 + lane] = m2;
-    row_sync<WPR>(grp);
-    if (!w.greedy) u24 = sh.xu;  // written by warp 1 before this barrier
-  }
-  const int kq = w.k_eff;
-  uint32_t t0 = 0, top = 0;
-  if (sub == 0) {
-    if constexpr (WPR > 1) {
-#pragma unroll
-      for (int s2 = 1; s2 < WPR; ++s2) TT::merge(m1, m2, sh.xm1[s2 * 32 + lane], sh.xm2[s2 * 32 + lane]);
-    }
-    uint32_t rep[2];
-    TT::keys2(m1, m2, rep[0], rep[1]);
-    if (has_e) {  // the lane's head / tail element joins its pair
-      rep[1] = max(rep[1], min(rep[0], ekey));
-      rep[0] = max(rep[0], ekey);
-    }
-    // ---- the k_eff-th largest of the 64 per-lane maxima: a lower bound ----
-    bitonic_desc<uint32_t, 2>(rep);
-    top = __shfl_sync(0xFFFFFFFFu, rep[0], 0);
-    t0 = kq <= 32 ? __shfl_sync(0xFFFFFFFFu, rep[0], kq - 1)
-                  : __shfl_sync(0xFFFFFFFFu, rep[1], kq - 33);
-    // a NaN as t0 would flag nothing (NaN rows are caught below either way)
-    if (t0 < K::kNegInf || t0 > K::kPosInf) t0 = K::kNegInf;
-    if constexpr (WPR > 1) {
-      if (lane == 0) {
-        sh.xb[0] = t0;
-        sh.xt[0] = top;
-      }
-    }
-  }
-  if constexpr (WPR > 1) {
-    row_sync<WPR>(grp);
-    t0 = sh.xb[0];
-    top = sh.xt[0];
-  }
-  const uint32_t t2 = TT::splat(t0);
-  // ---- candidates: chunks holding a logit >= t0 (or a NaN) ----
-  uint32_t fmask = 0;  // bit i: chunk lane + 32 (sub + i WPR) is flagged
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int j = sub + i * WPR;
-    if (j >= nch) break;
-    const int q = static_cast<int>(lane) + 32 * j;
-    if (q < nq && TT::flagged(sh.stage[q], t2)) fmask |= 1u << i;
-  }
-  // keys of the flagged chunks: count, then write
-  uint32_t mine = 0, bad = 0;
-  for (uint32_t fm = fmask; fm; fm &= fm - 1u) {
-    const int q = static_cast<int>(lane) + 32 * (sub + (__ffs(fm) - 1) * WPR);
-    const uint4 v = sh.stage[q];
-    const uint32_t c[4] = {K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w)};
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) {
-      const uint32_t k = K::elem(c, e);
-      bad |= (k < K::kNegInf) | (k > K::kPosInf - 1u);
-      mine += k >= t0 && k < K::kPosInf;
-    }
-  }
-  if (has_e) {
-    bad |= (ekey < K::kNegInf) | (ekey >= K::kPosInf);
-    mine += ekey >= t0 && ekey < K::kPosInf;
-  }
-  uint32_t total;
-  uint32_t pos = warp_excl_scan_u32(mine, &total);
-  bool any_bad = __any_sync(0xFFFFFFFFu, bad);
-  if constexpr (WPR > 1) {
-    if (lane == 0) {
-      sh.xn[sub] = total;
-      sh.xbad[sub] = any_bad ? 1u : 0u;
-    }
-    row_sync<WPR>(grp);
-    total = 0;
-#pragma unroll
-    for (int s2 = 0; s2 < WPR; ++s2) {
-      const uint32_t n2 = sh.xn[s2];
-      if (s2 < sub) pos += n2;
-      total += n2;
-      any_bad |= sh.xbad[s2] != 0u;
-    }
-  }
-  if (any_bad || top <= K::kNegInf) {  // a NaN / +inf, or no finite logit
-    if (sub == 0 && lane == 0) finish_row(p, r, w, -1, kRowNonFinite);
-    return;
-  }
-  if (total > static_cast<uint32_t>(kWarpCandMax)) {
-    // every warp of the row has staged its columns (the exchange above
-    // ordered them), so warp 0 may read the whole row
-    if (sub != 0) return;
-    auto keys = [&](int q) {
-      const uint4 v = sh.stage[q];
-      return make_uint4(K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w));
-    };
-    warp_slow_path<K>(p, r, w, sh.hist, sh.cand, keys, nq, head, tail, eidx, ekey, u24);
-    return;
-  }
-  for (uint32_t fm = fmask; fm; fm &= fm - 1u) {
-    const int q = static_cast<int>(lane) + 32 * (sub + (__ffs(fm) - 1) * WPR);
-    const uint4 v = sh.stage[q];
-    const uint32_t c[4] = {K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w)};
-#pragma unroll
-    for (int e = 0; e < EPC; ++e) {
-      const uint32_t k = K::elem(c, e);
-      if (k >= t0) sh.cand[pos++] = SW::make(k, static_cast<uint32_t>(head + q * EPC + e));
-    }
-  }
-  if (has_e && ekey >= t0) sh.cand[pos] = SW::make(ekey, static_cast<uint32_t>(eidx));
-  row_sync<WPR>(grp);
-  if (sub != 0) return;
-  const int nc = static_cast<int>(total);
-  typename SortWord<K>::T s0, s1;
-  if (nc <= 32)
-    warp_sort_cand<K, 1>(sh.cand, nc, s0, s1);
-  else if (nc <= 64)
-    warp_sort_cand<K, 2>(sh.cand, nc, s0, s1);
-  else
-    warp_sort_cand<K, 4>(sh.cand, nc, s0, s1);
-  warp_tail<K>(p, r, w, s0, s1, w.k_eff, u24);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int i = static_cast<int>(threadIdx.x); i < p.n_streams; i += static_cast<int>(blockDim.x))
+    p.step_out[i] += p.n_steps;
+  if (threadIdx.x == 0) atomicExch(p.ticket, 0u);
 }
 
 // MAXNCH = most 16-byte chunks per lane of any row in the launch (1, 2, 4, 8
-// or 16) sizes the shared-memory stage; every row runs the same body with
-// its own chunk count.  WPR = warps per row (1, 2 or 4): a block of four
-// warps samples 4 / WPR rows.
+// or 16) sizes the stage; WPR = warps per row (1, 2 or 4).  A block of four
+// warps holds 4 / WPR row groups; a group walks its rows in batches of 32.
 template <class K, int MAXNCH, int WPR>
-__global__ void __launch_bounds__(kTowerThreads, WPR == 4 ? 9 : 1) row_sampler_kernel(const Params p) {
+__global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Params p) {
+  using SW = SortWord<K>;
+  using T = typename SW::T;
+  using LN = Lane<K>;
+  using Acc = typename LN::Acc;
   constexpr int EPC = K::kPerChunk;
   constexpr int RPB = kTowerWarps / WPR;
-  __shared__ __align__(16) TowerShared<K, MAXNCH> shared_rows[RPB];
+  constexpr int NCHW = (MAXNCH + WPR - 1) / WPR;          // chunk columns per warp
+  constexpr int CPM = LN::kChunksPerMap;
+  constexpr int AW = acc_words<K>();
+  __shared__ __align__(16) TowerShared<K, MAXNCH, WPR> shared_rows[RPB];
+  // each warp's copy of its batch's row parameters (lane i: the i-th row)
+  __shared__ __align__(16) RowParams batch_rows[kTowerWarps][32];
   const int warp = static_cast<int>(threadIdx.x) >> 5;
   const int grp = warp / WPR, sub = warp % WPR;
   const uint32_t lane = lane_id();
-  const int r = static_cast<int>(blockIdx.x) * RPB + grp;
+  TowerShared<K, MAXNCH, WPR> &sh = shared_rows[grp];
+  const int64_t total = static_cast<int64_t>(p.n_rows) * p.n_steps;
+  const int64_t n_groups = static_cast<int64_t>(gridDim.x) * RPB;
   pdl_wait_and_release();
-  if (r >= p.n_rows) return;  // every warp of the row: its barriers are not reached
-  const Row w = load_row(p, r);
-  if (w.err) {
-    if (sub == 0 && lane == 0) finish_row(p, r, w, -1, w.err);
-    return;
+
+  int seen_step = -1;      // last step whose ready flag this warp has checked
+  bool step_ok = true;     // that step's flag was seen set
+  bool gave_up = false;    // a flag did not come in time: later flags get one look
+  bool first_row = true;
+#pragma unroll 1
+  // batches of B consecutive rows (B <= 32, about the rows per group): batch
+  // k covers rows [k B, k B + B), and group g takes batches g, g + G, ...
+  // Consecutive rows mix a frame's codebooks, so the groups' loads match
+  const int64_t per_group = (total + n_groups - 1) / n_groups;
+  const int bsz = per_group < 32 ? static_cast<int>(per_group) : 32;
+#pragma unroll 1
+  for (int64_t base = (static_cast<int64_t>(blockIdx.x) * RPB + grp) * bsz; base < total;
+       base += n_groups * bsz) {
+    const int nb = total - base < bsz ? static_cast<int>(total - base) : bsz;
+    // lane i: the parameters of the batch's i-th row
+    RowParams *rows = batch_rows[warp];
+    // every warp of a group loads its own copy: no barrier before the rows
+    if (static_cast<int>(lane) < nb) rows[lane] = load_params(p, base + lane);
+    __syncwarp();
+    bool drawn = false;
+#pragma unroll 1
+    for (int i = 0; i < nb; ++i) {
+      const uint32_t meta = rows[i].meta;
+      const int wstep = rows[i].s;
+      // a group sharing a row: the previous row's readers of the stage and
+      // the candidate words are done before they are overwritten
+      if (WPR > 1 && !first_row) row_sync<WPR>(grp);
+      first_row = false;
+      uint32_t err = meta_err(meta);
+      if (!err && p.ready) {
+        // warp 0 waits for the step's flag and tells the group (every warp
+        // of the group takes this branch for the same rows).  After its
+        // first flag that did not come in time, a group only looks at the
+        // later steps' flags once, without waiting.
+        if (wstep != seen_step) {
+          seen_step = wstep;
+          if (sub == 0) {
+            const bool ok = wait_ready(p.ready + wstep, gave_up ? 0ull : p.ready_timeout_ns);
+            if (lane == 0) sh.xready = ok ? 1u : 0u;
+          }
+          row_sync<WPR>(grp);
+          step_ok = sh.xready != 0u;
+          gave_up |= !step_ok;
+        }
+        if (!step_ok) err = kRowNotReady;
+      }
+      // ---- this warp's columns into the stage, all copies in flight ----
+      const int V = meta_vocab(meta);
+      const int64_t woff = rows[i].off;
+      const char *rowp = static_cast<const char *>(p.logits) + woff * K::kElemBytes;
+      const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
+      int head = static_cast<int>(((16u - (addr & 15u)) & 15u) / K::kElemBytes);
+      head = min(head, V);
+      const int nq = err ? 0 : (V - head) / EPC;
+      const int tail = V - head - nq * EPC;
+      const int nch = min((nq + 31) >> 5, MAXNCH);
+      const char *body = rowp + head * K::kElemBytes;
+      if (!err) {
+#pragma unroll
+        for (int c = 0; c < NCHW; ++c) {
+          const int j = sub + c * WPR;
+          if (j >= nch) break;  // uniform: narrower rows leave the unrolled loop early
+          const int q = static_cast<int>(lane) + 32 * j;
+          if (q < nq) cp_async16(&sh.stage[q], body + static_cast<size_t>(q) * 16);
+        }
+      }
+      // the batch's draws, while the first row's copies are in flight: lane
+      // i of the group's last warp draws for the batch's i-th row
+      if (!drawn) {
+        drawn = true;
+        if (sub == WPR - 1) {
+          uint32_t u24 = 0;
+          if (static_cast<int>(lane) < nb) {
+            const RowParams &mine = rows[lane];
+            if (!meta_err(mine.meta) && !meta_greedy(mine.meta)) {
+              const int r = mine.r;
+              const int64_t stepv = p.step[p.row_stream[r]] + mine.s;
+              u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(stepv),
+                               static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
+            }
+          }
+          sh.xu[lane] = u24;
+        }
+      }
+      if (err) {
+        const int wr = rows[i].r;
+        if (sub == 0 && lane == 0)
+          row_outputs(p, wr, static_cast<int64_t>(wstep) * p.out_step_stride + wr, -1, -1, -1, err);
+        continue;
+      }
+      // head / tail element of this lane of warp 0 (at most 7 + 7 of them)
+      int eidx = 0x7FFFFFFF;
+      if (sub == 0) {
+        if (static_cast<int>(lane) < head)
+          eidx = static_cast<int>(lane);
+        else if (static_cast<int>(lane) < head + tail)
+          eidx = nq * EPC + static_cast<int>(lane);
+      }
+      const bool has_e = eidx < V;
+      const uint32_t ekey = has_e ? K::key(K::load_one(rowp, eidx)) : 0u;
+      cp_async_wait_all();
+      __syncwarp();
+
+      // ---- the two largest logits of each of the lane's two streams ----
+      Acc acc = LN::init();
+#pragma unroll
+      for (int c = 0; c < NCHW; ++c) {
+        const int j = sub + c * WPR;
+        if (j >= nch) break;
+        const int q = static_cast<int>(lane) + 32 * j;
+        if (q < nq) LN::fold_chunk(sh.stage[q], acc);
+      }
+      if constexpr (WPR > 1) {
+        if (sub > 0) LN::store(&sh.xacc[((sub - 1) * 32 + lane) * AW], acc);
+        row_sync<WPR>(grp);
+      }
+      const int kq = meta_keff(meta);
+      uint32_t t0 = 0, top = 0;
+      bool bad = false;
+      if (sub == 0) {
+        if constexpr (WPR > 1) {
+#pragma unroll
+          for (int s2 = 1; s2 < WPR; ++s2) LN::merge(acc, LN::load(&sh.xacc[((s2 - 1) * 32 + lane) * AW]));
+        }
+        uint32_t sk[4];
+        LN::sample_keys(acc, sk);
+        // a NaN anywhere in the row reaches a lane's first maxima; +inf
+        // (or a positive NaN) is the row's maximum
+        const uint32_t ex = has_e ? ekey : 0u;
+        bad = __any_sync(0xFFFFFFFFu, LN::has_nan(acc) ||
+                                          (has_e && (ekey < K::kNegInf || ekey >= K::kPosInf)));
+        uint32_t t1 = max(sk[0], sk[1]), t2 = max(min(sk[0], sk[1]), max(sk[2], sk[3]));
+        if (has_e) {
+          t2 = max(t2, min(t1, ex));
+          t1 = max(t1, ex);
+        }
+        top = warp_max(t1);
+        bad = bad || top >= K::kPosInf;
+        if (!bad && top > K::kNegInf) {
+          // ---- the k_eff-th largest sample key: a lower bound ----
+          // every lane holds >= 1 (>= 2) sample keys >= its t1 (t2): the
+          // smallest t1 (t2) over the lanes has >= 32 (64) keys above it
+          const uint32_t lo = warp_min(kq <= 32 ? t1 : t2);
+          t0 = sample_kth<K>(acc, ex, __any_sync(0xFFFFFFFFu, has_e), kq, lo, top);
+        }
+        if (lane == 0) sh.xcnt = 0u;  // the row's candidate count
+        if constexpr (WPR > 1) {
+          if (lane == 0) {
+            sh.xt0 = t0;
+            sh.xtop = top;
+            sh.xbad[0] = bad ? 1u : 0u;
+          }
+        } else {
+          __syncwarp();
+        }
+      }
+      if constexpr (WPR > 1) {
+        row_sync<WPR>(grp);
+        t0 = sh.xt0;
+        top = sh.xtop;
+        bad = sh.xbad[0] != 0u;
+      }
+      if (bad || top <= K::kNegInf) {  // a NaN / +inf, or no finite logit
+        if (sub == 0 && lane == 0) {
+          const RowParams &rp = rows[i];
+          row_outputs(p, rp.r, static_cast<int64_t>(rp.s) * p.out_step_stride + rp.r, -1, -1, -1,
+                      kRowNonFinite);
+        }
+        continue;
+      }
+      // ---- candidates: the logits >= t0, CPM chunks (32 logits per lane) at
+      // a time: the group's map word per lane, a run of slots reserved with
+      // one shared atomic, the marked logits written out as sort words (in
+      // any order: they are sorted next) ----
+      const uint32_t t2 = LN::splat(t0);
+      const int ncol = sub < nch ? (nch - sub + WPR - 1) / WPR : 0;  // this warp's columns
+#pragma unroll 1
+      for (int g = 0; g * CPM < ncol; ++g) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int cs = 0; cs < CPM; ++cs) {
+          const int c = g * CPM + cs;
+          const int q = static_cast<int>(lane) + 32 * (sub + c * WPR);
+          if (c < ncol && q < nq) m |= LN::flags(sh.stage[q], t2, cs);
+        }
+        if (!__any_sync(0xFFFFFFFFu, m != 0u)) continue;
+        uint32_t at = m ? atomicAdd(&sh.xcnt, static_cast<uint32_t>(__popc(m))) : 0u;
+#pragma unroll 1
+        for (uint32_t fm = m; fm; fm &= fm - 1u) {
+          int cs, e;
+          LN::bit_elem(__ffs(fm) - 1, cs, e);
+          const int idx = (static_cast<int>(lane) + 32 * (sub + (g * CPM + cs) * WPR)) * EPC + e;
+          if (at < static_cast<uint32_t>(kWarpCandMax))
+            sh.u.cand[at] = SW::make(K::key(K::load_one(sh.stage, idx)),
+                                     static_cast<uint32_t>(head + idx));
+          ++at;
+        }
+      }
+      if (has_e && ekey >= t0) {
+        const uint32_t at = atomicAdd(&sh.xcnt, 1u);
+        if (at < static_cast<uint32_t>(kWarpCandMax))
+          sh.u.cand[at] = SW::make(ekey, static_cast<uint32_t>(eidx));
+      }
+      row_sync<WPR>(grp);
+      const uint32_t total_n = sh.xcnt;
+      const bool over = total_n > static_cast<uint32_t>(kWarpCandMax);
+      if (sub != 0) continue;
+      const TailParams tp = tail_params(p, rows[i]);
+      const uint32_t u24 = sh.xu[i];
+      int nc = static_cast<int>(total_n);
+      if (over) {
+        auto keys = [&](int q) {
+          const uint4 v = sh.stage[q];
+          return make_uint4(K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w));
+        };
+        warp_slow_select<K>(V, kq, sh.u.hist, sh.u.cand, keys, nq, head, tail, eidx, ekey);
+        nc = kq;
+      }
+      if (nc <= 32)
+        sort_and_tail<K, 1>(p, tp, sh.u.cand, nc, u24);
+      else if (nc <= 64)
+        sort_and_tail<K, 2>(p, tp, sh.u.cand, nc, u24);
+      else
+        sort_and_tail_128<K>(p, tp, sh.u.cand, nc, u24);
+    }
   }
-  const int V = w.vocab;
-  const char *rowp = static_cast<const char *>(p.logits) + w.off * K::kElemBytes;
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
-  int head = static_cast<int>(((16u - (addr & 15u)) & 15u) / K::kElemBytes);
-  head = min(head, V);
-  const int nq = (V - head) / EPC;
-  const int tail = V - head - nq * EPC;
-  TowerShared<K, MAXNCH> &sh = shared_rows[grp];
-  // the draw, on lane 0 (its result is needed only by the tail); a row
-  // shared by several warps has warp 1 compute it inside the body
-  uint32_t u24 = 0;
-  if (WPR == 1 && lane == 0 && !w.greedy)
-    u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
-                     static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
-  u24 = __shfl_sync(0xFFFFFFFFu, u24, 0);
-  tower_body<K, WPR>(p, r, w, u24, sh, head, nq, tail, rowp, min((nq + 31) >> 5, MAXNCH), sub,
-                     grp);
+  if (p.step_out) advance_steps_last_block(p);
 }
 
 }  // namespace ts

@@ -41,7 +41,8 @@
  * Every pointer in ts_batch is a DEVICE pointer owned by the caller and must
  * stay valid until the work queued on `stream` has run.  The library never
  * allocates, frees or synchronises inside ts_sample / ts_sample_debug /
- * ts_advance_steps, so those calls may be captured into a CUDA graph.  They
+ * ts_sample_steps / ts_advance_steps, so those calls may be captured into a
+ * CUDA graph.  They
  * run on the device that is current when they are called, which must be the
  * device the sampler was created on.
  */
@@ -100,8 +101,8 @@ typedef struct {
   const uint64_t *request;    /* [n_rows] Philox key word 1 */
   const int32_t *codebook;    /* [n_rows] Philox counter word 1 */
   const int32_t *row_stream;  /* [n_rows] index into step[] */
-  const int64_t *step;        /* [n_streams] Philox counter word 0; read only here,
-                                 advanced by ts_advance_steps */
+  int64_t *step;              /* [n_streams] Philox counter word 0 of the stream's
+                                 rows; written only when advance_steps is set */
   int32_t n_streams;
   const int32_t *eos_id;      /* [n_rows] EOS token of the row, -1 = none; may be NULL */
   int32_t *out_ids;           /* [n_rows] sampled token id, -1 on a row error */
@@ -110,6 +111,12 @@ typedef struct {
   const int32_t *feedback_slot; /* [n_rows] slot of the row in feedback_buf,
                                    -1 = none; required when feedback_buf is set */
   int64_t feedback_len;       /* elements in feedback_buf */
+  int32_t advance_steps;      /* nonzero: once every row of the call has read its
+                                 step, step[i] += 1 for i < n_streams (+= n_steps
+                                 for ts_sample_steps), as ts_advance_steps would do
+                                 after the call, but inside the call's own launch on
+                                 the warp path (its last block to finish does it) and
+                                 as one more small launch on the other paths */
 } ts_batch;
 
 /* Creates a sampler on CUDA device `device`.  max_top_k: 0 selects the
@@ -118,6 +125,8 @@ typedef struct {
  * workspace of ts_reserve, the only allocation the library makes).  Call it
  * before any stream capture. */
 ts_status ts_create(int device, int max_top_k, ts_sampler **out);
+/* (The status word shares its 8-byte allocation with the ticket counter that
+ * the warp path's fused step advance uses; both start at zero.) */
 
 /* Frees the sampler and its status word.  NULL is accepted. */
 ts_status ts_destroy(ts_sampler *s);
@@ -212,8 +221,48 @@ ts_status ts_reserve(ts_sampler *s, int32_t max_rows, int32_t max_row_vocab);
 ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *status,
                             void *stream);
 
+/* Several decode steps in one launch: ts_sample_steps samples st->n_steps
+ * steps of the batch `b` in step order, as that many ts_sample calls would,
+ * with step i of the launch (0 <= i < n_steps):
+ *   - reading its logits at element offset row_offsets[r] + i *
+ *     logits_step_stride of b->logits (rows reaching past logits_len are
+ *     errors),
+ *   - drawing with Philox counter word 0 = step[row_stream[r]] + i,
+ *   - writing out_ids / out_eos at i * out_step_stride + r and its frame at
+ *     feedback_buf[i * feedback_step_stride + feedback_slot[r]] (slots are
+ *     checked against feedback_len, the length of one frame).
+ * With b->advance_steps set, step[] grows by n_steps once the launch is done.
+ * It serves callers that queue several steps' logits ahead (their rows are
+ * streamed by one persistent grid, so the launch cost is paid once), and
+ * producers that finish steps one after another: with `ready` set, the rows
+ * of step i wait until ready[i] is nonzero (read with acquire semantics at
+ * system scope, so a flag written by the host or by a copy engine after the
+ * logits orders them).  A step's rows are sampled exactly when its flag is
+ * seen set; otherwise they get out_ids = -1, out_eos = 0, no write-back and
+ * the status bit TS_ROW_NOT_READY.  A warp waits at most ready_timeout_ns for
+ * a flag (0: one second; at most ten seconds), and after the first flag that
+ * has not come by then it looks at later flags only once, so a launch whose
+ * flags never come ends within about one limit.  No kernel waits on
+ * another kernel: a flag must be set by the host, by a copy, or before the
+ * launch.  Only the warp path runs it: top-k cap <= 64, rows of at most 4096
+ * bf16 / 2048 fp32 logits; anything else returns TS_ERR_UNSUPPORTED.
+ * Asynchronous and graph-capturable like ts_sample; ts_sample_debug has no
+ * multi-step form. */
+#define TS_ROW_NOT_READY 16u
+typedef struct {
+  int32_t n_steps;               /* >= 1 */
+  int64_t logits_step_stride;    /* elements from one step's logits to the next's */
+  int64_t out_step_stride;       /* entries from one step's outputs to the next's (>= n_rows) */
+  int64_t feedback_step_stride;  /* entries from one step's frame to the next's
+                                    (>= feedback_len when feedback_buf is set) */
+  const uint32_t *ready;         /* [n_steps] device-visible flags, or NULL: all ready */
+  uint64_t ready_timeout_ns;
+} ts_steps;
+ts_status ts_sample_steps(ts_sampler *s, const ts_batch *b, const ts_steps *st, void *stream);
+
 /* step[i] += 1 for i < n_streams, on the device (graph-capturable).  Call it
- * after the step's ts_sample so that sibling rows of one stream share a step. */
+ * after the step's ts_sample so that sibling rows of one stream share a step
+ * (or set ts_batch.advance_steps, which does the same inside the call). */
 ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream);
 
 /* Reads the OR of all row error bits since the last read, then clears it.
@@ -236,7 +285,7 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
  * TS_OPT_WIDE_EXACT: 1 makes paths 3 and 4 skip their sampled threshold and
  * always take their exact re-reading select (for tests).
  * TS_OPT_WARPS_PER_ROW: path 1's warps per row, 0 = automatic (4 for calls of
- * up to 4 rows per SM, 2 up to 16, else 1), or 1, 2 or 4.  Results never
+ * up to 1 row per SM, 2 up to 4, else 1), or 1, 2 or 4.  Results never
  * depend on any option. */
 #define TS_OPT_PATH 1
 #define TS_OPT_CLUSTER 2

@@ -1,0 +1,266 @@
+"""The fused step advance, the multi-step launch (ts_sample_steps) and the
+resident grid that walks several rows per row group, through the C ABI.
+
+* ts_batch.advance_steps: the step counters grow by one per call, inside the
+  warp path's own launch (its last block) or by one more launch on the other
+  paths; ids equal those of ts_sample followed by ts_advance_steps.
+* ts_sample_steps: R steps' logits in one buffer, sampled by one launch; every
+  step's ids, EOS flags and frame equal R separate ts_sample calls and, on
+  sampled steps, the oracle.
+* ready flags: a flag that never comes gives the step's rows -1 and the
+  TS_ROW_NOT_READY bit within the time limit; flags set by the host while the
+  launch runs are waited for.  Nothing here makes a kernel wait on another
+  kernel.
+"""
+import threading
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from parity import compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ts():
+    import codebook_token_sampling_gb300 as mod
+    return mod
+
+
+def _np_dtype(host):
+    return np.int16 if host["dtype"] == "bf16" else np.float32
+
+
+def _stacked(name, steps, first=0):
+    """`steps` consecutive steps of a workload: the first step's host batch and
+    one device buffer holding every step's logits back to back."""
+    hosts = [workloads.make(name, first + i) for i in range(steps)]
+    flat = np.concatenate([np.ascontiguousarray(h["logits"]) for h in hosts])
+    buf = torch.from_numpy(flat.view(_np_dtype(hosts[0]))).cuda()
+    return hosts, buf, int(np.asarray(hosts[0]["logits"]).size)
+
+
+@pytest.mark.parametrize("path", [1, 2, 4])
+def test_fused_advance_matches_separate(ts, path):
+    """Ten steps with advance_steps set vs ts_sample + ts_advance_steps."""
+    name = "drama3" if path == 1 else "mixed"
+    host = workloads.make(name, 0)
+    logits = [torch.from_numpy(np.ascontiguousarray(workloads.make(name, i)["logits"])
+                               .view(_np_dtype(host))).cuda() for i in range(3)]
+    outs = []
+    for fused in (True, False):
+        s = ts.Sampler(0, host["cap"])
+        if path == 4:
+            s.reserve(int(host["n_rows"]), int(host["max_row_vocab"]))
+        s.set_option(ts.TS_OPT_PATH, path)
+        b = ts.DeviceBatch(host, "cuda", advance_steps=fused)
+        ids = []
+        for i in range(10):
+            b.set_logits(logits[i % 3])
+            s.sample(b)
+            if not fused:
+                ts.ts_advance_steps(b.step)
+            ids.append(b.out_ids.clone())
+        torch.cuda.synchronize()
+        assert s.read_status() == 0
+        assert np.all(b.step.cpu().numpy() == np.asarray(host["step"]) + 10)
+        outs.append(torch.stack(ids).cpu().numpy())
+        s.close()
+    assert np.array_equal(outs[0], outs[1])
+    # step 7's rows against the oracle (step counters 7, logits of step 7 mod 3)
+    h = workloads.make(name, 7 % 3)
+    h["step"] = np.asarray(host["step"]) + 7
+    ref = oracle.sample(h, max_keep=h["cap"], n_threads=8)
+    safe = ref["margin"] > 1e-5
+    assert safe.sum() >= 0.9 * h["n_rows"]
+    assert np.array_equal(outs[0][7][safe], ref["ids"][safe])
+
+
+@pytest.mark.parametrize("wpr", [0, 1, 2, 4])
+@pytest.mark.parametrize("name,steps", [("drama3", 6), ("qwen3tts", 5), ("tiny", 9)])
+def test_sample_steps_matches_single_steps(ts, name, steps, wpr):
+    hosts, buf, per_step = _stacked(name, steps)
+    host = hosts[0]
+    n = int(host["n_rows"])
+    s = ts.Sampler(0, host["cap"])
+    if wpr:
+        s.set_option(ts.TS_OPT_WARPS_PER_ROW, wpr)
+    # separate calls, one per step
+    single = ts.DeviceBatch(host, "cuda")
+    want_ids, want_eos, want_fb = [], [], []
+    for i in range(steps):
+        single.set_logits(buf[i * per_step:(i + 1) * per_step])
+        s.sample(single)
+        ts.ts_advance_steps(single.step)
+        want_ids.append(single.out_ids.clone())
+        want_eos.append(single.out_eos.clone())
+        want_fb.append(single.feedback.clone())
+    # one launch over every step
+    multi = ts.DeviceBatch(host, "cuda", advance_steps=True)
+    multi.set_logits(buf)
+    out_ids = torch.full((steps, n), -3, dtype=torch.int32, device="cuda")
+    out_eos = torch.zeros((steps, n), dtype=torch.uint8, device="cuda")
+    fb_len = int(host["feedback_len"])
+    frames = torch.full((steps, fb_len), -3, dtype=torch.int32, device="cuda")
+    multi.c.out_ids = out_ids.data_ptr()
+    multi.c.out_eos = out_eos.data_ptr()
+    multi.c.feedback_buf = frames.data_ptr()
+    s.sample_steps(multi, steps, logits_step_stride=per_step, out_step_stride=n,
+                   feedback_step_stride=fb_len)
+    torch.cuda.synchronize()
+    assert s.read_status() == 0
+    assert np.array_equal(out_ids.cpu().numpy(), torch.stack(want_ids).cpu().numpy())
+    assert np.array_equal(out_eos.cpu().numpy(), torch.stack(want_eos).cpu().numpy())
+    assert np.array_equal(frames.cpu().numpy(), torch.stack(want_fb).cpu().numpy())
+    assert np.all(multi.step.cpu().numpy() == np.asarray(host["step"]) + steps)
+    # the last step against the oracle
+    h = dict(hosts[-1])
+    h["step"] = np.asarray(host["step"]) + steps - 1
+    ref = oracle.sample(h, max_keep=h["cap"], n_threads=8)
+    safe = ref["margin"] > 1e-5
+    assert safe.sum() >= 0.9 * n
+    assert np.array_equal(out_ids.cpu().numpy()[-1][safe], ref["ids"][safe])
+    s.close()
+
+
+def test_many_rows_per_group(ts):
+    """One ts_sample call over 64 steps' rows (81,920 rows: a resident grid
+    whose row groups walk many rows each) equals 64 separate calls."""
+    steps = 64
+    hosts, buf, per_step = _stacked("drama3", steps)
+    host = hosts[0]
+    n = int(host["n_rows"])
+    s = ts.Sampler(0, host["cap"])
+    # the 64 steps as one batch: rows r + i n read step i's logits
+    big = {k: v for k, v in host.items()}
+    big["logits"] = np.concatenate([np.asarray(h["logits"]) for h in hosts])
+    for k in ("row_vocab", "temp", "top_k", "top_p", "seed", "request", "codebook", "eos_id"):
+        big[k] = np.tile(np.asarray(host[k]), steps)
+    big["row_offsets"] = np.concatenate([np.asarray(host["row_offsets"]) + i * per_step
+                                         for i in range(steps)])
+    big["row_stream"] = np.concatenate([np.asarray(host["row_stream"]) + i * host["n_streams"]
+                                        for i in range(steps)]).astype(np.int32)
+    big["step"] = np.concatenate([np.asarray(host["step"]) + i for i in range(steps)])
+    big["n_streams"] = host["n_streams"] * steps
+    big["n_rows"] = n * steps
+    big["feedback_slot"] = np.arange(n * steps, dtype=np.int32)
+    big["feedback_len"] = n * steps
+    b = ts.DeviceBatch(big, "cuda")
+    plan = s.plan(b)
+    assert plan["path"] == 1 and plan["grid"] * (4 // plan["ctas_per_row"]) < n * steps
+    s.sample(b)
+    single = ts.DeviceBatch(host, "cuda")
+    want = []
+    for i in range(steps):
+        single.set_logits(buf[i * per_step:(i + 1) * per_step])
+        s.sample(single)
+        ts.ts_advance_steps(single.step)
+        want.append(single.out_ids.clone())
+    torch.cuda.synchronize()
+    assert s.read_status() == 0
+    assert np.array_equal(b.ids(), torch.cat(want).cpu().numpy())
+    s.close()
+
+
+def test_ready_flag_that_never_comes(ts):
+    """Steps 0, 1, 3 and 4 are ready, step 2 never is: step 2's rows get -1
+    and TS_ROW_NOT_READY within about one limit; the others are sampled."""
+    steps = 5
+    hosts, buf, per_step = _stacked("drama3", steps)
+    host = hosts[0]
+    n = int(host["n_rows"])
+    s = ts.Sampler(0, host["cap"])
+    b = ts.DeviceBatch(host, "cuda", feedback=False)
+    b.set_logits(buf)
+    out_ids = torch.full((steps, n), -3, dtype=torch.int32, device="cuda")
+    out_eos = torch.full((steps, n), 7, dtype=torch.uint8, device="cuda")
+    b.c.out_ids = out_ids.data_ptr()
+    b.c.out_eos = out_eos.data_ptr()
+    ready = torch.tensor([1, 1, 0, 1, 1], dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    s.sample_steps(b, steps, logits_step_stride=per_step, out_step_stride=n, ready=ready,
+                   ready_timeout_ns=2_000_000)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert elapsed < 5.0
+    assert s.read_status() == ts.TS_ROW_NOT_READY
+    got = out_ids.cpu().numpy()
+    assert np.all(got[2] == -1) and np.all(out_eos.cpu().numpy()[2] == 0)
+    assert np.all(got[[0, 1, 3, 4]] >= 0)
+    for i in (0, 1, 3, 4):
+        h = dict(hosts[i])
+        h["step"] = np.asarray(host["step"]) + i
+        ref = oracle.sample(h, max_keep=64, n_threads=8)
+        safe = ref["margin"] > 1e-5
+        assert np.array_equal(got[i][safe], ref["ids"][safe])
+    s.close()
+
+
+def test_ready_flags_set_by_the_host(ts):
+    """The launch starts with no step ready; a host thread sets the flags one
+    by one in pinned memory; every step is sampled as if it had been ready."""
+    steps = 4
+    hosts, buf, per_step = _stacked("qwen3tts", steps)
+    host = hosts[0]
+    n = int(host["n_rows"])
+    s = ts.Sampler(0, host["cap"])
+    b = ts.DeviceBatch(host, "cuda", feedback=False)
+    b.set_logits(buf)
+    out_ids = torch.full((steps, n), -3, dtype=torch.int32, device="cuda")
+    b.c.out_ids = out_ids.data_ptr()
+    eos = torch.zeros((steps, n), dtype=torch.uint8, device="cuda")
+    b.c.out_eos = eos.data_ptr()
+    flags = torch.zeros(steps, dtype=torch.int32).pin_memory()
+    torch.cuda.synchronize()
+
+    def producer():
+        for i in range(steps):
+            time.sleep(0.002)
+            flags[i] = 1
+
+    th = threading.Thread(target=producer)
+    s.sample_steps(b, steps, logits_step_stride=per_step, out_step_stride=n, ready=flags,
+                   ready_timeout_ns=2_000_000_000)
+    th.start()
+    torch.cuda.synchronize()
+    th.join()
+    assert s.read_status() == 0
+    # the same launch with every flag already set
+    ready = torch.ones(steps, dtype=torch.int32, device="cuda")
+    want = torch.full((steps, n), -3, dtype=torch.int32, device="cuda")
+    b.c.out_ids = want.data_ptr()
+    s.sample_steps(b, steps, logits_step_stride=per_step, out_step_stride=n, ready=ready)
+    torch.cuda.synchronize()
+    assert np.array_equal(out_ids.cpu().numpy(), want.cpu().numpy())
+    assert np.all(out_ids.cpu().numpy() >= 0)
+    s.close()
+
+
+def test_sample_steps_limits(ts):
+    """Outside the warp path, or with bad strides: a status, nothing launched."""
+    host = workloads.make("mixed", 0)  # cap 4096: not the warp path
+    s = ts.Sampler(0, host["cap"])
+    b = ts.DeviceBatch(host, "cuda")
+    with pytest.raises(ts.SamplerError) as e:
+        s.sample_steps(b, 2, logits_step_stride=0, out_step_stride=host["n_rows"],
+                       feedback_step_stride=host["feedback_len"])
+    assert e.value.status == ts.TS_ERR_UNSUPPORTED
+    s.close()
+    host = workloads.make("drama3", 0)
+    s = ts.Sampler(0, host["cap"])
+    b = ts.DeviceBatch(host, "cuda")
+    for kw in ({"n_steps": 0, "out_step_stride": host["n_rows"]},
+               {"n_steps": 2, "out_step_stride": host["n_rows"] - 1},
+               {"n_steps": 2, "out_step_stride": host["n_rows"], "feedback_step_stride": 1}):
+        n_steps = kw.pop("n_steps")
+        with pytest.raises(ts.SamplerError) as e:
+            s.sample_steps(b, n_steps, logits_step_stride=0, **kw)
+        assert e.value.status == ts.TS_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert np.all(b.ids() == -2)
+    s.close()
