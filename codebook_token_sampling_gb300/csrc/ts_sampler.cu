@@ -31,6 +31,7 @@ struct ts_sampler {
   uint32_t *status;   // device word (first of two: the status word, then the ticket)
   uint32_t *ticket;   // the warp path's fused step advance: blocks done so far
   int occ_warp[2][5][3];  // resident blocks per SM of each warp-path variant
+  int occ_seg[2];         // of the segmented 16-column, one-warp-per-row variant
   void *ws;           // split wide path workspace (ts_reserve), or null
   size_t ws_bytes;
   int ws_rows;        // row records it holds
@@ -82,6 +83,7 @@ struct Plan {
   int path;   // 1 warp(s) per row, 2 cluster, 3 wide, 4 split
   int nch;    // warp path: 16-byte chunks per lane
   int wpr;    // warp path: warps per row
+  int seg;    // warp path: 1 = the stage holds 8 of the 16 columns (segments)
   int g;      // cluster and wide paths: CTAs per row
   int slice;  // cluster and wide paths: elements per CTA
   int threads;
@@ -159,7 +161,14 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl, int n_step
     // that a resident grid whose groups walk several rows each
     const int ni = pl->nch == 1 ? 0 : pl->nch == 2 ? 1 : pl->nch == 4 ? 2 : pl->nch == 8 ? 3 : 4;
     const int occ = s->occ_warp[bf16 ? 1 : 0][ni][wpr == 1 ? 0 : wpr == 2 ? 1 : 2];
-    const long long resident = static_cast<long long>(s->num_sms) * std::max(occ, 1);
+    long long resident = static_cast<long long>(s->num_sms) * std::max(occ, 1);
+    // more rows than row groups on the GPU at once: the groups walk several
+    // rows each, and the 16-column variant stages 8 columns at a time (half
+    // the shared memory, so more warps per SM)
+    if (wpr == 1 && pl->nch == 16 && rows > resident * rpb) {
+      pl->seg = 1;
+      resident = static_cast<long long>(s->num_sms) * std::max(s->occ_seg[bf16 ? 1 : 0], 1);
+    }
     pl->grid = static_cast<int>(std::min<long long>((rows + rpb - 1) / rpb, resident));
     return TS_OK;
   }
@@ -246,7 +255,8 @@ void *warp_kernel_wpr(int nch) {
 }
 
 template <class K>
-void *warp_kernel_for(int nch, int wpr) {
+void *warp_kernel_for(int nch, int wpr, int seg = 0) {
+  if (seg) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 16, 1, 8>);
   if (wpr == 4) return warp_kernel_wpr<K, 4>(nch);
   if (wpr == 2) return warp_kernel_wpr<K, 2>(nch);
   return warp_kernel_wpr<K, 1>(nch);
@@ -325,6 +335,11 @@ ts_status warp_occupancy(ts_sampler *s) {
         s->occ_warp[d][i][k] = n;
       }
     }
+    int n = 0;
+    void *fn = d ? warp_kernel_for<ts::KeyBF16>(16, 1, 1) : warp_kernel_for<ts::KeyF32>(16, 1, 1);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, ts::kTowerThreads, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    s->occ_seg[d] = n;
   }
   return TS_OK;
 }
@@ -430,8 +445,8 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   }
   void *fn = nullptr;
   if (pl.path == 1) {
-    fn = bf16 ? warp_kernel_for<ts::KeyBF16>(pl.nch, pl.wpr)
-              : warp_kernel_for<ts::KeyF32>(pl.nch, pl.wpr);
+    fn = bf16 ? warp_kernel_for<ts::KeyBF16>(pl.nch, pl.wpr, pl.seg)
+              : warp_kernel_for<ts::KeyF32>(pl.nch, pl.wpr, pl.seg);
   } else if (pl.path == 3) {
     fn = wide_kernel_for(pl.g);
   } else {
@@ -557,6 +572,7 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->status = nullptr;
   s->ticket = nullptr;
   std::memset(s->occ_warp, 0, sizeof s->occ_warp);
+  std::memset(s->occ_seg, 0, sizeof s->occ_seg);
   s->ws = nullptr;
   s->ws_bytes = 0;
   s->ws_rows = 0;

@@ -338,13 +338,28 @@ __device__ __forceinline__ uint32_t sample_kth(const typename Lane<K>::Acc &a, u
   int b = 31 - __clz(diff);
   // the common prefix of lo and top, lower bits clear: <= lo
   uint32_t t16 = hi16 & ~((2u << b) - 1u);
-  const uint32_t need = 16u * static_cast<uint32_t>(kq);
+  const uint32_t need = static_cast<uint32_t>(kq);
+  // two bits per round: the counts at the three thresholds t16 + {1, 2, 3}
+  // << (b - 1), packed in 8-bit fields (at most 5 keys per lane, 160 per
+  // warp), go through one warp reduction
 #pragma unroll 1
-  for (; b >= 0; --b) {
-    const uint32_t c = (t16 | (1u << b)) << kShift;
-    uint32_t n = Lane<K>::count16_ge(a, c);
-    if (any_ex) n += ex >= c ? 16u : 0u;  // warp-uniform branch
-    if (warp_sum(n) >= need) t16 |= 1u << b;
+  for (; b >= 1; b -= 2) {
+    const uint32_t c1 = (t16 | (1u << (b - 1))) << kShift;
+    const uint32_t c2 = (t16 | (2u << (b - 1))) << kShift;
+    const uint32_t c3 = (t16 | (3u << (b - 1))) << kShift;
+    uint32_t n = (Lane<K>::count16_ge(a, c1) >> 4) | ((Lane<K>::count16_ge(a, c2) >> 4) << 8) |
+                 ((Lane<K>::count16_ge(a, c3) >> 4) << 16);
+    if (any_ex) n += (ex >= c1 ? 1u : 0u) + (ex >= c2 ? 0x100u : 0u) + (ex >= c3 ? 0x10000u : 0u);
+    const uint32_t tot = warp_sum(n);
+    const uint32_t step = (tot >> 16) >= need ? 3u : ((tot >> 8) & 0xFFu) >= need ? 2u
+                        : (tot & 0xFFu) >= need ? 1u : 0u;
+    t16 |= step << (b - 1);
+  }
+  if (b == 0) {
+    const uint32_t c = (t16 | 1u) << kShift;
+    uint32_t n = Lane<K>::count16_ge(a, c) >> 4;
+    if (any_ex) n += ex >= c ? 1u : 0u;
+    if (warp_sum(n) >= need) t16 |= 1u;
   }
   return t16 << kShift;
 }
@@ -358,6 +373,7 @@ struct RowParams {
   int64_t off;    // element offset of the row (its step's logits included)
   int32_t r;      // row of the batch
   int32_t s;      // step index within the launch
+  int32_t stream; // index into step[] (valid when the row has no shape error)
   uint32_t meta;  // vocab (bits 0-17) | k_eff (18-24) | greedy (25) | error bits (26-30)
   int32_t slot;   // write-back slot (its step's frame included), -1 = none
   int32_t eos;
@@ -386,6 +402,7 @@ __device__ __forceinline__ RowParams load_params(const Params &p, int64_t g) {
   w.temp = p.temp[r];
   w.top_p = p.top_p[r];
   const int32_t stream = p.row_stream[r];
+  w.stream = stream;
   const int32_t slot = p.feedback_buf ? p.feedback_slot[r] : -1;
   w.eos = p.eos_id ? p.eos_id[r] : -1;
   const int32_t tk = p.top_k[r];
@@ -735,12 +752,13 @@ __device__ __forceinline__ void warp_slow_select(int vocab, int k_eff, uint32_t 
   __syncwarp();
 }
 
-// Shared memory of one row group.  The slow path's histogram and the
-// candidate words are never live at once, so they share storage.
-template <class K, int MAXNCH, int WPR>
+// Shared memory of one row group: a stage of STG chunk columns (32 * STG
+// chunks).  The slow path's histogram and the candidate words are never live
+// at once, so they share storage.
+template <class K, int STG, int WPR>
 struct TowerShared {
   using T = typename SortWord<K>::T;
-  uint4 stage[32 * MAXNCH];
+  uint4 stage[32 * STG];
   union {
     T cand[kWarpCandMax];
     uint32_t hist[256];
@@ -771,25 +789,34 @@ __device__ __forceinline__ void row_sync(int grp) {
 // After every block of the launch has read step[]: the last block to arrive
 // adds n_steps to step_out[0 .. n_streams) and re-arms the ticket.  No block
 // waits for another; every thread of the block must reach this call.
+// The ticket is taken with an acquire-release atomic at GPU scope: the block's
+// reads of step[] (ordered before it by the block barrier) happen before the
+// last block's acquire, so its increments cannot reach a reader of this
+// launch.  The next launch in the stream sees them (and the re-armed ticket)
+// once this grid has completed.
 __device__ __forceinline__ void advance_steps_last_block(const Params &p) {
   __shared__ uint32_t last;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    last = atomicAdd(p.ticket, 1u) == gridDim.x - 1 ? 1u : 0u;
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(old) : "l"(p.ticket) : "memory");
+    last = old == gridDim.x - 1 ? 1u : 0u;
   }
   __syncthreads();
   if (!last) return;
-  __threadfence();
   for (int i = static_cast<int>(threadIdx.x); i < p.n_streams; i += static_cast<int>(blockDim.x))
     p.step_out[i] += p.n_steps;
-  if (threadIdx.x == 0) atomicExch(p.ticket, 0u);
+  if (threadIdx.x == 0) *p.ticket = 0u;
 }
 
 // MAXNCH = most 16-byte chunks per lane of any row in the launch (1, 2, 4, 8
-// or 16) sizes the stage; WPR = warps per row (1, 2 or 4).  A block of four
-// warps holds 4 / WPR row groups; a group walks its rows in batches of 32.
-template <class K, int MAXNCH, int WPR>
+// or 16); WPR = warps per row (1, 2 or 4); STG = chunk columns the stage
+// holds (MAXNCH, or fewer for one warp per row: wider rows then go through
+// the stage in segments of STG columns, read twice, the second time from L2;
+// a smaller stage lets more warps share an SM).  A block of four warps holds
+// 4 / WPR row groups; a group walks its rows in batches of up to 32.
+template <class K, int MAXNCH, int WPR, int STG = MAXNCH>
 __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Params p) {
   using SW = SortWord<K>;
   using T = typename SW::T;
@@ -800,13 +827,17 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
   constexpr int NCHW = (MAXNCH + WPR - 1) / WPR;          // chunk columns per warp
   constexpr int CPM = LN::kChunksPerMap;
   constexpr int AW = acc_words<K>();
-  __shared__ __align__(16) TowerShared<K, MAXNCH, WPR> shared_rows[RPB];
+  constexpr bool kSeg = STG < MAXNCH;
+  constexpr int NSEG = MAXNCH / STG;
+  static_assert(!kSeg || (WPR == 1 && MAXNCH % STG == 0 && STG % CPM == 0),
+                "segments: one warp per row, whole map words per segment");
+  __shared__ __align__(16) TowerShared<K, STG, WPR> shared_rows[RPB];
   // each warp's copy of its batch's row parameters (lane i: the i-th row)
   __shared__ __align__(16) RowParams batch_rows[kTowerWarps][32];
   const int warp = static_cast<int>(threadIdx.x) >> 5;
   const int grp = warp / WPR, sub = warp % WPR;
   const uint32_t lane = lane_id();
-  TowerShared<K, MAXNCH, WPR> &sh = shared_rows[grp];
+  TowerShared<K, STG, WPR> &sh = shared_rows[grp];
   const int64_t total = static_cast<int64_t>(p.n_rows) * p.n_steps;
   const int64_t n_groups = static_cast<int64_t>(gridDim.x) * RPB;
   pdl_wait_and_release();
@@ -815,7 +846,6 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
   bool step_ok = true;     // that step's flag was seen set
   bool gave_up = false;    // a flag did not come in time: later flags get one look
   bool first_row = true;
-#pragma unroll 1
   // batches of B consecutive rows (B <= 32, about the rows per group): batch
   // k covers rows [k B, k B + B), and group g takes batches g, g + G, ...
   // Consecutive rows mix a frame's codebooks, so the groups' loads match
@@ -868,15 +898,20 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
       const int tail = V - head - nq * EPC;
       const int nch = min((nq + 31) >> 5, MAXNCH);
       const char *body = rowp + head * K::kElemBytes;
-      if (!err) {
+      // this warp's column c is chunk column j = sub + c WPR of the row,
+      // chunk q = lane + 32 j, held in stage slot lane + 32 (j mod STG)
+      const auto issue = [&](int seg) {
 #pragma unroll
-        for (int c = 0; c < NCHW; ++c) {
+        for (int cc = 0; cc < (kSeg ? STG : NCHW); ++cc) {
+          const int c = seg * STG + cc;
           const int j = sub + c * WPR;
           if (j >= nch) break;  // uniform: narrower rows leave the unrolled loop early
           const int q = static_cast<int>(lane) + 32 * j;
-          if (q < nq) cp_async16(&sh.stage[q], body + static_cast<size_t>(q) * 16);
+          if (q < nq)
+            cp_async16(&sh.stage[lane + 32 * (j % STG)], body + static_cast<size_t>(q) * 16);
         }
-      }
+      };
+      if (!err) issue(0);
       // the batch's draws, while the first row's copies are in flight: lane
       // i of the group's last warp draws for the batch's i-th row
       if (!drawn) {
@@ -887,7 +922,7 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
             const RowParams &mine = rows[lane];
             if (!meta_err(mine.meta) && !meta_greedy(mine.meta)) {
               const int r = mine.r;
-              const int64_t stepv = p.step[p.row_stream[r]] + mine.s;
+              const int64_t stepv = p.step[mine.stream] + mine.s;
               u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(stepv),
                                static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
             }
@@ -915,14 +950,27 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
       __syncwarp();
 
       // ---- the two largest logits of each of the lane's two streams ----
-      Acc acc = LN::init();
+      // two independent running pairs (even and odd columns), then merged
+      Acc acc = LN::init(), acc_odd = LN::init();
 #pragma unroll
-      for (int c = 0; c < NCHW; ++c) {
-        const int j = sub + c * WPR;
-        if (j >= nch) break;
-        const int q = static_cast<int>(lane) + 32 * j;
-        if (q < nq) LN::fold_chunk(sh.stage[q], acc);
+      for (int seg = 0; seg < NSEG; ++seg) {
+        if (seg > 0) {  // the next segment over the same stage
+          if (seg * STG >= nch) break;
+          __syncwarp();
+          issue(seg);
+          cp_async_wait_all();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int cc = 0; cc < (kSeg ? STG : NCHW); ++cc) {
+          const int c = seg * STG + cc;
+          const int j = sub + c * WPR;
+          if (j >= nch) break;
+          const int q = static_cast<int>(lane) + 32 * j;
+          if (q < nq) LN::fold_chunk(sh.stage[lane + 32 * (j % STG)], (c & 1) ? acc_odd : acc);
+        }
       }
+      if (NCHW > 1) LN::merge(acc, acc_odd);
       if constexpr (WPR > 1) {
         if (sub > 0) LN::store(&sh.xacc[((sub - 1) * 32 + lane) * AW], acc);
         row_sync<WPR>(grp);
@@ -987,26 +1035,51 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
       // any order: they are sorted next) ----
       const uint32_t t2 = LN::splat(t0);
       const int ncol = sub < nch ? (nch - sub + WPR - 1) / WPR : 0;  // this warp's columns
+      // segments: the one in the stage first, then the others copied again
+      const int nseg = kSeg ? (ncol + STG - 1) / STG : 1;
+      constexpr int GPS = (kSeg ? STG : NCHW + CPM - 1) / CPM;  // map words per segment
 #pragma unroll 1
-      for (int g = 0; g * CPM < ncol; ++g) {
-        uint32_t m = 0;
-#pragma unroll
-        for (int cs = 0; cs < CPM; ++cs) {
-          const int c = g * CPM + cs;
-          const int q = static_cast<int>(lane) + 32 * (sub + c * WPR);
-          if (c < ncol && q < nq) m |= LN::flags(sh.stage[q], t2, cs);
+      for (int k = 0; k < nseg; ++k) {
+        const int seg = nseg - 1 - k;
+        if (k > 0) {
+          __syncwarp();
+          issue(seg);
+          cp_async_wait_all();
+          __syncwarp();
         }
-        if (!__any_sync(0xFFFFFFFFu, m != 0u)) continue;
-        uint32_t at = m ? atomicAdd(&sh.xcnt, static_cast<uint32_t>(__popc(m))) : 0u;
+        uint32_t bm[GPS];
+#pragma unroll
+        for (int g = 0; g < GPS; ++g) {
+          bm[g] = 0u;
+          if (seg * STG + g * CPM >= ncol) break;  // uniform
+#pragma unroll
+          for (int cs = 0; cs < CPM; ++cs) {
+            const int c = seg * STG + g * CPM + cs;
+            const int j = sub + c * WPR;
+            const int q = static_cast<int>(lane) + 32 * j;
+            if (c < ncol && q < nq) bm[g] |= LN::flags(sh.stage[lane + 32 * (j % STG)], t2, cs);
+          }
+        }
+        uint32_t mine_n = 0;
+#pragma unroll
+        for (int g = 0; g < GPS; ++g)
+          if (seg * STG + g * CPM < ncol) mine_n += __popc(bm[g]);
+        uint32_t at = mine_n ? atomicAdd(&sh.xcnt, mine_n) : 0u;
+#pragma unroll
+        for (int g = 0; g < GPS; ++g) {
+          if (seg * STG + g * CPM >= ncol) break;
 #pragma unroll 1
-        for (uint32_t fm = m; fm; fm &= fm - 1u) {
-          int cs, e;
-          LN::bit_elem(__ffs(fm) - 1, cs, e);
-          const int idx = (static_cast<int>(lane) + 32 * (sub + (g * CPM + cs) * WPR)) * EPC + e;
-          if (at < static_cast<uint32_t>(kWarpCandMax))
-            sh.u.cand[at] = SW::make(K::key(K::load_one(sh.stage, idx)),
-                                     static_cast<uint32_t>(head + idx));
-          ++at;
+          for (uint32_t fm = bm[g]; fm; fm &= fm - 1u) {
+            int cs, e;
+            LN::bit_elem(__ffs(fm) - 1, cs, e);
+            const int j = sub + (seg * STG + g * CPM + cs) * WPR;
+            const int q = static_cast<int>(lane) + 32 * j;
+            if (at < static_cast<uint32_t>(kWarpCandMax))
+              sh.u.cand[at] = SW::make(
+                  K::key(K::load_one(sh.stage, (lane + 32 * (j % STG)) * EPC + e)),
+                  static_cast<uint32_t>(head + q * EPC + e));
+            ++at;
+          }
         }
       }
       if (has_e && ekey >= t0) {
@@ -1022,8 +1095,10 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
       const uint32_t u24 = sh.xu[i];
       int nc = static_cast<int>(total_n);
       if (over) {
+        // the row's chunks from the stage, or (segmented) from memory again
         auto keys = [&](int q) {
-          const uint4 v = sh.stage[q];
+          const uint4 v = kSeg ? *reinterpret_cast<const uint4 *>(body + static_cast<size_t>(q) * 16)
+                               : sh.stage[q];
           return make_uint4(K::key_word(v.x), K::key_word(v.y), K::key_word(v.z), K::key_word(v.w));
         };
         warp_slow_select<K>(V, kq, sh.u.hist, sh.u.cand, keys, nq, head, tail, eidx, ekey);

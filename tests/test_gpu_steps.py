@@ -264,3 +264,87 @@ def test_sample_steps_limits(ts):
     torch.cuda.synchronize()
     assert np.all(b.ids() == -2)
     s.close()
+
+
+def _wide_edge_rows(n, seed):
+    """n rows of 2,900 to 4,096 bf16 logits at misaligned offsets: gaussian
+    rows with assorted parameters, huge ties (the slow path), -inf inside the
+    top-k set, and a few NaN / +inf rows."""
+    rng = np.random.default_rng(seed)
+    vals, offs, vocab, pos = [], [], [], 0
+    temp, top_k, top_p = [], [], []
+    for r in range(n):
+        v = int(rng.choice([4096, 4095, 4000, 2900]))
+        kind = r % 50
+        if kind == 7:
+            x = np.full(v, 0.75, np.float32)                       # all tied
+        elif kind == 13:
+            x = rng.choice([0.0, 0.5], v).astype(np.float32)        # huge ties
+        elif kind == 21:
+            x = np.full(v, -np.inf, np.float32)
+            x[rng.choice(v, 5, replace=False)] = rng.normal(0, 1, 5)
+        elif kind == 29:
+            x = rng.normal(0, 2, v).astype(np.float32)
+            x[int(rng.integers(0, v))] = np.nan
+        elif kind == 31:
+            x = rng.normal(0, 2, v).astype(np.float32)
+            x[int(rng.integers(0, v))] = np.inf
+        else:
+            x = rng.normal(0, 2, v).astype(np.float32)
+        g = int(rng.integers(0, 7))
+        vals.append(np.zeros(g, np.float32))
+        pos += g
+        offs.append(pos)
+        vals.append(x)
+        pos += v
+        vocab.append(v)
+        temp.append(float(rng.choice([1.0, 0.7, 0.0])))
+        top_k.append(int(rng.choice([30, 64, 1, 0])))
+        top_p.append(float(rng.choice([0.9, 1.0, 0.5])))
+    flat = np.concatenate(vals)
+    logits = workloads.to_bf16_bits(flat)
+    logits[np.isnan(flat)] = 0x7FC0
+    return {
+        "dtype": "bf16", "logits": logits, "n_rows": n, "n_streams": n, "n_codebooks": 1,
+        "row_vocab": np.array(vocab, np.int32), "row_offsets": np.array(offs, np.int64),
+        "max_row_vocab": 4096, "temp": np.array(temp, np.float32),
+        "top_k": np.array(top_k, np.int32), "top_p": np.array(top_p, np.float32),
+        "seed": rng.integers(0, 2**63, n, dtype=np.uint64), "request": np.arange(n, dtype=np.uint64),
+        "codebook": np.zeros(n, np.int32), "row_stream": np.arange(n, dtype=np.int32),
+        "step": np.full(n, 4, np.int64), "eos_id": np.full(n, 3, np.int32),
+        "feedback_slot": np.arange(n, dtype=np.int32), "feedback_len": n, "cap": 64,
+    }
+
+
+def test_segmented_stage_matches_unsegmented(ts):
+    """A launch with more rows than the GPU holds at once stages 4096-wide rows
+    in two segments (the second read again from L2; the slow path reads the
+    row back from memory).  Its ids, EOS flags, frame and status equal those
+    of the same rows sampled in slices small enough for the unsegmented
+    kernel, and a sample of rows equals the oracle."""
+    from parity import sub_batch
+    n = 12000
+    host = _wide_edge_rows(n, 77)
+    s = ts.Sampler(0, 64)
+    big = run_gpu(s, host)
+    slices = []
+    for a in range(0, n, 2000):
+        h = sub_batch(host, np.arange(a, min(n, a + 2000)))
+        h["step"] = np.full(h["n_rows"], 4, np.int64)
+        h["max_row_vocab"] = 4096
+        plan = s.plan(ts.DeviceBatch(h, "cuda"))
+        assert plan["path"] == 1 and plan["grid"] * 4 // plan["ctas_per_row"] >= h["n_rows"]
+        slices.append(run_gpu(s, h))
+    assert np.array_equal(big["ids"], np.concatenate([x["ids"] for x in slices]))
+    assert np.array_equal(big["eos"], np.concatenate([x["eos"] for x in slices]))
+    assert big["status"] == (ts.TS_ROW_NONFINITE if big["status"] else 0)
+    assert big["status"] == ts.TS_ROW_NONFINITE  # the NaN / +inf rows
+    rows = np.concatenate([np.arange(0, 400), np.arange(n - 100, n)])
+    sub = sub_batch(host, rows)
+    sub["max_row_vocab"] = 4096
+    ref = oracle.sample(sub, max_keep=64, n_threads=8)
+    safe = ref["margin"] > 1e-5
+    assert safe.sum() >= 0.9 * rows.size
+    assert np.array_equal(big["ids"][rows][safe], ref["ids"][safe])
+    assert np.all(big["ids"][rows][ref["err"] != 0] == -1)
+    s.close()
