@@ -77,6 +77,11 @@ class _Batch(ctypes.Structure):
         ("n_nucleus", ctypes.c_void_p),
         ("margin", ctypes.c_void_p),
         ("u24_used", ctypes.c_void_p),
+        ("stop_step", ctypes.c_void_p),
+        ("max_steps", ctypes.c_void_p),
+        ("finish_reason", ctypes.c_void_p),
+        ("pad_id", ctypes.c_int32),
+        ("row_finished", ctypes.c_void_p),
     ]
 
 
@@ -172,7 +177,8 @@ def draw_map(values, temp: float, top_k: int, top_p: float, cap_value: int):
 
 
 def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,
-            feedback_buf=None):
+            feedback_buf=None, stop_step=None, max_steps=None, finish_reason=None,
+            pad_id: int = -1):
     """Sample every row of ``batch`` (a dict of numpy arrays, see ``workloads``).
 
     Returns a dict with ``ids`` (int32), ``eos`` (uint8), ``err`` (uint32 per-row
@@ -180,6 +186,12 @@ def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,
     kept set ``kept_ids`` / ``kept_probs`` (fp64), ``n_kept``, ``n_nucleus`` and
     ``margin`` (distance of the draw or of top_p from the nearest boundary).
     ``feedback_buf`` (int32, modified in place) receives the write-back.
+    Finished streams (the handbook's EOS-starvation section): ``stop_step``
+    (int64 per stream, < 0 = running; updated in place when a row draws its
+    EOS) and ``max_steps`` (int64 per stream, the length cap on the stream's
+    step) make a stream's rows draw nothing and return ``pad_id``;
+    ``finish_reason`` (uint8 per stream, updated in place) gets 1 (stop) or 2
+    (length).  The result then also holds ``finished`` (uint8 per row).
     """
     n = int(batch["n_rows"])
     keep = {}
@@ -210,6 +222,21 @@ def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,
         assert u.size == n
         keep["u24"] = u
         b.u24_override = u.ctypes.data
+    finished = None
+    if stop_step is not None or max_steps is not None:
+        finished = np.zeros(n, np.uint8)
+        b.row_finished = finished.ctypes.data
+        b.pad_id = int(pad_id)
+        if stop_step is not None:
+            assert stop_step.dtype == np.int64 and stop_step.flags.c_contiguous
+            b.stop_step = stop_step.ctypes.data
+        if max_steps is not None:
+            ms = _arr(max_steps, np.int64)
+            keep["max_steps"] = ms
+            b.max_steps = ms.ctypes.data
+        if finish_reason is not None:
+            assert finish_reason.dtype == np.uint8 and finish_reason.flags.c_contiguous
+            b.finish_reason = finish_reason.ctypes.data
     out = {"ids": np.zeros(n, np.int32), "eos": np.zeros(n, np.uint8),
            "err": np.zeros(n, np.uint32), "u24": np.zeros(n, np.uint32)}
     b.out_ids = out["ids"].ctypes.data
@@ -231,6 +258,8 @@ def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,
     rc = lib.oracle_sample(ctypes.byref(b), int(n_threads))
     if rc != 0:
         raise ValueError("oracle_sample rejected the batch (dtype or cap)")
+    if finished is not None:
+        out["finished"] = finished
     return out
 
 

@@ -23,7 +23,9 @@
  *              back into a buffer as the next step's input.
  *   [QT-eos]   same page, section "一个真实问题：说完了却停不下来": an EOS whose
  *              probability has collapsed to ~1e-14 and ranks outside top-k is
- *              never sampled.
+ *              never sampled; the serving side must report how a request
+ *              ended (stop at EOS, or length at the generation cap) and cap
+ *              the generation length.
  *   [Philox]   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
  *              as 1, 2, 3", SC'11: the Philox4x64 bijection, 10 rounds.
  *
@@ -289,7 +291,24 @@ typedef struct {
   int32_t *n_nucleus;  /* [n_rows] */
   double *margin;      /* [n_rows] min distance to a draw or cutoff boundary */
   uint32_t *u24_used;  /* [n_rows] */
+  /* finished streams [QT-eos] (each may be NULL: off) */
+  int64_t *stop_step;       /* [n_streams] step of the stream's EOS, < 0 = none */
+  const int64_t *max_steps; /* [n_streams] length cap on the stream's step */
+  uint8_t *finish_reason;   /* [n_streams] 0 running, 1 stop, 2 length */
+  int32_t pad_id;           /* id of a finished stream's rows */
+  uint8_t *row_finished;    /* [n_rows] scratch: the row's finish reason */
 } orc_batch;
+
+/* The finish rule [QT-eos], read for a row of stream s at step t:
+ * the stream stopped at an earlier step (its EOS was drawn at stop_step[s] <
+ * t) -> 1 (stop); else t reached the stream's length cap -> 2 (length);
+ * else 0 (the row is sampled).  A finished row draws nothing: it gets the
+ * pad id, no EOS flag, and writes the pad id back. */
+static int finish_rule(const orc_batch *b, int32_t stream, int64_t t) {
+  if (b->stop_step && b->stop_step[stream] >= 0 && b->stop_step[stream] < t) return 1;
+  if (b->max_steps && t >= b->max_steps[stream]) return 2;
+  return 0;
+}
 
 typedef struct {
   const orc_batch *b;
@@ -315,12 +334,26 @@ static void run_rows(const orc_batch *b, int64_t r0, int64_t r1, int32_t width) 
 
     orc_row row;
     memset(&row, 0, sizeof row);
-    if (!(err & ORC_ERR_BAD_SHAPE))
-      err |= prepare_row(b->dtype, b->logits, off, vocab, b->temp[r], b->top_k[r],
-                         b->top_p[r], b->cap, scratch, qbuf, &row);
     if (b->n_kept) b->n_kept[r] = 0;
     if (b->n_nucleus) b->n_nucleus[r] = 0;
     if (b->margin) b->margin[r] = INFINITY;
+    if (b->row_finished) b->row_finished[r] = 0;
+    /* a finished stream's row: the pad id, no draw (shape and slot errors
+     * still come first; its logits and parameters are not looked at) */
+    if (!err) {
+      int fin = finish_rule(b, stream, b->step[stream]);
+      if (fin) {
+        b->out_ids[r] = b->pad_id;
+        b->out_eos[r] = 0;
+        if (b->out_err) b->out_err[r] = 0;
+        if (b->feedback_buf && slot >= 0) b->feedback_buf[slot] = b->pad_id;
+        if (b->row_finished) b->row_finished[r] = (uint8_t)fin;
+        continue;
+      }
+    }
+    if (!(err & ORC_ERR_BAD_SHAPE))
+      err |= prepare_row(b->dtype, b->logits, off, vocab, b->temp[r], b->top_k[r],
+                         b->top_p[r], b->cap, scratch, qbuf, &row);
     if (err) {
       b->out_ids[r] = -1;
       b->out_eos[r] = 0;
@@ -363,15 +396,19 @@ static void *job_main(void *arg) {
 /* Samples every row of the batch.  Rows are independent, so they may be
  * spread over n_threads plain threads (the arithmetic per row is unchanged).
  * Returns 0, or -1 for an invalid cap / dtype. */
+static void apply_finish(const orc_batch *b);
+
 int oracle_sample(const orc_batch *b, int n_threads) {
   if (b->dtype != 0 && b->dtype != 1) return -1;
   if (b->cap < 1) return -1;
+  if ((b->stop_step || b->max_steps) && !b->row_finished) return -1;
   int32_t width = 1;
   for (int64_t r = 0; r < b->n_rows; ++r)
     if (b->row_vocab[r] > width && b->row_vocab[r] <= b->max_row_vocab)
       width = b->row_vocab[r];
   if (n_threads <= 1 || b->n_rows < 2 * (int64_t)n_threads) {
     run_rows(b, 0, b->n_rows, width);
+    apply_finish(b);
     return 0;
   }
   pthread_t *tids = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
@@ -386,7 +423,27 @@ int oracle_sample(const orc_batch *b, int n_threads) {
   for (int t = 0; t < n_threads; ++t) pthread_join(tids[t], NULL);
   free(tids);
   free(jobs);
+  apply_finish(b);
   return 0;
+}
+
+/* After every row of the call [QT-eos]: a stream whose EOS was drawn at this
+ * step records the step (its later steps are finished, reason stop), and
+ * finished rows report their reason for their stream.  Done after all rows,
+ * so no row of the call sees another row's update. */
+static void apply_finish(const orc_batch *b) {
+  for (int64_t r = 0; r < b->n_rows; ++r) {
+    int32_t stream = b->row_stream[r];
+    if (stream < 0 || stream >= b->n_streams) continue;
+    if (b->row_finished && b->row_finished[r]) {
+      if (b->finish_reason) b->finish_reason[stream] = b->row_finished[r];
+      continue;
+    }
+    if (b->out_ids[r] >= 0 && b->out_eos[r]) {
+      if (b->stop_step) b->stop_step[stream] = b->step[stream];
+      if (b->finish_reason) b->finish_reason[stream] = 1;
+    }
+  }
 }
 
 /* Exhaustive draw map of one row: counts[id] += 1 for every u24 in

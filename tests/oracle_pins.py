@@ -451,6 +451,84 @@ def pin_writeback_and_frame(orc):
     assert np.array_equal(o4["ids"], o1["ids"])
 
 
+def finish_workload(step, forced_eos):
+    """A small frame batch: 6 streams x 3 codebooks (codebook 0 of 64 tokens
+    with EOS 63, codebooks 1-2 of 32 tokens), gaussian logits; streams in
+    forced_eos[step] get a dominant EOS logit at this step."""
+    rng = np.random.default_rng(500 + step)
+    n_streams, q = 6, 3
+    vocab = [64, 32, 32]
+    rows = n_streams * q
+    rv = np.array([vocab[r % q] for r in range(rows)], np.int32)
+    ro = np.concatenate([[0], np.cumsum(rv[:-1])]).astype(np.int64)
+    x = rng.normal(0, 1.5, int(rv.sum())).astype(np.float32)
+    for s in forced_eos.get(step, ()):
+        x[ro[s * q] + 63] = 30.0
+    return {
+        "dtype": "f32", "logits": x, "n_rows": rows, "n_streams": n_streams,
+        "row_vocab": rv, "row_offsets": ro, "max_row_vocab": 64,
+        "temp": np.full(rows, 1.0, np.float32), "top_k": np.full(rows, 30, np.int32),
+        "top_p": np.full(rows, 0.9, np.float32),
+        "seed": np.repeat(np.arange(n_streams, dtype=np.uint64) + np.uint64(9), q),
+        "request": np.repeat(np.arange(n_streams, dtype=np.uint64), q),
+        "codebook": np.tile(np.arange(q, dtype=np.int32), n_streams),
+        "row_stream": np.repeat(np.arange(n_streams, dtype=np.int32), q),
+        "step": np.full(n_streams, step, np.int64),
+        "eos_id": np.tile(np.array([63, -1, -1], np.int32), n_streams),
+        "feedback_slot": np.arange(rows, dtype=np.int32), "feedback_len": rows, "cap": 64,
+    }
+
+
+def pin_finish_rule(orc):
+    """The finished-stream rule of the handbook's EOS-starvation section, against
+    its restatement on plain sampling: a stream whose EOS is drawn at step s
+    pads every row from step s + 1 (reason stop); a stream at or past its
+    length cap pads (reason length), unless it stopped earlier; a padded row
+    draws nothing, so every other row equals the plain run."""
+    steps, pad = 9, -7
+    forced = {2: (1,), 5: (3,), 6: (5,), 7: (1,)}
+    max_steps = np.array([100, 5, 4, 100, 100, 6], np.int64)
+    plain = [orc.sample(finish_workload(t, forced)) for t in range(steps)]
+    stop = np.full(6, -1, np.int64)
+    reason = np.zeros(6, np.uint8)
+    got = []
+    for t in range(steps):
+        fb = np.full(18, -9, np.int32)
+        got.append(orc.sample(finish_workload(t, forced), stop_step=stop, max_steps=max_steps,
+                              finish_reason=reason, pad_id=pad, feedback_buf=fb))
+        assert np.array_equal(fb, got[-1]["ids"]), t
+    # the restatement
+    want_stop = np.full(6, -1, np.int64)
+    want_reason = np.zeros(6, np.uint8)
+    for t in range(steps):
+        ids, eos = plain[t]["ids"].copy(), plain[t]["eos"].astype(bool)
+        for s in range(6):
+            rows = slice(3 * s, 3 * s + 3)
+            if 0 <= want_stop[s] < t:
+                fin = 1
+            elif t >= max_steps[s]:
+                fin = 2
+            else:
+                fin = 0
+            if fin:
+                assert np.all(got[t]["ids"][rows] == pad) and not np.any(got[t]["eos"][rows]), (t, s)
+                assert np.all(got[t]["finished"][rows] == fin), (t, s)
+                want_reason[s] = fin
+                continue
+            assert np.array_equal(got[t]["ids"][rows], ids[rows]), (t, s)
+            assert np.array_equal(got[t]["eos"][rows].astype(bool), eos[rows]), (t, s)
+            if np.any(eos[rows]):
+                want_stop[s] = t
+                want_reason[s] = 1
+    assert np.array_equal(stop, want_stop) and np.array_equal(reason, want_reason)
+    # the forced events happened as planned: stream 1 stops at step 2 (and
+    # stays stopped past its cap 5; its forced EOS at step 7 is never drawn),
+    # stream 3 stops at step 5, stream 2 runs out at step 4, and stream 5
+    # reaches its cap (6) at the step of its EOS
+    assert want_stop[1] == 2 and want_stop[3] == 5 and want_stop[5] < 0
+    assert list(want_reason[[1, 2, 3, 5]]) == [1, 2, 1, 2]
+
+
 PINS = [
     pin_philox_matches_numpy,
     pin_uniform24_mapping,
@@ -461,6 +539,7 @@ PINS = [
     pin_k_clamp,
     pin_error_rows,
     pin_writeback_and_frame,
+    pin_finish_rule,
     pin_nucleus_bruteforce,
     pin_margin_bruteforce,
     pin_draw_map_exact,

@@ -41,6 +41,16 @@ MUTANTS = {
     "cap_upper_4095": ("if (requested < 32 || requested > 4096) return -1;",
                        "if (requested < 32 || requested > 2048) return -1;"),
     "offset_check_dropped": ("off > b->logits_len - (int64_t)vocab)", "off > b->logits_len)"),
+    # the finished-stream rule
+    "finish_length_before_stop": (
+        "  if (b->stop_step && b->stop_step[stream] >= 0 && b->stop_step[stream] < t) return 1;\n"
+        "  if (b->max_steps && t >= b->max_steps[stream]) return 2;",
+        "  if (b->max_steps && t >= b->max_steps[stream]) return 2;\n"
+        "  if (b->stop_step && b->stop_step[stream] >= 0 && b->stop_step[stream] < t) return 1;"),
+    "finish_stop_recorded_late": ("if (b->stop_step) b->stop_step[stream] = b->step[stream];",
+                                  "if (b->stop_step) b->stop_step[stream] = b->step[stream] + 1;"),
+    "finish_cap_exclusive": ("if (b->max_steps && t >= b->max_steps[stream]) return 2;",
+                             "if (b->max_steps && t > b->max_steps[stream]) return 2;"),
     # the boundary margin that excuses rows from the bit-exact rule
     "margin_draw_unnormalised": ("double d = fabs(c - u);", "double d = fabs(cum - u);"),
     "margin_cut_exclusive_prefix": ("double d = fabs(cum - (double)top_p);",
