@@ -76,6 +76,10 @@ class TsBatch(ctypes.Structure):
         ("feedback_slot", ctypes.c_void_p),
         ("feedback_len", ctypes.c_int64),
         ("advance_steps", ctypes.c_int32),
+        ("stop_step", ctypes.c_void_p),
+        ("max_steps", ctypes.c_void_p),
+        ("finish_reason", ctypes.c_void_p),
+        ("pad_id", ctypes.c_int32),
     ]
 
 
@@ -325,7 +329,7 @@ class DeviceBatch:
     """
 
     def __init__(self, host: dict, device="cuda", feedback: bool = True,
-                 advance_steps: bool = False):
+                 advance_steps: bool = False, finish=None):
         import torch
         self.device = torch.device(device)
         self.dtype = TS_DTYPE_BF16 if host["dtype"] == "bf16" else TS_DTYPE_F32
@@ -353,6 +357,19 @@ class DeviceBatch:
         c.step = self.step.data_ptr()
         c.n_streams = int(host["n_streams"])
         c.advance_steps = 1 if advance_steps else 0
+        # finished streams: finish = {"max_steps": per-stream caps or None,
+        # "pad_id": int}; stop_step starts at -1 and finish_reason at 0
+        self.stop_step = self.max_steps = self.finish_reason = None
+        if finish is not None:
+            n_streams = int(host["n_streams"])
+            self.stop_step = torch.full((n_streams,), -1, dtype=torch.int64, device=self.device)
+            self.finish_reason = torch.zeros(n_streams, dtype=torch.uint8, device=self.device)
+            c.stop_step = self.stop_step.data_ptr()
+            c.finish_reason = self.finish_reason.data_ptr()
+            if finish.get("max_steps") is not None:
+                self.max_steps = _to_device(finish["max_steps"], np.int64, self.device)
+                c.max_steps = self.max_steps.data_ptr()
+            c.pad_id = int(finish.get("pad_id", -1))
         c.out_ids = self.out_ids.data_ptr()
         c.out_eos = self.out_eos.data_ptr()
         if self.feedback is not None:

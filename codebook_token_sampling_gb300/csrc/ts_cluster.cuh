@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
   pdl_wait_and_release();
   if (r >= p.n_rows) return;  // whole cluster (grid is sized exactly)
   const Row w = load_row(p, r);
-  if (w.err) {  // identical in every CTA of the cluster: all leave before any barrier
+  if (w.err || w.fin) {  // identical in every CTA of the cluster: all leave before any barrier
     if (rank == 0 && tid == 0) finish_row(p, r, w, -1, w.err);
     return;
   }

@@ -71,7 +71,28 @@ struct Params {
   // step_out[0 .. n_streams) and re-arms the ticket; null: no advance
   int64_t *step_out;
   uint32_t *ticket;
+  // finished streams (null: off): the step of a stream's EOS (< 0: none),
+  // the length cap on a stream's step, the finish reason per stream (1 stop,
+  // 2 length) and the id a finished stream's rows return
+  int64_t *stop_step;
+  const int64_t *max_steps;
+  uint8_t *finish_reason;
+  int32_t pad_id;
 };
+
+// The finish rule for a row of a stream at step t: its EOS was drawn at an
+// earlier step (1, stop), else t reached its length cap (2, length), else 0.
+// Rows of one step that draw EOS record t, which no row of step t reads as
+// finished: the rule gives every row of a step the same answer, in any
+// order of the rows.
+__device__ __forceinline__ uint32_t finish_rule(const Params &p, int32_t stream, int64_t t) {
+  if (p.stop_step) {
+    const int64_t s = p.stop_step[stream];
+    if (s >= 0 && s < t) return 1u;
+  }
+  if (p.max_steps && t >= p.max_steps[stream]) return 2u;
+  return 0u;
+}
 
 // ---------------------------------------------------------------------------
 // Order-preserving keys.  A float's bit pattern becomes an unsigned integer
@@ -330,6 +351,7 @@ __device__ __forceinline__ void dsmem_st_v2(uint32_t addr, uint32_t a, uint32_t 
 // ---------------------------------------------------------------------------
 struct Row {
   int64_t off;
+  int64_t stepv;  // the stream's step (Philox counter word 0)
   int32_t vocab;
   int32_t k_eff;
   int32_t stream;
@@ -339,6 +361,7 @@ struct Row {
   float inv_temp;
   float top_p;
   uint32_t err;
+  uint32_t fin;  // finished stream: 1 stop, 2 length (the row draws nothing)
   bool greedy;
 };
 
@@ -358,6 +381,13 @@ __device__ __forceinline__ Row load_row(const Params &p, int r) {
   if (w.stream < 0 || w.stream >= p.n_streams) e |= kRowBadShape;
   if (isnan(w.temp) || isinf(w.temp) || isnan(w.top_p)) e |= kRowBadParam;
   if (w.slot >= 0 && static_cast<int64_t>(w.slot) >= p.feedback_len) e |= kRowBadSlot;
+  w.stepv = 0;
+  w.fin = 0;
+  if (!(e & (kRowBadShape | kRowBadSlot))) {
+    w.stepv = p.step[w.stream];
+    w.fin = finish_rule(p, w.stream, w.stepv);
+    if (w.fin) e = 0;  // a finished row's logits and parameters are not looked at
+  }
   const int32_t tk = p.top_k[r];
   int32_t k = tk > 0 ? tk : w.vocab;
   k = min(k, p.cap);
@@ -371,6 +401,17 @@ __device__ __forceinline__ Row load_row(const Params &p, int r) {
 
 __device__ __forceinline__ void finish_row(const Params &p, int r, const Row &w, int32_t id,
                                            uint32_t err) {
+  if (!err && w.fin) {  // a finished stream: the pad id, no EOS flag
+    p.out_ids[r] = p.pad_id;
+    p.out_eos[r] = 0;
+    if (w.slot >= 0) p.feedback_buf[w.slot] = p.pad_id;
+    if (p.finish_reason) p.finish_reason[w.stream] = static_cast<uint8_t>(w.fin);
+    if (p.kept_ids) {
+      p.n_kept[r] = 0;
+      p.n_nucleus[r] = 0;
+    }
+    return;
+  }
   if (err) {
     p.out_ids[r] = -1;
     p.out_eos[r] = 0;
@@ -382,8 +423,13 @@ __device__ __forceinline__ void finish_row(const Params &p, int r, const Row &w,
     return;
   }
   p.out_ids[r] = id;
-  p.out_eos[r] = static_cast<uint8_t>(w.eos >= 0 && id == w.eos);
+  const bool eos = w.eos >= 0 && id == w.eos;
+  p.out_eos[r] = static_cast<uint8_t>(eos);
   if (w.slot >= 0) p.feedback_buf[w.slot] = id;
+  if (eos) {  // the stream stops: its rows pad from the next step on
+    if (p.stop_step) p.stop_step[w.stream] = w.stepv;
+    if (p.finish_reason) p.finish_reason[w.stream] = 1u;
+  }
 }
 
 }  // namespace ts

@@ -242,6 +242,10 @@ ts::Params make_params(const ts_sampler *s, const ts_batch *b) {
   p.status = s->status;
   p.n_steps = 1;
   p.out_step_stride = b->n_rows;
+  p.stop_step = b->stop_step;
+  p.max_steps = b->max_steps;
+  p.finish_reason = b->finish_reason;
+  p.pad_id = b->pad_id;
   return p;
 }
 
@@ -655,6 +659,9 @@ ts_status ts_sample_steps(ts_sampler *s, const ts_batch *b, const ts_steps *st, 
   const bool bf16 = b->dtype == TS_DTYPE_BF16;
   if (s->cap > 64 || b->max_row_vocab > (bf16 ? kWarpMaxBF16 : kWarpMaxF32))
     return TS_ERR_UNSUPPORTED;
+  // a later step's rows may run before an earlier step's EOS row: the
+  // finished-stream rule needs one step per call
+  if (b->stop_step || b->max_steps) return TS_ERR_UNSUPPORTED;
   if (s->force_path != 0 && s->force_path != 1) return TS_ERR_INVALID_ARG;
   ts::Params p = make_params(s, b);
   p.n_steps = st->n_steps;

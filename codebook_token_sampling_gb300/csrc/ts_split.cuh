@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kSplitThreads) split_threshold_kernel(const Pa
   SplitWs ws = split_ws(p.workspace, p.ws_rows, p.ws_units);
   const Row w = load_row(p, r);
   uint32_t t_key = 0;
-  if (!w.err && !p.wide_exact) {
+  if (!w.err && !w.fin && !p.wide_exact) {
     const char *rowp = static_cast<const char *>(p.logits) + w.off * 2;
     // a row the tail CTA can gather whole, in slices each CTA can hold,
     // keeps every logit (t = lowest key); others sample
@@ -818,7 +818,7 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_stream_kernel(const Pa
     return;
   }
   const Row w = load_row(p, r);
-  if (w.err) {  // kernel C reports it
+  if (w.err || w.fin) {  // kernel C reports it
     pdl_wait_and_release();
     return;
   }
@@ -980,15 +980,15 @@ __global__ void __launch_bounds__(kSplitThreads, 4) split_tail_kernel(const Para
   }
   // the inputs were complete before the threshold kernel started
   const Row w = load_row(p, r);
-  if (t == 32 && !w.err && !w.greedy)
-    misc[kWU24] = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(p.step[w.stream]),
+  if (t == 32 && !w.err && !w.fin && !w.greedy)
+    misc[kWU24] = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(w.stepv),
                              static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
   pdl_wait_and_release();  // the streaming kernel has finished
   if (t == 0) {  // the row's counter starts at zero for the next call
     SplitWs ws0 = split_ws(p.workspace, p.ws_rows, p.ws_units);
     ws0.row[r].count = 0u;
   }
-  if (w.err) {
+  if (w.err || w.fin) {
     if (t == 0) finish_row(p, r, w, -1, w.err);
     return;
   }

@@ -371,10 +371,12 @@ __device__ __forceinline__ uint32_t sample_kth(const typename Lane<K>::Acc &a, u
 // ---------------------------------------------------------------------------
 struct RowParams {
   int64_t off;    // element offset of the row (its step's logits included)
+  int64_t t;      // the row's step (Philox counter word 0)
   int32_t r;      // row of the batch
   int32_t s;      // step index within the launch
   int32_t stream; // index into step[] (valid when the row has no shape error)
-  uint32_t meta;  // vocab (bits 0-17) | k_eff (18-24) | greedy (25) | error bits (26-30)
+  uint32_t meta;  // vocab (bits 0-12) | k_eff (13-19) | greedy (20) | error bits (21-25)
+                  // | finish reason (26-27)
   int32_t slot;   // write-back slot (its step's frame included), -1 = none
   int32_t eos;
   float temp;
@@ -382,10 +384,11 @@ struct RowParams {
   float top_p;
 };
 
-__device__ __forceinline__ int meta_vocab(uint32_t m) { return static_cast<int>(m & 0x3FFFFu); }
-__device__ __forceinline__ int meta_keff(uint32_t m) { return static_cast<int>((m >> 18) & 0x7Fu); }
-__device__ __forceinline__ bool meta_greedy(uint32_t m) { return ((m >> 25) & 1u) != 0u; }
-__device__ __forceinline__ uint32_t meta_err(uint32_t m) { return m >> 26; }
+__device__ __forceinline__ int meta_vocab(uint32_t m) { return static_cast<int>(m & 0x1FFFu); }
+__device__ __forceinline__ int meta_keff(uint32_t m) { return static_cast<int>((m >> 13) & 0x7Fu); }
+__device__ __forceinline__ bool meta_greedy(uint32_t m) { return ((m >> 20) & 1u) != 0u; }
+__device__ __forceinline__ uint32_t meta_err(uint32_t m) { return (m >> 21) & 0x1Fu; }
+__device__ __forceinline__ uint32_t meta_fin(uint32_t m) { return m >> 26; }
 
 // The parameters of row g of the launch (row g mod n_rows of step g / n_rows).
 // Every check that the warp path needs is made here: a row whose width
@@ -412,18 +415,25 @@ __device__ __forceinline__ RowParams load_params(const Params &p, int64_t g) {
   if (vocab <= 0 || vocab > p.max_row_vocab || w.off > p.logits_len - static_cast<int64_t>(vocab))
     e |= kRowBadShape;
   if (stream < 0 || stream >= p.n_streams) e |= kRowBadShape;
+  uint32_t fin = 0;
+  w.t = 0;
   if (isnan(w.temp) || isinf(w.temp) || isnan(w.top_p)) e |= kRowBadParam;
   if (slot >= 0 && static_cast<int64_t>(slot) >= p.feedback_len) e |= kRowBadSlot;
   w.slot = slot >= 0 ? static_cast<int32_t>(slot + static_cast<int64_t>(s) * p.feedback_step_stride)
                      : -1;
-  const int32_t v = e ? 1 : vocab;
+  if (!(e & (kRowBadShape | kRowBadSlot))) {
+    w.t = p.step[stream] + s;
+    fin = finish_rule(p, stream, w.t);
+    if (fin) e = 0;  // a finished row's logits and parameters are not looked at
+  }
+  const int32_t v = (e || fin) ? 1 : vocab;
   int32_t k = tk > 0 ? tk : v;
   k = min(k, p.cap);
   k = min(k, v);
   const bool greedy = !(w.temp > 0.0f) || k == 1;
   w.inv_temp = greedy ? 1.0f : 1.0f / w.temp;
-  w.meta = static_cast<uint32_t>(v) | (static_cast<uint32_t>(k) << 18) |
-           (greedy ? (1u << 25) : 0u) | (e << 26);
+  w.meta = static_cast<uint32_t>(v) | (static_cast<uint32_t>(k) << 13) |
+           (greedy ? (1u << 20) : 0u) | (e << 21) | (fin << 26);
   return w;
 }
 
@@ -431,7 +441,8 @@ __device__ __forceinline__ RowParams load_params(const Params &p, int64_t g) {
 // error marks.  `out` = the row's output index; eos / slot are used only
 // without an error.
 __device__ __forceinline__ void row_outputs(const Params &p, int r, int64_t out, int32_t eos,
-                                            int32_t slot, int32_t id, uint32_t err) {
+                                            int32_t slot, int32_t id, uint32_t err,
+                                            int32_t stream = 0, int64_t t = 0) {
   if (err) {
     p.out_ids[out] = -1;
     p.out_eos[out] = 0;
@@ -443,13 +454,33 @@ __device__ __forceinline__ void row_outputs(const Params &p, int r, int64_t out,
     return;
   }
   p.out_ids[out] = id;
-  p.out_eos[out] = static_cast<uint8_t>(eos >= 0 && id == eos);
+  const bool is_eos = eos >= 0 && id == eos;
+  p.out_eos[out] = static_cast<uint8_t>(is_eos);
   if (slot >= 0) p.feedback_buf[slot] = id;
+  if (is_eos) {  // the stream stops: its rows pad from the next step on
+    if (p.stop_step) p.stop_step[stream] = t;
+    if (p.finish_reason) p.finish_reason[stream] = 1u;
+  }
+}
+
+// A finished stream's row: the pad id, no EOS flag, the reason.
+__device__ __forceinline__ void row_padded(const Params &p, int r, int64_t out, int32_t slot,
+                                           int32_t stream, uint32_t fin) {
+  p.out_ids[out] = p.pad_id;
+  p.out_eos[out] = 0;
+  if (slot >= 0) p.feedback_buf[slot] = p.pad_id;
+  if (p.finish_reason) p.finish_reason[stream] = static_cast<uint8_t>(fin);
+  if (p.kept_ids) {
+    p.n_kept[r] = 0;
+    p.n_nucleus[r] = 0;
+  }
 }
 
 // What the tail needs of a row, broadcast from the lane that loaded it.
 struct TailParams {
   int r;
+  int32_t stream;
+  int64_t t;
   int64_t out;
   int32_t slot, eos;
   float temp, inv_temp, top_p;
@@ -460,6 +491,8 @@ struct TailParams {
 __device__ __forceinline__ TailParams tail_params(const Params &p, const RowParams &a) {
   TailParams t;
   t.r = a.r;
+  t.stream = a.stream;
+  t.t = a.t;
   t.out = static_cast<int64_t>(a.s) * p.out_step_stride + a.r;
   t.slot = a.slot;
   t.eos = a.eos;
@@ -556,7 +589,8 @@ __device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
   for (int i = 1; i < R; ++i)
     if ((pick % R) == i) vp = v[i];
   const T pw = __shfl_sync(0xFFFFFFFFu, vp, pick / R);
-  if (lane == 0) row_outputs(p, w.r, w.out, w.eos, w.slot, static_cast<int32_t>(SW::idx(pw)), 0u);
+  if (lane == 0)
+    row_outputs(p, w.r, w.out, w.eos, w.slot, static_cast<int32_t>(SW::idx(pw)), 0u, w.stream, w.t);
 
   if (p.kept_ids) {
     const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
@@ -920,10 +954,9 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
           uint32_t u24 = 0;
           if (static_cast<int>(lane) < nb) {
             const RowParams &mine = rows[lane];
-            if (!meta_err(mine.meta) && !meta_greedy(mine.meta)) {
+            if (!meta_err(mine.meta) && !meta_fin(mine.meta) && !meta_greedy(mine.meta)) {
               const int r = mine.r;
-              const int64_t stepv = p.step[mine.stream] + mine.s;
-              u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(stepv),
+              u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(mine.t),
                                static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
             }
           }
@@ -934,6 +967,13 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
         const int wr = rows[i].r;
         if (sub == 0 && lane == 0)
           row_outputs(p, wr, static_cast<int64_t>(wstep) * p.out_step_stride + wr, -1, -1, -1, err);
+        continue;
+      }
+      if (meta_fin(meta)) {  // a finished stream: no draw
+        const RowParams &rp = rows[i];
+        if (sub == 0 && lane == 0)
+          row_padded(p, rp.r, static_cast<int64_t>(wstep) * p.out_step_stride + rp.r, rp.slot,
+                     rp.stream, meta_fin(meta));
         continue;
       }
       // head / tail element of this lane of warp 0 (at most 7 + 7 of them)

@@ -1245,7 +1245,7 @@ __global__ void __launch_bounds__(kWideThreads, 4) wide_sampler_kernel(const Par
   pdl_wait_and_release();
   if (r >= p.n_rows) return;  // whole cluster (grid is sized exactly)
   const Row w = load_row(p, r);
-  if (w.err) {  // identical in every CTA of the cluster: all leave before any barrier
+  if (w.err || w.fin) {  // identical in every CTA of the cluster: all leave before any barrier
     if (rank == 0 && t == 0) finish_row(p, r, w, -1, w.err);
     return;
   }

@@ -117,6 +117,23 @@ typedef struct {
                                  after the call, but inside the call's own launch on
                                  the warp path (its last block to finish does it) and
                                  as one more small launch on the other paths */
+  /* Finished streams (each pointer may be NULL: no stopping / no length cap /
+   * no reasons).  The serving side must report how a request ended, stop at
+   * its EOS or length at the generation cap, and cap the generation length
+   * ("案例一：Qwen3-TTS——三个 stage 与首包延迟", section "一个真实问题：说完了
+   * 却停不下来").  A row of stream s at step t = step[s] is finished when
+   * 0 <= stop_step[s] < t (reason 1, stop) or else when t >= max_steps[s]
+   * (reason 2, length).  A finished row draws nothing: out_ids = pad_id,
+   * out_eos = 0, the frame slot gets pad_id, finish_reason[s] = the reason;
+   * its logits and parameters are not read (shape and slot errors still
+   * apply).  A row that draws its EOS sets stop_step[s] = t and
+   * finish_reason[s] = 1, so the stream's rows pad from step t + 1 on; every
+   * row of step t gets the same answer whatever order the rows run in.
+   * ts_sample_steps does not take them (TS_ERR_UNSUPPORTED). */
+  int64_t *stop_step;         /* [n_streams] step of the stream's EOS, < 0 = running */
+  const int64_t *max_steps;   /* [n_streams] length cap on the stream's step */
+  uint8_t *finish_reason;     /* [n_streams] 0 running, 1 stop, 2 length */
+  int32_t pad_id;             /* id of a finished stream's rows */
 } ts_batch;
 
 /* Creates a sampler on CUDA device `device`.  max_top_k: 0 selects the
