@@ -82,6 +82,10 @@ class _Batch(ctypes.Structure):
         ("finish_reason", ctypes.c_void_p),
         ("pad_id", ctypes.c_int32),
         ("row_finished", ctypes.c_void_p),
+        ("hist_ring", ctypes.c_void_p),
+        ("hist_len", ctypes.c_int32),
+        ("hist_codebooks", ctypes.c_int32),
+        ("rep_penalty", ctypes.c_void_p),
     ]
 
 
@@ -178,7 +182,7 @@ def draw_map(values, temp: float, top_k: int, top_p: float, cap_value: int):
 
 def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,
             feedback_buf=None, stop_step=None, max_steps=None, finish_reason=None,
-            pad_id: int = -1):
+            pad_id: int = -1, hist_ring=None, rep_penalty=None):
     """Sample every row of ``batch`` (a dict of numpy arrays, see ``workloads``).
 
     Returns a dict with ``ids`` (int32), ``eos`` (uint8), ``err`` (uint32 per-row
@@ -192,6 +196,9 @@ def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,
     step) make a stream's rows draw nothing and return ``pad_id``;
     ``finish_reason`` (uint8 per stream, updated in place) gets 1 (stop) or 2
     (length).  The result then also holds ``finished`` (uint8 per row).
+    Repetition penalty (CTRL, Keskar et al. 2019): ``hist_ring`` (int32,
+    shape [n_streams, T, Q], updated in place with each row's draw at slot
+    step mod T) and ``rep_penalty`` (float32 per row).
     """
     n = int(batch["n_rows"])
     keep = {}
@@ -217,6 +224,15 @@ def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,
         b.feedback_len = feedback_buf.size
     b.cap = int(batch["cap"])
     b.max_row_vocab = int(batch.get("max_row_vocab", int(np.max(keep["row_vocab"], initial=1))))
+    if hist_ring is not None:
+        assert hist_ring.dtype == np.int32 and hist_ring.flags.c_contiguous and hist_ring.ndim == 3
+        b.hist_ring = hist_ring.ctypes.data
+        b.hist_len = hist_ring.shape[1]
+        b.hist_codebooks = hist_ring.shape[2]
+        rp = _arr(rep_penalty, np.float32)
+        assert rp.size == n
+        keep["rep_penalty"] = rp
+        b.rep_penalty = rp.ctypes.data
     if u24 is not None:
         u = _arr(u24, np.uint32)
         assert u.size == n

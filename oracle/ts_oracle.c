@@ -26,6 +26,12 @@
  *              never sampled; the serving side must report how a request
  *              ended (stop at EOS, or length at the generation cap) and cap
  *              the generation length.
+ *              The same section names a repetition penalty among the
+ *              sampling knobs (it cannot lift the starved EOS either).
+ *   [CTRL]     Keskar et al., "CTRL: A Conditional Transformer Language Model
+ *              for Controllable Generation", 2019: the repetition penalty
+ *              divides a previously generated token's logit by theta when it
+ *              is positive and multiplies it by theta otherwise.
  *   [Philox]   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
  *              as 1, 2, 3", SC'11: the Philox4x64 bijection, 10 rounds.
  *
@@ -155,11 +161,32 @@ static int effective_k(int32_t top_k, int32_t vocab, int32_t cap) {
   return (int)k;
 }
 
-/* Returns error bits (0 = the row is valid and `row` is filled). */
+/* bf16 round to nearest even of a float (finite or infinite). */
+static float round_to_bf16(float x) {
+  uint32_t u;
+  memcpy(&u, &x, sizeof u);
+  u = (u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u;
+  memcpy(&x, &u, sizeof x);
+  return x;
+}
+
+/* The repetition penalty [CTRL] on one logit, in fp32, the result rounded to
+ * the logits' type (bf16 for dtype 1): an in-place update of the row. */
+static double penalised(int dtype, double v, float theta) {
+  float f = (float)v; /* exact: v came from a bf16 or fp32 value */
+  float pen = f > 0.0f ? f / theta : f * theta;
+  if (dtype == 1) pen = round_to_bf16(pen);
+  return (double)pen;
+}
+
+/* Returns error bits (0 = the row is valid and `row` is filled).  `hist`
+ * lists the row's distinct previously generated tokens (n_hist of them, each
+ * in [0, vocab)), whose logits get the repetition penalty theta first. */
 static uint32_t prepare_row(int dtype, const void *logits, int64_t offset,
                             int32_t vocab, float temp, int32_t top_k,
                             float top_p, int32_t cap, orc_entry *scratch,
-                            double *qbuf, orc_row *row) {
+                            double *qbuf, orc_row *row, const int32_t *hist,
+                            int n_hist, float theta) {
   uint32_t err = 0;
   if (isnan(temp) || isinf(temp) || isnan(top_p)) err |= ORC_ERR_BAD_PARAM;
   int any_finite = 0, bad_value = 0;
@@ -172,6 +199,8 @@ static uint32_t prepare_row(int dtype, const void *logits, int64_t offset,
   }
   if (bad_value || !any_finite) err |= ORC_ERR_NONFINITE;
   if (err) return err;
+  for (int j = 0; j < n_hist; ++j)
+    scratch[hist[j]].value = penalised(dtype, scratch[hist[j]].value, theta);
 
   /* top-k by a full sort: value descending, lower index first on ties */
   qsort(scratch, (size_t)vocab, sizeof(orc_entry), cmp_desc_value_asc_index);
@@ -297,6 +326,15 @@ typedef struct {
   uint8_t *finish_reason;   /* [n_streams] 0 running, 1 stop, 2 length */
   int32_t pad_id;           /* id of a finished stream's rows */
   uint8_t *row_finished;    /* [n_rows] scratch: the row's finish reason */
+  /* repetition penalty over the frame history ([CTRL]; NULL ring: off):
+   * the token of stream s at codebook q drawn at step t sits in
+   * hist_ring[(s * hist_len + t % hist_len) * hist_codebooks + q] (< 0:
+   * empty); a row penalises the distinct tokens of its column, then writes
+   * its own draw into the slot of its step */
+  int32_t *hist_ring;
+  int32_t hist_len;
+  int32_t hist_codebooks;
+  const float *rep_penalty; /* [n_rows] theta (1: no penalty) */
 } orc_batch;
 
 /* The finish rule [QT-eos], read for a row of stream s at step t:
@@ -351,9 +389,30 @@ static void run_rows(const orc_batch *b, int64_t r0, int64_t r1, int32_t width) 
         continue;
       }
     }
+    /* the row's distinct history tokens in [0, vocab) and its penalty */
+    int32_t hist[64];
+    int n_hist = 0;
+    float theta = 1.0f;
+    int64_t ring_col = -1;
+    if (b->hist_ring && !(err & ORC_ERR_BAD_SHAPE)) {
+      int32_t q = b->codebook[r];
+      theta = b->rep_penalty[r];
+      if (q < 0 || q >= b->hist_codebooks) err |= ORC_ERR_BAD_SHAPE;
+      if (isnan(theta) || isinf(theta) || !(theta > 0.0f)) err |= ORC_ERR_BAD_PARAM;
+      if (!err) {
+        ring_col = (int64_t)stream * b->hist_len * b->hist_codebooks + q;
+        for (int32_t j = 0; j < b->hist_len; ++j) {
+          int32_t x = b->hist_ring[ring_col + (int64_t)j * b->hist_codebooks];
+          if (x < 0 || x >= vocab) continue;
+          int seen = 0;
+          for (int i = 0; i < n_hist; ++i) seen |= hist[i] == x;
+          if (!seen) hist[n_hist++] = x;
+        }
+      }
+    }
     if (!(err & ORC_ERR_BAD_SHAPE))
       err |= prepare_row(b->dtype, b->logits, off, vocab, b->temp[r], b->top_k[r],
-                         b->top_p[r], b->cap, scratch, qbuf, &row);
+                         b->top_p[r], b->cap, scratch, qbuf, &row, hist, n_hist, theta);
     if (err) {
       b->out_ids[r] = -1;
       b->out_eos[r] = 0;
@@ -371,6 +430,11 @@ static void run_rows(const orc_batch *b, int64_t r0, int64_t r1, int32_t width) 
     b->out_eos[r] = (uint8_t)(b->eos_id[r] >= 0 && id == b->eos_id[r]);
     if (b->out_err) b->out_err[r] = 0;
     if (b->feedback_buf && slot >= 0) b->feedback_buf[slot] = id;
+    if (ring_col >= 0) { /* this step's draw joins the column's history */
+      int64_t t = b->step[stream];
+      int64_t j = ((t % b->hist_len) + b->hist_len) % b->hist_len;
+      b->hist_ring[ring_col + j * b->hist_codebooks] = id;
+    }
     if (b->u24_used) b->u24_used[r] = u24;
     if (b->margin) b->margin[r] = fmin(margin_draw, row.margin_cut);
     if (b->n_kept) b->n_kept[r] = row.k_eff;
@@ -401,6 +465,9 @@ static void apply_finish(const orc_batch *b);
 int oracle_sample(const orc_batch *b, int n_threads) {
   if (b->dtype != 0 && b->dtype != 1) return -1;
   if (b->cap < 1) return -1;
+  if (b->hist_ring && (b->hist_len < 1 || b->hist_len > 64 || b->hist_codebooks < 1 ||
+                       !b->rep_penalty))
+    return -1;
   if ((b->stop_step || b->max_steps) && !b->row_finished) return -1;
   int32_t width = 1;
   for (int64_t r = 0; r < b->n_rows; ++r)
@@ -458,7 +525,7 @@ uint32_t oracle_draw_map(const double *values, int32_t vocab, float temp,
   orc_row row;
   memset(&row, 0, sizeof row);
   uint32_t err = prepare_row(2, values, 0, vocab, temp, top_k, top_p, cap,
-                             scratch, qbuf, &row);
+                             scratch, qbuf, &row, NULL, 0, 1.0f);
   if (!err) {
     for (int32_t i = 0; i < vocab; ++i) counts[i] = 0;
     for (uint32_t u24 = 0; u24 < (1u << 24); ++u24)

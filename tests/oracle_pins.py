@@ -529,6 +529,64 @@ def pin_finish_rule(orc):
     assert list(want_reason[[1, 2, 3, 5]]) == [1, 2, 1, 2]
 
 
+def pin_repetition_penalty(orc):
+    """The repetition penalty (CTRL, Keskar et al. 2019) over the frame history,
+    against its restatement: the penalised logits computed here with numpy
+    (fp32 division or product, then bf16 round to nearest even for bf16 rows,
+    once per distinct token of the row's history column) and sampled without
+    the penalty.  theta = 1 changes nothing; the draw joins the ring at slot
+    step mod T and no other slot changes."""
+    rng = np.random.default_rng(21)
+    t_len, q = 5, 3
+    for dtype in ("f32", "bf16"):
+        for step in (0, 7):
+            h = finish_workload(step, {1: (0,)})
+            n, n_streams = h["n_rows"], h["n_streams"]
+            x32 = rng.normal(0, 2, h["logits"].size).astype(np.float32)
+            x32[rng.choice(x32.size, 30, replace=False)] += 6.0
+            if dtype == "bf16":
+                h["dtype"] = "bf16"
+                h["logits"] = workloads.to_bf16_bits(x32)
+                xs = workloads.bf16_bits_to_f32(h["logits"])
+            else:
+                h["logits"] = x32
+                xs = x32
+            ring = rng.integers(-2, 70, (n_streams, t_len, q)).astype(np.int32)
+            ring[:, 1, :] = ring[:, 0, :]          # duplicates in every column
+            theta = rng.choice([1.0, 1.3, 2.5, 0.7], n).astype(np.float32)
+            before = ring.copy()
+            got = orc.sample(h, max_keep=64, hist_ring=ring, rep_penalty=theta)
+            # restatement
+            y = np.array(xs, np.float32).copy()
+            for r in range(n):
+                s_, c = r // q, r % q
+                v, o = int(h["row_vocab"][r]), int(h["row_offsets"][r])
+                for tok in set(int(t) for t in before[s_, :, c]):
+                    if 0 <= tok < v:
+                        f = np.float32(y[o + tok])
+                        pen = np.float32(f / theta[r]) if f > 0 else np.float32(f * theta[r])
+                        if dtype == "bf16":
+                            pen = workloads.bf16_bits_to_f32(workloads.to_bf16_bits(
+                                np.array([pen], np.float32)))[0]
+                        y[o + tok] = pen
+            h2 = dict(h)
+            h2["logits"] = workloads.to_bf16_bits(y) if dtype == "bf16" else y
+            if dtype == "bf16":
+                assert np.array_equal(workloads.bf16_bits_to_f32(h2["logits"]), y)
+            want = orc.sample(h2, max_keep=64)
+            for key in ("ids", "eos", "n_kept", "n_nucleus", "kept_ids", "kept_probs", "margin"):
+                assert np.array_equal(got[key], want[key]), (dtype, step, key)
+            # theta = 1 rows equal the run without any penalty
+            plain = orc.sample(h, max_keep=64)
+            one = theta == 1.0
+            assert np.array_equal(got["ids"][one], plain["ids"][one])
+            # the ring: each row's draw at slot step mod T, nothing else moved
+            after = before.copy()
+            for r in range(n):
+                after[r // q, step % t_len, r % q] = got["ids"][r]
+            assert np.array_equal(ring, after), (dtype, step)
+
+
 PINS = [
     pin_philox_matches_numpy,
     pin_uniform24_mapping,
@@ -540,6 +598,7 @@ PINS = [
     pin_error_rows,
     pin_writeback_and_frame,
     pin_finish_rule,
+    pin_repetition_penalty,
     pin_nucleus_bruteforce,
     pin_margin_bruteforce,
     pin_draw_map_exact,

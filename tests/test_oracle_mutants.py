@@ -51,6 +51,13 @@ MUTANTS = {
                                   "if (b->stop_step) b->stop_step[stream] = b->step[stream] + 1;"),
     "finish_cap_exclusive": ("if (b->max_steps && t >= b->max_steps[stream]) return 2;",
                              "if (b->max_steps && t > b->max_steps[stream]) return 2;"),
+    # the repetition penalty
+    "penalty_on_duplicates": ("          if (!seen) hist[n_hist++] = x;", "          hist[n_hist++] = x;"),
+    "penalty_divides_negatives": ("float pen = f > 0.0f ? f / theta : f * theta;",
+                                  "float pen = f / theta;"),
+    "penalty_not_rounded": ("  if (dtype == 1) pen = round_to_bf16(pen);", ""),
+    "penalty_ring_slot_late": ("int64_t j = ((t % b->hist_len) + b->hist_len) % b->hist_len;",
+                               "int64_t j = ((t + 1) % b->hist_len + b->hist_len) % b->hist_len;"),
     # the boundary margin that excuses rows from the bit-exact rule
     "margin_draw_unnormalised": ("double d = fabs(c - u);", "double d = fabs(cum - u);"),
     "margin_cut_exclusive_prefix": ("double d = fabs(cum - (double)top_p);",
