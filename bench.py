@@ -362,6 +362,65 @@ def time_multi_step(sampler, host, big, bufs, n_steps, repeats, stream, dev, l2)
     return times
 
 
+def level_batches(host, dev):
+    """One DeviceBatch per codebook level of a frame: the rows of codebook q
+    (one per stream) over the same step logits, their own write-back slots in
+    the frame; the last level's call advances the steps (a frame shares one
+    step).  The tower samples the levels one after another."""
+    import codebook_token_sampling_gb300 as ts
+    q = int(host["n_codebooks"])
+    cb = np.asarray(host["codebook"])
+    out = []
+    for level in range(q):
+        rows = np.nonzero(cb == level)[0]
+        h = dict(host)
+        for k in ("row_vocab", "row_offsets", "temp", "top_k", "top_p", "seed", "request",
+                  "codebook", "row_stream", "eos_id", "feedback_slot"):
+            h[k] = np.asarray(host[k])[rows]
+        h["n_rows"] = rows.size
+        h["max_row_vocab"] = int(np.max(h["row_vocab"]))
+        out.append(ts.DeviceBatch(h, dev, advance_steps=level == q - 1))
+    return out
+
+
+def time_levels(sampler, host, bufs, dev, k, repeats, stream):
+    """Per-level calls: each frame is one ts_sample call per codebook level (in
+    order, all in one CUDA graph of k frames over the step buffers).  Returns
+    per-frame times (s)."""
+    import torch
+    levels = level_batches(host, dev)
+    frame = levels[0].feedback
+    for b in levels[1:]:  # one frame buffer and one step counter for every level
+        b.feedback = frame
+        b.c.feedback_buf = frame.data_ptr()
+        b.step = levels[0].step
+        b.c.step = levels[0].step.data_ptr()
+    n_buf = len(bufs)
+    with torch.cuda.stream(stream):
+        for b in levels:
+            sampler.sample(b, stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(k):
+            for b in levels:
+                b.set_logits(bufs[i % n_buf])
+                sampler.sample(b)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    times = []
+    for _ in range(repeats):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3 / k)
+    return times, len(levels)
+
+
 def summarize(times):
     t = sorted(times)
     return {"us_median": 1e6 * statistics.median(t), "us_min": 1e6 * t[0], "us_max": 1e6 * t[-1],
@@ -414,6 +473,14 @@ def measure_config(args, name, rows, dev, l2, peak, k, w, repeats, num_sms, mult
         out["multi_step"] = ms
         out["multi_step_how"] = ("ts_sample_steps: R steps' rows in one launch of a resident grid "
                                  "(fused step advance), launches over distinct buffers")
+        if int(host["n_codebooks"]) > 1:
+            lt, q = time_levels(sampler, host, bufs, dev, min(k, 200), repeats, stream)
+            lm = summarize(lt)
+            out["per_level"] = {"calls_per_frame": q, "us_per_frame": lm["us_median"],
+                                "us_per_call": lm["us_median"] / q,
+                                "rows_per_call": int(host["n_streams"]),
+                                "how": "one ts_sample call per codebook level (the tower samples "
+                                       "the levels in order), k frames in one CUDA graph, median"}
     res = {"summary": out, "host": host, "hosts": hosts, "bufs": bufs, "big": big,
            "sampler": sampler, "batch": batch, "stream": stream, "times": times, "plan": plan}
     return res

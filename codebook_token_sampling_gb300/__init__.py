@@ -80,6 +80,10 @@ class TsBatch(ctypes.Structure):
         ("max_steps", ctypes.c_void_p),
         ("finish_reason", ctypes.c_void_p),
         ("pad_id", ctypes.c_int32),
+        ("hist_ring", ctypes.c_void_p),
+        ("hist_len", ctypes.c_int32),
+        ("hist_codebooks", ctypes.c_int32),
+        ("rep_penalty", ctypes.c_void_p),
     ]
 
 
@@ -329,7 +333,7 @@ class DeviceBatch:
     """
 
     def __init__(self, host: dict, device="cuda", feedback: bool = True,
-                 advance_steps: bool = False, finish=None):
+                 advance_steps: bool = False, finish=None, history=None):
         import torch
         self.device = torch.device(device)
         self.dtype = TS_DTYPE_BF16 if host["dtype"] == "bf16" else TS_DTYPE_F32
@@ -370,6 +374,18 @@ class DeviceBatch:
                 self.max_steps = _to_device(finish["max_steps"], np.int64, self.device)
                 c.max_steps = self.max_steps.data_ptr()
             c.pad_id = int(finish.get("pad_id", -1))
+        # repetition penalty: history = {"len": T, "codebooks": Q, "penalty":
+        # per-row theta}; the ring [n_streams, T, Q] starts empty (-1)
+        self.hist_ring = self.rep_penalty = None
+        if history is not None:
+            n_streams = int(host["n_streams"])
+            self.hist_ring = torch.full((n_streams, int(history["len"]), int(history["codebooks"])),
+                                        -1, dtype=torch.int32, device=self.device)
+            self.rep_penalty = _to_device(history["penalty"], np.float32, self.device)
+            c.hist_ring = self.hist_ring.data_ptr()
+            c.hist_len = int(history["len"])
+            c.hist_codebooks = int(history["codebooks"])
+            c.rep_penalty = self.rep_penalty.data_ptr()
         c.out_ids = self.out_ids.data_ptr()
         c.out_eos = self.out_eos.data_ptr()
         if self.feedback is not None:

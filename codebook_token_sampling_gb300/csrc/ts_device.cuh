@@ -78,6 +78,13 @@ struct Params {
   const int64_t *max_steps;
   uint8_t *finish_reason;
   int32_t pad_id;
+  // repetition penalty over the frame history (warp path; null ring: off):
+  // stream s, codebook q, step t at hist_ring[(s * hist_len + t mod
+  // hist_len) * hist_q + q]; the row's penalty theta in rep_penalty
+  int32_t *hist_ring;
+  int32_t hist_len;
+  int32_t hist_q;
+  const float *rep_penalty;
 };
 
 // The finish rule for a row of a stream at step t: its EOS was drawn at an
@@ -385,8 +392,10 @@ __device__ __forceinline__ Row load_row(const Params &p, int r) {
   w.fin = 0;
   if (!(e & (kRowBadShape | kRowBadSlot))) {
     w.stepv = p.step[w.stream];
-    w.fin = finish_rule(p, w.stream, w.stepv);
-    if (w.fin) e = 0;  // a finished row's logits and parameters are not looked at
+    if (p.stop_step || p.max_steps) {
+      w.fin = finish_rule(p, w.stream, w.stepv);
+      if (w.fin) e = 0;  // a finished row's logits and parameters are not looked at
+    }
   }
   const int32_t tk = p.top_k[r];
   int32_t k = tk > 0 ? tk : w.vocab;

@@ -104,6 +104,7 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl, int n_step
   int path = s->force_path;
   if (!path) path = warp_ok ? 1 : (bf16 && vmax > kWideMinVocab ? (split_ok ? 4 : 3) : 2);
   if (path == 1 && !warp_ok) return TS_ERR_INVALID_ARG;
+  if (b->hist_ring && path != 1) return TS_ERR_UNSUPPORTED;  // the penalty is on the warp path
   if (path == 3 && !bf16) return TS_ERR_INVALID_ARG;
   std::memset(pl, 0, sizeof *pl);
   pl->path = path;
@@ -165,7 +166,7 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl, int n_step
     // more rows than row groups on the GPU at once: the groups walk several
     // rows each, and the 16-column variant stages 8 columns at a time (half
     // the shared memory, so more warps per SM)
-    if (wpr == 1 && pl->nch == 16 && rows > resident * rpb) {
+    if (wpr == 1 && pl->nch == 16 && rows > resident * rpb && !b->hist_ring) {
       pl->seg = 1;
       resident = static_cast<long long>(s->num_sms) * std::max(s->occ_seg[bf16 ? 1 : 0], 1);
     }
@@ -211,6 +212,9 @@ ts_status check_batch(const ts_batch *b) {
     return TS_ERR_INVALID_ARG;
   if (b->n_streams == 0) return TS_ERR_INVALID_ARG;
   if (b->feedback_buf && !b->feedback_slot) return TS_ERR_INVALID_ARG;
+  if (b->hist_ring && (b->hist_len < 1 || b->hist_len > 32 || b->hist_codebooks < 1 ||
+                       !b->rep_penalty || !b->codebook))
+    return TS_ERR_INVALID_ARG;
   return TS_OK;
 }
 
@@ -246,6 +250,10 @@ ts::Params make_params(const ts_sampler *s, const ts_batch *b) {
   p.max_steps = b->max_steps;
   p.finish_reason = b->finish_reason;
   p.pad_id = b->pad_id;
+  p.hist_ring = b->hist_ring;
+  p.hist_len = b->hist_len;
+  p.hist_q = b->hist_codebooks;
+  p.rep_penalty = b->rep_penalty;
   return p;
 }
 
@@ -659,9 +667,10 @@ ts_status ts_sample_steps(ts_sampler *s, const ts_batch *b, const ts_steps *st, 
   const bool bf16 = b->dtype == TS_DTYPE_BF16;
   if (s->cap > 64 || b->max_row_vocab > (bf16 ? kWarpMaxBF16 : kWarpMaxF32))
     return TS_ERR_UNSUPPORTED;
-  // a later step's rows may run before an earlier step's EOS row: the
-  // finished-stream rule needs one step per call
-  if (b->stop_step || b->max_steps) return TS_ERR_UNSUPPORTED;
+  // a later step's rows may run before an earlier step's EOS row (or the
+  // earlier step's draw into the history): the finished-stream rule and the
+  // repetition penalty need one step per call
+  if (b->stop_step || b->max_steps || b->hist_ring) return TS_ERR_UNSUPPORTED;
   if (s->force_path != 0 && s->force_path != 1) return TS_ERR_INVALID_ARG;
   ts::Params p = make_params(s, b);
   p.n_steps = st->n_steps;

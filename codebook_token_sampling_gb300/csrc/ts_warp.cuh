@@ -364,6 +364,24 @@ __device__ __forceinline__ uint32_t sample_kth(const typename Lane<K>::Acc &a, u
   return t16 << kShift;
 }
 
+// The repetition penalty (Keskar et al. 2019, CTRL) on one logit's bits: a
+// positive logit divided by theta, another multiplied by it, in fp32, the
+// result rounded to the logits' type (nearest even for bf16).
+template <class K>
+__device__ __forceinline__ uint32_t penalised_bits(uint32_t bits, float theta);
+template <>
+__device__ __forceinline__ uint32_t penalised_bits<KeyBF16>(uint32_t bits, float theta) {
+  const float f = __uint_as_float(bits << 16);
+  const float pen = f > 0.0f ? __fdiv_rn(f, theta) : __fmul_rn(f, theta);
+  const __nv_bfloat16 h = __float2bfloat16_rn(pen);
+  return static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(&h));
+}
+template <>
+__device__ __forceinline__ uint32_t penalised_bits<KeyF32>(uint32_t bits, float theta) {
+  const float f = __uint_as_float(bits);
+  return __float_as_uint(f > 0.0f ? __fdiv_rn(f, theta) : __fmul_rn(f, theta));
+}
+
 // ---------------------------------------------------------------------------
 // One row's parameters, as one lane of the batch holds them.  The fields the
 // row body needs early (offset, width, k_eff, flags) are broadcast when the
@@ -375,6 +393,8 @@ struct RowParams {
   int32_t r;      // row of the batch
   int32_t s;      // step index within the launch
   int32_t stream; // index into step[] (valid when the row has no shape error)
+  int32_t cb;     // the row's codebook (its history column)
+  float pen;      // the row's repetition penalty (1: none)
   uint32_t meta;  // vocab (bits 0-12) | k_eff (13-19) | greedy (20) | error bits (21-25)
                   // | finish reason (26-27)
   int32_t slot;   // write-back slot (its step's frame included), -1 = none
@@ -421,7 +441,17 @@ __device__ __forceinline__ RowParams load_params(const Params &p, int64_t g) {
   if (slot >= 0 && static_cast<int64_t>(slot) >= p.feedback_len) e |= kRowBadSlot;
   w.slot = slot >= 0 ? static_cast<int32_t>(slot + static_cast<int64_t>(s) * p.feedback_step_stride)
                      : -1;
-  if (!(e & (kRowBadShape | kRowBadSlot))) {
+  w.cb = 0;
+  w.pen = 1.0f;
+  if (p.hist_ring) {  // the history column and the penalty
+    w.cb = p.codebook[r];
+    w.pen = p.rep_penalty[r];
+    if (w.cb < 0 || w.cb >= p.hist_q) e |= kRowBadShape;
+    if (isnan(w.pen) || isinf(w.pen) || !(w.pen > 0.0f)) e |= kRowBadParam;
+  }
+  // the finish rule and the history ring need the row's step now; without
+  // them the step is read by the draw, while the row's logits are on their way
+  if ((p.stop_step || p.max_steps || p.hist_ring) && !(e & (kRowBadShape | kRowBadSlot))) {
     w.t = p.step[stream] + s;
     fin = finish_rule(p, stream, w.t);
     if (fin) e = 0;  // a finished row's logits and parameters are not looked at
@@ -463,6 +493,13 @@ __device__ __forceinline__ void row_outputs(const Params &p, int r, int64_t out,
   }
 }
 
+// The row's draw joins its history column at the slot of its step.
+__device__ __forceinline__ void history_write(const Params &p, int32_t stream, int32_t cb,
+                                              int64_t t, int32_t id) {
+  const int64_t j = ((t % p.hist_len) + p.hist_len) % p.hist_len;
+  p.hist_ring[(static_cast<int64_t>(stream) * p.hist_len + j) * p.hist_q + cb] = id;
+}
+
 // A finished stream's row: the pad id, no EOS flag, the reason.
 __device__ __forceinline__ void row_padded(const Params &p, int r, int64_t out, int32_t slot,
                                            int32_t stream, uint32_t fin) {
@@ -476,33 +513,10 @@ __device__ __forceinline__ void row_padded(const Params &p, int r, int64_t out, 
   }
 }
 
-// What the tail needs of a row, broadcast from the lane that loaded it.
-struct TailParams {
-  int r;
-  int32_t stream;
-  int64_t t;
-  int64_t out;
-  int32_t slot, eos;
-  float temp, inv_temp, top_p;
-  int k_eff;
-  bool greedy;
-};
-
-__device__ __forceinline__ TailParams tail_params(const Params &p, const RowParams &a) {
-  TailParams t;
-  t.r = a.r;
-  t.stream = a.stream;
-  t.t = a.t;
-  t.out = static_cast<int64_t>(a.s) * p.out_step_stride + a.r;
-  t.slot = a.slot;
-  t.eos = a.eos;
-  t.temp = a.temp;
-  t.inv_temp = a.inv_temp;
-  t.top_p = a.top_p;
-  t.k_eff = meta_keff(a.meta);
-  t.greedy = meta_greedy(a.meta);
-  return t;
-}
+// What the tail needs of a row: the row's parameters where the warp's batch
+// keeps them (shared memory), read where they are used, so that none of them
+// holds a register through the sort.
+using TailParams = RowParams;
 
 // Waits (lane 0, bounded) for a step's ready flag; true once it is set.  A
 // zero limit looks at the flag once.
@@ -544,12 +558,13 @@ __device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
   const uint32_t lane = lane_id();
   const int pos0 = R * static_cast<int>(lane);
   const float m = K::value(SW::key(__shfl_sync(0xFFFFFFFFu, v[0], 0)));
+  const bool greedy = meta_greedy(w.meta);
   float wt[R];
   uint64_t c[R];
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     wt[i] = 0.f;
-    if (!w.greedy && pos0 + i < kq) wt[i] = kept_weight(K::value(SW::key(v[i])), m, w.temp, w.inv_temp);
+    if (!greedy && pos0 + i < kq) wt[i] = kept_weight(K::value(SW::key(v[i])), m, w.temp, w.inv_temp);
     c[i] = to_fixed(wt[i]);
     if (i > 0) c[i] += c[i - 1];
   }
@@ -562,7 +577,7 @@ __device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
   const uint64_t s_k = __shfl_sync(0xFFFFFFFFu, incl, 31);
 
   int n_p = 1, pick = 0;
-  if (!w.greedy) {
+  if (!greedy) {
     if (w.top_p >= 1.0f) {
       n_p = kq;
     } else if (w.top_p > 0.0f) {
@@ -589,8 +604,12 @@ __device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
   for (int i = 1; i < R; ++i)
     if ((pick % R) == i) vp = v[i];
   const T pw = __shfl_sync(0xFFFFFFFFu, vp, pick / R);
-  if (lane == 0)
-    row_outputs(p, w.r, w.out, w.eos, w.slot, static_cast<int32_t>(SW::idx(pw)), 0u, w.stream, w.t);
+  if (lane == 0) {
+    const int32_t id = static_cast<int32_t>(SW::idx(pw));
+    row_outputs(p, w.r, static_cast<int64_t>(w.s) * p.out_step_stride + w.r, w.eos, w.slot, id,
+                0u, w.stream, w.t);
+    if (p.hist_ring) history_write(p, w.stream, w.cb, w.t, id);
+  }
 
   if (p.kept_ids) {
     const float s_real = static_cast<float>(static_cast<double>(s_k) * (1.0 / 1099511627776.0));
@@ -600,7 +619,7 @@ __device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
       const int q = pos0 + i;
       if (q < kq && q < p.max_keep) {
         p.kept_ids[rb + q] = static_cast<int32_t>(SW::idx(v[i]));
-        p.kept_probs[rb + q] = w.greedy ? (q == 0 ? 1.f : 0.f) : __fdiv_rn(wt[i], s_real);
+        p.kept_probs[rb + q] = greedy ? (q == 0 ? 1.f : 0.f) : __fdiv_rn(wt[i], s_real);
       }
     }
     if (lane == 0) {
@@ -622,7 +641,7 @@ __device__ __forceinline__ void sort_and_tail(const Params &p, const TailParams 
   for (int i = 0; i < R; ++i) v[i] = pos0 + i < nc ? cand[pos0 + i] : T(0);
   if (nc > 1) bitonic_desc<T, R>(v);
   if constexpr (R <= 2) {
-    warp_tail<K, R>(p, w, v, w.k_eff, u24);
+    warp_tail<K, R>(p, w, v, meta_keff(w.meta), u24);
   } else {
     // k_eff <= 64: the first 64 sorted positions, two per lane.  Position
     // 2l + h lives in lane (2l + h) / R, slot (2l + h) % R; readers want
@@ -640,7 +659,7 @@ __device__ __forceinline__ void sort_and_tail(const Params &p, const TailParams 
       }
       v2[h] = x;
     }
-    warp_tail<K, 2>(p, w, v2, w.k_eff, u24);
+    warp_tail<K, 2>(p, w, v2, meta_keff(w.meta), u24);
   }
 }
 
@@ -956,7 +975,8 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
             const RowParams &mine = rows[lane];
             if (!meta_err(mine.meta) && !meta_fin(mine.meta) && !meta_greedy(mine.meta)) {
               const int r = mine.r;
-              u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(mine.t),
+              const int64_t t = (p.stop_step || p.max_steps) ? mine.t : p.step[mine.stream] + mine.s;
+              u24 = philox_u24(p.seed[r], p.request[r], static_cast<uint64_t>(t),
                                static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
             }
           }
@@ -985,9 +1005,45 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
           eidx = nq * EPC + static_cast<int>(lane);
       }
       const bool has_e = eidx < V;
-      const uint32_t ekey = has_e ? K::key(K::load_one(rowp, eidx)) : 0u;
+      uint32_t ebits = has_e ? K::load_one(rowp, eidx) : 0u;
       cp_async_wait_all();
       __syncwarp();
+      // ---- the repetition penalty over the row's history column ----
+      if (p.hist_ring) {
+        const RowParams &rp = rows[i];
+        if (rp.pen != 1.0f) {
+          if constexpr (WPR > 1) row_sync<WPR>(grp);  // every warp's columns are staged
+          if (sub == 0) {
+            const int64_t col = static_cast<int64_t>(rp.stream) * p.hist_len * p.hist_q + rp.cb;
+            const int x = static_cast<int>(lane) < p.hist_len
+                              ? p.hist_ring[col + static_cast<int64_t>(lane) * p.hist_q] : -1;
+            const bool valid = x >= 0 && x < V;
+            // one lane per distinct token penalises it
+            const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? x : -1 - static_cast<int>(lane));
+            if (valid && __ffs(peers) - 1 == static_cast<int>(lane) && x >= head &&
+                x < head + nq * EPC) {
+              const int q = (x - head) / EPC, e = (x - head) % EPC;
+              const int idx = ((q & 31) + 32 * ((q >> 5) % STG)) * EPC + e;
+              if (K::kElemBytes == 2) {
+                uint16_t *el = reinterpret_cast<uint16_t *>(sh.stage) + idx;
+                *el = static_cast<uint16_t>(penalised_bits<K>(*el, rp.pen));
+              } else {
+                uint32_t *el = reinterpret_cast<uint32_t *>(sh.stage) + idx;
+                *el = penalised_bits<K>(*el, rp.pen);
+              }
+            }
+            // head / tail elements: their owning lanes look for them
+            if (__any_sync(0xFFFFFFFFu, has_e)) {
+              bool hit = false;
+              for (int j = 0; j < p.hist_len; ++j)
+                hit |= __shfl_sync(0xFFFFFFFFu, valid ? x : -1, j) == eidx;
+              if (has_e && hit) ebits = penalised_bits<K>(ebits, rp.pen);
+            }
+          }
+          row_sync<WPR>(grp);
+        }
+      }
+      const uint32_t ekey = has_e ? K::key(ebits) : 0u;
 
       // ---- the two largest logits of each of the lane's two streams ----
       // two independent running pairs (even and odd columns), then merged
@@ -1131,7 +1187,7 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
       const uint32_t total_n = sh.xcnt;
       const bool over = total_n > static_cast<uint32_t>(kWarpCandMax);
       if (sub != 0) continue;
-      const TailParams tp = tail_params(p, rows[i]);
+      const TailParams &tp = rows[i];
       const uint32_t u24 = sh.xu[i];
       int nc = static_cast<int>(total_n);
       if (over) {

@@ -134,6 +134,27 @@ typedef struct {
   const int64_t *max_steps;   /* [n_streams] length cap on the stream's step */
   uint8_t *finish_reason;     /* [n_streams] 0 running, 1 stop, 2 length */
   int32_t pad_id;             /* id of a finished stream's rows */
+  /* Repetition penalty over the fed-back frame history (NULL hist_ring: off).
+   * The handbook section above names a repetition penalty among the sampling
+   * knobs; the rule is the published one (Keskar et al., "CTRL", 2019): each
+   * distinct token of the row's history has its logit divided by theta when
+   * positive and multiplied by theta otherwise, before selection, in fp32 and
+   * rounded to the logits' type.  The history is a ring [n_streams][hist_len]
+   * [hist_codebooks] of token ids: the token of stream s at codebook q drawn
+   * at step t sits at ((s * hist_len) + t mod hist_len) * hist_codebooks + q;
+   * slots < 0 are empty and ids outside the row are ignored.  A row reads its
+   * own column (its stream, its codebook[r]) and, after its draw, writes the
+   * drawn id into the slot of its step (finished and error rows write
+   * nothing); no two rows of a call share a column.  The caller fills the
+   * ring with -1 to start.  Warp path only (top-k cap <= 64, rows up to 4096
+   * bf16 / 2048 fp32; others return TS_ERR_UNSUPPORTED), 1 <= hist_len <= 32,
+   * not in ts_sample_steps.  Row errors: codebook[r] outside [0,
+   * hist_codebooks) is a shape error, theta NaN, infinite or <= 0 a parameter
+   * error. */
+  int32_t *hist_ring;
+  int32_t hist_len;
+  int32_t hist_codebooks;
+  const float *rep_penalty;   /* [n_rows] theta (1: no penalty) */
 } ts_batch;
 
 /* Creates a sampler on CUDA device `device`.  max_top_k: 0 selects the

@@ -348,3 +348,41 @@ def test_segmented_stage_matches_unsegmented(ts):
     assert np.array_equal(big["ids"][rows][safe], ref["ids"][safe])
     assert np.all(big["ids"][rows][ref["err"] != 0] == -1)
     s.close()
+
+
+@pytest.mark.parametrize("name", ["drama3", "qwen3tts"])
+def test_per_level_calls_match_the_frame_call(ts, name):
+    """A frame sampled level by level (one ts_sample call per codebook, as the
+    tower samples them in order; the last call advances the steps) equals the
+    one-call frame: ids, EOS flags and the frame, for three frames."""
+    import bench
+    hosts = [workloads.make(name, i) for i in range(3)]
+    host = hosts[0]
+    s = ts.Sampler(0, host["cap"])
+    whole = ts.DeviceBatch(host, "cuda", advance_steps=True)
+    levels = bench.level_batches(host, "cuda")
+    frame = levels[0].feedback
+    for b in levels[1:]:
+        b.feedback, b.c.feedback_buf = frame, frame.data_ptr()
+        b.step, b.c.step = levels[0].step, levels[0].step.data_ptr()
+    n = int(host["n_rows"])
+    cb = np.asarray(host["codebook"])
+    for h in hosts:
+        lg = torch.from_numpy(np.ascontiguousarray(h["logits"]).view(np.int16)).cuda()
+        whole.set_logits(lg)
+        s.sample(whole)
+        got_ids = np.zeros(n, np.int32)
+        got_eos = np.zeros(n, np.uint8)
+        for q, b in enumerate(levels):
+            b.set_logits(lg)
+            s.sample(b)
+        torch.cuda.synchronize()
+        for q, b in enumerate(levels):
+            got_ids[cb == q] = b.ids()
+            got_eos[cb == q] = b.eos()
+        assert np.array_equal(got_ids, whole.ids())
+        assert np.array_equal(got_eos, whole.eos())
+        assert np.array_equal(frame.cpu().numpy(), whole.feedback.cpu().numpy())
+    assert np.array_equal(levels[0].step.cpu().numpy(), whole.step.cpu().numpy())
+    assert s.read_status() == 0
+    s.close()
