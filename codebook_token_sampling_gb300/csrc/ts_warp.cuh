@@ -393,16 +393,17 @@ struct RowParams {
   int32_t r;      // row of the batch
   int32_t s;      // step index within the launch
   int32_t stream; // index into step[] (valid when the row has no shape error)
-  int32_t cb;     // the row's codebook (its history column)
-  float pen;      // the row's repetition penalty (1: none)
   uint32_t meta;  // vocab (bits 0-12) | k_eff (13-19) | greedy (20) | error bits (21-25)
                   // | finish reason (26-27)
   int32_t slot;   // write-back slot (its step's frame included), -1 = none
   int32_t eos;
   float temp;
-  float inv_temp;
   float top_p;
 };
+// 48 bytes: a block's four batches of 32 rows take 6 KB of shared memory, and
+// the 16-column variant keeps five blocks per SM (the next step's blocks start
+// beside the current step's).
+static_assert(sizeof(RowParams) == 48, "RowParams is sized for the block's shared memory");
 
 __device__ __forceinline__ int meta_vocab(uint32_t m) { return static_cast<int>(m & 0x1FFFu); }
 __device__ __forceinline__ int meta_keff(uint32_t m) { return static_cast<int>((m >> 13) & 0x7Fu); }
@@ -441,13 +442,11 @@ __device__ __forceinline__ RowParams load_params(const Params &p, int64_t g) {
   if (slot >= 0 && static_cast<int64_t>(slot) >= p.feedback_len) e |= kRowBadSlot;
   w.slot = slot >= 0 ? static_cast<int32_t>(slot + static_cast<int64_t>(s) * p.feedback_step_stride)
                      : -1;
-  w.cb = 0;
-  w.pen = 1.0f;
-  if (p.hist_ring) {  // the history column and the penalty
-    w.cb = p.codebook[r];
-    w.pen = p.rep_penalty[r];
-    if (w.cb < 0 || w.cb >= p.hist_q) e |= kRowBadShape;
-    if (isnan(w.pen) || isinf(w.pen) || !(w.pen > 0.0f)) e |= kRowBadParam;
+  if (p.hist_ring) {  // the history column and the penalty (read again where used)
+    const int32_t cb = p.codebook[r];
+    const float pen = p.rep_penalty[r];
+    if (cb < 0 || cb >= p.hist_q) e |= kRowBadShape;
+    if (isnan(pen) || isinf(pen) || !(pen > 0.0f)) e |= kRowBadParam;
   }
   // the finish rule and the history ring need the row's step now; without
   // them the step is read by the draw, while the row's logits are on their way
@@ -461,7 +460,6 @@ __device__ __forceinline__ RowParams load_params(const Params &p, int64_t g) {
   k = min(k, p.cap);
   k = min(k, v);
   const bool greedy = !(w.temp > 0.0f) || k == 1;
-  w.inv_temp = greedy ? 1.0f : 1.0f / w.temp;
   w.meta = static_cast<uint32_t>(v) | (static_cast<uint32_t>(k) << 13) |
            (greedy ? (1u << 20) : 0u) | (e << 21) | (fin << 26);
   return w;
@@ -559,12 +557,13 @@ __device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
   const int pos0 = R * static_cast<int>(lane);
   const float m = K::value(SW::key(__shfl_sync(0xFFFFFFFFu, v[0], 0)));
   const bool greedy = meta_greedy(w.meta);
+  const float inv_temp = greedy ? 1.0f : 1.0f / w.temp;
   float wt[R];
   uint64_t c[R];
 #pragma unroll
   for (int i = 0; i < R; ++i) {
     wt[i] = 0.f;
-    if (!greedy && pos0 + i < kq) wt[i] = kept_weight(K::value(SW::key(v[i])), m, w.temp, w.inv_temp);
+    if (!greedy && pos0 + i < kq) wt[i] = kept_weight(K::value(SW::key(v[i])), m, w.temp, inv_temp);
     c[i] = to_fixed(wt[i]);
     if (i > 0) c[i] += c[i - 1];
   }
@@ -608,7 +607,7 @@ __device__ __forceinline__ void warp_tail(const Params &p, const TailParams &w,
     const int32_t id = static_cast<int32_t>(SW::idx(pw));
     row_outputs(p, w.r, static_cast<int64_t>(w.s) * p.out_step_stride + w.r, w.eos, w.slot, id,
                 0u, w.stream, w.t);
-    if (p.hist_ring) history_write(p, w.stream, w.cb, w.t, id);
+    if (p.hist_ring) history_write(p, w.stream, p.codebook[w.r], w.t, id);
   }
 
   if (p.kept_ids) {
@@ -1006,17 +1005,25 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
       }
       const bool has_e = eidx < V;
       uint32_t ebits = has_e ? K::load_one(rowp, eidx) : 0u;
+      // the row's penalty and history column (lane j: the frame in slot j),
+      // fetched while the row's logits arrive
+      float pen = 1.0f;
+      int hx = -1;
+      if (p.hist_ring) {
+        const int rr = rows[i].r;
+        pen = p.rep_penalty[rr];
+        if (sub == 0 && static_cast<int>(lane) < p.hist_len)
+          hx = p.hist_ring[(static_cast<int64_t>(rows[i].stream) * p.hist_len + lane) * p.hist_q +
+                           p.codebook[rr]];
+      }
       cp_async_wait_all();
       __syncwarp();
       // ---- the repetition penalty over the row's history column ----
       if (p.hist_ring) {
-        const RowParams &rp = rows[i];
-        if (rp.pen != 1.0f) {
+        if (pen != 1.0f) {
           if constexpr (WPR > 1) row_sync<WPR>(grp);  // every warp's columns are staged
           if (sub == 0) {
-            const int64_t col = static_cast<int64_t>(rp.stream) * p.hist_len * p.hist_q + rp.cb;
-            const int x = static_cast<int>(lane) < p.hist_len
-                              ? p.hist_ring[col + static_cast<int64_t>(lane) * p.hist_q] : -1;
+            const int x = hx;
             const bool valid = x >= 0 && x < V;
             // one lane per distinct token penalises it
             const uint32_t peers = __match_any_sync(0xFFFFFFFFu, valid ? x : -1 - static_cast<int>(lane));
@@ -1026,10 +1033,10 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
               const int idx = ((q & 31) + 32 * ((q >> 5) % STG)) * EPC + e;
               if (K::kElemBytes == 2) {
                 uint16_t *el = reinterpret_cast<uint16_t *>(sh.stage) + idx;
-                *el = static_cast<uint16_t>(penalised_bits<K>(*el, rp.pen));
+                *el = static_cast<uint16_t>(penalised_bits<K>(*el, pen));
               } else {
                 uint32_t *el = reinterpret_cast<uint32_t *>(sh.stage) + idx;
-                *el = penalised_bits<K>(*el, rp.pen);
+                *el = penalised_bits<K>(*el, pen);
               }
             }
             // head / tail elements: their owning lanes look for them
@@ -1037,7 +1044,7 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
               bool hit = false;
               for (int j = 0; j < p.hist_len; ++j)
                 hit |= __shfl_sync(0xFFFFFFFFu, valid ? x : -1, j) == eidx;
-              if (has_e && hit) ebits = penalised_bits<K>(ebits, rp.pen);
+              if (has_e && hit) ebits = penalised_bits<K>(ebits, pen);
             }
           }
           row_sync<WPR>(grp);
