@@ -170,6 +170,7 @@ struct Lane<KeyBF16> {
     uint32_t m1, m2;
   };
   static constexpr int kChunksPerMap = 4;  // a bitmap word covers 4 chunks (32 logits)
+  static constexpr uint32_t kNeutral = 0xFF80FF80u;  // a word that folds to nothing (-inf, -inf)
   __device__ __forceinline__ static __nv_bfloat162 b2(uint32_t x) {
     return *reinterpret_cast<__nv_bfloat162 *>(&x);
   }
@@ -249,6 +250,7 @@ struct Lane<KeyF32> {
     return r;
   }
   static constexpr int kChunksPerMap = 8;  // a bitmap word covers 8 chunks (32 logits)
+  static constexpr uint32_t kNeutral = 0xFF800000u;  // a word that folds to nothing (-inf)
   __device__ __forceinline__ static Acc init() {
     return {0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u};
   }
@@ -841,6 +843,9 @@ __device__ __forceinline__ void row_sync(int grp) {
 // After every block of the launch has read step[]: the last block to arrive
 // adds n_steps to step_out[0 .. n_streams) and re-arms the ticket.  No block
 // waits for another; every thread of the block must reach this call.
+// Only the last block writes step_out, so every block reads the values it
+// would add to before its ticket, while the block's other warps finish: the
+// last block then only stores (one round trip less after the ticket).
 // The ticket is taken with an acquire-release atomic at GPU scope: the block's
 // reads of step[] (ordered before it by the block barrier) happen before the
 // last block's acquire, so its increments cannot reach a reader of this
@@ -848,6 +853,10 @@ __device__ __forceinline__ void row_sync(int grp) {
 // once this grid has completed.
 __device__ __forceinline__ void advance_steps_last_block(const Params &p) {
   __shared__ uint32_t last;
+  const int tid = static_cast<int>(threadIdx.x);
+  const bool one_pass = p.n_streams <= static_cast<int>(blockDim.x);
+  int64_t cur = 0;
+  if (one_pass && tid < p.n_streams) cur = p.step_out[tid];
   __syncthreads();
   if (threadIdx.x == 0) {
     uint32_t old;
@@ -857,8 +866,11 @@ __device__ __forceinline__ void advance_steps_last_block(const Params &p) {
   }
   __syncthreads();
   if (!last) return;
-  for (int i = static_cast<int>(threadIdx.x); i < p.n_streams; i += static_cast<int>(blockDim.x))
-    p.step_out[i] += p.n_steps;
+  if (one_pass) {
+    if (tid < p.n_streams) p.step_out[tid] = cur + p.n_steps;
+  } else {
+    for (int i = tid; i < p.n_streams; i += static_cast<int>(blockDim.x)) p.step_out[i] += p.n_steps;
+  }
   if (threadIdx.x == 0) *p.ticket = 0u;
 }
 
@@ -881,6 +893,8 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
   constexpr int AW = acc_words<K>();
   constexpr bool kSeg = STG < MAXNCH;
   constexpr int NSEG = MAXNCH / STG;
+  constexpr int NCC = kSeg ? STG : NCHW;  // chunk columns a warp folds per segment
+  constexpr int LG = NCC < 4 ? NCC : 4;   // chunks loaded together
   static_assert(!kSeg || (WPR == 1 && MAXNCH % STG == 0 && STG % CPM == 0),
                 "segments: one warp per row, whole map words per segment");
   __shared__ __align__(16) TowerShared<K, STG, WPR> shared_rows[RPB];
@@ -1064,13 +1078,24 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
           cp_async_wait_all();
           __syncwarp();
         }
+        // LG chunks at a time: their loads go out together (a stage slot is
+        // read whatever the column; a chunk past the row folds as -inf)
 #pragma unroll
-        for (int cc = 0; cc < (kSeg ? STG : NCHW); ++cc) {
-          const int c = seg * STG + cc;
-          const int j = sub + c * WPR;
-          if (j >= nch) break;
-          const int q = static_cast<int>(lane) + 32 * j;
-          if (q < nq) LN::fold_chunk(sh.stage[lane + 32 * (j % STG)], (c & 1) ? acc_odd : acc);
+        for (int c0 = 0; c0 < NCC; c0 += LG) {
+          if (sub + (seg * STG + c0) * WPR >= nch) break;  // uniform
+          uint4 x[LG];
+#pragma unroll
+          for (int k = 0; k < LG; ++k)
+            x[k] = sh.stage[lane + 32 * ((sub + (seg * STG + c0 + k) * WPR) % STG)];
+#pragma unroll
+          for (int k = 0; k < LG; ++k) {
+            const int c = seg * STG + c0 + k;
+            const int j = sub + c * WPR;
+            const int q = static_cast<int>(lane) + 32 * j;
+            const uint4 v = (c0 + k < NCC && j < nch && q < nq)
+                                ? x[k] : make_uint4(LN::kNeutral, LN::kNeutral, LN::kNeutral, LN::kNeutral);
+            LN::fold_chunk(v, (c & 1) ? acc_odd : acc);
+          }
         }
       }
       if (NCHW > 1) LN::merge(acc, acc_odd);
@@ -1152,37 +1177,57 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
         }
         uint32_t bm[GPS];
 #pragma unroll
-        for (int g = 0; g < GPS; ++g) {
-          bm[g] = 0u;
-          if (seg * STG + g * CPM >= ncol) break;  // uniform
+        for (int g = 0; g < GPS; ++g) bm[g] = 0u;
 #pragma unroll
-          for (int cs = 0; cs < CPM; ++cs) {
-            const int c = seg * STG + g * CPM + cs;
-            const int j = sub + c * WPR;
-            const int q = static_cast<int>(lane) + 32 * j;
-            if (c < ncol && q < nq) bm[g] |= LN::flags(sh.stage[lane + 32 * (j % STG)], t2, cs);
+        for (int g = 0; g < GPS; ++g) {
+          if (seg * STG + g * CPM >= ncol) break;  // uniform
+          // LG chunks at a time, their loads together; a chunk past the row
+          // marks nothing
+#pragma unroll
+          for (int c0 = 0; c0 < CPM; c0 += LG) {
+            uint4 x[LG];
+#pragma unroll
+            for (int k = 0; k < LG; ++k)
+              x[k] = sh.stage[lane + 32 * ((sub + (seg * STG + g * CPM + c0 + k) * WPR) % STG)];
+#pragma unroll
+            for (int k = 0; k < LG; ++k) {
+              const int cs = c0 + k;
+              const int c = seg * STG + g * CPM + cs;
+              const int j = sub + c * WPR;
+              const int q = static_cast<int>(lane) + 32 * j;
+              const uint32_t fl = LN::flags(x[k], t2, cs);
+              bm[g] |= (cs < CPM && c < ncol && q < nq) ? fl : 0u;
+            }
           }
         }
         uint32_t mine_n = 0;
 #pragma unroll
-        for (int g = 0; g < GPS; ++g)
-          if (seg * STG + g * CPM < ncol) mine_n += __popc(bm[g]);
+        for (int g = 0; g < GPS; ++g) mine_n += __popc(bm[g]);
         uint32_t at = mine_n ? atomicAdd(&sh.xcnt, mine_n) : 0u;
-#pragma unroll
-        for (int g = 0; g < GPS; ++g) {
-          if (seg * STG + g * CPM >= ncol) break;
+        // the lane's marked logits, lowest bit first over its map words taken
+        // as two 64-bit words (one loop, as many turns as the lane has marks)
+        static_assert(GPS <= 4, "at most four map words per segment");
+        uint64_t mlo = bm[0], mhi = 0;
+        if constexpr (GPS > 1) mlo |= static_cast<uint64_t>(bm[1]) << 32;
+        if constexpr (GPS > 2) mhi = bm[2];
+        if constexpr (GPS > 3) mhi |= static_cast<uint64_t>(bm[3]) << 32;
 #pragma unroll 1
-          for (uint32_t fm = bm[g]; fm; fm &= fm - 1u) {
-            int cs, e;
-            LN::bit_elem(__ffs(fm) - 1, cs, e);
-            const int j = sub + (seg * STG + g * CPM + cs) * WPR;
-            const int q = static_cast<int>(lane) + 32 * j;
-            if (at < static_cast<uint32_t>(kWarpCandMax))
-              sh.u.cand[at] = SW::make(
-                  K::key(K::load_one(sh.stage, (lane + 32 * (j % STG)) * EPC + e)),
-                  static_cast<uint32_t>(head + q * EPC + e));
-            ++at;
-          }
+        for (uint32_t n = 0; n < mine_n; ++n) {
+          const bool in_lo = mlo != 0u;
+          const uint64_t cur = in_lo ? mlo : mhi;
+          const int bit = __ffsll(static_cast<long long>(cur)) - 1 + (in_lo ? 0 : 64);
+          if (in_lo)
+            mlo &= mlo - 1u;
+          else
+            mhi &= mhi - 1u;
+          int cs, e;
+          LN::bit_elem(bit & 31, cs, e);
+          const int j = sub + (seg * STG + (bit >> 5) * CPM + cs) * WPR;
+          const int q = static_cast<int>(lane) + 32 * j;
+          if (at < static_cast<uint32_t>(kWarpCandMax))
+            sh.u.cand[at] = SW::make(K::key(K::load_one(sh.stage, (lane + 32 * (j % STG)) * EPC + e)),
+                                     static_cast<uint32_t>(head + q * EPC + e));
+          ++at;
         }
       }
       if (has_e && ekey >= t0) {
