@@ -24,6 +24,7 @@ namespace ts {
 constexpr int kClusterThreads = 512;
 constexpr int kClusterWarps = kClusterThreads / 32;
 constexpr int kHistWords = 4096;  // words per histogram buffer
+static_assert(kHistWords >= 4096, "the leader keeps up to 4096 kept weights in hist_b");
 constexpr int kMassBins = 1024;   // bins per level of the mass descent
 constexpr int kSliceMaxBF16 = 20480;
 constexpr int kSliceMaxF32 = 10240;
@@ -176,9 +177,9 @@ __device__ void merged_select(const uint32_t *h, int nbins, uint32_t kk, uint32_
 // its mass is kept as three 32-bit partial sums (weight bits 0-12, 13-25 and
 // 26+), so only native 32-bit shared-memory atomics are used.
 template <class K>
-__device__ uint32_t mass_descent(const uint2 *cand, int kq, uint32_t maxk, uint32_t range,
-                                 float m, float temp, float inv_temp, bool cut_mode, uint64_t cut,
-                                 uint64_t target,
+__device__ uint32_t mass_descent(const uint2 *cand, const float *wt, int kq, uint32_t maxk,
+                                 uint32_t range, float m, float temp, float inv_temp, bool cut_mode,
+                                 uint64_t cut, uint64_t target,
                                  uint32_t *h, uint32_t *misc, uint64_t *scratch,
                                  uint64_t *above_out) {
   const int t = static_cast<int>(threadIdx.x);
@@ -201,7 +202,7 @@ __device__ uint32_t mass_descent(const uint2 *cand, int kq, uint32_t maxk, uint3
         if (exact) {
           atomicAdd(&h[d], 1u);
         } else {
-          const uint64_t f = to_fixed(kept_weight(K::value(key), m, temp, inv_temp));
+          const uint64_t f = to_fixed(wt[i]);
           if (f) {
             atomicAdd(&h[d], static_cast<uint32_t>(f & 0x1FFFu));
             atomicAdd(&h[kMassBins + d], static_cast<uint32_t>((f >> 13) & 0x1FFFu));
@@ -523,12 +524,17 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
   int32_t id;
   int n_p = 1;
   uint64_t s_k = 0;
+  // the kept weights, computed once (hist_b is free once the top-k set is in)
+  float *wt = reinterpret_cast<float *>(hist_b);
   if (w.greedy) {
     id = rank_select(cand, kq, maxk, 0, misc, scratch);
   } else {
     uint64_t part = 0;
-    for (int i = tid; i < kq; i += kClusterThreads)
-      part += to_fixed(kept_weight(K::value(cand[i].x), mval, w.temp, w.inv_temp));
+    for (int i = tid; i < kq; i += kClusterThreads) {
+      const float wi = kept_weight(K::value(cand[i].x), mval, w.temp, w.inv_temp);
+      wt[i] = wi;
+      part += to_fixed(wi);
+    }
     block_excl_scan_u64(part, scratch, &s_k);
     const uint32_t range = maxk - thr;
     uint64_t s_p;
@@ -541,8 +547,8 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
     } else {
       const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
       uint64_t above;
-      const uint32_t key_c = mass_descent<K>(cand, kq, maxk, range, mval, w.temp, w.inv_temp, true,
-                                             cut, 0, mh, misc, scratch, &above);
+      const uint32_t key_c = mass_descent<K>(cand, wt, kq, maxk, range, mval, w.temp, w.inv_temp,
+                                             true, cut, 0, mh, misc, scratch, &above);
       const uint64_t wc = to_fixed(kept_weight(K::value(key_c), mval, w.temp, w.inv_temp));
       // smallest n >= 1 with above + n * wc >= cut (above < cut; the crossing
       // group has positive mass, the guard only protects the division)
@@ -560,8 +566,8 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
                                     static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
     const uint64_t target = scale_u24(u24, s_p);
     uint64_t above_d;
-    const uint32_t key_d = mass_descent<K>(cand, kq, maxk, range, mval, w.temp, w.inv_temp, false,
-                                           0, target, mh, misc, scratch, &above_d);
+    const uint32_t key_d = mass_descent<K>(cand, wt, kq, maxk, range, mval, w.temp, w.inv_temp,
+                                           false, 0, target, mh, misc, scratch, &above_d);
     const uint64_t wd = to_fixed(kept_weight(K::value(key_d), mval, w.temp, w.inv_temp));
     id = rank_select(cand, kq, key_d, wd > 0 ? (target - above_d) / wd : 0, misc, scratch);
   }
@@ -574,7 +580,7 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
       p.kept_ids[rb + i] = tok;
       p.kept_probs[rb + i] =
           w.greedy ? (tok == id ? 1.f : 0.f)
-                   : __fdiv_rn(kept_weight(K::value(cand[i].x), mval, w.temp, w.inv_temp), s_real);
+                   : __fdiv_rn(wt[i], s_real);
     }
     if (tid == 0) {
       p.n_kept[r] = kq;
