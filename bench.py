@@ -281,15 +281,22 @@ def step_buffers(name, rows, dev, l2, n_gen):
 
 def time_steps(sampler, batch, bufs, k, w, repeats, stream):
     """Per-step times (s) of `repeats` timed runs of exactly k steps.  Each step
-    is one ts_sample call (with the fused step advance) on the next step
+    is one ts_sample call (with the step advance inside it) on the next step
     buffer; the k-step runs are CUDA graphs over consecutive buffers, replayed
-    in turn, so a buffer is read again only after the others."""
+    in turn, so a buffer is read again only after the others.  A batch with two
+    step arrays swaps them after every call (k even, so that a graph ends where
+    it started)."""
     import torch
+    double = batch.step_next is not None
+    if double and k % 2:
+        raise ValueError("double-buffered steps need an even step count per graph")
     n_buf = len(bufs)
     n_graph = -(-n_buf // k) if k < n_buf else 1
     graphs = []
     with torch.cuda.stream(stream):
         sampler.sample(batch, stream)  # first launch outside capture
+    if double:
+        batch.swap_steps()
     stream.synchronize()
     for gi in range(n_graph):
         g = torch.cuda.CUDAGraph()
@@ -297,6 +304,8 @@ def time_steps(sampler, batch, bufs, k, w, repeats, stream):
             for i in range(k):
                 batch.set_logits(bufs[(gi * k + i) % n_buf])
                 sampler.sample(batch)
+                if double:
+                    batch.swap_steps()
         graphs.append(g)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -427,7 +436,8 @@ def summarize(times):
             "repeats": len(t)}
 
 
-def measure_config(args, name, rows, dev, l2, peak, k, w, repeats, num_sms, multi=(8, 64)):
+def measure_config(args, name, rows, dev, l2, peak, k, w, repeats, num_sms, multi=(8, 64),
+                   in_place_too=False):
     """One workload's single-step and multi-step figures."""
     import torch
     import codebook_token_sampling_gb300 as ts
@@ -440,12 +450,21 @@ def measure_config(args, name, rows, dev, l2, peak, k, w, repeats, num_sms, mult
         sampler.set_option(ts.TS_OPT_PATH, args.path)
     if args.warps_per_row:
         sampler.set_option(ts.TS_OPT_WARPS_PER_ROW, args.warps_per_row)
-    batch = ts.DeviceBatch(host, dev, advance_steps=True)
+    # the decode loop's two step arrays: each call reads one and writes the
+    # advanced steps to the other (no ordering between the launch's blocks);
+    # an odd step count (a graph that must end where it started) advances in place
+    double = k % 2 == 0
+    batch = ts.DeviceBatch(host, dev, advance_steps=True, double_steps=double)
     plan = sampler.plan(batch)
     stream = torch.cuda.Stream(device=dev)
     times = time_steps(sampler, batch, bufs, k, w, repeats, stream)
     if sampler.read_status(stream) != 0:
         raise RuntimeError(f"row errors in {name}")
+    in_place = None
+    if in_place_too and double:  # the same loop advancing one step array in place
+        b1 = ts.DeviceBatch(host, dev, advance_steps=True)
+        in_place = summarize(time_steps(sampler, b1, bufs, k, w, repeats, stream))
+        del b1
     alg = algorithmic_bytes(host)
     sm = summarize(times)
     t = sm["us_median"] / 1e6
@@ -459,9 +478,17 @@ def measure_config(args, name, rows, dev, l2, peak, k, w, repeats, num_sms, mult
         "gb_per_s": alg / t / 1e9, "algorithmic_bytes_per_step": alg,
         "frac": alg / t / 1e9 / peak, "frac_of_nominal": alg / t / 1e9 / NOMINAL_HBM_GBS,
         "kernel": plan, "launches_per_step": launches, "dtype": host["dtype"],
+        "step_arrays": ("two, swapped every call (step_out)" if double
+                        else "one, advanced in place"),
         "l2": f"{len(bufs)} step buffers ({len(bufs) * workloads.logit_bytes(host) / 2**20:.0f} MiB "
               f"> 2x L2 {l2 / 2**20:.0f} MiB)",
     }
+    if in_place is not None:
+        out["in_place_advance"] = {"us_per_step": in_place["us_median"],
+                                   "us_per_step_min": in_place["us_min"],
+                                   "rows_per_s": n_rows / (in_place["us_median"] / 1e6),
+                                   "how": "the same loop with one step array advanced in place "
+                                          "(a ticket between the launch's blocks)"}
     if plan["path"] == 1 and multi:
         ms = {}
         for r in multi:
@@ -663,7 +690,7 @@ def main():
         clocks.start()
     barrier(world)
     head = measure_config(args, args.config, args.rows, dev, l2, peak, k, w, reps, num_sms,
-                          multi=() if args.no_multi_step else (8, 64))
+                          multi=() if args.no_multi_step else (8, 64), in_place_too=True)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if clocks else None
@@ -710,7 +737,8 @@ def main():
         "config": {"workload": summ["workload"], "rows_per_step": n_rows, "streams": n_streams,
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                    "l2": "inputs larger than L2: " + summ["l2"],
-                   "graph": "each step = one ts_sample call with the fused step advance; "
+                   "graph": "each step = one ts_sample call with the step advance inside it, "
+                            "two step arrays swapped every call; "
                             f"k-step CUDA graphs, {reps} timed runs of exactly k steps, median",
                    "kernel": plan},
         "us_per_step": 1e6 * t_step,
@@ -729,6 +757,7 @@ def main():
                      "us_per_launch": 1e6 * t_step,
                      "us_per_launch_measured_as": "median per-step time of the timed step loop "
                                                   "(CUDA events on the launching stream)"},
+        "in_place_advance": summ.get("in_place_advance"),
         "multi_step": summ.get("multi_step"),
         "e2e": e2e,
         "gpu_launches": summ["launches_per_step"] * k,

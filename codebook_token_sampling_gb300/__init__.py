@@ -84,6 +84,7 @@ class TsBatch(ctypes.Structure):
         ("hist_len", ctypes.c_int32),
         ("hist_codebooks", ctypes.c_int32),
         ("rep_penalty", ctypes.c_void_p),
+        ("step_out", ctypes.c_void_p),
     ]
 
 
@@ -333,7 +334,8 @@ class DeviceBatch:
     """
 
     def __init__(self, host: dict, device="cuda", feedback: bool = True,
-                 advance_steps: bool = False, finish=None, history=None):
+                 advance_steps: bool = False, finish=None, history=None,
+                 double_steps: bool = False):
         import torch
         self.device = torch.device(device)
         self.dtype = TS_DTYPE_BF16 if host["dtype"] == "bf16" else TS_DTYPE_F32
@@ -361,6 +363,12 @@ class DeviceBatch:
         c.step = self.step.data_ptr()
         c.n_streams = int(host["n_streams"])
         c.advance_steps = 1 if advance_steps else 0
+        # double_steps: a second step array receives the advanced steps
+        # (step_out); swap_steps() exchanges the two between calls
+        self.step_next = None
+        if double_steps:
+            self.step_next = torch.empty_like(self.step)
+            c.step_out = self.step_next.data_ptr()
         # finished streams: finish = {"max_steps": per-stream caps or None,
         # "pad_id": int}; stop_step starts at -1 and finish_reason at 0
         self.stop_step = self.max_steps = self.finish_reason = None
@@ -397,6 +405,15 @@ class DeviceBatch:
             c.feedback_len = 0
         self.c = c
         self.set_logits(self.logits)
+
+    def swap_steps(self) -> None:
+        """With double_steps: the array the last call wrote becomes the one the
+        next call reads (host-side pointer swap; capture it between calls)."""
+        if self.step_next is None:
+            raise ValueError("the batch has no second step array")
+        self.step, self.step_next = self.step_next, self.step
+        self.c.step = self.step.data_ptr()
+        self.c.step_out = self.step_next.data_ptr()
 
     def set_logits(self, t) -> None:
         """Point the batch at another device tensor of logits (same layout)."""

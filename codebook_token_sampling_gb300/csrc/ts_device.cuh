@@ -71,6 +71,10 @@ struct Params {
   // step_out[0 .. n_streams) and re-arms the ticket; null: no advance
   int64_t *step_out;
   uint32_t *ticket;
+  // a second step array (warp path): step_next[i] = step[i] + n_steps for
+  // i < n_streams, written by any thread (nothing in the launch reads it);
+  // null: none
+  int64_t *step_next;
   // finished streams (null: off): the step of a stream's EOS (< 0: none),
   // the length cap on a stream's step, the finish reason per stream (1 stop,
   // 2 length) and the id a finished stream's rows return

@@ -211,6 +211,10 @@ ts_status check_batch(const ts_batch *b) {
       !b->request || !b->codebook || !b->row_stream || !b->step || !b->out_ids || !b->out_eos)
     return TS_ERR_INVALID_ARG;
   if (b->n_streams == 0) return TS_ERR_INVALID_ARG;
+  if (b->step_out && b->step_out != b->step) {  // a second step array must not overlap the first
+    const int64_t *a = b->step, *o = b->step_out;
+    if (o < a + b->n_streams && a < o + b->n_streams) return TS_ERR_INVALID_ARG;
+  }
   if (b->feedback_buf && !b->feedback_slot) return TS_ERR_INVALID_ARG;
   if (b->hist_ring && (b->hist_len < 1 || b->hist_len > 32 || b->hist_codebooks < 1 ||
                        !b->rep_penalty || !b->codebook))
@@ -254,6 +258,7 @@ ts::Params make_params(const ts_sampler *s, const ts_batch *b) {
   p.hist_len = b->hist_len;
   p.hist_q = b->hist_codebooks;
   p.rep_penalty = b->rep_penalty;
+  p.step_next = (b->advance_steps && b->step_out && b->step_out != b->step) ? b->step_out : nullptr;
   return p;
 }
 
@@ -324,10 +329,11 @@ ts_status set_attributes(int device) {
   return TS_OK;
 }
 
-__global__ void advance_steps_kernel(int64_t *step, int32_t n, int64_t by) {
+// dst[i] = src[i] + by for i < n (dst == src: in place), one thread per stream.
+__global__ void advance_steps_kernel(const int64_t *src, int64_t *dst, int32_t n, int64_t by) {
   ts::pdl_wait_and_release();
   const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
-  if (i < n) step[i] += by;
+  if (i < n) dst[i] = src[i] + by;
 }
 
 // step[i] += by for i < n_streams, one thread per stream.
@@ -356,7 +362,8 @@ ts_status warp_occupancy(ts_sampler *s) {
   return TS_OK;
 }
 
-ts_status launch_advance(int64_t *step, int32_t n_streams, int64_t by, cudaStream_t stream) {
+ts_status launch_advance(const int64_t *step, int64_t *dst, int32_t n_streams, int64_t by,
+                         cudaStream_t stream) {
   if (n_streams == 0) return TS_OK;
   const int threads = 256;
   cudaLaunchConfig_t cfg;
@@ -369,7 +376,7 @@ ts_status launch_advance(int64_t *step, int32_t n_streams, int64_t by, cudaStrea
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, advance_steps_kernel, step, n_streams, by);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, advance_steps_kernel, step, dst, n_streams, by);
   return e == cudaSuccess ? TS_OK : cuda_fail(e, "advance_steps launch");
 }
 
@@ -384,7 +391,8 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
     // the other paths advance the steps by one more small launch
     rc = launch(s, b, base, st, pl);
     if (rc != TS_OK) return rc;
-    return launch_advance(b->step, b->n_streams, base.n_steps, st);
+    return launch_advance(b->step, base.step_next ? base.step_next : b->step, b->n_streams,
+                          base.n_steps, st);
   }
   return launch(s, b, base, st, pl);
 }
@@ -394,10 +402,11 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
   ts::Params p = base;
   p.slice = pl.slice;
   p.wide_exact = s->wide_exact;
-  if (pl.path == 1 && b->advance_steps) {
+  if (pl.path == 1 && b->advance_steps && !p.step_next) {  // in place: the ticket
     p.step_out = b->step;
     p.ticket = s->ticket;
   }
+  if (pl.path != 1) p.step_next = nullptr;  // the advance launch writes step_out
   const bool bf16 = b->dtype == TS_DTYPE_BF16;
   if (pl.path == 4) {
     p.workspace = s->ws;
@@ -773,7 +782,7 @@ ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *stat
 
 ts_status ts_advance_steps(int64_t *step, int32_t n_streams, void *stream) {
   if (n_streams < 0 || (n_streams > 0 && !step)) return TS_ERR_INVALID_ARG;
-  return launch_advance(step, n_streams, 1, static_cast<cudaStream_t>(stream));
+  return launch_advance(step, step, n_streams, 1, static_cast<cudaStream_t>(stream));
 }
 
 ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream) {

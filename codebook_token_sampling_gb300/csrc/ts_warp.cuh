@@ -908,6 +908,12 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
   const int64_t n_groups = static_cast<int64_t>(gridDim.x) * RPB;
   pdl_wait_and_release();
 
+  // a second step array: each thread stores the advanced step of at most one
+  // stream, its load sent out with the first batch's parameter loads
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  bool next_due = p.step_next != nullptr && gtid < p.n_streams;
+  const int64_t next_v = next_due ? p.step[gtid] : 0;
+
   int seen_step = -1;      // last step whose ready flag this warp has checked
   bool step_ok = true;     // that step's flag was seen set
   bool gave_up = false;    // a flag did not come in time: later flags get one look
@@ -926,6 +932,10 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
     // every warp of a group loads its own copy: no barrier before the rows
     if (static_cast<int>(lane) < nb) rows[lane] = load_params(p, base + lane);
     __syncwarp();
+    if (next_due) {
+      p.step_next[gtid] = next_v + p.n_steps;
+      next_due = false;
+    }
     bool drawn = false;
 #pragma unroll 1
     for (int i = 0; i < nb; ++i) {
@@ -1259,6 +1269,11 @@ __global__ void __launch_bounds__(kTowerThreads, 8) row_sampler_kernel(const Par
       else
         sort_and_tail_128<K>(p, tp, sh.u.cand, nc, u24);
     }
+  }
+  if (next_due) p.step_next[gtid] = next_v + p.n_steps;  // a warp without rows
+  if (p.step_next) {  // more streams than threads
+    const int64_t all = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = gtid + all; i < p.n_streams; i += all) p.step_next[i] = p.step[i] + p.n_steps;
   }
   if (p.step_out) advance_steps_last_block(p);
 }

@@ -116,7 +116,8 @@ typedef struct {
                                  for ts_sample_steps), as ts_advance_steps would do
                                  after the call, but inside the call's own launch on
                                  the warp path (its last block to finish does it) and
-                                 as one more small launch on the other paths */
+                                 as one more small launch on the other paths; with
+                                 step_out (below) the advanced steps go there */
   /* Finished streams (each pointer may be NULL: no stopping / no length cap /
    * no reasons).  The serving side must report how a request ended, stop at
    * its EOS or length at the generation cap, and cap the generation length
@@ -155,6 +156,16 @@ typedef struct {
   int32_t hist_len;
   int32_t hist_codebooks;
   const float *rep_penalty;   /* [n_rows] theta (1: no penalty) */
+  /* Where the advanced steps go when advance_steps is set.  NULL (or step
+   * itself): step is advanced in place, which on the warp path needs an
+   * acquire-release ticket between the launch's blocks, the last of them
+   * storing the steps.  Another array of n_streams entries, not overlapping
+   * step: step_out[i] = step[i] + 1 (+ n_steps for ts_sample_steps) for every
+   * i < n_streams and step is only read, so no block waits for another; a
+   * decode loop alternates the two arrays (step and step_out swapped from
+   * one call to the next, e.g. in consecutive calls captured in one CUDA
+   * graph).  Overlapping arrays are TS_ERR_INVALID_ARG. */
+  int64_t *step_out;
 } ts_batch;
 
 /* Creates a sampler on CUDA device `device`.  max_top_k: 0 selects the

@@ -4,6 +4,8 @@ resident grid that walks several rows per row group, through the C ABI.
 * ts_batch.advance_steps: the step counters grow by one per call, inside the
   warp path's own launch (its last block) or by one more launch on the other
   paths; ids equal those of ts_sample followed by ts_advance_steps.
+* ts_batch.step_out: calls that read one step array and write the advanced
+  steps to another, swapped after each call, equal in-place advancing.
 * ts_sample_steps: R steps' logits in one buffer, sampled by one launch; every
   step's ids, EOS flags and frame equal R separate ts_sample calls and, on
   sampled steps, the oracle.
@@ -385,4 +387,90 @@ def test_per_level_calls_match_the_frame_call(ts, name):
         assert np.array_equal(frame.cpu().numpy(), whole.feedback.cpu().numpy())
     assert np.array_equal(levels[0].step.cpu().numpy(), whole.step.cpu().numpy())
     assert s.read_status() == 0
+    s.close()
+
+
+def _with_idle_streams(host, extra):
+    """The batch with `extra` more streams that no row belongs to (their steps
+    must advance all the same)."""
+    h = dict(host)
+    n = int(h["n_streams"]) + extra
+    h["n_streams"] = n
+    h["step"] = np.concatenate([np.asarray(host["step"], np.int64),
+                                np.arange(extra, dtype=np.int64) * 7 + 100])
+    return h
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_two_step_arrays_match_in_place(ts, path):
+    """step_out: eight calls that read one step array and write the other,
+    swapped after each call, give the ids, EOS flags and steps of eight calls
+    advancing one array in place; streams without rows advance too."""
+    name = "drama3" if path == 1 else "mixed"
+    host = _with_idle_streams(workloads.make(name, 0), 37)
+    logits = [torch.from_numpy(np.ascontiguousarray(workloads.make(name, i)["logits"])
+                               .view(_np_dtype(host))).cuda() for i in range(3)]
+    runs = []
+    for double in (True, False):
+        s = ts.Sampler(0, host["cap"])
+        s.set_option(ts.TS_OPT_PATH, path)
+        b = ts.DeviceBatch(host, "cuda", advance_steps=True, double_steps=double)
+        ids, eos = [], []
+        for i in range(8):
+            b.set_logits(logits[i % 3])
+            s.sample(b)
+            if double:
+                b.swap_steps()
+            ids.append(b.out_ids.clone())
+            eos.append(b.out_eos.clone())
+        torch.cuda.synchronize()
+        assert s.read_status() == 0
+        runs.append((torch.stack(ids).cpu().numpy(), torch.stack(eos).cpu().numpy(),
+                     b.step.cpu().numpy()))
+        s.close()
+    (ia, ea, sa), (ib, eb, sb) = runs
+    assert np.array_equal(ia, ib) and np.array_equal(ea, eb)
+    assert np.array_equal(sa, sb)
+    assert np.array_equal(sa, np.asarray(host["step"]) + 8)
+
+
+def test_two_step_arrays_with_several_steps_per_launch(ts):
+    """ts_sample_steps with step_out: the launch reads step and writes
+    step + R to the other array, leaving step as it was."""
+    steps = 3
+    hosts, buf, per_step = _stacked("qwen3tts", steps)
+    host = _with_idle_streams(hosts[0], 5)
+    n = int(host["n_rows"])
+    s = ts.Sampler(0, host["cap"])
+    b = ts.DeviceBatch(host, "cuda", feedback=False, advance_steps=True, double_steps=True)
+    b.set_logits(buf)
+    out = torch.full((steps, n), -3, dtype=torch.int32, device="cuda")
+    eos = torch.zeros((steps, n), dtype=torch.uint8, device="cuda")
+    b.c.out_ids, b.c.out_eos = out.data_ptr(), eos.data_ptr()
+    before = b.step.cpu().numpy().copy()
+    s.sample_steps(b, steps, logits_step_stride=per_step, out_step_stride=n)
+    torch.cuda.synchronize()
+    assert s.read_status() == 0
+    assert np.array_equal(b.step.cpu().numpy(), before)
+    assert np.array_equal(b.step_next.cpu().numpy(), before + steps)
+    got = out.cpu().numpy()
+    for i in range(steps):
+        h = dict(hosts[i])
+        h["step"] = np.asarray(hosts[0]["step"]) + i
+        ref = oracle.sample(h, max_keep=64, n_threads=8)
+        safe = ref["margin"] > 1e-5
+        assert np.array_equal(got[i][safe], ref["ids"][safe])
+    s.close()
+
+
+def test_overlapping_step_arrays_are_refused(ts):
+    host = workloads.make("drama3", 0)
+    s = ts.Sampler(0, 64)
+    b = ts.DeviceBatch(host, "cuda", advance_steps=True, double_steps=True)
+    b.c.step_out = b.step.data_ptr() + 8  # one entry past step: overlaps it
+    with pytest.raises(ts.SamplerError) as e:
+        s.sample(b)
+    assert e.value.status == ts.TS_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert np.all(b.ids() == -2)
     s.close()
