@@ -567,7 +567,8 @@ def profile_launches(args):
         sampler.set_option(ts.TS_OPT_PATH, args.path)
     if args.warps_per_row:
         sampler.set_option(ts.TS_OPT_WARPS_PER_ROW, args.warps_per_row)
-    batch = ts.DeviceBatch(host, "cuda", advance_steps=True)
+    # as the step loop runs: two step arrays, swapped after every call
+    batch = ts.DeviceBatch(host, "cuda", advance_steps=True, double_steps=True)
     if args.profile_steps > 1:
         hosts = [workloads.make(args.config, i, rows=args.rows) for i in range(args.profile_steps)]
         np_dt = np.int16 if host["dtype"] == "bf16" else np.float32
@@ -588,6 +589,7 @@ def profile_launches(args):
     else:
         for _ in range(args.profile):
             sampler.sample(batch)
+            batch.swap_steps()
     torch.cuda.synchronize()
     print(json.dumps({"profile": args.config, "rows": int(host["n_rows"]), "launches": args.profile,
                       "steps_per_launch": args.profile_steps, "plan": sampler.plan(batch),
