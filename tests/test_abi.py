@@ -45,3 +45,29 @@ def test_status_codes_match_the_oracle_bits():
     import oracle
     assert (ts.TS_ROW_BAD_SHAPE, ts.TS_ROW_BAD_PARAM, ts.TS_ROW_NONFINITE, ts.TS_ROW_BAD_SLOT) == \
         (oracle.ERR_BAD_SHAPE, oracle.ERR_BAD_PARAM, oracle.ERR_NONFINITE, oracle.ERR_BAD_SLOT)
+
+
+def _c_layout(tmp_path, struct, fields):
+    """Offsets of `fields` in the header's `struct`, then its size, from a C
+    program compiled against the header (gcc, no GPU)."""
+    import subprocess
+    body = "".join(f'printf("%zu\\n", offsetof({struct}, {f}));' for f in fields)
+    src = tmp_path / f"{struct}.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "ts_sampler.h"\n'
+                   f'int main(void) {{ {body} printf("%zu\\n", sizeof({struct})); return 0; }}\n')
+    exe = tmp_path / struct
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    return [int(x) for x in out.split()]
+
+
+def test_binding_structs_match_the_header(tmp_path):
+    """Every field of the binding's ts_batch and ts_steps mirrors sits at the
+    header's offset, and the sizes agree (a field missing, added or moved on
+    either side fails here)."""
+    import codebook_token_sampling_gb300 as ts
+    for struct, mirror in (("ts_batch", ts.TsBatch), ("ts_steps", ts.TsSteps)):
+        fields = [name for name, _ in mirror._fields_]
+        want = [getattr(mirror, f).offset for f in fields] + [ctypes.sizeof(mirror)]
+        assert _c_layout(tmp_path, struct, fields) == want, struct
