@@ -176,18 +176,16 @@ __device__ void merged_select(const uint32_t *h, int nbins, uint32_t kk, uint32_
 // its mass is (count x weight of that key); above it a bin mixes keys and
 // its mass is kept as three 32-bit partial sums (weight bits 0-12, 13-25 and
 // 26+), so only native 32-bit shared-memory atomics are used.
+// descend_levels continues a descent whose levels above have put the
+// position in offsets off_lo .. off_lo + 2^span - 1 with mass `above` before
+// them; its next level bins those offsets >> shift.  wt: the kept weights.
 template <class K>
-__device__ uint32_t mass_descent(const uint2 *cand, const float *wt, int kq, uint32_t maxk,
-                                 uint32_t range, float m, float temp, float inv_temp, bool cut_mode,
-                                 uint64_t cut, uint64_t target,
-                                 uint32_t *h, uint32_t *misc, uint64_t *scratch,
-                                 uint64_t *above_out) {
+__device__ uint32_t descend_levels(const uint2 *cand, const float *wt, int kq, uint32_t maxk,
+                                   float m, float temp, float inv_temp, bool cut_mode, uint64_t cut,
+                                   uint64_t target, uint32_t off_lo, int span, int shift,
+                                   uint64_t above, uint32_t *h, uint32_t *misc, uint64_t *scratch,
+                                   uint64_t *above_out) {
   const int t = static_cast<int>(threadIdx.x);
-  const int bits = range ? 32 - __clz(range) : 0;
-  int span = bits;
-  int shift = bits > 10 ? bits - 10 : 0;
-  uint32_t off_lo = 0;
-  uint64_t above = 0;
   uint64_t *wide = reinterpret_cast<uint64_t *>(misc + kMiscWide);
   for (;;) {
     const bool exact = shift == 0;
@@ -247,6 +245,51 @@ __device__ uint32_t mass_descent(const uint2 *cand, const float *wt, int kq, uin
   }
   *above_out = above;
   return maxk - off_lo;
+}
+
+// The descent from its first level: offsets 0 .. 2^bits - 1, bits = the bit
+// width of range = maxk - (smallest kept key).
+template <class K>
+__device__ uint32_t mass_descent(const uint2 *cand, const float *wt, int kq, uint32_t maxk,
+                                 uint32_t range, float m, float temp, float inv_temp, bool cut_mode,
+                                 uint64_t cut, uint64_t target,
+                                 uint32_t *h, uint32_t *misc, uint64_t *scratch,
+                                 uint64_t *above_out) {
+  const int bits = range ? 32 - __clz(range) : 0;
+  return descend_levels<K>(cand, wt, kq, maxk, m, temp, inv_temp, cut_mode, cut, target, 0u, bits,
+                           bits > 10 ? bits - 10 : 0, 0ull, h, misc, scratch, above_out);
+}
+
+// The first level of a descent whose offsets need more than one level
+// (shift1 = bits - 10 > 0), from the level's bin masses that the caller has
+// built once for both descents: thread t holds bins 2t and 2t + 1, their
+// masses a and b and the exclusive prefix p0 of bin 2t.  The bin where the
+// cumulative mass reaches `cut` (cut_mode) or passes `target` is found, and
+// the descent goes on below it.
+template <class K>
+__device__ uint32_t mass_descent_from_l1(const uint2 *cand, const float *wt, int kq, uint32_t maxk,
+                                         float m, float temp, float inv_temp, bool cut_mode,
+                                         uint64_t cut, uint64_t target, int shift1, uint64_t p0,
+                                         uint64_t a, uint64_t b, uint32_t *h, uint32_t *misc,
+                                         uint64_t *scratch, uint64_t *above_out) {
+  const int t = static_cast<int>(threadIdx.x);
+  uint64_t *wide = reinterpret_cast<uint64_t *>(misc + kMiscWide);
+  auto reached = [&](uint64_t cum) { return cut_mode ? cum >= cut : cum > target; };
+  const uint64_t p1 = p0 + a, p2 = p1 + b;
+  __syncthreads();  // misc may still be read
+  if (!reached(p0) && reached(p1)) {
+    misc[kMiscDigit] = static_cast<uint32_t>(2 * t);
+    wide[0] = p0;
+  } else if (!reached(p1) && reached(p2)) {
+    misc[kMiscDigit] = static_cast<uint32_t>(2 * t + 1);
+    wide[0] = p1;
+  }
+  __syncthreads();
+  const uint32_t off_lo = misc[kMiscDigit] << shift1;
+  const uint64_t above = wide[0];
+  return descend_levels<K>(cand, wt, kq, maxk, m, temp, inv_temp, cut_mode, cut, target, off_lo,
+                           shift1, shift1 > 10 ? shift1 - 10 : 0, above, h, misc, scratch,
+                           above_out);
 }
 
 // Index (token id) of the `rank`-th kept token, in index order, among those
@@ -529,14 +572,41 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
   if (w.greedy) {
     id = rank_select(cand, kq, maxk, 0, misc, scratch);
   } else {
+    // the descents' first level, when their offsets need more than one: the
+    // kept masses binned by (maxk - key) >> shift1, built with the weights
+    const uint32_t range = maxk - thr;
+    const int bits = range ? 32 - __clz(range) : 0;
+    const int shift1 = bits > 10 ? bits - 10 : 0;
+    if (shift1 > 0) {
+      for (int i = tid; i < 3 * kMassBins; i += kClusterThreads) mh[i] = 0u;
+      __syncthreads();
+    }
     uint64_t part = 0;
     for (int i = tid; i < kq; i += kClusterThreads) {
-      const float wi = kept_weight(K::value(cand[i].x), mval, w.temp, w.inv_temp);
+      const uint32_t key = cand[i].x;
+      const float wi = kept_weight(K::value(key), mval, w.temp, w.inv_temp);
       wt[i] = wi;
-      part += to_fixed(wi);
+      const uint64_t f = to_fixed(wi);
+      part += f;
+      if (shift1 > 0 && f) {
+        const uint32_t d = (maxk - key) >> shift1;
+        atomicAdd(&mh[d], static_cast<uint32_t>(f & 0x1FFFu));
+        atomicAdd(&mh[kMassBins + d], static_cast<uint32_t>((f >> 13) & 0x1FFFu));
+        atomicAdd(&mh[2 * kMassBins + d], static_cast<uint32_t>(f >> 26));
+      }
     }
-    block_excl_scan_u64(part, scratch, &s_k);
-    const uint32_t range = maxk - thr;
+    block_excl_scan_u64(part, scratch, &s_k);  // its first barrier: every bin is in
+    uint64_t l1_p0 = 0, l1_a = 0, l1_b = 0;    // this thread's two first-level bins
+    if (shift1 > 0) {
+      auto bin_mass = [&](int d) {
+        return (static_cast<uint64_t>(mh[2 * kMassBins + d]) << 26) +
+               (static_cast<uint64_t>(mh[kMassBins + d]) << 13) + mh[d];
+      };
+      l1_a = bin_mass(2 * tid);
+      l1_b = bin_mass(2 * tid + 1);
+      uint64_t tot1;
+      l1_p0 = block_excl_scan_u64(l1_a + l1_b, scratch, &tot1);
+    }
     uint64_t s_p;
     if (w.top_p >= 1.0f) {
       n_p = kq;
@@ -547,8 +617,12 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
     } else {
       const uint64_t cut = ceil_mul_p(w.top_p, s_k);  // C reaches top_p * S_k iff C >= cut
       uint64_t above;
-      const uint32_t key_c = mass_descent<K>(cand, wt, kq, maxk, range, mval, w.temp, w.inv_temp,
-                                             true, cut, 0, mh, misc, scratch, &above);
+      const uint32_t key_c =
+          shift1 > 0 ? mass_descent_from_l1<K>(cand, wt, kq, maxk, mval, w.temp, w.inv_temp, true,
+                                               cut, 0, shift1, l1_p0, l1_a, l1_b, mh, misc,
+                                               scratch, &above)
+                     : mass_descent<K>(cand, wt, kq, maxk, range, mval, w.temp, w.inv_temp, true,
+                                       cut, 0, mh, misc, scratch, &above);
       const uint64_t wc = to_fixed(kept_weight(K::value(key_c), mval, w.temp, w.inv_temp));
       // smallest n >= 1 with above + n * wc >= cut (above < cut; the crossing
       // group has positive mass, the guard only protects the division)
@@ -566,8 +640,12 @@ __global__ void __launch_bounds__(kClusterThreads, 2) cluster_sampler_kernel(con
                                     static_cast<uint64_t>(static_cast<int64_t>(p.codebook[r])));
     const uint64_t target = scale_u24(u24, s_p);
     uint64_t above_d;
-    const uint32_t key_d = mass_descent<K>(cand, wt, kq, maxk, range, mval, w.temp, w.inv_temp,
-                                           false, 0, target, mh, misc, scratch, &above_d);
+    const uint32_t key_d =
+        shift1 > 0 ? mass_descent_from_l1<K>(cand, wt, kq, maxk, mval, w.temp, w.inv_temp, false, 0,
+                                             target, shift1, l1_p0, l1_a, l1_b, mh, misc, scratch,
+                                             &above_d)
+                   : mass_descent<K>(cand, wt, kq, maxk, range, mval, w.temp, w.inv_temp, false, 0,
+                                     target, mh, misc, scratch, &above_d);
     const uint64_t wd = to_fixed(kept_weight(K::value(key_d), mval, w.temp, w.inv_temp));
     id = rank_select(cand, kq, key_d, wd > 0 ? (target - above_d) / wd : 0, misc, scratch);
   }
