@@ -4,7 +4,8 @@ TEST INFRASTRUCTURE ONLY.  The tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` call this module; the product library never does,
 and this module imports nothing from it.  The arithmetic lives in
 ``ts_oracle.c`` (plain C, fp64, full sort, explicit renormalisation,
-inverse-CDF draw on a Philox4x64-10 stream written from the SC'11 paper); this
+inverse-CDF draw on a Philox4x64-10 stream written from the SC'11 paper; the
+LM head that produces a frame's logits, in fp64 rounded once to fp32); this
 file only marshals numpy arrays through ctypes.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
@@ -104,6 +105,11 @@ def _bind(path: str):
                                     ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
                                     ctypes.c_void_p]
     lib.oracle_draw_map.restype = ctypes.c_uint32
+    lib.oracle_lm_head.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                   ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                   ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64]
+    lib.oracle_lm_head.restype = None
     return lib
 
 
@@ -131,6 +137,9 @@ class Oracle:
 
     def draw_map(self, values, temp, top_k, top_p, cap_value):
         return _draw_map(self.lib, values, temp, top_k, top_p, cap_value)
+
+    def lm_head(self, batch, head):
+        return _lm_head(self.lib, batch, head)
 
 
 _default = None
@@ -178,6 +187,38 @@ def sample(batch, **kw):
 def draw_map(values, temp: float, top_k: int, top_p: float, cap_value: int):
     """Counts of each token over all 2^24 values of u24 for one row."""
     return default().draw_map(values, temp, top_k, top_p, cap_value)
+
+
+def lm_head(batch, head):
+    """The LM head's fp32 logits for ``batch`` (see ``_lm_head``)."""
+    return default().lm_head(batch, head)
+
+
+def _lm_head(lib, batch, head):
+    """The fp32 logits of every row of ``batch`` from its codebook's head.
+
+    ``head`` holds ``hidden`` (bf16 bits, [n_rows, dim]), ``weights`` (bf16
+    bits), ``head_offsets`` (int64 per head), ``n_heads`` and ``dim``; row r
+    uses head r mod n_heads.  Returns a float32 array of the batch's logits length: the
+    rows' logits at their offsets (NaN for a row whose head lies outside the
+    weights), zeros elsewhere.  The batch's own ``logits`` are not read.
+    """
+    n = int(batch["n_rows"])
+    hidden = _arr(head["hidden"], np.uint16)
+    weights = _arr(head["weights"], np.uint16)
+    offs = _arr(head["head_offsets"], np.int64)
+    n_heads = int(head["n_heads"])
+    dim = int(head["dim"])
+    assert hidden.size == n * dim and offs.size == n_heads
+    rv = _arr(batch["row_vocab"], np.int32)
+    ro = _arr(batch["row_offsets"], np.int64)
+    n_out = int(batch.get("logits_len", np.asarray(batch["logits"]).size))
+    out = np.zeros(n_out, np.float32)
+    mrv = int(batch.get("max_row_vocab", int(np.max(rv, initial=1))))
+    lib.oracle_lm_head(hidden.ctypes.data, weights.ctypes.data, weights.size, offs.ctypes.data,
+                       n_heads, dim, n, rv.ctypes.data, ro.ctypes.data, mrv,
+                       out.ctypes.data, out.size)
+    return out
 
 
 def _sample(lib, batch, *, n_threads: int = 1, u24=None, max_keep: int = 0,

@@ -34,6 +34,10 @@
  *              is positive and multiplies it by theta otherwise.
  *   [Philox]   Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy
  *              as 1, 2, 3", SC'11: the Philox4x64 bijection, 10 rounds.
+ *   [QT-topo]  "案例一：Qwen3-TTS——三个 stage 与首包延迟", section "拓扑": the
+ *              talker's hidden size is 1024 and a frame has 16 codebooks of
+ *              2048 entries; the logits each codebook samples from are the
+ *              product of a hidden state and that codebook's output head.
  *
  *   Readings where the pages are silent (all listed in the design notes):
  *   order temperature -> top-k -> top-p on the top-k-renormalised mass;
@@ -534,4 +538,42 @@ uint32_t oracle_draw_map(const double *values, int32_t vocab, float temp,
   free(scratch);
   free(qbuf);
   return err;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The LM head of a frame's rows, the step before sampling ([QT-topo]; one     */
+/* forward per frame samples every codebook, [D3-run]).  Row r (stream        */
+/* r / Q, codebook q = r mod Q) gets                                           */
+/*   l_r[v] = sum_k h_r[k] * W_q[v][k]   for v < V_r,                           */
+/* h_r = hidden[r D .. r D + D) and W_q[v] = weights[off_q + v D ..) as bf16   */
+/* bits, every product and sum in fp64 (a bf16 product is exact there), the    */
+/* sum rounded once to fp32.  A row whose head does not lie inside the        */
+/* weights (off_q < 0, off_q not a multiple of 8 elements, or                  */
+/* off_q + V_r D > weights_len) gets NaN logits, a NONFINITE row error once   */
+/* sampled.  A row with a shape error (V_r <= 0, V_r > max_row_vocab, logits   */
+/* outside the buffer) is left unwritten: sampling reports it.                  */
+/* ------------------------------------------------------------------------ */
+void oracle_lm_head(const uint16_t *hidden, const uint16_t *weights, int64_t weights_len,
+                    const int64_t *head_offsets, int32_t n_heads, int32_t dim,
+                    int64_t n_rows, const int32_t *row_vocab, const int64_t *row_offsets,
+                    int32_t max_row_vocab, float *logits, int64_t logits_len) {
+  for (int64_t r = 0; r < n_rows; ++r) {
+    const int32_t vr = row_vocab[r];
+    const int64_t off = row_offsets[r];
+    if (vr <= 0 || vr > max_row_vocab || off < 0 || off > logits_len - vr) continue;
+    const int64_t hoff = head_offsets[r % n_heads];
+    const int head_ok = hoff >= 0 && hoff % 8 == 0 && hoff <= weights_len - (int64_t)vr * dim;
+    const int64_t h0 = r * (int64_t)dim;
+    for (int32_t v = 0; v < vr; ++v) {
+      if (!head_ok) {
+        logits[off + v] = NAN;
+        continue;
+      }
+      const int64_t w0 = hoff + (int64_t)v * dim;
+      double acc = 0.0;
+      for (int32_t k = 0; k < dim; ++k)
+        acc += load_value(1, hidden, h0 + k) * load_value(1, weights, w0 + k);
+      logits[off + v] = (float)acc;
+    }
+  }
 }

@@ -15,6 +15,10 @@ when the oracle disagrees with:
   set is never drawn;
 * the cap rule of the Drama 3 article (section "能跑通的命令，和文档写明的边界"):
   default 64, else a power of two in [32, 4096], read from tests/golden.
+* the LM head (Qwen3-TTS handbook page, section "拓扑": hidden size 1024, a
+  head per codebook): exact rational dot products on tiny rows, one-hot heads
+  that pick and scale hidden entries, and the documented rule for heads that
+  lie outside the weights.
 
 ``PINS`` lists them cheapest first; the mutation test runs them against
 deliberately broken copies of the oracle.
@@ -587,10 +591,120 @@ def pin_repetition_penalty(orc):
             assert np.array_equal(ring, after), (dtype, step)
 
 
+def lm_head_case(rng, n_heads, n_streams, dim, vocabs, *, lo=-6, hi=3):
+    """A frame of n_streams x n_heads rows (row = stream * Q + q) with packed
+    logits, bf16 hidden states and one head per codebook, heads packed one
+    after another at offsets that are multiples of 8 elements.  Values are
+    +-m 2^e with an 8-bit m and e in [lo, hi], so that every dot product of a
+    few dozen terms is exact in fp64."""
+    def bf16(shape):
+        m = rng.integers(128, 256, shape).astype(np.float64)
+        e = rng.integers(lo, hi + 1, shape)
+        sgn = rng.choice([-1.0, 1.0], shape)
+        x = (sgn * m * np.exp2(e - 7)).astype(np.float32)
+        bits = workloads.to_bf16_bits(x)
+        assert np.array_equal(workloads.bf16_bits_to_f32(bits), x)
+        return bits
+    n = n_streams * n_heads
+    rv = np.array([vocabs[r % n_heads] for r in range(n)], np.int32)
+    ro = np.concatenate([[0], np.cumsum(rv)[:-1]]).astype(np.int64)
+    offs, cur = [], 0
+    for q in range(n_heads):
+        offs.append(cur)
+        cur += -(-vocabs[q] * dim // 8) * 8
+    batch = {"n_rows": n, "row_vocab": rv, "row_offsets": ro, "logits_len": int(rv.sum()),
+             "logits": np.zeros(int(rv.sum()), np.float32), "max_row_vocab": int(max(vocabs))}
+    head = {"hidden": bf16(n * dim), "weights": bf16(cur), "head_offsets": np.array(offs, np.int64),
+            "n_heads": n_heads, "dim": dim}
+    return batch, head
+
+
+def pin_lm_head_exact(orc):
+    """Every logit of tiny rows equals the exact rational dot product of the
+    row's hidden state with its codebook's head row (head r mod Q), rounded
+    once to fp32; rows with a head outside the weights or misaligned are NaN,
+    rows with a shape error are left unwritten."""
+    from fractions import Fraction
+    rng = np.random.default_rng(31)
+    for n_heads, n_streams, dim, vocabs in ((3, 2, 16, (5, 7, 3)), (1, 3, 24, (9,)),
+                                            (4, 1, 8, (2, 6, 1, 4))):
+        batch, head = lm_head_case(rng, n_heads, n_streams, dim, vocabs)
+        got = orc.lm_head(batch, head)
+        hv = workloads.bf16_bits_to_f32(head["hidden"]).astype(np.float64)
+        wv = workloads.bf16_bits_to_f32(head["weights"]).astype(np.float64)
+        for r in range(batch["n_rows"]):
+            q, v_r, o = r % n_heads, int(batch["row_vocab"][r]), int(batch["row_offsets"][r])
+            w0 = int(head["head_offsets"][q])
+            for v in range(v_r):
+                exact = sum(Fraction(float(hv[r * dim + k])) * Fraction(float(wv[w0 + v * dim + k]))
+                            for k in range(dim))
+                assert Fraction(float(exact)) == exact  # no rounding before the fp32 one
+                want = np.float32(float(exact))
+                assert got[o + v].view(np.uint32) == want.view(np.uint32), (n_heads, r, v)
+    # heads outside the weights: negative, misaligned, one row past the end
+    batch, head = lm_head_case(rng, 3, 2, 16, (5, 7, 3))
+    w_len = head["weights"].size
+    # a view into a longer buffer: an oracle that reads past weights_len
+    # reads zeros, not unmapped memory
+    head["weights"] = np.concatenate([head["weights"], np.zeros(64, np.uint16)])[:w_len]
+    base = orc.lm_head(batch, head)
+    for q, bad in ((0, -8), (1, int(head["head_offsets"][1]) + 4), (2, w_len - 3 * 16 + 8)):
+        h2 = dict(head)
+        h2["head_offsets"] = head["head_offsets"].copy()
+        h2["head_offsets"][q] = bad
+        got = orc.lm_head(batch, h2)
+        for r in range(batch["n_rows"]):
+            o, v_r = int(batch["row_offsets"][r]), int(batch["row_vocab"][r])
+            seg = got[o:o + v_r]
+            if r % 3 == q:
+                assert np.all(np.isnan(seg)), (q, bad, r)
+            else:
+                assert np.array_equal(seg.view(np.uint32), base[o:o + v_r].view(np.uint32))
+    # the last head ending exactly at the end of the weights is inside them
+    h2 = dict(head)
+    h2["weights"] = head["weights"][:int(head["head_offsets"][2]) + 3 * 16]
+    got = orc.lm_head(batch, h2)
+    assert not np.any(np.isnan(got)) and np.array_equal(got.view(np.uint32), base.view(np.uint32))
+    # a shape error (V = 0 or V above max_row_vocab) leaves the row unwritten
+    b2 = dict(batch)
+    b2["row_vocab"] = batch["row_vocab"].copy()
+    b2["row_vocab"][1] = 0
+    b2["max_row_vocab"] = 6
+    got = orc.lm_head(b2, head)
+    o1, o4 = int(batch["row_offsets"][1]), int(batch["row_offsets"][4])
+    assert not np.any(got[o1:o1 + 7]) and not np.any(got[o4:o4 + 7])  # row 4 is 7 wide
+    o0 = int(batch["row_offsets"][0])
+    assert np.array_equal(got[o0:o0 + 5].view(np.uint32), base[o0:o0 + 5].view(np.uint32))
+
+
+def pin_lm_head_one_hot(orc):
+    """One-hot heads: head q's row v is 2^q at column pi_q(v), so row r's logit
+    v is exactly 2^q h_r[pi_q(v)] (q = r mod Q): a transposed head, a wrong
+    head or a wrong hidden row changes these values."""
+    rng = np.random.default_rng(32)
+    n_heads, n_streams, dim, vocab = 4, 3, 64, 24
+    batch, head = lm_head_case(rng, n_heads, n_streams, dim, (vocab,) * n_heads)
+    w = np.zeros(head["weights"].size, np.float32)
+    perms = [rng.permutation(dim)[:vocab] for _ in range(n_heads)]
+    for q in range(n_heads):
+        w0 = int(head["head_offsets"][q])
+        for v in range(vocab):
+            w[w0 + v * dim + perms[q][v]] = 2.0 ** q
+    head["weights"] = workloads.to_bf16_bits(w)
+    got = orc.lm_head(batch, head)
+    hv = workloads.bf16_bits_to_f32(head["hidden"]).reshape(-1, dim)
+    for r in range(batch["n_rows"]):
+        q, o = r % n_heads, int(batch["row_offsets"][r])
+        want = (hv[r, perms[q]] * np.float32(2.0 ** q)).astype(np.float32)
+        assert np.array_equal(got[o:o + vocab].view(np.uint32), want.view(np.uint32)), r
+
+
 PINS = [
     pin_philox_matches_numpy,
     pin_uniform24_mapping,
     pin_cap_rule,
+    pin_lm_head_one_hot,
+    pin_lm_head_exact,
     pin_greedy_is_argmax,
     pin_topk_set_bruteforce,
     pin_softmax_special_case,

@@ -58,6 +58,18 @@ MUTANTS = {
     "penalty_not_rounded": ("  if (dtype == 1) pen = round_to_bf16(pen);", ""),
     "penalty_ring_slot_late": ("int64_t j = ((t % b->hist_len) + b->hist_len) % b->hist_len;",
                                "int64_t j = ((t + 1) % b->hist_len + b->hist_len) % b->hist_len;"),
+    # the LM head
+    "lm_head_wrong_head": ("const int64_t hoff = head_offsets[r % n_heads];",
+                           "const int64_t hoff = head_offsets[(r / n_heads) % n_heads];"),
+    "lm_head_transposed": ("load_value(1, weights, w0 + k);",
+                           "load_value(1, weights, hoff + (int64_t)k * vr + v);"),
+    "lm_head_float_sum": ("      double acc = 0.0;\n      for (int32_t k = 0; k < dim; ++k)\n",
+                          "      float acc = 0.0f;\n      for (int32_t k = 0; k < dim; ++k)\n"),
+    "lm_head_no_alignment_rule": ("hoff >= 0 && hoff % 8 == 0 && hoff <=", "hoff >= 0 && hoff <="),
+    "lm_head_bound_one_row_short": ("hoff <= weights_len - (int64_t)vr * dim;",
+                                    "hoff <= weights_len - (int64_t)(vr - 1) * dim;"),
+    "lm_head_next_hidden_row": ("const int64_t h0 = r * (int64_t)dim;",
+                                "const int64_t h0 = ((r + 1) % n_rows) * (int64_t)dim;"),
     # the boundary margin that excuses rows from the bit-exact rule
     "margin_draw_unnormalised": ("double d = fabs(c - u);", "double d = fabs(cum - u);"),
     "margin_cut_exclusive_prefix": ("double d = fabs(cum - (double)top_p);",
