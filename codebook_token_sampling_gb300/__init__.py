@@ -6,10 +6,13 @@ only for device memory and streams.  The functions keep the C names:
 
     ts_create, ts_destroy, ts_max_top_k, ts_sample, ts_sample_debug,
     ts_sample_steps, ts_reserve, ts_sample_noalloc, ts_advance_steps,
-    ts_read_status, ts_set_option, ts_plan, ts_status_string, ts_last_error
+    ts_read_status, ts_set_option, ts_plan, ts_status_string, ts_last_error,
+    ts_lm_head_logits, ts_lm_head_sample
 
 ``Sampler`` wraps a handle; ``DeviceBatch`` holds one step's per-row arrays on
-the GPU with a prebuilt ``ts_batch`` so that repeated calls marshal nothing.
+the GPU with a prebuilt ``ts_batch`` so that repeated calls marshal nothing;
+``LmHead`` holds a frame's hidden states and output heads with a prebuilt
+``ts_lm_head``.
 Importing this module loads the compiled library and raises if it is missing;
 there is no fallback.
 """
@@ -44,10 +47,13 @@ TS_MAX_VOCAB_BF16 = 163840
 TS_MAX_VOCAB_F32 = 81920
 TS_NOALLOC_SCRATCH_BYTES = 4194304
 TS_NOALLOC_MAX_ROWS = 64
+TS_LM_HEAD_DIM_STEP = 64
+TS_LM_HEAD_MAX_DIM = 16384
 
 EXPORTED = ("ts_create", "ts_destroy", "ts_max_top_k", "ts_sample", "ts_sample_debug",
             "ts_sample_steps", "ts_reserve", "ts_sample_noalloc", "ts_advance_steps",
-            "ts_read_status", "ts_set_option", "ts_plan", "ts_status_string", "ts_last_error")
+            "ts_read_status", "ts_set_option", "ts_plan", "ts_status_string", "ts_last_error",
+            "ts_lm_head_logits", "ts_lm_head_sample")
 
 
 class TsBatch(ctypes.Structure):
@@ -100,6 +106,18 @@ class TsSteps(ctypes.Structure):
     ]
 
 
+class TsLmHead(ctypes.Structure):
+    """Mirror of ``ts_lm_head``."""
+    _fields_ = [
+        ("hidden", ctypes.c_void_p),
+        ("weights", ctypes.c_void_p),
+        ("weights_len", ctypes.c_int64),
+        ("head_offsets", ctypes.c_void_p),
+        ("dim", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32),
+    ]
+
+
 class SamplerError(RuntimeError):
     def __init__(self, status: int, what: str):
         detail = _lib.ts_last_error().decode() if status == TS_ERR_CUDA else ""
@@ -127,6 +145,10 @@ def _load(path: str):
         "ts_read_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
         "ts_set_option": ([vp, i32, i32], ctypes.c_int),
         "ts_plan": ([vp, ctypes.POINTER(TsBatch)] + [ctypes.POINTER(i32)] * 5, ctypes.c_int),
+        "ts_lm_head_logits": ([vp, ctypes.POINTER(TsLmHead), ctypes.POINTER(TsBatch), vp],
+                              ctypes.c_int),
+        "ts_lm_head_sample": ([vp, ctypes.POINTER(TsLmHead), ctypes.POINTER(TsBatch), vp],
+                              ctypes.c_int),
         "ts_status_string": ([ctypes.c_int], ctypes.c_char_p),
         "ts_last_error": ([], ctypes.c_char_p),
     }
@@ -231,6 +253,16 @@ def ts_plan(handle: int, batch: "DeviceBatch") -> dict:
            "ts_plan")
     keys = ("path", "ctas_per_row", "threads", "smem_bytes", "grid")
     return {k: int(o.value) for k, o in zip(keys, out)}
+
+
+def ts_lm_head_logits(handle: int, head: "LmHead", batch: "DeviceBatch", stream=None) -> None:
+    _check(_lib.ts_lm_head_logits(handle, ctypes.byref(head.c), ctypes.byref(batch.c),
+                                  _stream_ptr(stream)), "ts_lm_head_logits")
+
+
+def ts_lm_head_sample(handle: int, head: "LmHead", batch: "DeviceBatch", stream=None) -> None:
+    _check(_lib.ts_lm_head_sample(handle, ctypes.byref(head.c), ctypes.byref(batch.c),
+                                  _stream_ptr(stream)), "ts_lm_head_sample")
 
 
 def ts_status_string(status: int) -> str:
@@ -426,3 +458,37 @@ class DeviceBatch:
 
     def eos(self) -> np.ndarray:
         return self.out_eos.cpu().numpy()
+
+
+class LmHead:
+    """A frame's hidden states and output heads in device memory plus the
+    ``ts_lm_head`` (see ``ts_lm_head_logits``).
+
+    ``head`` is a dict of numpy arrays: ``hidden`` (bf16 bits, n_rows x dim),
+    ``weights`` (bf16 bits), ``head_offsets`` (int64 per head), ``n_heads``
+    and ``dim``; row r uses head r mod n_heads.  ``set_weights`` and
+    ``set_hidden`` point the call at other device tensors of the same layout.
+    """
+
+    def __init__(self, head: dict, device="cuda"):
+        import torch
+        self.device = torch.device(device)
+        self.hidden = _to_device(np.asarray(head["hidden"], np.uint16), np.uint16, self.device)
+        self.weights = _to_device(np.asarray(head["weights"], np.uint16), np.uint16, self.device)
+        self.head_offsets = _to_device(head["head_offsets"], np.int64, self.device)
+        c = TsLmHead()
+        c.head_offsets = self.head_offsets.data_ptr()
+        c.dim = int(head["dim"])
+        c.n_heads = int(head["n_heads"])
+        self.c = c
+        self.set_hidden(self.hidden)
+        self.set_weights(self.weights)
+
+    def set_hidden(self, t) -> None:
+        self.hidden = t
+        self.c.hidden = t.data_ptr()
+
+    def set_weights(self, t) -> None:
+        self.weights = t
+        self.c.weights = t.data_ptr()
+        self.c.weights_len = t.numel()

@@ -14,6 +14,7 @@
 #include "../../include/ts_sampler.h"
 #include "ts_cluster.cuh"
 #include "ts_device.cuh"
+#include "ts_lmhead.cuh"
 #include "ts_split.cuh"
 #include "ts_warp.cuh"
 #include "ts_wide.cuh"
@@ -32,6 +33,7 @@ struct ts_sampler {
   uint32_t *ticket;   // the warp path's fused step advance: blocks done so far
   int occ_warp[2][5][3];  // resident blocks per SM of each warp-path variant
   int occ_seg[2];         // of the segmented 16-column, one-warp-per-row variant
+  int occ_seg32;          // of the fp32 32-column variant (16 columns staged at a time)
   void *ws;           // split wide path workspace (ts_reserve), or null
   size_t ws_bytes;
   int ws_rows;        // row records it holds
@@ -62,7 +64,8 @@ int cap_of(int requested) {
 }
 
 constexpr int kWarpMaxBF16 = 4096;
-constexpr int kWarpMaxF32 = 2048;
+constexpr int kWarpMaxF32 = 4096;
+constexpr int kWarpMaxF32Penalty = 2048;  // rows the penalty edits in one staged pass
 // bf16 rows wider than this take a single-pass wide path
 constexpr int kWideMinVocab = 32768;
 // split path: slices of about this many tokens at most (76 KB of bf16)
@@ -83,7 +86,7 @@ struct Plan {
   int path;   // 1 warp(s) per row, 2 cluster, 3 wide, 4 split
   int nch;    // warp path: 16-byte chunks per lane
   int wpr;    // warp path: warps per row
-  int seg;    // warp path: 1 = the stage holds 8 of the 16 columns (segments)
+  int seg;    // warp path: 1 = the stage holds 8 of 16 columns, 2 = 16 of 32 (fp32)
   int g;      // cluster and wide paths: CTAs per row
   int slice;  // cluster and wide paths: elements per CTA
   int threads;
@@ -105,6 +108,9 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl, int n_step
   if (!path) path = warp_ok ? 1 : (bf16 && vmax > kWideMinVocab ? (split_ok ? 4 : 3) : 2);
   if (path == 1 && !warp_ok) return TS_ERR_INVALID_ARG;
   if (b->hist_ring && path != 1) return TS_ERR_UNSUPPORTED;  // the penalty is on the warp path
+  // the penalty edits the staged row in place: rows staged in two passes
+  // (fp32 wider than 2048) would lose the first pass's edits
+  if (b->hist_ring && !bf16 && vmax > kWarpMaxF32Penalty) return TS_ERR_UNSUPPORTED;
   if (path == 3 && !bf16) return TS_ERR_INVALID_ARG;
   std::memset(pl, 0, sizeof *pl);
   pl->path = path;
@@ -146,13 +152,15 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl, int n_step
   if (path == 1) {
     const int epc = bf16 ? 8 : 4;
     const int per_lane = (vmax + 32 * epc - 1) / (32 * epc);  // 16-byte chunks per lane
-    pl->nch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8 : 16;
+    pl->nch = per_lane <= 1 ? 1 : per_lane <= 2 ? 2 : per_lane <= 4 ? 4 : per_lane <= 8 ? 8
+            : per_lane <= 16 ? 16 : 32;
     // small batches share each row among several warps (a shorter chain per
     // row while the GPU has room); large ones keep one warp per row
     const long long rows = static_cast<long long>(b->n_rows) * n_steps;
     // (measured on the 128 x 10 step: 1 warp per row 9.5 us, 2 10.2 us, 4 12.2 us)
     int wpr = s->force_wpr;
     if (!wpr) wpr = rows <= s->num_sms ? 4 : rows <= 4LL * s->num_sms ? 2 : 1;
+    if (pl->nch == 32) wpr = 1;  // fp32 rows wider than 2048: one warp, two staged passes
     const int rpb = ts::kTowerWarps / wpr;
     pl->wpr = wpr;
     pl->g = wpr;
@@ -161,8 +169,10 @@ ts_status make_plan(const ts_sampler *s, const ts_batch *b, Plan *pl, int n_step
     // one row per row group while the grid fits on the GPU at once; beyond
     // that a resident grid whose groups walk several rows each
     const int ni = pl->nch == 1 ? 0 : pl->nch == 2 ? 1 : pl->nch == 4 ? 2 : pl->nch == 8 ? 3 : 4;
-    const int occ = s->occ_warp[bf16 ? 1 : 0][ni][wpr == 1 ? 0 : wpr == 2 ? 1 : 2];
+    const int occ = pl->nch == 32 ? s->occ_seg32
+                                  : s->occ_warp[bf16 ? 1 : 0][ni][wpr == 1 ? 0 : wpr == 2 ? 1 : 2];
     long long resident = static_cast<long long>(s->num_sms) * std::max(occ, 1);
+    if (pl->nch == 32) pl->seg = 2;
     // more rows than row groups on the GPU at once: the groups walk several
     // rows each, and the 16-column variant stages 8 columns at a time (half
     // the shared memory, so more warps per SM)
@@ -273,6 +283,11 @@ void *warp_kernel_wpr(int nch) {
 
 template <class K>
 void *warp_kernel_for(int nch, int wpr, int seg = 0) {
+  if (seg == 2) {  // fp32 only: 32 columns, 16 staged at a time
+    if constexpr (std::is_same<K, ts::KeyF32>::value)
+      return reinterpret_cast<void *>(ts::row_sampler_kernel<ts::KeyF32, 32, 1, 16>);
+    return nullptr;
+  }
   if (seg) return reinterpret_cast<void *>(ts::row_sampler_kernel<K, 16, 1, 8>);
   if (wpr == 4) return warp_kernel_wpr<K, 4>(nch);
   if (wpr == 2) return warp_kernel_wpr<K, 2>(nch);
@@ -318,6 +333,8 @@ ts_status set_attributes(int device) {
   }
   fns[n++] = reinterpret_cast<void *>(ts::split_stream_kernel);
   fns[n++] = reinterpret_cast<void *>(ts::split_tail_kernel);
+  fns[n++] = warp_kernel_for<ts::KeyF32>(32, 1, 2);
+  fns[n++] = reinterpret_cast<void *>(ts::lm_head_kernel);
   for (int i = 0; i < n; ++i) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, fns[i]);
@@ -359,6 +376,9 @@ ts_status warp_occupancy(ts_sampler *s) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
     s->occ_seg[d] = n;
   }
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &s->occ_seg32, warp_kernel_for<ts::KeyF32>(32, 1, 2), ts::kTowerThreads, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
   return TS_OK;
 }
 
@@ -500,6 +520,59 @@ ts_status launch(const ts_sampler *s, const ts_batch *b, const ts::Params &base,
 }
 
 // ---------------------------------------------------------------------------
+// The LM head (ts_lm_head_logits / ts_lm_head_sample)
+// ---------------------------------------------------------------------------
+ts_status check_lm_head(const ts_lm_head *h, const ts_batch *b) {
+  if (!h || !b) return TS_ERR_INVALID_ARG;
+  if (b->dtype != TS_DTYPE_F32) return TS_ERR_INVALID_ARG;  // the head writes fp32 logits
+  if (h->n_heads < 1 || h->dim < TS_LM_HEAD_DIM_STEP || h->dim > TS_LM_HEAD_MAX_DIM ||
+      h->dim % TS_LM_HEAD_DIM_STEP || h->weights_len < 0)
+    return TS_ERR_INVALID_ARG;
+  if (b->n_rows % h->n_heads) return TS_ERR_INVALID_ARG;
+  if (b->n_rows == 0) return TS_OK;
+  if (!h->hidden || !h->weights || !h->head_offsets) return TS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(h->hidden) % 16 || reinterpret_cast<uintptr_t>(h->weights) % 16)
+    return TS_ERR_INVALID_ARG;
+  if (b->max_row_vocab > TS_MAX_VOCAB_F32) return TS_ERR_UNSUPPORTED;
+  return TS_OK;
+}
+
+ts_status launch_lm_head(const ts_sampler *s, const ts_lm_head *h, const ts_batch *b,
+                         cudaStream_t st) {
+  static_assert(ts::kLmKC == TS_LM_HEAD_DIM_STEP, "the header's dim rule is the stage depth");
+  ts::LmParams p;
+  std::memset(&p, 0, sizeof p);
+  p.hidden = static_cast<const uint16_t *>(h->hidden);
+  p.weights = static_cast<const uint16_t *>(h->weights);
+  p.weights_len = h->weights_len;
+  p.head_offsets = h->head_offsets;
+  p.n_heads = h->n_heads;
+  p.dim = h->dim;
+  p.n_rows = b->n_rows;
+  p.max_row_vocab = b->max_row_vocab;
+  p.row_vocab = b->row_vocab;
+  p.row_offsets = b->row_offsets;
+  p.logits = static_cast<float *>(const_cast<void *>(b->logits));
+  p.logits_len = b->logits_len;
+  const int streams = b->n_rows / h->n_heads;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>((b->max_row_vocab + ts::kLmN - 1) / ts::kLmN),
+                     static_cast<unsigned>(h->n_heads),
+                     static_cast<unsigned>((streams + ts::kLmM - 1) / ts::kLmM));
+  cfg.blockDim = dim3(ts::kLmThreads);
+  cfg.dynamicSmemBytes = ts::kLmSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = s->pdl ? 1 : 0;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ts::lm_head_kernel, p);
+  return e == cudaSuccess ? TS_OK : cuda_fail(e, "LM head launch");
+}
+
+// ---------------------------------------------------------------------------
 // ts_sample_noalloc: per-device set-up and geometry
 // ---------------------------------------------------------------------------
 constexpr size_t kNoallocWsOff = 256;  // the workspace follows the status slot
@@ -594,6 +667,7 @@ ts_status ts_create(int device, int max_top_k, ts_sampler **out) {
   s->ticket = nullptr;
   std::memset(s->occ_warp, 0, sizeof s->occ_warp);
   std::memset(s->occ_seg, 0, sizeof s->occ_seg);
+  s->occ_seg32 = 0;
   s->ws = nullptr;
   s->ws_bytes = 0;
   s->ws_rows = 0;
@@ -646,6 +720,30 @@ ts_status ts_sample(ts_sampler *s, const ts_batch *b, void *stream) {
   ts_status rc = check_batch(b);
   if (rc != TS_OK || b->n_rows == 0) return rc;
   return launch(s, b, make_params(s, b), static_cast<cudaStream_t>(stream));
+}
+
+ts_status ts_lm_head_logits(ts_sampler *s, const ts_lm_head *h, const ts_batch *b, void *stream) {
+  if (!s) return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK) return rc;
+  rc = check_lm_head(h, b);
+  if (rc != TS_OK || b->n_rows == 0) return rc;
+  return launch_lm_head(s, h, b, static_cast<cudaStream_t>(stream));
+}
+
+ts_status ts_lm_head_sample(ts_sampler *s, const ts_lm_head *h, const ts_batch *b, void *stream) {
+  if (!s) return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK) return rc;
+  rc = check_lm_head(h, b);
+  if (rc != TS_OK || b->n_rows == 0) return rc;
+  Plan pl;  // refuse what the sampler would refuse before the head runs
+  rc = make_plan(s, b, &pl);
+  if (rc != TS_OK) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  rc = launch_lm_head(s, h, b, st);
+  if (rc != TS_OK) return rc;
+  return launch(s, b, make_params(s, b), st);
 }
 
 ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep, int32_t *kept_ids,

@@ -1,4 +1,4 @@
-// ts_warp.cuh -- warp-path sampler for rows of up to 4096 bf16 / 2048 fp32
+// ts_warp.cuh -- warp-path sampler for rows of up to 4096 bf16 or fp32
 // logits with a top-k cap of at most 64 (the serving configuration: top_k 30
 // under the default cap 64, Drama 3 article sections "测试口径" and
 // "能跑通的命令，和文档写明的边界").
@@ -874,8 +874,9 @@ __device__ __forceinline__ void advance_steps_last_block(const Params &p) {
   if (threadIdx.x == 0) *p.ticket = 0u;
 }
 
-// MAXNCH = most 16-byte chunks per lane of any row in the launch (1, 2, 4, 8
-// or 16); WPR = warps per row (1, 2 or 4); STG = chunk columns the stage
+// MAXNCH = most 16-byte chunks per lane of any row in the launch (1, 2, 4, 8,
+// 16, or 32 for fp32 rows wider than 2048); WPR = warps per row (1, 2 or 4);
+// STG = chunk columns the stage
 // holds (MAXNCH, or fewer for one warp per row: wider rows then go through
 // the stage in segments of STG columns, read twice, the second time from L2;
 // a smaller stage lets more warps share an SM).  A block of four warps holds

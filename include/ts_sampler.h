@@ -148,7 +148,8 @@ typedef struct {
    * drawn id into the slot of its step (finished and error rows write
    * nothing); no two rows of a call share a column.  The caller fills the
    * ring with -1 to start.  Warp path only (top-k cap <= 64, rows up to 4096
-   * bf16 / 2048 fp32; others return TS_ERR_UNSUPPORTED), 1 <= hist_len <= 32,
+   * bf16 / 2048 fp32: a wider fp32 row is staged in two passes and would lose
+   * the first pass's edits; others return TS_ERR_UNSUPPORTED), 1 <= hist_len <= 32,
    * not in ts_sample_steps.  Row errors: codebook[r] outside [0,
    * hist_codebooks) is a shape error, theta NaN, infinite or <= 0 a parameter
    * error. */
@@ -294,7 +295,7 @@ ts_status ts_sample_noalloc(int32_t max_top_k, const ts_batch *b, uint32_t *stat
  * flags never come ends within about one limit.  No kernel waits on
  * another kernel: a flag must be set by the host, by a copy, or before the
  * launch.  Only the warp path runs it: top-k cap <= 64, rows of at most 4096
- * bf16 / 2048 fp32 logits; anything else returns TS_ERR_UNSUPPORTED.
+ * bf16 or fp32 logits; anything else returns TS_ERR_UNSUPPORTED.
  * Asynchronous and graph-capturable like ts_sample; ts_sample_debug has no
  * multi-step form. */
 #define TS_ROW_NOT_READY 16u
@@ -309,6 +310,64 @@ typedef struct {
 } ts_steps;
 ts_status ts_sample_steps(ts_sampler *s, const ts_batch *b, const ts_steps *st, void *stream);
 
+/* The LM head of a frame's rows, the step before sampling.  The Qwen3-TTS
+ * handbook page ("案例一：Qwen3-TTS——三个 stage 与首包延迟", section "拓扑")
+ * gives the shape: a hidden size of 1024, 16 codebooks of 2048 entries per
+ * frame, each codebook's logits the product of a hidden state and that
+ * codebook's output head; the Drama 3 article (section "两阶段共享一张卡")
+ * has one forward per frame produce every codebook's logits and sample them
+ * on the device with no host synchronisation.
+ *
+ * Rows are a frame in stream-major order: n_rows = streams x n_heads and row r
+ * (stream r / n_heads) uses head q = r mod n_heads.  Row r's logits are
+ *   l_r[v] = sum_k hidden[r * dim + k] * weights[head_offsets[q] + v * dim + k]
+ * for v < row_vocab[r], bf16 products accumulated in fp32 on the tensor cores
+ * (in an order the kernel fixes, so they differ from the exactly rounded sum
+ * by a few fp32 roundings), written as fp32 to the batch's logits at
+ * row_offsets[r].  Rows of one head may have different widths; head q must
+ * then hold as many rows as its widest row.
+ *
+ * Every pointer is a device pointer owned by the caller.  hidden: [n_rows]
+ * [dim] bf16 bits, 16-byte aligned.  weights: bf16 bits, 16-byte aligned,
+ * weights_len elements; head q's rows of dim elements start at element
+ * head_offsets[q] (a device array of n_heads entries).  dim: a multiple of
+ * TS_LM_HEAD_DIM_STEP up to TS_LM_HEAD_MAX_DIM.
+ *
+ * Errors.  Host side (nothing launched): TS_ERR_INVALID_ARG for a NULL or
+ * misaligned pointer, a dim or n_heads outside the rules, n_rows not a
+ * multiple of n_heads, or a batch whose dtype is not TS_DTYPE_F32 (the head
+ * writes fp32 logits); TS_ERR_UNSUPPORTED for max_row_vocab above
+ * TS_MAX_VOCAB_F32.  Per row: a head that does not lie inside the weights
+ * (a negative offset, an offset that is not a multiple of 8 elements, or
+ * fewer than row_vocab[r] rows before weights_len) gives NaN logits, which
+ * sampling reports as TS_ROW_NONFINITE; a row with a shape error (width <= 0
+ * or above max_row_vocab, logits outside the buffer) is not written and
+ * sampling reports TS_ROW_BAD_SHAPE. */
+#define TS_LM_HEAD_DIM_STEP 64
+#define TS_LM_HEAD_MAX_DIM 16384
+typedef struct {
+  const void *hidden;            /* [n_rows][dim] bf16 bits */
+  const void *weights;           /* bf16 bits, the heads' rows */
+  int64_t weights_len;           /* elements in weights */
+  const int64_t *head_offsets;   /* [n_heads] element offset of each head's first row */
+  int32_t dim;                   /* hidden size */
+  int32_t n_heads;               /* codebooks per frame */
+} ts_lm_head;
+
+/* Writes the LM head's fp32 logits into b->logits (which must be writable
+ * device memory of logits_len floats) on `stream`; samples nothing.  Only the
+ * batch's shape fields are used (n_rows, max_row_vocab, row_vocab,
+ * row_offsets, logits, logits_len, dtype), but the batch must pass the checks
+ * of ts_sample.  Asynchronous, graph-capturable, no allocation. */
+ts_status ts_lm_head_logits(ts_sampler *s, const ts_lm_head *h, const ts_batch *b, void *stream);
+
+/* ts_lm_head_logits, then ts_sample on the same batch, in one call: two
+ * launches on `stream`, the sampler's scheduled while the head drains
+ * (programmatic dependent launch) and reading the logits after the head has
+ * completed.  The logits (a few MB per frame) go through L2 between the two;
+ * a host-side refusal of the sampler is returned before the head launches. */
+ts_status ts_lm_head_sample(ts_sampler *s, const ts_lm_head *h, const ts_batch *b, void *stream);
+
 /* step[i] += 1 for i < n_streams, on the device (graph-capturable).  Call it
  * after the step's ts_sample so that sibling rows of one stream share a step
  * (or set ts_batch.advance_steps, which does the same inside the call). */
@@ -320,7 +379,8 @@ ts_status ts_read_status(ts_sampler *s, uint32_t *bits, void *stream);
 
 /* Testing / tuning options.  TS_OPT_PATH: 0 = automatic, 1 = one to four
  * warps per row with a bounded candidate set (requires cap <= 64 and
- * max_row_vocab <= 4096 bf16 / 2048 fp32), 2 = CTA or cluster per row that
+ * max_row_vocab <= 4096; fp32 rows wider than 2048 always take one warp per
+ * row), 2 = CTA or cluster per row that
  * holds the row in shared memory, 3 = the single-pass wide-row cluster path
  * (bf16 only; automatic for bf16 rows wider than 32,768 without a
  * workspace), 4 = the split wide-row path (bf16 only; needs ts_reserve;

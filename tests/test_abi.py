@@ -63,11 +63,12 @@ def _c_layout(tmp_path, struct, fields):
 
 
 def test_binding_structs_match_the_header(tmp_path):
-    """Every field of the binding's ts_batch and ts_steps mirrors sits at the
-    header's offset, and the sizes agree (a field missing, added or moved on
-    either side fails here)."""
+    """Every field of the binding's ts_batch, ts_steps and ts_lm_head mirrors
+    sits at the header's offset, and the sizes agree (a field missing, added
+    or moved on either side fails here)."""
     import codebook_token_sampling_gb300 as ts
-    for struct, mirror in (("ts_batch", ts.TsBatch), ("ts_steps", ts.TsSteps)):
+    for struct, mirror in (("ts_batch", ts.TsBatch), ("ts_steps", ts.TsSteps),
+                           ("ts_lm_head", ts.TsLmHead)):
         fields = [name for name, _ in mirror._fields_]
         want = [getattr(mirror, f).offset for f in fields] + [ctypes.sizeof(mirror)]
         assert _c_layout(tmp_path, struct, fields) == want, struct

@@ -138,6 +138,16 @@ def test_history_limits(ts):
     with pytest.raises(ts.SamplerError) as e:
         s.sample(b)
     assert e.value.status == ts.TS_ERR_INVALID_ARG
+    # fp32 rows wider than 2048 go through the stage in two passes, and the
+    # penalty edits the staged row in place: refused
+    host = workloads.make("qwen3tts", 0)
+    host["logits"] = workloads.bf16_bits_to_f32(host["logits"])
+    host["dtype"] = "f32"
+    b = ts.DeviceBatch(host, "cuda", history={"len": 4, "codebooks": 16,
+                                              "penalty": np.ones(host["n_rows"], np.float32)})
+    with pytest.raises(ts.SamplerError) as e:
+        s.sample(b)
+    assert e.value.status == ts.TS_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert np.all(b.ids() == -2)
     s.close()

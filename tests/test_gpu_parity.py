@@ -213,6 +213,74 @@ def test_edge_rows(ts, dtype, path, wpr):
     s.close()
 
 
+def _wide_f32_batch(rng):
+    """fp32 rows of 2049 to 4096 logits (the warp path's two staged passes):
+    gaussian, spiked, full ties (more candidates than the sorted set holds),
+    a NaN or +inf in the second pass only, -inf everywhere but the second
+    pass, and misaligned starts."""
+    rows = []
+    nrm = lambda n, sd=2.0: rng.normal(0, sd, n).astype(np.float32)
+    rows += [(nrm(2049), 1.0, 30, 0.9), (nrm(3072), 1.0, 30, 0.9), (nrm(4096), 0.8, 64, 0.95),
+             (nrm(3500, 0.3), 1.2, 1, 0.9), (nrm(4001), 1.0, 0, 1.0)]
+    x = nrm(3072)
+    x[rng.choice(3072, 4, replace=False)] += 12.0
+    rows += [(x, 1.0, 30, 0.9)]
+    rows += [(np.full(4096, 0.25, np.float32), 1.0, 30, 0.9)]             # full ties
+    rows += [(rng.choice([0.0, 0.5, 1.0], 3333).astype(np.float32), 1.0, 64, 0.9)]
+    y = nrm(3000)
+    y[2900] = np.nan
+    rows += [(y, 1.0, 30, 0.9)]
+    y = nrm(4096)
+    y[4095] = np.inf
+    rows += [(y, 1.0, 30, 0.9)]
+    y = np.full(3100, -np.inf, np.float32)
+    y[[2100, 2500, 3099]] = [0.0, 1.0, 0.5]
+    rows += [(y, 1.0, 30, 0.9)]
+    rows += [(nrm(700), 1.0, 30, 0.9), (nrm(5), 1.0, 30, 0.9)]            # narrow rows beside them
+    n = len(rows)
+    gap = rng.integers(0, 4, n)
+    offs, parts, pos = [], [], 0
+    for (vals, *_), g in zip(rows, gap):
+        parts.append(np.zeros(int(g), np.float32))
+        pos += int(g)
+        offs.append(pos)
+        parts.append(vals)
+        pos += vals.size
+    host = {
+        "dtype": "f32", "logits": np.concatenate(parts), "n_rows": n, "n_streams": n,
+        "n_codebooks": 1, "row_vocab": np.array([r[0].size for r in rows], np.int32),
+        "row_offsets": np.array(offs, np.int64),
+        "temp": np.array([r[1] for r in rows], np.float32),
+        "top_k": np.array([r[2] for r in rows], np.int32),
+        "top_p": np.array([r[3] for r in rows], np.float32),
+        "seed": np.arange(n, dtype=np.uint64) * np.uint64(131), "request": np.arange(n, dtype=np.uint64),
+        "codebook": np.zeros(n, np.int32), "row_stream": np.arange(n, dtype=np.int32),
+        "step": np.full(n, 9, np.int64), "eos_id": np.full(n, 3, np.int32),
+        "feedback_slot": np.arange(n, dtype=np.int32), "feedback_len": n, "cap": 64,
+    }
+    host["max_row_vocab"] = int(host["row_vocab"].max())
+    return host
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_wide_f32_rows_on_the_warp_path(ts, seed):
+    """fp32 rows wider than 2048 stay on the warp path (one warp per row, 16
+    of 32 chunk columns staged at a time) and match the oracle."""
+    host = _wide_f32_batch(np.random.default_rng(40 + seed))
+    ref = oracle.sample(host, max_keep=64)
+    assert np.any(ref["err"] == 4)
+    s = make_sampler(ts, 64)
+    gpu = run_gpu(s, host, debug_keep=64)
+    b = ts.DeviceBatch(host, "cuda")
+    assert s.plan(b)["path"] == 1
+    compare(host, gpu, ref, label=f"wide f32 {seed}")
+    r = 6  # full ties: the kept set is the 30 lowest indices
+    assert sorted(gpu["kept_ids"][r, :30].tolist()) == list(range(30))
+    plain = run_gpu(s, host)
+    assert np.array_equal(plain["ids"], gpu["ids"])
+    s.close()
+
+
 def test_shape_and_slot_errors(ts):
     host = workloads.make("tiny", 2)
     host["row_vocab"] = np.array([2048, 0, 2048, 2048], np.int32)

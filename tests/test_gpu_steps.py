@@ -130,6 +130,53 @@ def test_sample_steps_matches_single_steps(ts, name, steps, wpr):
     s.close()
 
 
+def test_sample_steps_wide_f32(ts):
+    """The qwen3tts frame with fp32 logits (rows of 3072 and 2048: the warp
+    path's 32-column fp32 variant, two staged passes per 3072-wide row): one
+    launch over five steps equals five separate calls and the oracle."""
+    steps = 5
+    hosts = []
+    for i in range(steps):
+        h = workloads.make("qwen3tts", i)
+        h["logits"] = workloads.bf16_bits_to_f32(h["logits"])
+        h["dtype"] = "f32"
+        hosts.append(h)
+    host = hosts[0]
+    n, per_step = int(host["n_rows"]), int(host["logits"].size)
+    buf = torch.from_numpy(np.concatenate([h["logits"] for h in hosts])).cuda()
+    s = ts.Sampler(0, host["cap"])
+    single = ts.DeviceBatch(host, "cuda")
+    assert s.plan(single)["path"] == 1
+    want = []
+    for i in range(steps):
+        single.set_logits(buf[i * per_step:(i + 1) * per_step])
+        s.sample(single)
+        ts.ts_advance_steps(single.step)
+        want.append(single.out_ids.clone())
+    multi = ts.DeviceBatch(host, "cuda", advance_steps=True)
+    multi.set_logits(buf)
+    out_ids = torch.full((steps, n), -3, dtype=torch.int32, device="cuda")
+    out_eos = torch.zeros((steps, n), dtype=torch.uint8, device="cuda")
+    multi.c.out_ids = out_ids.data_ptr()
+    multi.c.out_eos = out_eos.data_ptr()
+    multi.c.feedback_buf = None
+    multi.c.feedback_slot = None
+    multi.c.feedback_len = 0
+    s.sample_steps(multi, steps, logits_step_stride=per_step, out_step_stride=n)
+    torch.cuda.synchronize()
+    assert s.read_status() == 0
+    got = out_ids.cpu().numpy()
+    assert np.array_equal(got, torch.stack(want).cpu().numpy())
+    for i in (0, steps - 1):
+        h = dict(hosts[i])
+        h["step"] = np.asarray(host["step"]) + i
+        ref = oracle.sample(h, max_keep=h["cap"], n_threads=8)
+        safe = ref["margin"] > 1e-5
+        assert safe.sum() >= 0.9 * n
+        assert np.array_equal(got[i][safe], ref["ids"][safe])
+    s.close()
+
+
 def test_many_rows_per_group(ts):
     """One ts_sample call over 64 steps' rows (81,920 rows: a resident grid
     whose row groups walk many rows each) equals 64 separate calls."""

@@ -21,6 +21,13 @@ oracle.  The shapes stand in for the model outputs of the pages' serving runs
 * mixed     256 rows x V=4096 bf16 Student-t(3); per-row top_k from
             {1, 32, 64, ..., 4096}, top_p ~ U[0.5, 1] (16 rows forced to 1),
             temperature ~ U[0.6, 1.4]; cap 4096.
+* lm_head   (``make_lm_head``) the qwen3tts frame (32 streams x 16 codebooks,
+            V = 3072 / 2048, EOS 2150) with its logits produced by an LM head:
+            hidden states bf16 N(0, 1) of size 1024 (the talker's hidden size,
+            "案例一：Qwen3-TTS", section "拓扑"), drawn anew each step, and one
+            head per codebook with bf16 N(0, (2.5 / 32)^2) weights, fixed
+            across steps, so that the logits are about N(0, 2.5^2); fp32
+            logits; top_k 30, top_p 0.9, T 1.0, cap 64.
 * stress    rows x V=151936 bf16, l_i = -1.1 ln(r_i) + 3 z_i with r a random
             permutation of 1..V (a Zipf(1.1)-shaped tail) and z ~ N(0,1);
             top_k 4096, top_p 0.9, cap 4096.
@@ -183,3 +190,26 @@ def logit_bytes(batch: dict) -> int:
     """Bytes of logits a step reads (sum of row widths times element size)."""
     es = 2 if batch["dtype"] == "bf16" else 4
     return int(np.asarray(batch["row_vocab"], np.int64).sum()) * es
+
+
+def make_lm_head(step: int = 0, *, streams: int = 32, dim: int = 1024, vocabs=None,
+                 eos_ids=None, weight_seed: int = 0) -> tuple[dict, dict]:
+    """One frame for the LM head: the batch (fp32 logits buffer, zeroed, that
+    the head fills) and the head inputs (``hidden``, ``weights``,
+    ``head_offsets``, ``n_heads``, ``dim``); row r uses head r mod Q."""
+    vocabs = [3072] + [2048] * 15 if vocabs is None else list(vocabs)
+    q = len(vocabs)
+    eos_ids = ([2150] + [-1] * (q - 1)) if eos_ids is None else list(eos_ids)
+    n, cb, rs, rv, ro, eos = _frame_layout(streams, vocabs, eos_ids)
+    t, k, p = _params(n, 1.0, 30, 0.9)
+    batch = _batch("lm_head", "f32", np.zeros(int(rv.sum()), np.float32), streams, q, cb, rs,
+                   rv, ro, eos, t, k, p, 64, step, 5000)
+    rng = _rng("qwen3tts", 1 << 20, step, streams, dim)
+    hidden = to_bf16_bits(rng.standard_normal(n * dim, dtype=np.float32))
+    offs = np.zeros(q, np.int64)
+    offs[1:] = np.cumsum(np.asarray(vocabs[:-1], np.int64) * dim)
+    wrng = _rng("qwen3tts", 1 << 21, weight_seed, dim)
+    sigma = np.float32(2.5 / np.sqrt(dim))
+    weights = to_bf16_bits(sigma * wrng.standard_normal(int(sum(vocabs)) * dim, dtype=np.float32))
+    head = {"hidden": hidden, "weights": weights, "head_offsets": offs, "n_heads": q, "dim": dim}
+    return batch, head
