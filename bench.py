@@ -430,6 +430,93 @@ def time_levels(sampler, host, bufs, dev, k, repeats, stream):
     return times, len(levels)
 
 
+def lm_head_bytes(batch, head) -> int:
+    """Algorithmic bytes of one LM-head call: every head row and hidden state
+    read once (bf16), every fp32 logit written once."""
+    return int(np.asarray(head["weights"]).size * 2 + np.asarray(head["hidden"]).size * 2 +
+               int(np.asarray(batch["row_vocab"], np.int64).sum()) * 4)
+
+
+def time_lm_head(sampler, dev, k, repeats, stream, peak):
+    """The LM head in front of the sampler (qwen3tts frame: 32 streams x 16
+    codebooks, hidden 1024, V 3072 / 2048; synthetic weights): k calls per
+    CUDA graph over three weight sets and three frames of hidden states (3 x
+    69 MB of weights, more than L2), 'repeats' timed replays, median.  Times
+    ts_lm_head_logits alone (the head kernel's roofline) and
+    ts_lm_head_sample (head and sampler in one call, the step advance into a
+    second step array)."""
+    import torch
+    import codebook_token_sampling_gb300 as ts
+    k = max(2, k - k % 2)
+    sets = [workloads.make_lm_head(i, weight_seed=i) for i in range(3)]
+    batch, head = sets[0]
+    b = ts.DeviceBatch(batch, dev, advance_steps=True, double_steps=True)
+    h = ts.LmHead(head, dev)
+    weights = [h.weights] + [torch.from_numpy(np.asarray(hd["weights"]).view(np.int16)).to(dev)
+                             for _, hd in sets[1:]]
+    hidden = [h.hidden] + [torch.from_numpy(np.asarray(hd["hidden"]).view(np.int16)).to(dev)
+                           for _, hd in sets[1:]]
+
+    def graph_of(call):
+        with torch.cuda.stream(stream):
+            for i in range(4):
+                h.set_weights(weights[i % 3])
+                h.set_hidden(hidden[i % 3])
+                call()
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(k):
+                h.set_weights(weights[i % 3])
+                h.set_hidden(hidden[i % 3])
+                call()
+        return g
+
+    def run(g):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = []
+        with torch.cuda.stream(stream):
+            g.replay()
+            stream.synchronize()
+            for _ in range(repeats):
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) / 1e3 / k)
+        return times
+
+    def fused():
+        ts.ts_lm_head_sample(sampler.handle, h, b, stream)
+        b.swap_steps()
+
+    t_logits = run(graph_of(lambda: ts.ts_lm_head_logits(sampler.handle, h, b, stream)))
+    t_fused = run(graph_of(fused))
+    del weights, hidden
+    alg = lm_head_bytes(batch, head)
+    tl = statistics.median(t_logits)
+    tf = statistics.median(t_fused)
+    n_rows, n_streams = int(batch["n_rows"]), int(batch["n_streams"])
+    return {
+        "workload": "qwen3tts frame through an LM head: 32 streams x 16 codebooks, hidden 1024, "
+                    "V 3072 (codebook 0) / 2048, bf16 weights N(0, (2.5/32)^2) and hidden "
+                    "states N(0, 1), fp32 logits; T 1.0, top_k 30, top_p 0.9, cap 64",
+        "l2": "three weight sets of %.1f MB rotated (more than L2)" % (2 * np.asarray(head["weights"]).size / 1e6),
+        "calls_per_graph": k, "repeats": repeats,
+        "head": {"kernel": "lm_head_kernel", "us_per_call": 1e6 * tl,
+                 "us_min": 1e6 * min(t_logits), "us_max": 1e6 * max(t_logits),
+                 "algorithmic_bytes_per_launch": alg, "gb_per_s": alg / tl / 1e9,
+                 "roofline": {"bound": "hbm", "achieved": alg / tl / 1e9, "peak": peak,
+                              "unit": "GB/s", "frac": alg / tl / 1e9 / peak,
+                              "traffic": recorded_traffic("lm_head", None)},
+                 "tflops": 2.0 * n_rows / int(batch["n_codebooks"]) *
+                           np.asarray(head["weights"]).size / tl / 1e12},
+        "head_and_sample": {"us_per_frame": 1e6 * tf, "us_min": 1e6 * min(t_fused),
+                            "us_max": 1e6 * max(t_fused), "frames_per_s": n_streams / tf,
+                            "rows_per_s": n_rows / tf, "launches_per_call": 2},
+    }
+
+
 def summarize(times):
     t = sorted(times)
     return {"us_median": 1e6 * statistics.median(t), "us_min": 1e6 * t[0], "us_max": 1e6 * t[-1],
@@ -613,6 +700,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-multi-step", action="store_true",
                     help="skip the multi-step batched figure (R steps' rows in one launch)")
+    ap.add_argument("--no-lm-head", action="store_true",
+                    help="skip the LM-head figure (the head kernel and head + sampler)")
     ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2, 3, 4],
                     help="force the kernel family (0 = automatic, 1 = warp per row, 2 = CTA / "
                          "cluster per row, 3 = wide cluster, 4 = wide split)")
@@ -715,6 +804,10 @@ def main():
             import torch.distributed as dist
             dist.destroy_process_group()
         return
+    lm = None
+    if not args.no_lm_head:
+        lm = time_lm_head(head["sampler"], dev, min(k, 60), reps, head["stream"], peak)
+        torch.cuda.empty_cache()
     host = head["host"]
     n_rows = int(host["n_rows"])
     n_streams = int(host["n_streams"])
@@ -761,6 +854,7 @@ def main():
                                                   "(CUDA events on the launching stream)"},
         "in_place_advance": summ.get("in_place_advance"),
         "multi_step": summ.get("multi_step"),
+        "lm_head": lm,
         "e2e": e2e,
         "gpu_launches": summ["launches_per_step"] * k,
         "clocks": clk,

@@ -62,3 +62,11 @@ def test_traffic_record_follows_the_kernel_sources(tmp_path):
     f.write_text(f.read_text() + "\nconstexpr int kUnused = 1;\n")
     assert bench.kernel_source_hash(str(src)) != h
     assert bench.recorded_traffic("drama3", None, str(rec), str(src)) is None
+
+
+def test_lm_head_bytes_of_the_qwen3tts_frame():
+    """Weights (bf16), hidden states (bf16) and fp32 logits, once each:
+    (3072 + 15 x 2048) x 1024 x 2 + 512 x 1024 x 2 + 32 x (3072 + 15 x 2048) x 4."""
+    batch, head = workloads.make_lm_head(0)
+    v = 3072 + 15 * 2048
+    assert bench.lm_head_bytes(batch, head) == v * 1024 * 2 + 512 * 1024 * 2 + 32 * v * 4
