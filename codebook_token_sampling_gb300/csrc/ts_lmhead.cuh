@@ -9,10 +9,10 @@
 // the Drama 3 article (section "两阶段共享一张卡") has one forward per frame
 // produce every codebook's logits, sampled on the device.
 //
-// One CTA computes a 32-stream x 128-entry tile of one codebook: the head's
-// 128 rows stream once through a four-stage cp.async ring (64 hidden elements
-// per stage), the tile's 32 hidden states ride along, and four warps each take
-// 32 entries with bf16 m16n8k16 MMAs (fp32 accumulators).  At the frame sizes
+// One CTA computes a 32-stream x NT-entry tile of one codebook: the head's NT
+// rows stream once through an NS-stage cp.async ring (KC hidden elements per
+// stage), the tile's 32 hidden states ride along, and four warps each take
+// NT / 4 entries with bf16 m16n8k16 MMAs (fp32 accumulators).  At the frame sizes
 // of the pages (32 or 128 streams per codebook) the weights dominate the
 // bytes, so the kernel is bound by the weight stream, not by the MMAs.
 //
@@ -29,14 +29,19 @@ namespace ts {
 
 constexpr int kLmThreads = 128;            // four warps
 constexpr int kLmM = 32;                   // streams of one codebook per CTA
-constexpr int kLmN = 128;                  // vocabulary entries per CTA (32 per warp)
-constexpr int kLmKC = 64;                  // hidden elements per pipeline stage
-constexpr int kLmStages = 4;
-constexpr int kLmPitch = kLmKC + 8;        // bf16 per shared row: 144 bytes, so the
-                                           // eight rows of an ldmatrix hit distinct banks
-constexpr int kLmStageA = kLmM * kLmPitch;  // bf16 elements per stage
-constexpr int kLmStageB = kLmN * kLmPitch;
-constexpr uint32_t kLmSmemBytes = kLmStages * (kLmStageA + kLmStageB) * 2;  // 92,160 B
+
+// A tile of NT vocabulary entries (NT / 4 per warp, a multiple of 16) with an
+// NS-stage ring of KC hidden elements per stage.  Shared rows are KC + 8
+// elements long (a 16-byte pad), so the eight rows of an ldmatrix start 4
+// banks apart.
+template <int NT, int NS, int KC>
+struct LmTile {
+  static_assert(NT % 64 == 0 && NS >= 2 && KC % 64 == 0, "tile, ring and stage shapes");
+  static constexpr int kPitch = KC + 8;
+  static constexpr int kStageA = kLmM * kPitch;  // bf16 elements of hidden states per stage
+  static constexpr int kStageB = NT * kPitch;    // of head rows per stage
+  static constexpr uint32_t kSmemBytes = NS * (kStageA + kStageB) * 2;
+};
 
 struct LmParams {
   const uint16_t *hidden;        // [n_rows][dim] bf16 bits
@@ -44,7 +49,7 @@ struct LmParams {
   int64_t weights_len;           // elements
   const int64_t *head_offsets;   // [n_heads]
   int32_t n_heads;               // Q: row r uses head r mod Q
-  int32_t dim;                   // a multiple of kLmKC
+  int32_t dim;                   // a multiple of the tile's KC
   int32_t n_rows;                // a multiple of n_heads
   int32_t max_row_vocab;
   const int32_t *row_vocab;
@@ -83,19 +88,26 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// grid (ceil(max_row_vocab / 128), Q, ceil(streams / 32)), kLmThreads threads,
-// kLmSmemBytes of dynamic shared memory.
+// grid (ceil(max_row_vocab / NT), Q, ceil(streams / 32)), kLmThreads threads,
+// LmTile<NT, NS, KC>::kSmemBytes of dynamic shared memory; dim a multiple of KC.
+template <int NT, int NS, int KC>
 __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const LmParams p) {
+  using Tile = LmTile<NT, NS, KC>;
+  constexpr int kPitch = Tile::kPitch;
+  constexpr int kStageA = Tile::kStageA;
+  constexpr int kStageB = Tile::kStageB;
+  constexpr int kWarpN = NT / 4;       // entries per warp
+  constexpr int kTilesN = kWarpN / 8;  // 8-entry MMA tiles per warp (even)
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t *sa = reinterpret_cast<uint16_t *>(smem);
-  uint16_t *sb = sa + kLmStages * kLmStageA;
+  uint16_t *sb = sa + NS * kStageA;
   __shared__ int64_t tile_off[kLmM];   // the tile's rows: logits offset
   __shared__ int32_t tile_vocab[kLmM]; // and width (0: nothing to write)
   __shared__ int32_t tile_vmax, head_rows;
   __shared__ int64_t head_off;
 
   const int q = static_cast<int>(blockIdx.y);
-  const int v0 = static_cast<int>(blockIdx.x) * kLmN;
+  const int v0 = static_cast<int>(blockIdx.x) * NT;
   const int s0 = static_cast<int>(blockIdx.z) * kLmM;
   const int t = static_cast<int>(threadIdx.x);
   const int lane = t & 31, warp = t >> 5;
@@ -136,77 +148,77 @@ __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const LmParams p) {
   if (wrows <= 0) {  // no row of this head lies inside the weights
     for (int i = t >> 5; i < kLmM; i += kLmThreads / 32) {
       const int vr = tile_vocab[i];
-      for (int v = v0 + lane; v < vr && v < v0 + kLmN; v += 32)
+      for (int v = v0 + lane; v < vr && v < v0 + NT; v += 32)
         p.logits[tile_off[i] + v] = __int_as_float(0x7FC00000);
     }
     return;
   }
 
-  // ---- the ring: stage st holds hidden elements [64 kc, 64 kc + 64) of the
-  // tile's 32 hidden states and of its 128 head rows (rows past the tile's
+  // ---- the ring: stage st holds hidden elements [KC kc, KC kc + KC) of the
+  // tile's 32 hidden states and of its NT head rows (rows past the tile's
   // streams or the head's rows repeat the last one; their results are not
   // stored) ----
   const uint16_t *wbase = p.weights + head_off;
-  const int nk = p.dim / kLmKC;
+  const int nk = p.dim / KC;
   auto load_stage = [&](int kc, int st) {
-    uint16_t *a = sa + st * kLmStageA;
-    uint16_t *b = sb + st * kLmStageB;
-    const int k0 = kc * kLmKC;
+    uint16_t *a = sa + st * kStageA;
+    uint16_t *b = sb + st * kStageB;
+    const int k0 = kc * KC;
 #pragma unroll
-    for (int j = 0; j < (kLmM * kLmKC / 8) / kLmThreads; ++j) {
+    for (int j = 0; j < (kLmM * KC / 8) / kLmThreads; ++j) {
       const int c = t + kLmThreads * j;
-      const int i = c >> 3, part = c & 7;
+      const int i = c / (KC / 8), part = c % (KC / 8);
       const int s = min(s0 + i, n_streams - 1);
       const uint16_t *src =
           p.hidden + (static_cast<int64_t>(s) * p.n_heads + q) * p.dim + k0 + part * 8;
-      cp_async16(a + i * kLmPitch + part * 8, src);
+      cp_async16(a + i * kPitch + part * 8, src);
     }
 #pragma unroll
-    for (int j = 0; j < (kLmN * kLmKC / 8) / kLmThreads; ++j) {
+    for (int j = 0; j < (NT * KC / 8) / kLmThreads; ++j) {
       const int c = t + kLmThreads * j;
-      const int i = c >> 3, part = c & 7;
+      const int i = c / (KC / 8), part = c % (KC / 8);
       const int v = min(v0 + i, wrows - 1);
-      cp_async16(b + i * kLmPitch + part * 8,
+      cp_async16(b + i * kPitch + part * 8,
                  wbase + static_cast<int64_t>(v) * p.dim + k0 + part * 8);
     }
   };
 
 #pragma unroll
-  for (int st = 0; st < kLmStages - 1; ++st) {
+  for (int st = 0; st < NS - 1; ++st) {
     if (st < nk) load_stage(st, st);
     cp_async_commit();
   }
-  float acc[2][4][4];
+  float acc[2][kTilesN][4];
 #pragma unroll
   for (int m = 0; m < 2; ++m)
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < kTilesN; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[m][n][e] = 0.0f;
 
 #pragma unroll 1
   for (int kc = 0; kc < nk; ++kc) {
-    cp_async_wait_group<kLmStages - 2>();  // this thread's copies of stage kc are in
+    cp_async_wait_group<NS - 2>();  // this thread's copies of stage kc are in
     __syncthreads();  // everyone's are, and stage kc - 1 is no longer read
-    const int nxt = kc + kLmStages - 1;
-    if (nxt < nk) load_stage(nxt, nxt % kLmStages);
+    const int nxt = kc + NS - 1;
+    if (nxt < nk) load_stage(nxt, nxt % NS);
     cp_async_commit();
-    const uint16_t *a = sa + (kc % kLmStages) * kLmStageA;
-    const uint16_t *b = sb + (kc % kLmStages) * kLmStageB;
+    const uint16_t *a = sa + (kc % NS) * kStageA;
+    const uint16_t *b = sb + (kc % NS) * kStageB;
 #pragma unroll
-    for (int kk = 0; kk < kLmKC / 16; ++kk) {
+    for (int kk = 0; kk < KC / 16; ++kk) {
       // A: matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15) of each 16-row tile
       uint32_t af[2][4];
 #pragma unroll
       for (int m = 0; m < 2; ++m)
-        ldmatrix_x4(af[m], a + (m * 16 + (lane & 15)) * kLmPitch + kk * 16 + (lane >> 4) * 8);
+        ldmatrix_x4(af[m], a + (m * 16 + (lane & 15)) * kPitch + kk * 16 + (lane >> 4) * 8);
       // B: for each pair of 8-entry tiles, (tile 0 | tile 1) x (k 0-7 | 8-15)
-      uint32_t bf[4][2];
+      uint32_t bf[kTilesN][2];
 #pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
+      for (int pr = 0; pr < kTilesN / 2; ++pr) {
         uint32_t r4[4];
-        const int n = warp * 32 + pr * 16 + ((lane >> 4) << 3) + (lane & 7);
-        ldmatrix_x4(r4, b + n * kLmPitch + kk * 16 + (((lane >> 3) & 1) << 3));
+        const int n = warp * kWarpN + pr * 16 + ((lane >> 4) << 3) + (lane & 7);
+        ldmatrix_x4(r4, b + n * kPitch + kk * 16 + (((lane >> 3) & 1) << 3));
         bf[2 * pr][0] = r4[0];
         bf[2 * pr][1] = r4[1];
         bf[2 * pr + 1][0] = r4[2];
@@ -215,13 +227,13 @@ __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const LmParams p) {
 #pragma unroll
       for (int m = 0; m < 2; ++m)
 #pragma unroll
-        for (int n = 0; n < 4; ++n) mma_bf16_16816(acc[m][n], af[m], bf[n][0], bf[n][1]);
+        for (int n = 0; n < kTilesN; ++n) mma_bf16_16816(acc[m][n], af[m], bf[n][0], bf[n][1]);
     }
   }
   cp_async_wait_group<0>();  // the trailing (empty) groups
 
   // ---- the tile's logits: accumulator (m, n, 2 h + e) is stream s0 + 16 m +
-  // g + 8 h, entry v0 + 32 warp + 8 n + 2 tg + e ----
+  // g + 8 h, entry v0 + (NT / 4) warp + 8 n + 2 tg + e ----
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
 #pragma unroll
@@ -231,10 +243,10 @@ __global__ void __launch_bounds__(kLmThreads) lm_head_kernel(const LmParams p) {
       const int64_t off = tile_off[i];
       const bool inside = vr <= wrows;
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
+      for (int n = 0; n < kTilesN; ++n) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int v = v0 + warp * 32 + n * 8 + 2 * tg + e;
+          const int v = v0 + warp * kWarpN + n * 8 + 2 * tg + e;
           if (v < vr) p.logits[off + v] = inside ? acc[m][n][2 * h + e] : __int_as_float(0x7FC00000);
         }
       }

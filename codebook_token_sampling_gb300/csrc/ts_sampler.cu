@@ -65,6 +65,11 @@ int cap_of(int requested) {
 
 constexpr int kWarpMaxBF16 = 4096;
 constexpr int kWarpMaxF32 = 4096;
+// The LM head's tile: vocabulary entries per CTA, pipeline stages and hidden
+// elements per stage (the hidden size must be a multiple of it).
+constexpr int kLmN = 128;
+constexpr int kLmStages = 4;
+constexpr int kLmKC = 64;
 constexpr int kWarpMaxF32Penalty = 2048;  // rows the penalty edits in one staged pass
 // bf16 rows wider than this take a single-pass wide path
 constexpr int kWideMinVocab = 32768;
@@ -334,7 +339,7 @@ ts_status set_attributes(int device) {
   fns[n++] = reinterpret_cast<void *>(ts::split_stream_kernel);
   fns[n++] = reinterpret_cast<void *>(ts::split_tail_kernel);
   fns[n++] = warp_kernel_for<ts::KeyF32>(32, 1, 2);
-  fns[n++] = reinterpret_cast<void *>(ts::lm_head_kernel);
+  fns[n++] = reinterpret_cast<void *>(ts::lm_head_kernel<kLmN, kLmStages, kLmKC>);
   for (int i = 0; i < n; ++i) {
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, fns[i]);
@@ -539,7 +544,8 @@ ts_status check_lm_head(const ts_lm_head *h, const ts_batch *b) {
 
 ts_status launch_lm_head(const ts_sampler *s, const ts_lm_head *h, const ts_batch *b,
                          cudaStream_t st) {
-  static_assert(ts::kLmKC == TS_LM_HEAD_DIM_STEP, "the header's dim rule is the stage depth");
+  using Tile = ts::LmTile<kLmN, kLmStages, kLmKC>;
+  static_assert(kLmKC == TS_LM_HEAD_DIM_STEP, "the header's dim rule is the stage depth");
   ts::LmParams p;
   std::memset(&p, 0, sizeof p);
   p.hidden = static_cast<const uint16_t *>(h->hidden);
@@ -557,18 +563,18 @@ ts_status launch_lm_head(const ts_sampler *s, const ts_lm_head *h, const ts_batc
   const int streams = b->n_rows / h->n_heads;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>((b->max_row_vocab + ts::kLmN - 1) / ts::kLmN),
+  cfg.gridDim = dim3(static_cast<unsigned>((b->max_row_vocab + kLmN - 1) / kLmN),
                      static_cast<unsigned>(h->n_heads),
                      static_cast<unsigned>((streams + ts::kLmM - 1) / ts::kLmM));
   cfg.blockDim = dim3(ts::kLmThreads);
-  cfg.dynamicSmemBytes = ts::kLmSmemBytes;
+  cfg.dynamicSmemBytes = Tile::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr.val.programmaticStreamSerializationAllowed = s->pdl ? 1 : 0;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, ts::lm_head_kernel, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, ts::lm_head_kernel<kLmN, kLmStages, kLmKC>, p);
   return e == cudaSuccess ? TS_OK : cuda_fail(e, "LM head launch");
 }
 
