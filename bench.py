@@ -647,6 +647,24 @@ def profile_launches(args):
     """A few plain launches of one step, for a profiler to capture."""
     import torch
     import codebook_token_sampling_gb300 as ts
+    if args.profile_lm_head:
+        # the LM head's qwen3tts frame: ts_lm_head_sample calls (the head
+        # kernel, then the sampler), weight sets rotated as the bench loop does
+        sets = [workloads.make_lm_head(i, weight_seed=i) for i in range(3)]
+        lb, lh = sets[0]
+        sampler = ts.Sampler(0, lb["cap"])
+        batch = ts.DeviceBatch(lb, "cuda", advance_steps=True, double_steps=True)
+        head = ts.LmHead(lh, "cuda")
+        weights = [head.weights] + [torch.from_numpy(np.asarray(h["weights"]).view(np.int16)).cuda()
+                                    for _, h in sets[1:]]
+        for i in range(args.profile):
+            head.set_weights(weights[i % 3])
+            ts.ts_lm_head_sample(sampler.handle, head, batch)
+            batch.swap_steps()
+        torch.cuda.synchronize()
+        print(json.dumps({"profile": "lm_head", "rows": int(lb["n_rows"]), "launches": args.profile,
+                          "plan": sampler.plan(batch), "status": sampler.read_status()}))
+        return
     host = workloads.make(args.config, 0, rows=args.rows)
     sampler = ts.Sampler(0, host["cap"])
     sampler.reserve(int(host["n_rows"]), int(host["max_row_vocab"]))
@@ -709,6 +727,8 @@ def main():
                     help="the warp path's warps per row (0 = automatic)")
     ap.add_argument("--profile", type=int, default=0, metavar="N",
                     help="profiling mode: N plain launches of one step, no timing (for ncu)")
+    ap.add_argument("--profile-lm-head", action="store_true",
+                    help="profiling mode: the LM head's frame (ts_lm_head_sample) instead of --config")
     ap.add_argument("--profile-steps", type=int, default=1, metavar="R",
                     help="profiling mode: each launch samples R steps (ts_sample_steps)")
     args = ap.parse_args()
