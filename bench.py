@@ -80,9 +80,13 @@ def kernel_source_hash(src: str | None = None) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(config: str, rows, path: str | None = None, src: str | None = None):
+def recorded_traffic(config: str, rows, path: str | None = None, src: str | None = None,
+                     field: str = "dram_bytes_per_launch"):
     """DRAM bytes per launch from the committed ncu record of this workload,
-    or None when there is none or the kernels changed since it was taken."""
+    or None when there is none or the kernels changed since it was taken.
+    ``field``: "dram_bytes_per_launch" (caches flushed before each profiled
+    kernel, ncu's default) or "dram_bytes_per_launch_no_flush" (caches left as
+    the previous kernel left them)."""
     path = path or os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -93,7 +97,7 @@ def recorded_traffic(config: str, rows, path: str | None = None, src: str | None
     e = rec.get(key)
     if not e or e.get("source_hash") != kernel_source_hash(src):
         return None
-    return e.get("dram_bytes_per_launch")
+    return e.get(field)
 
 
 def concat_steps(hosts):
@@ -508,7 +512,9 @@ def time_lm_head(sampler, dev, k, repeats, stream, peak):
                  "algorithmic_bytes_per_launch": alg, "gb_per_s": alg / tl / 1e9,
                  "roofline": {"bound": "hbm", "achieved": alg / tl / 1e9, "peak": peak,
                               "unit": "GB/s", "frac": alg / tl / 1e9 / peak,
-                              "traffic": recorded_traffic("lm_head", None)},
+                              "traffic": recorded_traffic("lm_head", None),
+                              "traffic_no_flush": recorded_traffic(
+                                  "lm_head", None, field="dram_bytes_per_launch_no_flush")},
                  "tflops": 2.0 * n_rows / int(batch["n_codebooks"]) *
                            np.asarray(head["weights"]).size / tl / 1e12},
         "head_and_sample": {"us_per_frame": 1e6 * tf, "us_min": 1e6 * min(t_fused),
@@ -817,6 +823,8 @@ def main():
             key = f"stress{rows}" if name == "stress" else name
             others[key] = res["summary"]
             res["summary"]["traffic"] = recorded_traffic(name, rows)
+            res["summary"]["traffic_no_flush"] = recorded_traffic(
+                name, rows, field="dram_bytes_per_launch_no_flush")
             del res
             torch.cuda.empty_cache()
     if rank != 0:
@@ -865,6 +873,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": recorded_traffic(args.config, args.rows),
+                     "traffic_no_flush": recorded_traffic(args.config, args.rows,
+                                                          field="dram_bytes_per_launch_no_flush"),
                      "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)",
                      "kernel": kname, "launches_per_step": summ["launches_per_step"],
