@@ -362,10 +362,11 @@ typedef struct {
 ts_status ts_lm_head_logits(ts_sampler *s, const ts_lm_head *h, const ts_batch *b, void *stream);
 
 /* ts_lm_head_logits, then ts_sample on the same batch, in one call: two
- * launches on `stream`, the sampler's scheduled while the head drains
- * (programmatic dependent launch) and reading the logits after the head has
- * completed.  The logits (a few MB per frame) go through L2 between the two;
- * a host-side refusal of the sampler is returned before the head launches. */
+ * launches on `stream`.  The head is launched like the sampler's kernels
+ * (programmatic dependent launch unless TS_OPT_PDL is 0); the sampler follows
+ * it plainly, so that its blocks are placed once the head's shared memory is
+ * free.  The logits (a few MB per frame) go through L2 between the two; a
+ * host-side refusal of the sampler is returned before the head launches. */
 ts_status ts_lm_head_sample(ts_sampler *s, const ts_lm_head *h, const ts_batch *b, void *stream);
 
 /* step[i] += 1 for i < n_streams, on the device (graph-capturable).  Call it
