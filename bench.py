@@ -607,10 +607,11 @@ def measure_config(args, name, rows, dev, l2, peak, k, w, repeats, num_sms, mult
 
 
 def e2e_host_calls(res, dev, k, world):
-    """End to end through the public API: per step, the step's logits go from
-    pinned host memory to the device, one ts_sample call samples them (fused
-    step advance), the ids and EOS flags come back to pinned host memory and
-    the host waits for them.  Host wall clock over k steps (at least 200)."""
+    """End to end through the public API: one ts_sample_host call per step,
+    which copies the step's logits from pinned host memory to the device,
+    samples them (fused step advance), copies the ids and EOS flags back to
+    pinned host memory and waits for them.  Host wall clock over k steps (at
+    least 200)."""
     import torch
     import codebook_token_sampling_gb300 as ts
     host, hosts = res["host"], res["hosts"]
@@ -627,12 +628,8 @@ def e2e_host_calls(res, dev, k, world):
     n = max(200, k)
 
     def step(i):
-        with torch.cuda.stream(stream):
-            dev_in.copy_(pinned[i % len(pinned)], non_blocking=True)
-            ts.ts_sample(sampler.handle, batch, stream)
-            ids_host.copy_(batch.out_ids, non_blocking=True)
-            eos_host.copy_(batch.out_eos, non_blocking=True)
-        stream.synchronize()
+        ts.ts_sample_host(sampler.handle, batch, pinned[i % len(pinned)], ids_host, eos_host,
+                          stream)
 
     for i in range(20):
         step(i)
@@ -645,8 +642,9 @@ def e2e_host_calls(res, dev, k, world):
     return {"value": world * n_rows / t, "unit": "rows/s",
             "h2d_bytes_per_step": int(dev_in.numel() * dev_in.element_size()),
             "d2h_bytes_per_step": n_rows * 5, "us_per_step": 1e6 * t, "steps": n,
-            "how": "host wall clock; per step: pinned H2D copy of the logits, one ts_sample "
-                   "call (fused step advance), D2H of ids and EOS flags, stream sync"}
+            "how": "host wall clock; per step one ts_sample_host call: pinned H2D copy of "
+                   "the logits, sampling (fused step advance), D2H of ids and EOS flags, "
+                   "stream wait"}
 
 
 def profile_launches(args):

@@ -7,7 +7,7 @@ only for device memory and streams.  The functions keep the C names:
     ts_create, ts_destroy, ts_max_top_k, ts_sample, ts_sample_debug,
     ts_sample_steps, ts_reserve, ts_sample_noalloc, ts_advance_steps,
     ts_read_status, ts_set_option, ts_plan, ts_status_string, ts_last_error,
-    ts_lm_head_logits, ts_lm_head_sample
+    ts_lm_head_logits, ts_lm_head_sample, ts_sample_host
 
 ``Sampler`` wraps a handle; ``DeviceBatch`` holds one step's per-row arrays on
 the GPU with a prebuilt ``ts_batch`` so that repeated calls marshal nothing;
@@ -53,7 +53,7 @@ TS_LM_HEAD_MAX_DIM = 16384
 EXPORTED = ("ts_create", "ts_destroy", "ts_max_top_k", "ts_sample", "ts_sample_debug",
             "ts_sample_steps", "ts_reserve", "ts_sample_noalloc", "ts_advance_steps",
             "ts_read_status", "ts_set_option", "ts_plan", "ts_status_string", "ts_last_error",
-            "ts_lm_head_logits", "ts_lm_head_sample")
+            "ts_lm_head_logits", "ts_lm_head_sample", "ts_sample_host")
 
 
 class TsBatch(ctypes.Structure):
@@ -145,6 +145,7 @@ def _load(path: str):
         "ts_read_status": ([vp, ctypes.POINTER(ctypes.c_uint32), vp], ctypes.c_int),
         "ts_set_option": ([vp, i32, i32], ctypes.c_int),
         "ts_plan": ([vp, ctypes.POINTER(TsBatch)] + [ctypes.POINTER(i32)] * 5, ctypes.c_int),
+        "ts_sample_host": ([vp, ctypes.POINTER(TsBatch), vp, vp, vp, vp], ctypes.c_int),
         "ts_lm_head_logits": ([vp, ctypes.POINTER(TsLmHead), ctypes.POINTER(TsBatch), vp],
                               ctypes.c_int),
         "ts_lm_head_sample": ([vp, ctypes.POINTER(TsLmHead), ctypes.POINTER(TsBatch), vp],
@@ -253,6 +254,18 @@ def ts_plan(handle: int, batch: "DeviceBatch") -> dict:
            "ts_plan")
     keys = ("path", "ctas_per_row", "threads", "smem_bytes", "grid")
     return {k: int(o.value) for k, o in zip(keys, out)}
+
+
+def ts_sample_host(handle: int, batch: "DeviceBatch", host_logits, host_ids, host_eos,
+                   stream=None) -> None:
+    """Host logits in, host ids and EOS flags out (see the header).  The
+    three host buffers are CPU tensors (pinned for asynchronous copies) or
+    numpy arrays: logits in the batch's layout (int16 / uint16 bits for bf16,
+    float32), int32 ids and uint8 flags of n_rows each."""
+    def ptr(a):
+        return a.data_ptr() if hasattr(a, "data_ptr") else a.ctypes.data
+    _check(_lib.ts_sample_host(handle, ctypes.byref(batch.c), ptr(host_logits), ptr(host_ids),
+                               ptr(host_eos), _stream_ptr(stream)), "ts_sample_host")
 
 
 def ts_lm_head_logits(handle: int, head: "LmHead", batch: "DeviceBatch", stream=None) -> None:

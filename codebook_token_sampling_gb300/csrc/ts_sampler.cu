@@ -764,6 +764,31 @@ ts_status ts_lm_head_sample(ts_sampler *s, const ts_lm_head *h, const ts_batch *
   return launch(s, b, make_params(s, b), st, false);
 }
 
+ts_status ts_sample_host(ts_sampler *s, const ts_batch *b, const void *host_logits,
+                         int32_t *host_ids, uint8_t *host_eos, void *stream) {
+  if (!s || !host_logits || !host_ids || !host_eos) return TS_ERR_INVALID_ARG;
+  ts_status rc = check_batch(b);
+  if (rc != TS_OK || b->n_rows == 0) return rc;
+  Plan pl;  // refuse what the sampler would refuse before anything is queued
+  rc = make_plan(s, b, &pl);
+  if (rc != TS_OK) return rc;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t es = b->dtype == TS_DTYPE_BF16 ? 2 : 4;
+  cudaError_t e = cudaMemcpyAsync(const_cast<void *>(b->logits), host_logits,
+                                  static_cast<size_t>(b->logits_len) * es,
+                                  cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "ts_sample_host: logits copy");
+  rc = launch(s, b, make_params(s, b), st);
+  if (rc != TS_OK) return rc;
+  const size_t n = static_cast<size_t>(b->n_rows);
+  e = cudaMemcpyAsync(host_ids, b->out_ids, n * sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "ts_sample_host: ids copy");
+  e = cudaMemcpyAsync(host_eos, b->out_eos, n, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "ts_sample_host: EOS flags copy");
+  e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? TS_OK : cuda_fail(e, "ts_sample_host: stream wait");
+}
+
 ts_status ts_sample_debug(ts_sampler *s, const ts_batch *b, int32_t max_keep, int32_t *kept_ids,
                           float *kept_probs, int32_t *n_kept, int32_t *n_nucleus, void *stream) {
   if (!s || max_keep <= 0 || !kept_ids || !kept_probs || !n_kept || !n_nucleus)

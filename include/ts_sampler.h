@@ -192,6 +192,19 @@ int32_t ts_max_top_k(const ts_sampler *s);
  * word. */
 ts_status ts_sample(ts_sampler *s, const ts_batch *b, void *stream);
 
+/* ts_sample for logits that are in host memory, end to end in one call: the
+ * host's logits_len logits (host_logits, in the batch's dtype and layout) are
+ * copied into b->logits (device, caller-owned, writable), the batch is
+ * sampled, the n_rows ids and EOS flags are copied back into host_ids and
+ * host_eos, and the call waits for `stream` before it returns, so the results
+ * can be read at once.  Pinned host memory makes the copies asynchronous DMA
+ * on the stream; pageable memory also works, more slowly.  Because it waits,
+ * it cannot be captured in a CUDA graph.  Host-side refusals (as for
+ * ts_sample, plus a NULL host pointer) are returned before anything is
+ * queued; row errors are reported through the status word as for ts_sample. */
+ts_status ts_sample_host(ts_sampler *s, const ts_batch *b, const void *host_logits,
+                         int32_t *host_ids, uint8_t *host_eos, void *stream);
+
 /* Same draw as ts_sample, and additionally writes, per row r: the top-k set
  * (kept_ids[r * max_keep + j], unspecified order), each kept token's
  * probability renormalised over the top-k set (kept_probs, fp32; greedy rows

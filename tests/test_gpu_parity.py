@@ -442,3 +442,43 @@ def test_graph_loop_with_feedback(ts, name, steps):
     assert n_safe >= 0.9 * n_checked, (n_safe, n_checked)
     assert s.read_status() == 0
     s.close()
+
+
+def test_sample_host_matches_the_device_call(ts):
+    """ts_sample_host (host logits in, host ids and EOS flags out, one call)
+    gives the ids and flags of ts_sample on the same logits and steps, advances
+    the steps the same way, and refuses a NULL host buffer before queueing
+    anything."""
+    import ctypes
+    hosts = [workloads.make("drama3", i) for i in range(3)]
+    host = hosts[0]
+    n = int(host["n_rows"])
+    s = make_sampler(ts, host["cap"])
+    dev = ts.DeviceBatch(host, "cuda", advance_steps=True)
+    hb = ts.DeviceBatch(host, "cuda", advance_steps=True)
+    pinned = [torch.from_numpy(np.ascontiguousarray(h["logits"]).view(np.int16)).pin_memory()
+              for h in hosts]
+    ids = torch.empty(n, dtype=torch.int32).pin_memory()
+    eos = torch.empty(n, dtype=torch.uint8).pin_memory()
+    for i in range(3):
+        dev.set_logits(pinned[i].cuda())
+        s.sample(dev)
+        torch.cuda.synchronize()
+        ts.ts_sample_host(s.handle, hb, pinned[i], ids, eos)
+        assert np.array_equal(ids.numpy(), dev.ids()), i
+        assert np.array_equal(eos.numpy(), dev.eos()), i
+        assert torch.equal(hb.logits.cpu(), pinned[i])
+    assert np.array_equal(hb.step.cpu().numpy(), dev.step.cpu().numpy())
+    assert s.read_status() == 0
+    # numpy host buffers (pageable) work too
+    ids_np = np.zeros(n, np.int32)
+    eos_np = np.zeros(n, np.uint8)
+    ts.ts_sample_host(s.handle, hb, pinned[0].numpy(), ids_np, eos_np)
+    ref = oracle.sample(dict(host, step=np.asarray(host["step"]) + 3), max_keep=64, n_threads=8)
+    safe = ref["margin"] > 1e-5
+    assert safe.sum() >= 0.98 * n
+    assert np.array_equal(ids_np[safe], ref["ids"][safe])
+    st = ts.library().ts_sample_host(s.handle, ctypes.byref(hb.c), None, ids.data_ptr(),
+                                     eos.data_ptr(), None)
+    assert st == ts.TS_ERR_INVALID_ARG
+    s.close()
