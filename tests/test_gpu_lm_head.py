@@ -238,3 +238,26 @@ def test_lm_head_sample_in_a_graph(ts):
         g.replay()
         torch.cuda.synchronize()
         assert np.array_equal(b2.ids(), plain[i]), i
+
+
+def test_lm_head_sample_refusal_comes_before_the_head(ts):
+    """A refusal of the sampler (the repetition penalty on fp32 rows wider
+    than 2048) is returned before the head runs: the logits are untouched.
+    The head alone still runs."""
+    batch, head = workloads.make_lm_head(0, streams=4, dim=128, vocabs=(3072, 2048),
+                                         eos_ids=[-1, -1])
+    s = ts.Sampler(0, 64)
+    b = ts.DeviceBatch(batch, "cuda", history={"len": 4, "codebooks": 2,
+                                               "penalty": np.ones(batch["n_rows"], np.float32)})
+    h = ts.LmHead(head, "cuda")
+    b.set_logits(torch.full_like(b.logits, 7.0))
+    with pytest.raises(ts.SamplerError) as e:
+        ts.ts_lm_head_sample(s.handle, h, b)
+    assert e.value.status == ts.TS_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert torch.all(b.logits == 7.0)
+    ts.ts_lm_head_logits(s.handle, h, b)
+    torch.cuda.synchronize()
+    got = b.logits.cpu().numpy()
+    want = oracle.lm_head(batch, head)
+    check_logits(batch, head, got, want)
