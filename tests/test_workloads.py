@@ -69,3 +69,24 @@ def test_stress_shape():
     assert s["row_vocab"].tolist() == [workloads.STRESS_VOCAB] * 2
     assert s["logits"].dtype == np.uint16 and s["logits"].size == 2 * workloads.STRESS_VOCAB
     assert np.all(s["top_k"] == 4096) and s["cap"] == 4096
+
+
+def test_lm_head_frame_layout():
+    """The LM head's frame: stream-major rows with head r mod Q, heads packed
+    one after another (offsets multiples of the hidden size), fp32 logits
+    buffer, hidden states that change with the step and weights that do not."""
+    b0, h0 = workloads.make_lm_head(0)
+    b1, h1 = workloads.make_lm_head(1)
+    q, dim = h0["n_heads"], h0["dim"]
+    assert (q, dim, b0["n_rows"], b0["dtype"]) == (16, 1024, 512, "f32")
+    v = np.asarray(b0["row_vocab"])
+    assert v[0] == 3072 and np.all(v[1:16] == 2048) and np.array_equal(v[:16], v[16:32])
+    assert np.array_equal(np.asarray(b0["codebook"]), np.arange(512) % 16)
+    offs = np.asarray(h0["head_offsets"])
+    assert offs[0] == 0 and np.array_equal(np.diff(offs), v[:15].astype(np.int64) * dim)
+    assert h0["weights"].size == int(v[:16].sum()) * dim and h0["hidden"].size == 512 * dim
+    assert np.asarray(b0["logits"]).dtype == np.float32 and b0["logits"].size == int(v.sum())
+    assert np.array_equal(h0["weights"], h1["weights"])
+    assert not np.array_equal(h0["hidden"], h1["hidden"])
+    w = workloads.bf16_bits_to_f32(h0["weights"][:1 << 20])
+    assert abs(float(w.std()) - 2.5 / 32) < 0.002
