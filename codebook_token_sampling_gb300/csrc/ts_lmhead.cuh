@@ -14,7 +14,9 @@
 // stage), the tile's 32 hidden states ride along, and four warps each take
 // NT / 4 entries with bf16 m16n8k16 MMAs (fp32 accumulators).  At the frame sizes
 // of the pages (32 or 128 streams per codebook) the weights dominate the
-// bytes, so the kernel is bound by the weight stream, not by the MMAs.
+// bytes, so the kernel is bound by what each SM takes in through L2 (its
+// tiles' head rows plus a quarter as much again in hidden states), not by
+// the MMAs.
 //
 // A row whose head does not lie inside the weights (a negative offset, an
 // offset that is not a multiple of 8 elements, or fewer than V_r rows left)
